@@ -1,0 +1,237 @@
+// api.cu -- the extern "C" entry points declared in include/moe.h: host-side
+// validation, buffer layout, and the launch sequence of each step.
+#include <string.h>
+
+#include "internal.cuh"
+
+using namespace moe;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status check_shape(const moe_shape* s) {
+    if (!s) return MOE_ERR_INVALID_ARG;
+    if (s->T < 1 || s->H < 16 || s->H > 16384 || s->H % 16) return MOE_ERR_INVALID_ARG;
+    if (s->I < 16 || s->I > 16384 || s->I % 16) return MOE_ERR_INVALID_ARG;
+    if (s->E_log < 1 || s->E_phys < s->E_log || s->E_phys > 1024) return MOE_ERR_INVALID_ARG;
+    if (s->k < 1 || s->k > s->E_log || s->k > 32) return MOE_ERR_INVALID_ARG;
+    if (s->n_ranks < 1 || s->E_phys % s->n_ranks) return MOE_ERR_INVALID_ARG;
+    if (s->n_src_ranks < 1 || s->T % s->n_src_ranks) return MOE_ERR_INVALID_ARG;
+    if ((long long)s->T * s->k >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
+    if (s->dispatch_fmt != MOE_MSG_BF16 && s->dispatch_fmt != MOE_MSG_INT8) return MOE_ERR_INVALID_ARG;
+    if (s->combine_fmt != MOE_MSG_BF16 && s->combine_fmt != MOE_MSG_INT8) return MOE_ERR_INVALID_ARG;
+    Dims d = make_dims(*s);
+    if (d.nslots >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+void fill_layout(const Dims& d, moe_layout* L) {
+    L->max_tokens = d.mt;
+    L->dispatch_row_bytes = d.drow;
+    L->dispatch_meta_offset = align_up(d.nslots * d.drow, 256);
+    L->dispatch_bytes = align_up(L->dispatch_meta_offset + d.nslots * (long long)sizeof(moe_dispatch_meta), 256);
+    L->combine_row_bytes = d.crow;
+    L->combine_scale_offset = align_up((long long)d.T * d.k * d.crow, 256);
+    L->combine_bytes = align_up(L->combine_scale_offset + 4LL * d.T * d.k, 256);
+    L->workspace_bytes = make_ws(d).total;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status check_weights(const Dims& d, const moe_expert_weights* w) {
+    if (!w || !w->w_gate_up || !w->s_gate_up || !w->w_down || !w->s_down) return MOE_ERR_INVALID_ARG;
+    if (w->n_sets < 1) return MOE_ERR_INVALID_ARG;
+    if (!w->phys_to_weight && w->n_sets < d.E_phys) return MOE_ERR_INVALID_ARG;
+    if (!aligned(w->w_gate_up, 16) || !aligned(w->w_down, 16)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_WORKSPACE: return "buffer or workspace too small";
+        case MOE_ERR_CAPACITY: return "static buffer capacity exceeded";
+        case MOE_ERR_CUDA: return "CUDA launch error";
+        case MOE_ERR_TIMEOUT: return "device wait timed out";
+        case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    }
+    return "unknown status";
+}
+
+moe_status moe_static_buffer_bytes(int64_t rank_num, int64_t local_batch, int64_t topk,
+                                   int64_t experts_per_rank, int64_t msg_size, int64_t* bytes) {
+    if (!bytes || rank_num < 1 || local_batch < 1 || topk < 1 || experts_per_rank < 1 || msg_size < 1)
+        return MOE_ERR_INVALID_ARG;
+    const int64_t m = topk < experts_per_rank ? topk : experts_per_rank;
+    // rank_num * (local_batch * m) * msg_size without signed overflow
+    unsigned __int128 v = (unsigned __int128)rank_num * (unsigned __int128)local_batch;
+    v *= (unsigned __int128)m;
+    v *= (unsigned __int128)msg_size;
+    if (v > (unsigned __int128)INT64_MAX) return MOE_ERR_INVALID_ARG;
+    *bytes = (int64_t)v;
+    return MOE_OK;
+}
+
+moe_status moe_query_layout(const moe_shape* shape, moe_layout* layout) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (!layout) return MOE_ERR_INVALID_ARG;
+    fill_layout(make_dims(*shape), layout);
+    return MOE_OK;
+}
+
+moe_status moe_route(const moe_shape* shape, const float* logits, const int32_t* rep_table,
+                     const int32_t* n_copies, int32_t max_copies, int32_t* topk_idx,
+                     float* topk_w, int32_t* phys_idx, int32_t* expert_counts,
+                     moe_stream_t stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (!logits || !topk_idx || !topk_w || !phys_idx || !expert_counts) return MOE_ERR_INVALID_ARG;
+    if (rep_table) {
+        if (!n_copies || max_copies < 1) return MOE_ERR_INVALID_ARG;
+    } else if (shape->E_phys != shape->E_log) {
+        return MOE_ERR_INVALID_ARG;
+    }
+    Dims d = make_dims(*shape);
+    return cuda_status(launch_route(d, logits, rep_table, n_copies, max_copies, topk_idx, topk_w,
+                                    phys_idx, expert_counts, (cudaStream_t)stream));
+}
+
+moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, const int32_t* phys_idx,
+                        void* dispatch_buf, int64_t dispatch_bytes, int32_t* rank_counts,
+                        int32_t* expert_offsets, int32_t* expert_rows, void* workspace,
+                        int64_t workspace_bytes, moe_stream_t stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (!x || !phys_idx || !dispatch_buf || !rank_counts || !expert_offsets || !expert_rows ||
+        !workspace)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(dispatch_buf, 256) || !aligned(workspace, 256))
+        return MOE_ERR_INVALID_ARG;
+    Dims d = make_dims(*shape);
+    moe_layout L;
+    fill_layout(d, &L);
+    if (dispatch_bytes < L.dispatch_bytes || workspace_bytes < L.workspace_bytes)
+        return MOE_ERR_WORKSPACE;
+    return cuda_status(launch_dispatch(d, x, phys_idx, dispatch_buf, L.dispatch_meta_offset,
+                                       rank_counts, expert_offsets, expert_rows, workspace,
+                                       make_ws(d), (cudaStream_t)stream));
+}
+
+moe_status moe_expert_ffn(const moe_shape* shape, const void* dispatch_buf,
+                          int64_t dispatch_bytes, const int32_t* expert_offsets,
+                          const int32_t* expert_rows, const moe_expert_weights* weights,
+                          void* combine_buf, int64_t combine_bytes, void* workspace,
+                          int64_t workspace_bytes, moe_stream_t stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (shape->dispatch_fmt != MOE_MSG_INT8) return MOE_ERR_UNSUPPORTED;
+    if (!dispatch_buf || !expert_offsets || !expert_rows || !combine_buf || !workspace)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(dispatch_buf, 256) || !aligned(combine_buf, 256) || !aligned(workspace, 256))
+        return MOE_ERR_INVALID_ARG;
+    Dims d = make_dims(*shape);
+    if ((st = check_weights(d, weights)) != MOE_OK) return st;
+    moe_layout L;
+    fill_layout(d, &L);
+    if (dispatch_bytes < L.dispatch_bytes || combine_bytes < L.combine_bytes ||
+        workspace_bytes < L.workspace_bytes)
+        return MOE_ERR_WORKSPACE;
+    return cuda_status(launch_ffn(d, dispatch_buf, L.dispatch_meta_offset, expert_offsets,
+                                  expert_rows, *weights, combine_buf, L.combine_scale_offset,
+                                  workspace, make_ws(d), (cudaStream_t)stream));
+}
+
+moe_status moe_combine(const moe_shape* shape, const void* combine_buf, int64_t combine_bytes,
+                       const float* topk_w, uint16_t* out, moe_stream_t stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (!combine_buf || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned(combine_buf, 256) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+    Dims d = make_dims(*shape);
+    moe_layout L;
+    fill_layout(d, &L);
+    if (combine_bytes < L.combine_bytes) return MOE_ERR_WORKSPACE;
+    return cuda_status(launch_combine(d, combine_buf, L.combine_scale_offset, topk_w, out,
+                                      (cudaStream_t)stream));
+}
+
+moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t* x,
+                     const int32_t* rep_table, const int32_t* n_copies, int32_t max_copies,
+                     const moe_expert_weights* weights, const moe_routing* routing,
+                     void* dispatch_buf, int64_t dispatch_bytes, void* combine_buf,
+                     int64_t combine_bytes, void* workspace, int64_t workspace_bytes,
+                     uint16_t* out, moe_stream_t stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (shape->dispatch_fmt != MOE_MSG_INT8) return MOE_ERR_UNSUPPORTED;
+    if (!routing || !logits || !x || !out) return MOE_ERR_INVALID_ARG;
+    const moe_routing& r = *routing;
+    if (!r.topk_idx || !r.topk_w || !r.phys_idx || !r.expert_counts || !r.rank_counts ||
+        !r.expert_offsets || !r.expert_rows)
+        return MOE_ERR_INVALID_ARG;
+    if (!dispatch_buf || !combine_buf || !workspace) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(out, 16) || !aligned(dispatch_buf, 256) ||
+        !aligned(combine_buf, 256) || !aligned(workspace, 256))
+        return MOE_ERR_INVALID_ARG;
+    if (rep_table) {
+        if (!n_copies || max_copies < 1) return MOE_ERR_INVALID_ARG;
+    } else if (shape->E_phys != shape->E_log) {
+        return MOE_ERR_INVALID_ARG;
+    }
+    Dims d = make_dims(*shape);
+    if ((st = check_weights(d, weights)) != MOE_OK) return st;
+    moe_layout L;
+    fill_layout(d, &L);
+    if (dispatch_bytes < L.dispatch_bytes || combine_bytes < L.combine_bytes ||
+        workspace_bytes < L.workspace_bytes)
+        return MOE_ERR_WORKSPACE;
+    const WsLayout wl = make_ws(d);
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((launch_route(d, logits, rep_table, n_copies, max_copies, r.topk_idx, r.topk_w,
+                          r.phys_idx, r.expert_counts, s)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if ((launch_dispatch(d, x, r.phys_idx, dispatch_buf, L.dispatch_meta_offset,
+                             r.rank_counts, r.expert_offsets, r.expert_rows, workspace, wl, s)) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    if ((launch_ffn(d, dispatch_buf, L.dispatch_meta_offset, r.expert_offsets, r.expert_rows,
+                        *weights, combine_buf, L.combine_scale_offset, workspace, wl, s)) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    if ((launch_combine(d, combine_buf, L.combine_scale_offset, r.topk_w, out, s)) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int64_t moe_gemm_workspace_bytes(int32_t n_groups, int64_t max_rows) {
+    (void)max_rows;
+    if (n_groups < 1) return -1;
+    return align_up(4LL * (n_groups + 1), 256);
+}
+
+moe_status moe_grouped_gemm_s8(int32_t n_groups, const int32_t* offsets, int64_t max_rows,
+                               const int32_t* row_index, const int8_t* A, int64_t lda,
+                               const int8_t* B, int32_t N, int32_t K, int32_t* C,
+                               void* workspace, int64_t workspace_bytes, moe_stream_t stream) {
+    if (n_groups < 1 || !offsets || max_rows < 0 || !A || !B || !C || !workspace)
+        return MOE_ERR_INVALID_ARG;
+    if (K < 16 || K % 16 || K >= (1 << 20) || N < 16 || N % 16 || lda < K || lda % 16)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < moe_gemm_workspace_bytes(n_groups, max_rows)) return MOE_ERR_WORKSPACE;
+    if (max_rows == 0) return MOE_OK;
+    return cuda_status(launch_grouped_gemm_s8(n_groups, offsets, max_rows, row_index, A, lda, B,
+                                              (long long)N * K, nullptr, N, K, C,
+                                              static_cast<int32_t*>(workspace),
+                                              (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,291 @@
+// dispatch.cu -- FusedDispatch: token-wise INT8 quantisation fused with the
+// scatter of one message per (token, route) into static per-rank buffers.
+//
+// "CloudMatrix384 LLM Serving", section "EP320：token 去找专家" (fused_moe
+// listing: quantise the bf16 row once, then per route_slot write
+// {q_token, scale, source_rank, batch_slot, route_slot} into the owner rank's
+// static buffer and count the messages per target) and section "缓冲区公式"
+// (max_tokens = local_batch * min(topK, experts_per_die)).
+// "xDeepServe on CloudMatrix384", section "合设 MoE-Attention 的 All-to-All"
+// (P039-P040: per-source counts, prefix sums give each source's place in the
+// receiver's area; token-wise INT8 quantisation in the dispatch kernel).
+//
+// Three kernels:
+//   layout_src     one block per source rank: an ordered multi-split of the
+//                  rank's lb*k messages by destination rank and by physical
+//                  expert (warp match_any + popc, an exclusive scan across
+//                  warps) -> slot within (dst, src), rank within (src, expert),
+//                  rank_counts[dst][src], hist[src][expert].  No atomics.
+//   layout_expert  one block: per-expert prefix over sources and over experts
+//                  -> src_base, expert_offsets.
+//   scatter        one block per token: bf16 row -> shared memory, absmax,
+//                  codes into shared memory, then k bulk asynchronous copies
+//                  (shared -> global) of the code row into the k slots, plus
+//                  the 16-byte metadata and the expert row list entries.
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kLayoutWarps = 4;
+
+__global__ void __launch_bounds__(kLayoutWarps * 32)
+layout_src_kernel(int lb, int k, int epr, int R, int E_phys, int S,
+                  const int32_t* __restrict__ phys_idx, int32_t* __restrict__ slot_local,
+                  int32_t* __restrict__ erank, int32_t* __restrict__ rank_counts,
+                  int32_t* __restrict__ hist) {
+    extern __shared__ int smem[];
+    int* cntD = smem;                          // [W][R]
+    int* cntE = cntD + kLayoutWarps * R;       // [W][E_phys]
+    int* totD = cntE + kLayoutWarps * E_phys;  // [R]
+    int* totE = totD + R;                      // [E_phys]
+    const int src = blockIdx.x;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int N = lb * k;
+    const long long base = (long long)src * N;
+    for (int i = threadIdx.x; i < kLayoutWarps * (R + E_phys); i += blockDim.x) smem[i] = 0;
+    __syncthreads();
+
+    const int rounds = (N + 31) / 32;
+    const int rpw = (rounds + kLayoutWarps - 1) / kLayoutWarps;
+    const int r0 = w * rpw, r1 = min(rounds, r0 + rpw);
+    const unsigned lt = (1u << lane) - 1u;
+
+    for (int r = r0; r < r1; ++r) {
+        int i = r * 32 + lane;
+        bool valid = i < N;
+        int p = valid ? phys_idx[base + i] : -1;
+        int dst = valid ? p / epr : -1;
+        unsigned pd = __match_any_sync(0xffffffffu, dst);
+        unsigned pe = __match_any_sync(0xffffffffu, p);
+        if (valid && (pd & lt) == 0) cntD[w * R + dst] += __popc(pd);
+        if (valid && (pe & lt) == 0) cntE[w * E_phys + p] += __popc(pe);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int b = threadIdx.x; b < R; b += blockDim.x) {
+        int run = 0;
+        for (int ww = 0; ww < kLayoutWarps; ++ww) {
+            int c = cntD[ww * R + b];
+            cntD[ww * R + b] = run;
+            run += c;
+        }
+        totD[b] = run;
+    }
+    for (int b = threadIdx.x; b < E_phys; b += blockDim.x) {
+        int run = 0;
+        for (int ww = 0; ww < kLayoutWarps; ++ww) {
+            int c = cntE[ww * E_phys + b];
+            cntE[ww * E_phys + b] = run;
+            run += c;
+        }
+        totE[b] = run;
+    }
+    __syncthreads();
+    for (int r = r0; r < r1; ++r) {
+        int i = r * 32 + lane;
+        bool valid = i < N;
+        int p = valid ? phys_idx[base + i] : -1;
+        int dst = valid ? p / epr : -1;
+        unsigned pd = __match_any_sync(0xffffffffu, dst);
+        unsigned pe = __match_any_sync(0xffffffffu, p);
+        int sl = 0, er = 0;
+        if (valid) {
+            sl = cntD[w * R + dst] + __popc(pd & lt);
+            er = cntE[w * E_phys + p] + __popc(pe & lt);
+        }
+        __syncwarp();
+        if (valid && (pd & lt) == 0) cntD[w * R + dst] += __popc(pd);
+        if (valid && (pe & lt) == 0) cntE[w * E_phys + p] += __popc(pe);
+        __syncwarp();
+        if (valid) {
+            slot_local[base + i] = sl;
+            erank[base + i] = er;
+        }
+    }
+    for (int b = threadIdx.x; b < R; b += blockDim.x) rank_counts[(long long)b * S + src] = totD[b];
+    for (int b = threadIdx.x; b < E_phys; b += blockDim.x) hist[(long long)src * E_phys + b] = totE[b];
+}
+
+__global__ void __launch_bounds__(1024)
+layout_expert_kernel(int S, int E_phys, const int32_t* __restrict__ hist,
+                     int32_t* __restrict__ src_base, int32_t* __restrict__ expert_offsets) {
+    __shared__ int s_warp[32];
+    const int p = threadIdx.x;
+    int run = 0;
+    if (p < E_phys) {
+        for (int s = 0; s < S; ++s) {
+            int c = hist[(long long)s * E_phys + p];
+            src_base[(long long)s * E_phys + p] = run;
+            run += c;
+        }
+    }
+    // exclusive scan of run over p (block of 1024 threads)
+    const int lane = p & 31, w = p >> 5;
+    int v = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
+    }
+    if (lane == 31) s_warp[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        int x = s_warp[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int o = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += o;
+        }
+        s_warp[lane] = x;  // inclusive over warps
+    }
+    __syncthreads();
+    int incl = v + (w > 0 ? s_warp[w - 1] : 0);
+    if (p < E_phys) expert_offsets[p] = incl - run;
+    if (p == E_phys - 1) expert_offsets[E_phys] = incl;
+}
+
+__device__ __forceinline__ void bulk_store_s2g(void* gdst, const void* ssrc, unsigned bytes) {
+    unsigned saddr = static_cast<unsigned>(__cvta_generic_to_shared(ssrc));
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gdst),
+                 "r"(saddr), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ float bf16_lo(unsigned w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(unsigned w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ unsigned quant4(float a, float b, float c, float d, float s) {
+    int q0 = __float2int_rn(__fdiv_rn(a, s));
+    int q1 = __float2int_rn(__fdiv_rn(b, s));
+    int q2 = __float2int_rn(__fdiv_rn(c, s));
+    int q3 = __float2int_rn(__fdiv_rn(d, s));
+    q0 = max(-127, min(127, q0));
+    q1 = max(-127, min(127, q1));
+    q2 = max(-127, min(127, q2));
+    q3 = max(-127, min(127, q3));
+    return (unsigned)(q0 & 0xff) | ((unsigned)(q1 & 0xff) << 8) | ((unsigned)(q2 & 0xff) << 16) |
+           ((unsigned)(q3 & 0xff) << 24);
+}
+
+constexpr int kScatterThreads = 128;
+
+__global__ void __launch_bounds__(kScatterThreads)
+scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int8_msgs,
+               long long drow, const uint16_t* __restrict__ x,
+               const int32_t* __restrict__ phys_idx, const int32_t* __restrict__ slot_local,
+               const int32_t* __restrict__ erank, const int32_t* __restrict__ src_base,
+               const int32_t* __restrict__ expert_offsets, char* __restrict__ dbuf,
+               moe_dispatch_meta* __restrict__ meta, int32_t* __restrict__ expert_rows) {
+    extern __shared__ __align__(128) unsigned char sm[];
+    uint4* srow = reinterpret_cast<uint4*>(sm);                 // bf16 row, 2H bytes
+    uint2* scode = reinterpret_cast<uint2*>(sm + 2 * (size_t)H);  // H codes
+    __shared__ float s_red[kScatterThreads / 32];
+    __shared__ float s_scale;
+
+    const int t = blockIdx.x;
+    const int src = t / lb, bs = t - src * lb;
+    const int nch = H / 8;  // 16-byte chunks of 8 bf16
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (long long)t * H);
+    float amax = 0.f;
+    for (int c = threadIdx.x; c < nch; c += kScatterThreads) {
+        uint4 v = __ldg(xr + c);
+        srow[c] = v;
+        if (int8_msgs) {
+            amax = fmaxf(amax, fabsf(bf16_lo(v.x)));
+            amax = fmaxf(amax, fabsf(bf16_hi(v.x)));
+            amax = fmaxf(amax, fabsf(bf16_lo(v.y)));
+            amax = fmaxf(amax, fabsf(bf16_hi(v.y)));
+            amax = fmaxf(amax, fabsf(bf16_lo(v.z)));
+            amax = fmaxf(amax, fabsf(bf16_hi(v.z)));
+            amax = fmaxf(amax, fabsf(bf16_lo(v.w)));
+            amax = fmaxf(amax, fabsf(bf16_hi(v.w)));
+        }
+    }
+    const unsigned char* src_row = sm;
+    float scale = 0.f;
+    if (int8_msgs) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = amax;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float a = s_red[0];
+            for (int i = 1; i < kScatterThreads / 32; ++i) a = fmaxf(a, s_red[i]);
+            s_scale = a == 0.f ? 0.f : __fdiv_rn(a, 127.0f);
+        }
+        __syncthreads();
+        scale = s_scale;
+        for (int c = threadIdx.x; c < nch; c += kScatterThreads) {
+            uint4 v = srow[c];
+            uint2 q;
+            if (scale == 0.f) {
+                q.x = 0u; q.y = 0u;
+            } else {
+                q.x = quant4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y), scale);
+                q.y = quant4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w), scale);
+            }
+            scode[c] = q;
+        }
+        src_row = reinterpret_cast<const unsigned char*>(scode);
+    }
+    // generic-proxy shared writes -> visible to the bulk-copy (async) proxy
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    __syncthreads();
+    const long long tk = (long long)t * k;
+    if (threadIdx.x == 0) {
+        for (int j = 0; j < k; ++j) {
+            int p = phys_idx[tk + j];
+            int dst = p / epr;
+            long long g = ((long long)dst * S + src) * mt + slot_local[tk + j];
+            bulk_store_s2g(dbuf + g * drow, src_row, (unsigned)drow);
+        }
+        asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+    }
+    if (threadIdx.x >= 32 && threadIdx.x < 32 + k) {
+        int j = threadIdx.x - 32;
+        int p = phys_idx[tk + j];
+        int dst = p / epr;
+        long long g = ((long long)dst * S + src) * mt + slot_local[tk + j];
+        moe_dispatch_meta m;
+        m.scale = scale;
+        m.src_rank = src;
+        m.batch_slot = bs;
+        m.route_slot = j;
+        meta[g] = m;
+        expert_rows[expert_offsets[p] + src_base[(long long)src * E_phys + p] + erank[tk + j]] =
+            (int32_t)g;
+    }
+    if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const Dims& d, const uint16_t* x, const int32_t* phys_idx,
+                            void* dbuf, long long meta_off, int32_t* rank_counts,
+                            int32_t* expert_offsets, int32_t* expert_rows, void* ws,
+                            const WsLayout& wl, cudaStream_t st) {
+    int32_t* slot_local = ws_ptr<int32_t>(ws, wl.slot_local);
+    int32_t* erank = ws_ptr<int32_t>(ws, wl.erank);
+    int32_t* hist = ws_ptr<int32_t>(ws, wl.hist);
+    int32_t* src_base = ws_ptr<int32_t>(ws, wl.src_base);
+    size_t smem1 = sizeof(int) * (size_t)(kLayoutWarps + 1) * (d.R + d.E_phys);
+    layout_src_kernel<<<d.S, kLayoutWarps * 32, smem1, st>>>(d.lb, d.k, d.epr, d.R, d.E_phys,
+                                                             d.S, phys_idx, slot_local, erank,
+                                                             rank_counts, hist);
+    layout_expert_kernel<<<1, 1024, 0, st>>>(d.S, d.E_phys, hist, src_base, expert_offsets);
+    size_t smem3 = (size_t)d.H * 2 + (d.dfmt == MOE_MSG_INT8 ? (size_t)d.H : 0);
+    if (smem3 > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(scatter_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem3);
+        if (e != cudaSuccess) return e;
+    }
+    scatter_kernel<<<d.T, kScatterThreads, smem3, st>>>(
+        d.H, d.k, d.lb, d.epr, d.S, d.mt, d.E_phys, d.dfmt == MOE_MSG_INT8 ? 1 : 0, d.drow, x,
+        phys_idx, slot_local, erank, src_base, expert_offsets, static_cast<char*>(dbuf),
+        reinterpret_cast<moe_dispatch_meta*>(static_cast<char*>(dbuf) + meta_off), expert_rows);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,338 @@
+// ffn.cu -- grouped W8A8 SwiGLU expert FFN.
+//
+// "xDeepServe on CloudMatrix384", section "DeepSeek INT8 量化": P085 (token-wise
+// activation scales, channel-wise weight scales, y_ij ~ s_i s^w_j
+// sum_k q(x_ik) q(w_jk) on the INT8 matmul unit), P088 (up_proj and gate_proj
+// fused into one kernel), P089 (expert inputs and outputs are INT8 in
+// communication).  "CloudMatrix384 LLM Serving", section "EP320：token 去找专家"
+// (assemble_expert_inputs / run_local_experts / remote_write_combine by
+// (source_rank, batch_slot, route_slot)).
+//
+// Steps (one stream):
+//   tiles      per-expert M-tile prefix sums (one block)
+//   gemm       C[r][n] = sum_k A[row(r)][k] * B[set(p)][n][k]   exact int32
+//              (gate/up: A = dispatch codes gathered by expert_rows, N = 2I)
+//   swiglu     g, u -> h = SiLU(g) u -> token-wise INT8 requantisation
+//   gemm       down projection, A = requantised rows, N = H
+//   ret        y = (acc * s_h) * sd -> return message into the combine
+//              buffer at (t, j) (INT8 codes + scale, or bf16)
+#include <cuda_bf16.h>
+
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+// ------------------------------------------------------------ exp spec
+// Binary32, one rounding per operation (explicit _rn intrinsics, never
+// contracted):  x > 88 -> +inf;  x < -87 -> 0;  otherwise
+//   n = rint(x * RCP_LN2);  r = (x - n*LN2_HI) - n*LN2_LO
+//   p = Horner(r; 1/7!, 1/6!, ..., 1/1!, 1/0!)   (Taylor series of e^r)
+//   e = p * 2^n
+// Cody-Waite argument reduction with a 14-bit LN2_HI (n*LN2_HI exact for
+// |n| <= 127).  Constants are the binary32 values nearest to ln 2 pieces and
+// to 1/m!.
+__device__ __forceinline__ float exp_spec(float x) {
+    const float RCP_LN2 = 0x1.715476p+0f;
+    const float LN2_HI = 0x1.62e4p-1f;
+    const float LN2_LO = 0x1.7f7d1cp-20f;
+    if (x > 88.0f) return __int_as_float(0x7f800000);
+    if (x < -87.0f) return 0.0f;
+    float n = rintf(__fmul_rn(x, RCP_LN2));
+    float r = __fsub_rn(x, __fmul_rn(n, LN2_HI));
+    r = __fsub_rn(r, __fmul_rn(n, LN2_LO));
+    float p = 0x1.a01a02p-13f;                    // 1/5040
+    p = __fadd_rn(0x1.6c16c2p-10f, __fmul_rn(r, p));  // 1/720
+    p = __fadd_rn(0x1.111112p-7f, __fmul_rn(r, p));   // 1/120
+    p = __fadd_rn(0x1.555556p-5f, __fmul_rn(r, p));   // 1/24
+    p = __fadd_rn(0x1.555556p-3f, __fmul_rn(r, p));   // 1/6
+    p = __fadd_rn(0.5f, __fmul_rn(r, p));
+    p = __fadd_rn(1.0f, __fmul_rn(r, p));
+    p = __fadd_rn(1.0f, __fmul_rn(r, p));
+    int ni = (int)n;
+    return __fmul_rn(p, __int_as_float((ni + 127) << 23));
+}
+
+// SwiGLU gate: SiLU(g) = g / (1 + e(-g))
+__device__ __forceinline__ float silu_spec(float g) {
+    return __fdiv_rn(g, __fadd_rn(1.0f, exp_spec(-g)));
+}
+
+// --------------------------------------------------------- tile prefix
+// tile_prefix[g] = sum_{g' < g} ceil(M_g' / BM), g = 0..G (one block).
+__global__ void __launch_bounds__(1024)
+tile_prefix_kernel(int G, int BM, const int32_t* __restrict__ offsets,
+                   int32_t* __restrict__ tile_prefix) {
+    __shared__ int s_warp[32];
+    __shared__ int s_carry;
+    if (threadIdx.x == 0) s_carry = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    for (int b0 = 0; b0 < G; b0 += 1024) {
+        int g = b0 + threadIdx.x;
+        int n = 0;
+        if (g < G) {
+            int m = offsets[g + 1] - offsets[g];
+            n = (m + BM - 1) / BM;
+        }
+        int v = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int o = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += o;
+        }
+        if (lane == 31) s_warp[w] = v;
+        __syncthreads();
+        if (w == 0) {
+            int x = s_warp[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                int o = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += o;
+            }
+            s_warp[lane] = x;
+        }
+        __syncthreads();
+        int incl = v + (w > 0 ? s_warp[w - 1] : 0) + s_carry;
+        if (g < G) tile_prefix[g] = incl - n;
+        __syncthreads();
+        if (threadIdx.x == 1023) s_carry = incl;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) tile_prefix[G] = s_carry;
+}
+
+__device__ __forceinline__ int find_group(const int32_t* __restrict__ prefix, int G, int v) {
+    // largest g in [0, G) with prefix[g] <= v
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= v) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ------------------------------------------------------- SIMT int8 GEMM
+// 64x64 output tile per 256-thread block, K in 64-byte steps, dp4a
+// (4 int8 products summed into int32, exact).
+constexpr int kBM = 64, kBN = 64, kBKW = 16;  // BK = 64 bytes = 16 words
+
+__global__ void __launch_bounds__(256)
+gemm_s8_simt_kernel(int G, const int32_t* __restrict__ offsets,
+                    const int32_t* __restrict__ tile_prefix, const int32_t* __restrict__ row_index,
+                    const int8_t* __restrict__ A, long long lda, const int8_t* __restrict__ B,
+                    long long bstride, const int32_t* __restrict__ g2s, int N, int K,
+                    int32_t* __restrict__ C) {
+    __shared__ int As[kBM][kBKW + 1];
+    __shared__ int Bs[kBN][kBKW + 1];
+    const int tile = blockIdx.x;
+    if (tile >= tile_prefix[G]) return;
+    const int g = find_group(tile_prefix, G, tile);
+    const int m0 = offsets[g] + (tile - tile_prefix[g]) * kBM;
+    const int mend = offsets[g + 1];
+    const int n0 = blockIdx.y * kBN;
+    const int set = g2s ? g2s[g] : g;
+    const int8_t* Bg = B + (long long)set * bstride;
+
+    const int tid = threadIdx.x;
+    const int lr = tid >> 2, lq = tid & 3;  // load row, 16-byte quarter
+    const bool a_ok = m0 + lr < mend;
+    long long arow = 0;
+    if (a_ok) arow = row_index ? row_index[m0 + lr] : (m0 + lr);
+    const int8_t* ap = A + arow * lda + lq * 16;
+    const bool b_ok = n0 + lr < N;
+    const int8_t* bp = Bg + (long long)(n0 + lr) * K + lq * 16;
+
+    const int ty = tid >> 4, tx = tid & 15;
+    int acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0;
+
+    for (int k0 = 0; k0 < K; k0 += 64) {
+        const bool kin = k0 + lq * 16 < K;
+        int4 va = make_int4(0, 0, 0, 0), vb = make_int4(0, 0, 0, 0);
+        if (a_ok && kin) va = __ldg(reinterpret_cast<const int4*>(ap + k0));
+        if (b_ok && kin) vb = __ldg(reinterpret_cast<const int4*>(bp + k0));
+        As[lr][lq * 4 + 0] = va.x; As[lr][lq * 4 + 1] = va.y;
+        As[lr][lq * 4 + 2] = va.z; As[lr][lq * 4 + 3] = va.w;
+        Bs[lr][lq * 4 + 0] = vb.x; Bs[lr][lq * 4 + 1] = vb.y;
+        Bs[lr][lq * 4 + 2] = vb.z; Bs[lr][lq * 4 + 3] = vb.w;
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < kBKW; ++kk) {
+            int a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = As[ty * 4 + i][kk];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Bs[tx * 4 + j][kk];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = __dp4a(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int m = m0 + ty * 4 + i;
+        if (m >= mend) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            int n = n0 + tx * 4 + j;
+            if (n < N) C[(long long)m * N + n] = acc[i][j];
+        }
+    }
+}
+
+// ----------------------------------------------------- block reductions
+template <int NT>
+__device__ __forceinline__ float block_max(float v, float* s_red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = s_red[0];
+#pragma unroll
+    for (int i = 1; i < NT / 32; ++i) r = fmaxf(r, s_red[i]);
+    __syncthreads();
+    return r;
+}
+
+__device__ __forceinline__ int quant1(float v, float s) {
+    int q = __float2int_rn(__fdiv_rn(v, s));
+    return max(-127, min(127, q));
+}
+
+constexpr int kRowThreads = 256;
+
+// SwiGLU + token-wise requantisation of one routed row.
+__global__ void __launch_bounds__(kRowThreads)
+swiglu_requant_kernel(int I, int E_phys, const int32_t* __restrict__ expert_offsets,
+                      const int32_t* __restrict__ expert_rows,
+                      const moe_dispatch_meta* __restrict__ meta,
+                      const int32_t* __restrict__ p2w, const float* __restrict__ s_gu,
+                      const int32_t* __restrict__ acc_gu, int8_t* __restrict__ hq,
+                      float* __restrict__ sh) {
+    extern __shared__ float s_h[];
+    __shared__ float s_red[kRowThreads / 32];
+    const int r = blockIdx.x;
+    const int p = find_group(expert_offsets, E_phys, r);
+    const int set = p2w ? p2w[p] : p;
+    const float s = meta[expert_rows[r]].scale;
+    const int32_t* acc = acc_gu + (long long)r * 2 * I;
+    const float* sg = s_gu + (long long)set * 2 * I;
+    float amax = 0.f;
+    for (int i = threadIdx.x; i < I; i += kRowThreads) {
+        float gv = __fmul_rn(__fmul_rn(__int2float_rn(acc[i]), s), sg[i]);
+        float uv = __fmul_rn(__fmul_rn(__int2float_rn(acc[I + i]), s), sg[I + i]);
+        float h = __fmul_rn(silu_spec(gv), uv);
+        s_h[i] = h;
+        amax = fmaxf(amax, fabsf(h));
+    }
+    amax = block_max<kRowThreads>(amax, s_red);
+    const float sc = amax == 0.f ? 0.f : __fdiv_rn(amax, 127.0f);
+    int8_t* out = hq + (long long)r * I;
+    for (int i = threadIdx.x; i < I; i += kRowThreads)
+        out[i] = (int8_t)(sc == 0.f ? 0 : quant1(s_h[i], sc));
+    if (threadIdx.x == 0) sh[r] = sc;
+}
+
+// Down-projection epilogue: y, then the return message into the combine row.
+__global__ void __launch_bounds__(kRowThreads)
+return_kernel(int H, int k, int lb, int E_phys, int int8_msgs, long long crow,
+              const int32_t* __restrict__ expert_offsets, const int32_t* __restrict__ expert_rows,
+              const moe_dispatch_meta* __restrict__ meta, const int32_t* __restrict__ p2w,
+              const float* __restrict__ s_d, const int32_t* __restrict__ acc_d,
+              const float* __restrict__ sh, unsigned char* __restrict__ cbuf,
+              float* __restrict__ cscale) {
+    extern __shared__ float s_y[];
+    __shared__ float s_red[kRowThreads / 32];
+    const int r = blockIdx.x;
+    const int p = find_group(expert_offsets, E_phys, r);
+    const int set = p2w ? p2w[p] : p;
+    const moe_dispatch_meta m = meta[expert_rows[r]];
+    const long long tj = ((long long)m.src_rank * lb + m.batch_slot) * k + m.route_slot;
+    const int32_t* acc = acc_d + (long long)r * H;
+    const float* sd = s_d + (long long)set * H;
+    const float shr = sh[r];
+    unsigned char* row = cbuf + tj * crow;
+    float amax = 0.f;
+    for (int c = threadIdx.x; c < H; c += kRowThreads) {
+        float y = __fmul_rn(__fmul_rn(__int2float_rn(acc[c]), shr), sd[c]);
+        if (int8_msgs) {
+            s_y[c] = y;
+            amax = fmaxf(amax, fabsf(y));
+        } else {
+            reinterpret_cast<__nv_bfloat16*>(row)[c] = __float2bfloat16_rn(y);
+        }
+    }
+    if (!int8_msgs) return;
+    amax = block_max<kRowThreads>(amax, s_red);
+    const float sc = amax == 0.f ? 0.f : __fdiv_rn(amax, 127.0f);
+    for (int c = threadIdx.x; c < H; c += kRowThreads)
+        reinterpret_cast<int8_t*>(row)[c] = (int8_t)(sc == 0.f ? 0 : quant1(s_y[c], sc));
+    if (threadIdx.x == 0) cscale[tj] = sc;
+}
+
+cudaError_t set_smem(const void* fn, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_s8(int n_groups, const int32_t* offsets, long long max_rows,
+                                   const int32_t* row_index, const int8_t* A, long long lda,
+                                   const int8_t* B, long long b_group_stride,
+                                   const int32_t* group_to_set, int N, int K, int32_t* C,
+                                   int32_t* tile_prefix, cudaStream_t st) {
+    tile_prefix_kernel<<<1, 1024, 0, st>>>(n_groups, kBM, offsets, tile_prefix);
+    long long max_tiles = (max_rows + kBM - 1) / kBM + n_groups;
+    if (max_tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+    dim3 grid((unsigned)max_tiles, (unsigned)((N + kBN - 1) / kBN));
+    gemm_s8_simt_kernel<<<grid, 256, 0, st>>>(n_groups, offsets, tile_prefix, row_index, A, lda,
+                                              B, b_group_stride, group_to_set, N, K, C);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ffn(const Dims& d, const void* dbuf, long long meta_off,
+                       const int32_t* expert_offsets, const int32_t* expert_rows,
+                       const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
+                       const WsLayout& wl, cudaStream_t st) {
+    const long long M = (long long)d.T * d.k;
+    const moe_dispatch_meta* meta =
+        reinterpret_cast<const moe_dispatch_meta*>(static_cast<const char*>(dbuf) + meta_off);
+    int32_t* tiles = ws_ptr<int32_t>(ws, wl.tiles);
+    int32_t* acc_gu = ws_ptr<int32_t>(ws, wl.acc_gu);
+    int8_t* hq = ws_ptr<int8_t>(ws, wl.hq);
+    float* sh = ws_ptr<float>(ws, wl.sh);
+    int32_t* acc_d = ws_ptr<int32_t>(ws, wl.acc_d);
+    unsigned char* cb = static_cast<unsigned char*>(cbuf);
+    cudaError_t e;
+
+    e = launch_grouped_gemm_s8(d.E_phys, expert_offsets, M, expert_rows,
+                               static_cast<const int8_t*>(dbuf), d.drow, w.w_gate_up,
+                               2LL * d.I * d.H, w.phys_to_weight, 2 * d.I, d.H, acc_gu, tiles, st);
+    if (e != cudaSuccess) return e;
+    size_t sm1 = sizeof(float) * (size_t)d.I;
+    if ((e = set_smem((const void*)swiglu_requant_kernel, sm1)) != cudaSuccess) return e;
+    swiglu_requant_kernel<<<(unsigned)M, kRowThreads, sm1, st>>>(
+        d.I, d.E_phys, expert_offsets, expert_rows, meta, w.phys_to_weight, w.s_gate_up, acc_gu,
+        hq, sh);
+    e = launch_grouped_gemm_s8(d.E_phys, expert_offsets, M, nullptr, hq, d.I, w.w_down,
+                               (long long)d.H * d.I, w.phys_to_weight, d.H, d.I, acc_d, tiles, st);
+    if (e != cudaSuccess) return e;
+    const int int8_msgs = d.cfmt == MOE_MSG_INT8 ? 1 : 0;
+    size_t sm2 = int8_msgs ? sizeof(float) * (size_t)d.H : 0;
+    if ((e = set_smem((const void*)return_kernel, sm2)) != cudaSuccess) return e;
+    return_kernel<<<(unsigned)M, kRowThreads, sm2, st>>>(
+        d.H, d.k, d.lb, d.E_phys, int8_msgs, d.crow, expert_offsets, expert_rows, meta,
+        w.phys_to_weight, w.s_down, acc_d, sh, cb,
+        reinterpret_cast<float*>(cb + scale_off));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,97 @@
+// internal.cuh -- shared definitions of the CUDA library (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Derived sizes of one layer shape.
+struct Dims {
+    int T, H, E_log, E_phys, k, I, R, S;
+    int lb, epr, mt;
+    int dfmt, cfmt;
+    long long drow;  // dispatch row bytes
+    long long crow;  // combine row bytes
+    long long nslots;
+};
+
+inline Dims make_dims(const moe_shape& s) {
+    Dims d;
+    d.T = s.T; d.H = s.H; d.E_log = s.E_log; d.E_phys = s.E_phys; d.k = s.k; d.I = s.I;
+    d.R = s.n_ranks; d.S = s.n_src_ranks;
+    d.lb = d.T / d.S;
+    d.epr = d.E_phys / d.R;
+    d.mt = d.lb * (d.k < d.epr ? d.k : d.epr);
+    d.dfmt = s.dispatch_fmt; d.cfmt = s.combine_fmt;
+    d.drow = (long long)d.H * (d.dfmt == MOE_MSG_INT8 ? 1 : 2);
+    d.crow = (long long)d.H * (d.cfmt == MOE_MSG_INT8 ? 1 : 2);
+    d.nslots = (long long)d.R * d.S * d.mt;
+    return d;
+}
+
+inline long long align_up(long long v, long long a) { return (v + a - 1) / a * a; }
+
+// Grouped GEMM tile sizes (used to size the tile table).
+constexpr int kGemmBM = 128;
+
+// Workspace carve-up.  Every region is 256-byte aligned.
+struct WsLayout {
+    long long slot_local;  // int32 [T*k]   slot of (t, j) within its (dst, src) pair
+    long long erank;       // int32 [T*k]   rank of token t among its source's tokens for expert p
+    long long hist;        // int32 [S][E_phys]
+    long long src_base;    // int32 [S][E_phys]
+    long long tiles;       // int32 [E_phys + 1]  grouped-GEMM tile prefix
+    long long gemm_tiles;  // int32 [gemm groups + 1] for moe_grouped_gemm_s8 (same region)
+    long long acc_gu;      // int32 [T*k][2I]
+    long long hq;          // int8  [T*k][I]
+    long long sh;          // f32   [T*k]
+    long long acc_d;       // int32 [T*k][H]
+    long long total;
+};
+
+inline WsLayout make_ws(const Dims& d) {
+    WsLayout w;
+    long long o = 0;
+    const long long tk = (long long)d.T * d.k;
+    w.slot_local = o; o = align_up(o + 4 * tk, 256);
+    w.erank = o;      o = align_up(o + 4 * tk, 256);
+    w.hist = o;       o = align_up(o + 4LL * d.S * d.E_phys, 256);
+    w.src_base = o;   o = align_up(o + 4LL * d.S * d.E_phys, 256);
+    w.tiles = o;      o = align_up(o + 4LL * (d.E_phys + 1), 256);
+    w.gemm_tiles = w.tiles;
+    w.acc_gu = o;     o = align_up(o + 4 * tk * 2 * d.I, 256);
+    w.hq = o;         o = align_up(o + tk * d.I, 256);
+    w.sh = o;         o = align_up(o + 4 * tk, 256);
+    w.acc_d = o;      o = align_up(o + 4 * tk * d.H, 256);
+    w.total = o;
+    return w;
+}
+
+template <typename T>
+inline T* ws_ptr(void* ws, long long off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+// Kernel launchers (each returns cudaGetLastError() after its launches).
+cudaError_t launch_route(const Dims& d, const float* logits, const int32_t* rep_table,
+                         const int32_t* n_copies, int max_copies, int32_t* topk_idx,
+                         float* topk_w, int32_t* phys_idx, int32_t* expert_counts,
+                         cudaStream_t st);
+cudaError_t launch_dispatch(const Dims& d, const uint16_t* x, const int32_t* phys_idx,
+                            void* dbuf, long long meta_off, int32_t* rank_counts,
+                            int32_t* expert_offsets, int32_t* expert_rows, void* ws,
+                            const WsLayout& wl, cudaStream_t st);
+cudaError_t launch_combine(const Dims& d, const void* cbuf, long long scale_off,
+                           const float* topk_w, uint16_t* out, cudaStream_t st);
+cudaError_t launch_grouped_gemm_s8(int n_groups, const int32_t* offsets, long long max_rows,
+                                   const int32_t* row_index, const int8_t* A, long long lda,
+                                   const int8_t* B, long long b_group_stride,
+                                   const int32_t* group_to_set, int N, int K, int32_t* C,
+                                   int32_t* tile_prefix, cudaStream_t st);
+cudaError_t launch_ffn(const Dims& d, const void* dbuf, long long meta_off,
+                       const int32_t* expert_offsets, const int32_t* expert_rows,
+                       const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
+                       const WsLayout& wl, cudaStream_t st);
+
+}  // namespace moe

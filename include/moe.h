@@ -1,0 +1,278 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) decode-time MoE layer library.
+ *
+ * The library computes one DeepSeek-V3/R1-shaped MoE layer on one GPU:
+ *   moe_route       gate top-k + renormalised softmax weights + EPLB
+ *                   logical->physical map + per-expert counts
+ *   moe_dispatch    FusedDispatch: token-wise INT8 quantisation fused with the
+ *                   scatter of one message per (token, route) into static
+ *                   per-rank buffers, plus the per-expert row lists
+ *   moe_expert_ffn  grouped W8A8 SwiGLU expert FFN reading the dispatch
+ *                   buffer and writing one return message per (token, route)
+ *   moe_combine     FusedCombine: dequantise and gate-weighted sum
+ *   moe_layer       the four steps above, in order, on one stream
+ * "Ranks" are partitions of this GPU's memory: source rank s owns tokens
+ * [s*lb, (s+1)*lb), destination rank d owns physical experts
+ * [d*epr, (d+1)*epr).  There are no collectives.
+ *
+ * Sources (page title, section):
+ *   [X] "xDeepServe on CloudMatrix384": "合设 MoE-Attention 的 All-to-All"
+ *       (P038-P041, DISPATCH/COMBINE procedures), "专家负载均衡" (P068-P079),
+ *       "DeepSeek INT8 量化" (P085 equation, P088, P089).
+ *   [C] "CloudMatrix384 LLM Serving": "EP320：token 去找专家" (fused_moe
+ *       listing), "缓冲区公式" (max_tokens and buffer_size equations).
+ *
+ * Conventions for every entry point:
+ *   - The caller owns all memory.  Pointers marked (device) are CUDA device
+ *     pointers on the current device; (host) are host pointers.  The library
+ *     never allocates and never synchronises the stream; work is enqueued on
+ *     `stream` (a cudaStream_t; NULL is the legacy default stream) and the
+ *     call returns before it runs.
+ *   - Arguments are validated on the host before anything is enqueued;
+ *     a failure returns MOE_ERR_INVALID_ARG (bad shape, null pointer,
+ *     misaligned buffer) or MOE_ERR_WORKSPACE (a buffer smaller than
+ *     moe_query_layout reports) and enqueues nothing.
+ *   - MOE_ERR_CUDA means a launch failed; the stream may hold part of the
+ *     work.  MOE_ERR_CAPACITY is reserved: the static buffers are sized for
+ *     the worst case, so no valid input can overflow them.
+ *   - Device buffers passed as `void*` must be 256-byte aligned.
+ *   - All integer outputs (indices, counts, offsets, slots, INT8 codes, int32
+ *     accumulators) are deterministic and bit-exact with respect to the
+ *     written definitions below; float outputs follow the stated operation
+ *     order.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,
+    MOE_ERR_WORKSPACE = 2,
+    MOE_ERR_CAPACITY = 3,
+    MOE_ERR_CUDA = 4,
+    MOE_ERR_TIMEOUT = 5,
+    MOE_ERR_UNSUPPORTED = 6
+} moe_status;
+
+/* Message formats ([X] P041/P089: INT8 halves message bytes; bf16 is the
+ * unquantised form). */
+typedef enum { MOE_MSG_BF16 = 0, MOE_MSG_INT8 = 1 } moe_msg_format;
+
+/* Layer shape.  Limits checked by every entry point:
+ *   1 <= T, 16 <= H <= 16384 and H % 16 == 0, 16 <= I <= 16384 and
+ *   I % 16 == 0, 1 <= k <= min(E_log, 32), E_log <= E_phys <= 1024,
+ *   E_phys % n_ranks == 0, T % n_src_ranks == 0, T * k < 2^31. */
+typedef struct {
+    int32_t T;            /* tokens in the batch */
+    int32_t H;            /* hidden size */
+    int32_t E_log;        /* logical (routed) experts */
+    int32_t E_phys;       /* physical expert slots = E_log + redundant slots */
+    int32_t k;            /* experts per token (top-k) */
+    int32_t I;            /* SwiGLU intermediate size per expert */
+    int32_t n_ranks;      /* R: destination ranks, epr = E_phys / R experts each */
+    int32_t n_src_ranks;  /* S: source ranks, lb = T / S tokens each */
+    int32_t dispatch_fmt; /* moe_msg_format of dispatch messages */
+    int32_t combine_fmt;  /* moe_msg_format of return (combine) messages */
+} moe_shape;
+
+/* Metadata that travels with every dispatch message ([C] fused_moe listing:
+ * scale, source_rank, batch_slot, route_slot).  16 bytes. */
+typedef struct {
+    float scale;        /* token scale (INT8 messages), 0 for bf16 messages */
+    int32_t src_rank;   /* source rank s */
+    int32_t batch_slot; /* token index within the source rank, t - s*lb */
+    int32_t route_slot; /* j: position of the expert in the token's top-k */
+} moe_dispatch_meta;
+
+/* Sizes and offsets of the caller-owned buffers for one shape.
+ *
+ * Dispatch buffer ([C] "缓冲区公式"): for each destination rank d, a static
+ * area of n_src_ranks * max_tokens messages, max_tokens = lb * min(k, epr):
+ *   rows: [R][S][max_tokens][dispatch_row_bytes] at offset 0, where a row is
+ *         H INT8 codes or H bf16 values;
+ *   meta: [R][S][max_tokens] moe_dispatch_meta at dispatch_meta_offset.
+ *   Message (t, j) to rank d from source s sits in slot
+ *   g = (d*S + s)*max_tokens + n, n counting that pair's messages in
+ *   ascending (batch_slot, route_slot) order.
+ * Combine buffer ([C]: results are written back to (source_rank, batch_slot,
+ * route_slot)): rows [T][k][combine_row_bytes] at offset 0 (H INT8 codes or
+ * H bf16 values), and for INT8 one float scale per row, [T][k] at
+ * combine_scale_offset.
+ * Workspace: scratch for the library's kernels, workspace_bytes covers every
+ * entry point for this shape (moe_layer included). */
+typedef struct {
+    int64_t max_tokens;           /* lb * min(k, epr) */
+    int64_t dispatch_row_bytes;   /* H or 2H */
+    int64_t dispatch_meta_offset; /* bytes */
+    int64_t dispatch_bytes;       /* total dispatch buffer bytes */
+    int64_t combine_row_bytes;    /* H or 2H */
+    int64_t combine_scale_offset; /* bytes; equals combine rows bytes */
+    int64_t combine_bytes;        /* total combine buffer bytes */
+    int64_t workspace_bytes;      /* scratch bytes */
+} moe_layout;
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status s);
+
+/* The page's static-buffer formula ([C] "缓冲区公式"):
+ *   *bytes = rank_num * (local_batch * min(topk, experts_per_rank)) * msg_size.
+ * Host only.  INVALID_ARG if any input is < 1 or the product overflows. */
+moe_status moe_static_buffer_bytes(int64_t rank_num, int64_t local_batch, int64_t topk,
+                                   int64_t experts_per_rank, int64_t msg_size,
+                                   int64_t* bytes);
+
+/* Buffer layout for `shape` (host only). */
+moe_status moe_query_layout(const moe_shape* shape, moe_layout* layout);
+
+/* EPLB replica planner ([X] "专家负载均衡", P069-P076), host only.
+ * token_count (host) [n_slices][E_log]: tokens routed to each logical expert
+ * in each time slice.  Selects E_phys - E_log redundant copies greedily (each
+ * round, among the experts that are the hottest of some slice, add a copy to
+ * the one whose even split gives the smallest sum over slices of the hottest
+ * load; ties to the lower id), then places them heaviest first on the rank
+ * with the least load that has a free redundant slot and does not yet host
+ * that expert (if none, any rank with a free slot; ties to the lower rank).
+ * A rank's load starts as the sum of load/copies of its primary experts.
+ * Rank r owns physical slots r*epr .. r*epr+epr-1; the first E_log/R hold
+ * logical experts r*(E_log/R)+m, the rest are the redundant slots.
+ * Outputs (host): rep_table [E_log][max_copies] (physical ids of each
+ * logical expert in ascending order, padded with -1), n_copies [E_log],
+ * phys_to_logical [E_phys].  INVALID_ARG if E_log or E_phys is not a
+ * multiple of n_ranks, E_phys < E_log, or max_copies is too small. */
+moe_status moe_eplb_plan(int32_t n_slices, int32_t E_log, int32_t E_phys, int32_t n_ranks,
+                         const double* token_count, int32_t max_copies,
+                         int32_t* rep_table, int32_t* n_copies, int32_t* phys_to_logical);
+
+/* Gate top-k ([X] P038) with renormalised softmax weights and the EPLB map
+ * ([X] P078-P079), plus per-physical-expert counts (the Collect kernel of
+ * [X] P068).
+ *   logits (device) f32 [T][E_log], finite.
+ *   Selection: logit descending, ties to the lower expert id; topk_idx[t][j]
+ *   (device, int32 [T][k]) is the j-th selected logical expert (route_slot j).
+ *   topk_w[t][j] (device, f32 [T][k]) = e^(l_j - l_0) / sum_i e^(l_i - l_0)
+ *   in binary32.
+ *   rep_table (device, nullable) int32 [E_log][max_copies], n_copies (device)
+ *   int32 [E_log]: phys_idx[t][j] = rep_table[e][t mod n_copies[e]] for
+ *   e = topk_idx[t][j]; with rep_table NULL, phys_idx = topk_idx and
+ *   E_phys must equal E_log.
+ *   expert_counts (device) int32 [E_phys]: messages per physical expert.
+ * No workspace is used. */
+moe_status moe_route(const moe_shape* shape, const float* logits, const int32_t* rep_table,
+                     const int32_t* n_copies, int32_t max_copies, int32_t* topk_idx,
+                     float* topk_w, int32_t* phys_idx, int32_t* expert_counts,
+                     moe_stream_t stream);
+
+/* FusedDispatch ([C] fused_moe listing; [X] DISPATCH procedure, P039-P040).
+ *   x (device) bf16 [T][H] (raw 16-bit patterns); phys_idx (device) int32
+ *   [T][k] from moe_route.
+ *   INT8 messages: per token, scale = absmax/127 (binary32 division), code =
+ *   round-half-even(x / scale) clamped to [-127, 127]; a zero row has scale
+ *   0 and codes 0.  BF16 messages carry the row unchanged.
+ *   Writes each message (t, j) to its slot of dispatch_buf (layout above)
+ *   with its moe_dispatch_meta.
+ *   rank_counts (device) int32 [R][S]: messages from source s to rank d.
+ *   expert_offsets (device) int32 [E_phys+1]: exclusive prefix of messages
+ *   per physical expert; expert_rows (device) int32 [T*k]: for each expert,
+ *   the slot ids g of its messages in ascending token order (the expert's
+ *   gathered input rows, [C] assemble_expert_inputs).
+ *   Slots not written keep their previous contents.  Uses the workspace. */
+moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, const int32_t* phys_idx,
+                        void* dispatch_buf, int64_t dispatch_bytes, int32_t* rank_counts,
+                        int32_t* expert_offsets, int32_t* expert_rows, void* workspace,
+                        int64_t workspace_bytes, moe_stream_t stream);
+
+/* Expert weights: W8A8 with one binary32 scale per output channel ([X] P085).
+ *   w_gate_up (device) int8 [E_w][2I][H]: rows 0..I-1 are gate_proj, I..2I-1
+ *   up_proj (fused, [X] P088); s_gate_up (device) f32 [E_w][2I];
+ *   w_down (device) int8 [E_w][H][I]; s_down (device) f32 [E_w][H].
+ *   phys_to_weight (device, nullable) int32 [E_phys]: weight set of each
+ *   physical expert (replicas alias their logical expert); NULL means
+ *   physical expert p uses set p (E_w >= E_phys). */
+typedef struct {
+    const int8_t* w_gate_up;
+    const float* s_gate_up;
+    const int8_t* w_down;
+    const float* s_down;
+    int32_t n_sets; /* E_w */
+    const int32_t* phys_to_weight;
+} moe_expert_weights;
+
+/* Grouped W8A8 SwiGLU expert FFN ([X] P085 equation, P088, P089; [C]
+ * run_local_experts and remote_write_combine).  Requires INT8 dispatch
+ * messages.  For every routed row (dispatch slot g of physical expert p,
+ * codes q, scale s):
+ *   acc_g[i] = sum_h q[h] Wg[i][h], acc_u[i] = sum_h q[h] Wu[i][h]  (exact int32)
+ *   g = (acc_g * s) * sg[i], u = (acc_u * s) * su[i]   (binary32, two roundings)
+ *   h = g / (1 + e(-g)) * u, e the binary32 exp specification (Cody-Waite
+ *       reduction, degree-7 Taylor polynomial, see the design notes)
+ *   hq, s_h = token-wise INT8 quantisation of h (as in moe_dispatch)
+ *   acc_d[c] = sum_i hq[i] Wd[c][i] (exact int32), y = (acc_d * s_h) * sd[c]
+ *   return message at combine row (t, j), t = src_rank*lb + batch_slot,
+ *   j = route_slot: INT8 codes of y + scale (combine_fmt INT8) or bf16(y).
+ * Uses the workspace. */
+moe_status moe_expert_ffn(const moe_shape* shape, const void* dispatch_buf,
+                          int64_t dispatch_bytes, const int32_t* expert_offsets,
+                          const int32_t* expert_rows, const moe_expert_weights* weights,
+                          void* combine_buf, int64_t combine_bytes, void* workspace,
+                          int64_t workspace_bytes, moe_stream_t stream);
+
+/* FusedCombine ([C] fused_moe listing; [X] COMBINE procedure):
+ *   out[t][h] = bf16_rne( sum_{j=0..k-1} topk_w[t][j] * v[t][j][h] )
+ * with v = code * scale (INT8, one binary32 product) or the bf16 value, the
+ * sum taken in binary32 in ascending j (product and sum rounded separately).
+ *   topk_w (device) f32 [T][k]; out (device) bf16 [T][H].  No workspace. */
+moe_status moe_combine(const moe_shape* shape, const void* combine_buf, int64_t combine_bytes,
+                       const float* topk_w, uint16_t* out, moe_stream_t stream);
+
+/* Routing arrays produced inside moe_layer (all device, caller-owned). */
+typedef struct {
+    int32_t* topk_idx;       /* [T][k] */
+    float* topk_w;           /* [T][k] */
+    int32_t* phys_idx;       /* [T][k] */
+    int32_t* expert_counts;  /* [E_phys] */
+    int32_t* rank_counts;    /* [R][S] */
+    int32_t* expert_offsets; /* [E_phys+1] */
+    int32_t* expert_rows;    /* [T*k] */
+} moe_routing;
+
+/* The whole layer: moe_route -> moe_dispatch -> moe_expert_ffn ->
+ * moe_combine on one stream, with the same definitions.  rep_table /
+ * n_copies may be NULL (no replicas). */
+moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t* x,
+                     const int32_t* rep_table, const int32_t* n_copies, int32_t max_copies,
+                     const moe_expert_weights* weights, const moe_routing* routing,
+                     void* dispatch_buf, int64_t dispatch_bytes, void* combine_buf,
+                     int64_t combine_bytes, void* workspace, int64_t workspace_bytes,
+                     uint16_t* out, moe_stream_t stream);
+
+/* Exact grouped INT8 GEMM with int32 output -- the contraction inside
+ * moe_expert_ffn ([X] P085: sum_k q(x_ik) q(w_jk)), exposed on its own.
+ *   For group gi in [0, n_groups) and rows r in [offsets[gi], offsets[gi+1]):
+ *     C[r][n] = sum_{kk<K} A[arow(r)][kk] * B[gi][n][kk]     (exact int32)
+ *   arow(r) = row_index[r] if row_index != NULL, else r.
+ *   offsets (device) int32 [n_groups+1], nondecreasing, offsets[0] = 0,
+ *   offsets[n_groups] = M_total <= max_rows; A (device) int8 rows of lda
+ *   bytes; B (device) int8 [n_groups][N][K]; C (device) int32 [M_total][N].
+ *   K % 16 == 0, N % 16 == 0, lda % 16 == 0, lda >= K, K < 2^20.
+ *   max_rows bounds M_total (it sizes the launch).  Uses the workspace
+ *   (at least moe_gemm_workspace_bytes(n_groups, max_rows)). */
+int64_t moe_gemm_workspace_bytes(int32_t n_groups, int64_t max_rows);
+moe_status moe_grouped_gemm_s8(int32_t n_groups, const int32_t* offsets, int64_t max_rows,
+                               const int32_t* row_index, const int8_t* A, int64_t lda,
+                               const int8_t* B, int32_t N, int32_t K, int32_t* C,
+                               void* workspace, int64_t workspace_bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -169,8 +169,9 @@ def static_buffer_bytes(rank_num, local_batch, topk, experts_per_rank, msg_size)
 
 # --------------------------------------------------------------- dispatch
 def dispatch(x_bits: np.ndarray, phys_idx: np.ndarray, E_phys: int, R: int, S: int,
-             fmt: int = 1) -> dict:
-    """FusedDispatch layout and messages.  fmt 1 = INT8 codes, 0 = bf16 rows."""
+             fmt: int = 1, with_rows: bool = True) -> dict:
+    """FusedDispatch layout and messages.  fmt 1 = INT8 codes, 0 = bf16 rows.
+    with_rows=False skips the message rows (layout and metadata only)."""
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     phys_idx = np.ascontiguousarray(phys_idx, dtype=np.int32)
     T, H = x_bits.shape
@@ -179,7 +180,7 @@ def dispatch(x_bits: np.ndarray, phys_idx: np.ndarray, E_phys: int, R: int, S: i
     mt = lb * min(k, epr)
     nslots = R * S * mt
     rowb = H if fmt == 1 else 2 * H
-    rows = np.zeros((nslots, rowb), np.uint8)
+    rows = np.zeros((nslots, rowb), np.uint8) if with_rows else None
     ms = np.zeros(nslots, np.float32)
     msrc = np.full(nslots, -1, np.int32)
     mbs = np.full(nslots, -1, np.int32)

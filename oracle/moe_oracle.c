@@ -252,7 +252,8 @@ int64_t orc_static_buffer_bytes(int64_t rank_num, int64_t local_batch, int64_t t
  * rank_counts[dst][src] = messages; expert_offsets = exclusive prefix of
  * per-physical-expert message counts; expert_rows lists, per expert, the
  * global slot id (dst*S + src)*mt + slot of each message, ascending t.
- * slot_of[t*k + j] = global slot id of message (t, j). */
+ * slot_of[t*k + j] = global slot id of message (t, j).  `rows` may be NULL
+ * (layout and metadata only). */
 int orc_dispatch(int T, int H, int E_phys, int k, int R, int S, int fmt,
                  const uint16_t* x, const int32_t* phys_idx,
                  uint8_t* rows, float* meta_scale, int32_t* meta_src,
@@ -284,8 +285,10 @@ int orc_dispatch(int T, int H, int E_phys, int k, int R, int S, int fmt,
                 int slot = rank_counts[dst * S + src]++;
                 if (slot >= mt) { free(q); free(tmp); free(cnt_e); free(fill); return ORC_BAD; }
                 size_t g = ((size_t)dst * S + src) * mt + slot;
-                if (fmt == 1) memcpy(rows + g * rowb, q, (size_t)H);
-                else memcpy(rows + g * rowb, xr, rowb);
+                if (rows) {
+                    if (fmt == 1) memcpy(rows + g * rowb, q, (size_t)H);
+                    else memcpy(rows + g * rowb, xr, rowb);
+                }
                 meta_scale[g] = sc;
                 meta_src[g] = src;
                 meta_bs[g] = bs;

@@ -1,0 +1,223 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle.
+
+Integer results (indices, counts, offsets, slots, metadata, INT8 codes,
+int32 accumulators) must match bit for bit; binary32 scales bit for bit;
+routing weights within 2e-6; bf16 layer outputs within max-abs 2e-2 and
+relative L2 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from expert_dispatch_combine_gb300 import binding as B
+from expert_dispatch_combine_gb300 import synth
+
+from gpu_util import (MAX_ABS, REL_L2, LayerBuffers, bf16_tensor_to_bits, bits_to_bf16_tensor,
+                      compare_bf16, eplb_map, lib, make_layer, shape_of)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lib()
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+# ------------------------------------------------------------------- route
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_route_parity(name):
+    w = synth.WORKLOADS[name]
+    lg = synth.logits(w)
+    rep = nc = None
+    if w.eplb:
+        rep, nc, _ = eplb_map(w)
+    idx, wt, pidx, cnt = oracle.route(lg, w.k, w.E_phys, rep, nc)
+    shape = shape_of(w)
+    dev = torch.device("cuda")
+    g_idx = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
+    g_w = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+    g_p = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
+    g_c = torch.full((w.E_phys,), -7, dtype=torch.int32, device=dev)
+    rep_d = torch.from_numpy(rep).to(dev) if rep is not None else None
+    nc_d = torch.from_numpy(nc).to(dev) if nc is not None else None
+    B.moe_route(shape, torch.from_numpy(lg).to(dev), g_idx, g_w, g_p, g_c, rep_d, nc_d)
+    torch.cuda.synchronize()
+    assert (_np(g_idx) == idx).all()
+    assert (_np(g_p) == pidx).all()
+    assert (_np(g_c) == cnt).all()
+    assert np.abs(_np(g_w) - wt).max() <= 2e-6
+
+
+def test_route_ties_and_k_equals_e():
+    T, E = 33, 16
+    lg = np.random.default_rng(0).integers(0, 3, size=(T, E)).astype(np.float32)
+    for k in (1, 5, 16):
+        idx, wt, _, cnt = oracle.route(lg, k)
+        shape = B.Shape(T, 16, E, E, k, 16, 1, 1)
+        dev = torch.device("cuda")
+        g_idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+        g_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        g_p = torch.empty((T, k), dtype=torch.int32, device=dev)
+        g_c = torch.empty((E,), dtype=torch.int32, device=dev)
+        B.moe_route(shape, torch.from_numpy(lg).to(dev), g_idx, g_w, g_p, g_c)
+        torch.cuda.synchronize()
+        assert (_np(g_idx) == idx).all()
+        assert (_np(g_c) == cnt).all()
+        assert np.abs(_np(g_w) - wt).max() <= 2e-6
+
+
+# -------------------------------------------------------------- whole layer
+def _full_layer_check(w, cfmt):
+    """Every intermediate and the output of moe_layer against the oracle."""
+    layer = make_layer(w, cfmt)
+    lg = synth.logits(w)
+    xb = synth.hidden_bits(w)
+    out = layer.forward(torch.from_numpy(lg).cuda(), bits_to_bf16_tensor(xb))
+    torch.cuda.synchronize()
+    rep = nc = p2l = None
+    if w.eplb:
+        rep, nc, p2l = eplb_map(w)
+    need = range(w.E_log)
+    weights = {e: synth.expert_weights_np(w, e) for e in need}
+    ref = oracle.layer(lg, xb, weights, w.E_phys, w.R, w.S, w.k, w.I, cfmt, rep, nc, p2l)
+    b = layer.buf
+    r = b.routing
+    assert (_np(r["topk_idx"]) == ref["topk_idx"]).all()
+    assert (_np(r["phys_idx"]) == ref["phys_idx"]).all()
+    assert (_np(r["expert_counts"]) == ref["counts"]).all()
+    assert np.abs(_np(r["topk_w"]) - ref["topk_w"]).max() <= 2e-6
+    d = ref["dispatch"]
+    assert (_np(r["rank_counts"]) == d["rank_counts"]).all()
+    assert (_np(r["expert_offsets"]) == d["expert_offsets"]).all()
+    assert (_np(r["expert_rows"]) == d["expert_rows"]).all()
+    used = d["slot_of"].ravel()
+    rows = _np(b.dispatch_rows())
+    assert (rows[used] == d["rows"][used]).all()
+    meta = _np(b.dispatch_meta())
+    assert (meta[used, 0].view(np.float32) == d["meta_scale"][used]).all()
+    assert (meta[used, 1] == d["meta_src"][used]).all()
+    assert (meta[used, 2] == d["meta_bs"][used]).all()
+    assert (meta[used, 3] == d["meta_rs"][used]).all()
+    crow = _np(b.combine_rows())
+    if cfmt == B.MOE_MSG_INT8:
+        assert (crow.view(np.int8) == ref["cbuf"]).all()
+        assert (_np(b.combine_scales()) == ref["cscale"]).all()
+    else:
+        assert (crow.view(np.uint16) == ref["cbuf"]).all()
+    max_abs, rel = compare_bf16(bf16_tensor_to_bits(out), ref["out"])
+    assert max_abs <= MAX_ABS and rel <= REL_L2, (max_abs, rel)
+
+
+@pytest.mark.parametrize("cfmt", [B.MOE_MSG_INT8, B.MOE_MSG_BF16])
+def test_layer_tiny_full(cfmt):
+    _full_layer_check(synth.WORKLOADS["c0_tiny"], cfmt)
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(T=1, H=16, E_log=4, k=1, I=16, R=1),             # one token
+    dict(T=31, H=48, E_log=8, k=8, I=32, R=2, S=1),       # k = E, ragged
+    dict(T=40, H=64, E_log=12, k=3, I=48, R=3, S=5),      # epr = 4 > k
+    dict(T=130, H=272, E_log=16, k=2, I=144, R=16, S=2),  # epr = 1, ragged tiles
+])
+def test_layer_edge_shapes(cfg):
+    _full_layer_check(synth.custom(seed=5, **cfg), B.MOE_MSG_INT8)
+
+
+def test_layer_eplb_tiny():
+    w = synth.custom("eplb_tiny", T=96, H=128, E_log=16, E_phys=24, k=2, I=64, R=8, seed=3,
+                     zipf=1.2, eplb=True)
+    _full_layer_check(w, B.MOE_MSG_INT8)
+
+
+# ----------------------------------------------------------------- combine
+@pytest.mark.parametrize("cfmt", [B.MOE_MSG_INT8, B.MOE_MSG_BF16])
+def test_combine_on_synthetic_messages(cfmt):
+    T, H, k, E = 77, 7168, 8, 256
+    rng = np.random.default_rng(12)
+    _, wt, _, _ = oracle.route(rng.standard_normal((T, E)).astype(np.float32), k)
+    shape = B.Shape(T, H, E, E, k, 16, 32, 1, B.MOE_MSG_INT8, cfmt)
+    buf = LayerBuffers(shape)
+    if cfmt == B.MOE_MSG_INT8:
+        cb = rng.integers(-127, 128, size=(T, k, H)).astype(np.int8)
+        cs = rng.uniform(1e-4, 1e-2, size=(T, k)).astype(np.float32)
+        buf.combine_rows().copy_(torch.from_numpy(cb.view(np.uint8)).cuda())
+        buf.combine_scales().copy_(torch.from_numpy(cs).cuda())
+    else:
+        cb = synth.f32_to_bf16_bits(rng.standard_normal((T, k, H)).astype(np.float32))
+        cs = np.zeros((T, k), np.float32)
+        buf.combine_rows().copy_(torch.from_numpy(cb.view(np.uint8).reshape(T, k, 2 * H)).cuda())
+    B.moe_combine(shape, buf.combine, torch.from_numpy(wt).cuda(), buf.out)
+    torch.cuda.synchronize()
+    ref = oracle.combine(cb, cs, wt, cfmt)
+    max_abs, rel = compare_bf16(bf16_tensor_to_bits(buf.out), ref)
+    assert max_abs <= MAX_ABS and rel <= REL_L2
+    # binary32 accumulation vs binary64: the difference is bounded by one bf16
+    # ulp of the result plus the binary32 rounding of k products and sums
+    g = synth.bf16_bits_to_f32(bf16_tensor_to_bits(buf.out)).astype(np.float64)
+    r = synth.bf16_bits_to_f32(ref).astype(np.float64)
+    if cfmt == B.MOE_MSG_INT8:
+        v = cb.astype(np.float64) * cs[:, :, None].astype(np.float64)
+    else:
+        v = synth.bf16_bits_to_f32(cb).astype(np.float64)
+    mag = np.abs(wt[:, :, None].astype(np.float64) * v).sum(axis=1)
+    ulp = np.maximum(np.abs(r), np.abs(g)) * 2.0 ** -7
+    assert (np.abs(g - r) <= ulp + 3 * k * 2.0 ** -24 * mag + 1e-38).all()
+    assert (g == r).mean() > 0.99
+
+
+# ------------------------------------------------------ grouped int8 GEMM
+@pytest.mark.parametrize("K,N", [(7168, 64), (2048, 256), (48, 32)])
+def test_grouped_gemm_exact_worst_case(K, N):
+    """|sum| up to K*127*127 (> 2^24 for K >= 1041): int32 must be exact."""
+    rng = np.random.default_rng(K)
+    G = 5
+    sizes = np.array([0, 130, 1, 64, 257])
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    M = int(offs[-1])
+    A = np.where(rng.random((M, K)) < 0.5, 127, -127).astype(np.int8)
+    A[::7] = 127
+    Bw = np.where(rng.random((G, N, K)) < 0.5, 127, -127).astype(np.int8)
+    Bw[:, ::5] = 127
+    Bw[:, 1::5] = -127
+    ref = np.empty((M, N), np.int64)
+    for g in range(G):
+        a = A[offs[g]:offs[g + 1]].astype(np.int64)
+        ref[offs[g]:offs[g + 1]] = a @ Bw[g].astype(np.int64).T
+    ws = torch.empty(B.moe_gemm_workspace_bytes(G, M), dtype=torch.uint8, device="cuda")
+    C = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    B.moe_grouped_gemm_s8(torch.from_numpy(offs).cuda(), M, torch.from_numpy(A).cuda(), K,
+                          torch.from_numpy(Bw).cuda(), C, ws)
+    torch.cuda.synchronize()
+    assert (_np(C).astype(np.int64) == ref).all()
+
+
+def test_grouped_gemm_gather_rows():
+    rng = np.random.default_rng(1)
+    G, N, K, lda = 3, 48, 96, 112
+    sizes = [5, 0, 9]
+    offs = np.array([0, 5, 5, 14], np.int32)
+    A = rng.integers(-127, 128, size=(40, lda)).astype(np.int8)
+    ridx = rng.permutation(40)[:14].astype(np.int32)
+    Bw = rng.integers(-127, 128, size=(G, N, K)).astype(np.int8)
+    ref = np.empty((14, N), np.int64)
+    for g in range(G):
+        for r in range(offs[g], offs[g + 1]):
+            ref[r] = Bw[g].astype(np.int64) @ A[ridx[r], :K].astype(np.int64)
+    ws = torch.empty(B.moe_gemm_workspace_bytes(G, 14), dtype=torch.uint8, device="cuda")
+    C = torch.empty((14, N), dtype=torch.int32, device="cuda")
+    B.moe_grouped_gemm_s8(torch.from_numpy(offs).cuda(), 14, torch.from_numpy(A).cuda(), lda,
+                          torch.from_numpy(Bw).cuda(), C, ws, row_index=torch.from_numpy(ridx).cuda())
+    torch.cuda.synchronize()
+    assert (_np(C).astype(np.int64) == ref).all()
+
+
+def test_weights_generated_on_device_equal_host():
+    w = synth.WORKLOADS["c1_decode"]
+    a = synth.int8_tensor_torch(w.seed, 17, synth.GATE_UP, (2 * w.I, w.H), device="cuda")
+    b = synth.int8_tensor_np(w.seed, 17, synth.GATE_UP, (2 * w.I, w.H))
+    assert (_np(a) == b).all()
