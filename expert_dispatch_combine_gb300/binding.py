@@ -54,7 +54,7 @@ class moe_routing(ctypes.Structure):
 
 EXPORTED = ("moe_status_string", "moe_static_buffer_bytes", "moe_query_layout", "moe_eplb_plan",
             "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_layer",
-            "moe_gemm_workspace_bytes", "moe_grouped_gemm_s8")
+            "moe_gemm_workspace_bytes", "moe_grouped_gemm_s8", "moe_launch_count")
 
 _lib = None
 
@@ -83,6 +83,7 @@ def load(path: str = LIB_PATH):
         "moe_layer": ([PS, P, P, P, P, i32, ctypes.POINTER(moe_expert_weights),
                        ctypes.POINTER(moe_routing), P, i64, P, i64, P, i64, P, P], ctypes.c_int),
         "moe_gemm_workspace_bytes": ([i32, i64], i64),
+        "moe_launch_count": ([], i64),
         "moe_grouped_gemm_s8": ([i32, P, i64, P, P, i64, P, i32, i32, P, P, i64, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
@@ -219,6 +220,10 @@ def moe_layer(shape: Shape, logits, x, w_gate_up, s_gate_up, w_down, s_down, rou
         ctypes.byref(w), ctypes.byref(r), _ptr(dispatch_buf), dispatch_buf.numel(),
         _ptr(combine_buf), combine_buf.numel(), _ptr(workspace), workspace.numel(), _ptr(out),
         _stream(stream)))
+
+
+def moe_launch_count() -> int:
+    return int(load().moe_launch_count())
 
 
 def moe_gemm_workspace_bytes(n_groups: int, max_rows: int) -> int:

@@ -2,9 +2,16 @@
 // validation, buffer layout, and the launch sequence of each step.
 #include <string.h>
 
+#include <atomic>
+
 #include "internal.cuh"
 
 using namespace moe;
+
+namespace moe {
+static std::atomic<long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace moe
 
 namespace {
 
@@ -210,6 +217,8 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t
         return MOE_ERR_CUDA;
     return MOE_OK;
 }
+
+int64_t moe_launch_count(void) { return (int64_t)g_launches.load(std::memory_order_relaxed); }
 
 int64_t moe_gemm_workspace_bytes(int32_t n_groups, int64_t max_rows) {
     (void)max_rows;

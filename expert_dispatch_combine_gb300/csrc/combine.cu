@@ -92,6 +92,7 @@ cudaError_t launch_combine(const Dims& d, const void* cbuf, long long scale_off,
     else
         combine_kernel<false><<<d.T, kCombineThreads, 0, st>>>(d.H, d.k, d.crow, cb, nullptr,
                                                                 topk_w, out);
+    count_launches(1);
     return cudaGetLastError();
 }
 

@@ -285,6 +285,7 @@ cudaError_t launch_dispatch(const Dims& d, const uint16_t* x, const int32_t* phy
         d.H, d.k, d.lb, d.epr, d.S, d.mt, d.E_phys, d.dfmt == MOE_MSG_INT8 ? 1 : 0, d.drow, x,
         phys_idx, slot_local, erank, src_base, expert_offsets, static_cast<char*>(dbuf),
         reinterpret_cast<moe_dispatch_meta*>(static_cast<char*>(dbuf) + meta_off), expert_rows);
+    count_launches(3);
     return cudaGetLastError();
 }
 

@@ -295,6 +295,7 @@ cudaError_t launch_grouped_gemm_s8(int n_groups, const int32_t* offsets, long lo
     dim3 grid((unsigned)max_tiles, (unsigned)((N + kBN - 1) / kBN));
     gemm_s8_simt_kernel<<<grid, 256, 0, st>>>(n_groups, offsets, tile_prefix, row_index, A, lda,
                                               B, b_group_stride, group_to_set, N, K, C);
+    count_launches(2);
     return cudaGetLastError();
 }
 
@@ -332,6 +333,7 @@ cudaError_t launch_ffn(const Dims& d, const void* dbuf, long long meta_off,
         d.H, d.k, d.lb, d.E_phys, int8_msgs, d.crow, expert_offsets, expert_rows, meta,
         w.phys_to_weight, w.s_down, acc_d, sh, cb,
         reinterpret_cast<float*>(cb + scale_off));
+    count_launches(2);
     return cudaGetLastError();
 }
 

@@ -73,6 +73,9 @@ inline WsLayout make_ws(const Dims& d) {
 template <typename T>
 inline T* ws_ptr(void* ws, long long off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
 
+// Number of kernels (and memsets) this library has enqueued in this process.
+void count_launches(int n);
+
 // Kernel launchers (each returns cudaGetLastError() after its launches).
 cudaError_t launch_route(const Dims& d, const float* logits, const int32_t* rep_table,
                          const int32_t* n_copies, int max_copies, int32_t* topk_idx,

@@ -114,6 +114,7 @@ cudaError_t launch_route(const Dims& d, const float* logits, const int32_t* rep_
     else if (vpl <= 16) MOE_ROUTE_CASE(16);
     else MOE_ROUTE_CASE(32);
 #undef MOE_ROUTE_CASE
+    count_launches(2);
     return cudaGetLastError();
 }
 

@@ -271,6 +271,10 @@ moe_status moe_grouped_gemm_s8(int32_t n_groups, const int32_t* offsets, int64_t
                                const int8_t* B, int32_t N, int32_t K, int32_t* C,
                                void* workspace, int64_t workspace_bytes, moe_stream_t stream);
 
+/* Number of GPU operations (kernel launches and memsets) the library has
+ * enqueued in this process since it was loaded.  Host only, thread-safe. */
+int64_t moe_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif
