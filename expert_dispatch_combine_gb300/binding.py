@@ -54,7 +54,8 @@ class moe_routing(ctypes.Structure):
 
 EXPORTED = ("moe_status_string", "moe_static_buffer_bytes", "moe_query_layout", "moe_eplb_plan",
             "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_layer",
-            "moe_gemm_workspace_bytes", "moe_grouped_gemm_s8", "moe_launch_count")
+            "moe_gemm_workspace_bytes", "moe_grouped_gemm_s8", "moe_launch_count",
+            "moe_device_status")
 
 _lib = None
 
@@ -82,7 +83,8 @@ def load(path: str = LIB_PATH):
         "moe_combine": ([PS, P, i64, P, P, P], ctypes.c_int),
         "moe_layer": ([PS, P, P, P, P, i32, ctypes.POINTER(moe_expert_weights),
                        ctypes.POINTER(moe_routing), P, i64, P, i64, P, i64, P, P], ctypes.c_int),
-        "moe_gemm_workspace_bytes": ([i32, i64], i64),
+        "moe_gemm_workspace_bytes": ([i32, i64, i32], i64),
+        "moe_device_status": ([P, ctypes.POINTER(i32), P], ctypes.c_int),
         "moe_launch_count": ([], i64),
         "moe_grouped_gemm_s8": ([i32, P, i64, P, P, i64, P, i32, i32, P, P, i64, P], ctypes.c_int),
     }
@@ -226,8 +228,15 @@ def moe_launch_count() -> int:
     return int(load().moe_launch_count())
 
 
-def moe_gemm_workspace_bytes(n_groups: int, max_rows: int) -> int:
-    return int(load().moe_gemm_workspace_bytes(n_groups, max_rows))
+def moe_gemm_workspace_bytes(n_groups: int, max_rows: int, K: int) -> int:
+    return int(load().moe_gemm_workspace_bytes(n_groups, max_rows, K))
+
+
+def moe_device_status(workspace, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    _check("moe_device_status", load().moe_device_status(_ptr(workspace), ctypes.byref(v),
+                                                         _stream(stream)))
+    return v.value
 
 
 def moe_grouped_gemm_s8(offsets, max_rows: int, A, lda: int, B, C, workspace, row_index=None,

@@ -220,10 +220,20 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t
 
 int64_t moe_launch_count(void) { return (int64_t)g_launches.load(std::memory_order_relaxed); }
 
-int64_t moe_gemm_workspace_bytes(int32_t n_groups, int64_t max_rows) {
-    (void)max_rows;
-    if (n_groups < 1) return -1;
-    return align_up(4LL * (n_groups + 1), 256);
+int64_t moe_gemm_workspace_bytes(int32_t n_groups, int64_t max_rows, int32_t K) {
+    if (n_groups < 1 || max_rows < 0 || K < 16) return -1;
+    return gemm_ws_bytes(n_groups, max_rows, K);
+}
+
+moe_status moe_device_status(const void* workspace, int32_t* status, moe_stream_t stream) {
+    if (!workspace || !status) return MOE_ERR_INVALID_ARG;
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, (cudaStream_t)stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    *status = v;
+    return MOE_OK;
 }
 
 moe_status moe_grouped_gemm_s8(int32_t n_groups, const int32_t* offsets, int64_t max_rows,
@@ -235,11 +245,16 @@ moe_status moe_grouped_gemm_s8(int32_t n_groups, const int32_t* offsets, int64_t
     if (K < 16 || K % 16 || K >= (1 << 20) || N < 16 || N % 16 || lda < K || lda % 16)
         return MOE_ERR_INVALID_ARG;
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
-    if (workspace_bytes < moe_gemm_workspace_bytes(n_groups, max_rows)) return MOE_ERR_WORKSPACE;
+    if (workspace_bytes < gemm_ws_bytes(n_groups, max_rows, K)) return MOE_ERR_WORKSPACE;
     if (max_rows == 0) return MOE_OK;
+    if (K % 64 == 0)
+        return cuda_status(launch_grouped_gemm_tc(n_groups, offsets, max_rows, row_index, A, lda, B,
+                                                  N, K, C, workspace, (cudaStream_t)stream));
+    if (cudaMemsetAsync(workspace, 0, 256, (cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+    count_launches(1);
     return cuda_status(launch_grouped_gemm_s8(n_groups, offsets, max_rows, row_index, A, lda, B,
                                               (long long)N * K, nullptr, N, K, C,
-                                              static_cast<int32_t*>(workspace),
+                                              ws_ptr<int32_t>(workspace, 256),
                                               (cudaStream_t)stream));
 }
 

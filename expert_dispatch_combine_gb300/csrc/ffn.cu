@@ -18,45 +18,11 @@
 //              buffer at (t, j) (INT8 codes + scale, or bf16)
 #include <cuda_bf16.h>
 
+#include "device_math.cuh"
 #include "internal.cuh"
 
 namespace moe {
 namespace {
-
-// ------------------------------------------------------------ exp spec
-// Binary32, one rounding per operation (explicit _rn intrinsics, never
-// contracted):  x > 88 -> +inf;  x < -87 -> 0;  otherwise
-//   n = rint(x * RCP_LN2);  r = (x - n*LN2_HI) - n*LN2_LO
-//   p = Horner(r; 1/7!, 1/6!, ..., 1/1!, 1/0!)   (Taylor series of e^r)
-//   e = p * 2^n
-// Cody-Waite argument reduction with a 14-bit LN2_HI (n*LN2_HI exact for
-// |n| <= 127).  Constants are the binary32 values nearest to ln 2 pieces and
-// to 1/m!.
-__device__ __forceinline__ float exp_spec(float x) {
-    const float RCP_LN2 = 0x1.715476p+0f;
-    const float LN2_HI = 0x1.62e4p-1f;
-    const float LN2_LO = 0x1.7f7d1cp-20f;
-    if (x > 88.0f) return __int_as_float(0x7f800000);
-    if (x < -87.0f) return 0.0f;
-    float n = rintf(__fmul_rn(x, RCP_LN2));
-    float r = __fsub_rn(x, __fmul_rn(n, LN2_HI));
-    r = __fsub_rn(r, __fmul_rn(n, LN2_LO));
-    float p = 0x1.a01a02p-13f;                    // 1/5040
-    p = __fadd_rn(0x1.6c16c2p-10f, __fmul_rn(r, p));  // 1/720
-    p = __fadd_rn(0x1.111112p-7f, __fmul_rn(r, p));   // 1/120
-    p = __fadd_rn(0x1.555556p-5f, __fmul_rn(r, p));   // 1/24
-    p = __fadd_rn(0x1.555556p-3f, __fmul_rn(r, p));   // 1/6
-    p = __fadd_rn(0.5f, __fmul_rn(r, p));
-    p = __fadd_rn(1.0f, __fmul_rn(r, p));
-    p = __fadd_rn(1.0f, __fmul_rn(r, p));
-    int ni = (int)n;
-    return __fmul_rn(p, __int_as_float((ni + 127) << 23));
-}
-
-// SwiGLU gate: SiLU(g) = g / (1 + e(-g))
-__device__ __forceinline__ float silu_spec(float g) {
-    return __fdiv_rn(g, __fadd_rn(1.0f, exp_spec(-g)));
-}
 
 // --------------------------------------------------------- tile prefix
 // tile_prefix[g] = sum_{g' < g} ceil(M_g' / BM), g = 0..G (one block).
@@ -100,17 +66,6 @@ tile_prefix_kernel(int G, int BM, const int32_t* __restrict__ offsets,
         __syncthreads();
     }
     if (threadIdx.x == 0) tile_prefix[G] = s_carry;
-}
-
-__device__ __forceinline__ int find_group(const int32_t* __restrict__ prefix, int G, int v) {
-    // largest g in [0, G) with prefix[g] <= v
-    int lo = 0, hi = G - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (prefix[mid] <= v) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
 }
 
 // ------------------------------------------------------- SIMT int8 GEMM
@@ -201,11 +156,6 @@ __device__ __forceinline__ float block_max(float v, float* s_red) {
     return r;
 }
 
-__device__ __forceinline__ int quant1(float v, float s) {
-    int q = __float2int_rn(__fdiv_rn(v, s));
-    return max(-127, min(127, q));
-}
-
 constexpr int kRowThreads = 256;
 
 // SwiGLU + token-wise requantisation of one routed row.
@@ -284,25 +234,33 @@ cudaError_t set_smem(const void* fn, size_t bytes) {
 
 }  // namespace
 
+cudaError_t launch_tile_prefix(int G, int BM, const int32_t* offsets, int32_t* tile_prefix,
+                               cudaStream_t st) {
+    tile_prefix_kernel<<<1, 1024, 0, st>>>(G, BM, offsets, tile_prefix);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_grouped_gemm_s8(int n_groups, const int32_t* offsets, long long max_rows,
                                    const int32_t* row_index, const int8_t* A, long long lda,
                                    const int8_t* B, long long b_group_stride,
                                    const int32_t* group_to_set, int N, int K, int32_t* C,
                                    int32_t* tile_prefix, cudaStream_t st) {
-    tile_prefix_kernel<<<1, 1024, 0, st>>>(n_groups, kBM, offsets, tile_prefix);
+    cudaError_t e0 = launch_tile_prefix(n_groups, kBM, offsets, tile_prefix, st);
+    if (e0 != cudaSuccess) return e0;
     long long max_tiles = (max_rows + kBM - 1) / kBM + n_groups;
     if (max_tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
     dim3 grid((unsigned)max_tiles, (unsigned)((N + kBN - 1) / kBN));
     gemm_s8_simt_kernel<<<grid, 256, 0, st>>>(n_groups, offsets, tile_prefix, row_index, A, lda,
                                               B, b_group_stride, group_to_set, N, K, C);
-    count_launches(2);
+    count_launches(1);
     return cudaGetLastError();
 }
 
-cudaError_t launch_ffn(const Dims& d, const void* dbuf, long long meta_off,
-                       const int32_t* expert_offsets, const int32_t* expert_rows,
-                       const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                       const WsLayout& wl, cudaStream_t st) {
+cudaError_t launch_ffn_simt(const Dims& d, const void* dbuf, long long meta_off,
+                            const int32_t* expert_offsets, const int32_t* expert_rows,
+                            const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
+                            const WsLayout& wl, cudaStream_t st) {
     const long long M = (long long)d.T * d.k;
     const moe_dispatch_meta* meta =
         reinterpret_cast<const moe_dispatch_meta*>(static_cast<const char*>(dbuf) + meta_off);
@@ -314,6 +272,8 @@ cudaError_t launch_ffn(const Dims& d, const void* dbuf, long long meta_off,
     unsigned char* cb = static_cast<unsigned char*>(cbuf);
     cudaError_t e;
 
+    if ((e = cudaMemsetAsync(ws_ptr<int>(ws, 0), 0, 256, st)) != cudaSuccess) return e;
+    count_launches(1);
     e = launch_grouped_gemm_s8(d.E_phys, expert_offsets, M, expert_rows,
                                static_cast<const int8_t*>(dbuf), d.drow, w.w_gate_up,
                                2LL * d.I * d.H, w.phys_to_weight, 2 * d.I, d.H, acc_gu, tiles, st);

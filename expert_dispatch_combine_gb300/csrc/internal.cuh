@@ -34,40 +34,63 @@ inline Dims make_dims(const moe_shape& s) {
 
 inline long long align_up(long long v, long long a) { return (v + a - 1) / a * a; }
 
-// Grouped GEMM tile sizes (used to size the tile table).
-constexpr int kGemmBM = 128;
+// The tensor-core expert FFN needs K multiples of 64 for both GEMMs.
+inline bool ffn_uses_tc(const Dims& d) { return d.H % 64 == 0 && d.I % 64 == 0; }
 
-// Workspace carve-up.  Every region is 256-byte aligned.
+// Workspace carve-up.  Every region is 256-byte aligned; offset 0 holds the
+// int32 device status word (MOE_OK or MOE_ERR_TIMEOUT).
 struct WsLayout {
     long long slot_local;  // int32 [T*k]   slot of (t, j) within its (dst, src) pair
     long long erank;       // int32 [T*k]   rank of token t among its source's tokens for expert p
     long long hist;        // int32 [S][E_phys]
     long long src_base;    // int32 [S][E_phys]
     long long tiles;       // int32 [E_phys + 1]  grouped-GEMM tile prefix
-    long long gemm_tiles;  // int32 [gemm groups + 1] for moe_grouped_gemm_s8 (same region)
+    long long sh;          // f32   [T*k]   requantisation scale of h
+    // SIMT expert FFN
     long long acc_gu;      // int32 [T*k][2I]
     long long hq;          // int8  [T*k][I]
-    long long sh;          // f32   [T*k]
     long long acc_d;       // int32 [T*k][H]
+    // tensor-core expert FFN
+    long long rowmax;      // u32   [2][T*k]  absmax of h and of y (float bits)
+    long long s_row;       // f32   [T*k]     dispatch scale of each expert row
+    long long a16;         // fp16  [T*k][H]  expert input rows
+    long long hbuf;        // f32   [T*k][I]  SwiGLU output
+    long long hq16;        // fp16  [T*k][I]  requantised SwiGLU output
+    long long ybuf;        // f32   [T*k][H]  expert output (INT8 return messages only)
     long long total;
+    bool tc;
 };
 
 inline WsLayout make_ws(const Dims& d) {
-    WsLayout w;
-    long long o = 0;
+    WsLayout w = {};
+    long long o = 256;
     const long long tk = (long long)d.T * d.k;
     w.slot_local = o; o = align_up(o + 4 * tk, 256);
     w.erank = o;      o = align_up(o + 4 * tk, 256);
     w.hist = o;       o = align_up(o + 4LL * d.S * d.E_phys, 256);
     w.src_base = o;   o = align_up(o + 4LL * d.S * d.E_phys, 256);
     w.tiles = o;      o = align_up(o + 4LL * (d.E_phys + 1), 256);
-    w.gemm_tiles = w.tiles;
-    w.acc_gu = o;     o = align_up(o + 4 * tk * 2 * d.I, 256);
-    w.hq = o;         o = align_up(o + tk * d.I, 256);
     w.sh = o;         o = align_up(o + 4 * tk, 256);
-    w.acc_d = o;      o = align_up(o + 4 * tk * d.H, 256);
+    w.tc = ffn_uses_tc(d);
+    if (w.tc) {
+        w.rowmax = o; o = align_up(o + 8 * tk, 256);
+        w.s_row = o;  o = align_up(o + 4 * tk, 256);
+        w.a16 = o;    o = align_up(o + 2 * tk * d.H, 256);
+        w.hbuf = o;   o = align_up(o + 4 * tk * d.I, 256);
+        w.hq16 = o;   o = align_up(o + 2 * tk * d.I, 256);
+        if (d.cfmt == MOE_MSG_INT8) { w.ybuf = o; o = align_up(o + 4 * tk * d.H, 256); }
+    } else {
+        w.acc_gu = o; o = align_up(o + 4 * tk * 2 * d.I, 256);
+        w.hq = o;     o = align_up(o + tk * d.I, 256);
+        w.acc_d = o;  o = align_up(o + 4 * tk * d.H, 256);
+    }
     w.total = o;
     return w;
+}
+
+// Workspace of moe_grouped_gemm_s8: [status][tile prefix][fp16 A rows].
+inline long long gemm_ws_bytes(int n_groups, long long max_rows, int K) {
+    return 256 + align_up(4LL * (n_groups + 1), 256) + align_up(2LL * max_rows * K, 256);
 }
 
 template <typename T>
@@ -92,9 +115,28 @@ cudaError_t launch_grouped_gemm_s8(int n_groups, const int32_t* offsets, long lo
                                    const int8_t* B, long long b_group_stride,
                                    const int32_t* group_to_set, int N, int K, int32_t* C,
                                    int32_t* tile_prefix, cudaStream_t st);
-cudaError_t launch_ffn(const Dims& d, const void* dbuf, long long meta_off,
-                       const int32_t* expert_offsets, const int32_t* expert_rows,
-                       const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                       const WsLayout& wl, cudaStream_t st);
+cudaError_t launch_tile_prefix(int G, int BM, const int32_t* offsets, int32_t* tile_prefix,
+                               cudaStream_t st);
+cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long long max_rows,
+                                   const int32_t* row_index, const int8_t* A, long long lda,
+                                   const int8_t* B, int N, int K, int32_t* C, void* ws,
+                                   cudaStream_t st);
+cudaError_t launch_ffn_simt(const Dims& d, const void* dbuf, long long meta_off,
+                            const int32_t* expert_offsets, const int32_t* expert_rows,
+                            const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
+                            const WsLayout& wl, cudaStream_t st);
+cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
+                          const int32_t* expert_offsets, const int32_t* expert_rows,
+                          const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
+                          const WsLayout& wl, cudaStream_t st);
+inline cudaError_t launch_ffn(const Dims& d, const void* dbuf, long long meta_off,
+                              const int32_t* expert_offsets, const int32_t* expert_rows,
+                              const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
+                              const WsLayout& wl, cudaStream_t st) {
+    return wl.tc ? launch_ffn_tc(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf, scale_off,
+                                 ws, wl, st)
+                 : launch_ffn_simt(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
+                                   scale_off, ws, wl, st);
+}
 
 }  // namespace moe

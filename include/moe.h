@@ -256,6 +256,9 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t
 
 /* Exact grouped INT8 GEMM with int32 output -- the contraction inside
  * moe_expert_ffn ([X] P085: sum_k q(x_ik) q(w_jk)), exposed on its own.
+ * With K % 64 == 0 it runs the same tensor-core kernel as moe_expert_ffn
+ * (fp16 operands, fp32 accumulation drained to int32 every 1024 K, which is
+ * exact); otherwise a CUDA-core dp4a kernel.
  *   For group gi in [0, n_groups) and rows r in [offsets[gi], offsets[gi+1]):
  *     C[r][n] = sum_{kk<K} A[arow(r)][kk] * B[gi][n][kk]     (exact int32)
  *   arow(r) = row_index[r] if row_index != NULL, else r.
@@ -264,12 +267,18 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t
  *   bytes; B (device) int8 [n_groups][N][K]; C (device) int32 [M_total][N].
  *   K % 16 == 0, N % 16 == 0, lda % 16 == 0, lda >= K, K < 2^20.
  *   max_rows bounds M_total (it sizes the launch).  Uses the workspace
- *   (at least moe_gemm_workspace_bytes(n_groups, max_rows)). */
-int64_t moe_gemm_workspace_bytes(int32_t n_groups, int64_t max_rows);
+ *   (at least moe_gemm_workspace_bytes(n_groups, max_rows, K)). */
+int64_t moe_gemm_workspace_bytes(int32_t n_groups, int64_t max_rows, int32_t K);
 moe_status moe_grouped_gemm_s8(int32_t n_groups, const int32_t* offsets, int64_t max_rows,
                                const int32_t* row_index, const int8_t* A, int64_t lda,
                                const int8_t* B, int32_t N, int32_t K, int32_t* C,
                                void* workspace, int64_t workspace_bytes, moe_stream_t stream);
+
+/* Reads the device status word that the library's kernels keep at the start
+ * of `workspace` (device): MOE_OK, or MOE_ERR_TIMEOUT if a bounded device
+ * wait gave up during the last moe_expert_ffn / moe_layer /
+ * moe_grouped_gemm_s8 call that used this workspace.  Synchronises `stream`. */
+moe_status moe_device_status(const void* workspace, int32_t* status, moe_stream_t stream);
 
 /* Number of GPU operations (kernel launches and memsets) the library has
  * enqueued in this process since it was loaded.  Host only, thread-safe. */

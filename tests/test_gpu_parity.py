@@ -111,6 +111,7 @@ def _full_layer_check(w, cfmt):
         assert (crow.view(np.uint16) == ref["cbuf"]).all()
     max_abs, rel = compare_bf16(bf16_tensor_to_bits(out), ref["out"])
     assert max_abs <= MAX_ABS and rel <= REL_L2, (max_abs, rel)
+    assert B.moe_device_status(b.workspace) == 0
 
 
 @pytest.mark.parametrize("cfmt", [B.MOE_MSG_INT8, B.MOE_MSG_BF16])
@@ -119,6 +120,11 @@ def test_layer_tiny_full(cfmt):
 
 
 @pytest.mark.parametrize("cfg", [
+    # tensor-core expert path (H, I multiples of 64)
+    dict(T=130, H=128, E_log=16, k=2, I=64, R=16, S=2),   # epr = 1, ragged token tiles
+    dict(T=40, H=1088, E_log=12, k=3, I=192, R=3, S=5),   # K = 17 stages (2 exact chunks), partial channel block
+    dict(T=300, H=256, E_log=4, k=4, I=128, R=2, S=3),    # k = E: 300 rows per expert, 3 token tiles
+    # CUDA-core expert path (H or I not a multiple of 64)
     dict(T=1, H=16, E_log=4, k=1, I=16, R=1),             # one token
     dict(T=31, H=48, E_log=8, k=8, I=32, R=2, S=1),       # k = E, ragged
     dict(T=40, H=64, E_log=12, k=3, I=48, R=3, S=5),      # epr = 4 > k
@@ -188,17 +194,19 @@ def test_grouped_gemm_exact_worst_case(K, N):
     for g in range(G):
         a = A[offs[g]:offs[g + 1]].astype(np.int64)
         ref[offs[g]:offs[g + 1]] = a @ Bw[g].astype(np.int64).T
-    ws = torch.empty(B.moe_gemm_workspace_bytes(G, M), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(B.moe_gemm_workspace_bytes(G, M, K), dtype=torch.uint8, device="cuda")
     C = torch.empty((M, N), dtype=torch.int32, device="cuda")
     B.moe_grouped_gemm_s8(torch.from_numpy(offs).cuda(), M, torch.from_numpy(A).cuda(), K,
                           torch.from_numpy(Bw).cuda(), C, ws)
     torch.cuda.synchronize()
     assert (_np(C).astype(np.int64) == ref).all()
+    assert B.moe_device_status(ws) == 0
 
 
-def test_grouped_gemm_gather_rows():
+@pytest.mark.parametrize("N,K,lda", [(48, 96, 112), (144, 128, 160), (16, 1024, 1024)])
+def test_grouped_gemm_gather_rows(N, K, lda):
     rng = np.random.default_rng(1)
-    G, N, K, lda = 3, 48, 96, 112
+    G = 3
     sizes = [5, 0, 9]
     offs = np.array([0, 5, 5, 14], np.int32)
     A = rng.integers(-127, 128, size=(40, lda)).astype(np.int8)
@@ -208,12 +216,13 @@ def test_grouped_gemm_gather_rows():
     for g in range(G):
         for r in range(offs[g], offs[g + 1]):
             ref[r] = Bw[g].astype(np.int64) @ A[ridx[r], :K].astype(np.int64)
-    ws = torch.empty(B.moe_gemm_workspace_bytes(G, 14), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(B.moe_gemm_workspace_bytes(G, 14, K), dtype=torch.uint8, device="cuda")
     C = torch.empty((14, N), dtype=torch.int32, device="cuda")
     B.moe_grouped_gemm_s8(torch.from_numpy(offs).cuda(), 14, torch.from_numpy(A).cuda(), lda,
                           torch.from_numpy(Bw).cuda(), C, ws, row_index=torch.from_numpy(ridx).cuda())
     torch.cuda.synchronize()
     assert (_np(C).astype(np.int64) == ref).all()
+    assert B.moe_device_status(ws) == 0
 
 
 def test_weights_generated_on_device_equal_host():
