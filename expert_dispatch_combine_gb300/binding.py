@@ -55,7 +55,7 @@ class moe_routing(ctypes.Structure):
 EXPORTED = ("moe_status_string", "moe_static_buffer_bytes", "moe_query_layout", "moe_eplb_plan",
             "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_layer",
             "moe_gemm_workspace_bytes", "moe_grouped_gemm_s8", "moe_launch_count",
-            "moe_device_status")
+            "moe_device_status", "moe_last_cuda_error")
 
 _lib = None
 
@@ -86,6 +86,7 @@ def load(path: str = LIB_PATH):
         "moe_gemm_workspace_bytes": ([i32, i64, i32], i64),
         "moe_device_status": ([P, ctypes.POINTER(i32), P], ctypes.c_int),
         "moe_launch_count": ([], i64),
+        "moe_last_cuda_error": ([], ctypes.c_char_p),
         "moe_grouped_gemm_s8": ([i32, P, i64, P, P, i64, P, i32, i32, P, P, i64, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
@@ -115,6 +116,8 @@ def _stream(stream):
 
 def _check(fn, rc):
     if rc != 0:
+        if rc == 4:  # MOE_ERR_CUDA: attach the CUDA error text
+            raise MoeError(fn + " [" + load().moe_last_cuda_error().decode() + "]", rc)
         raise MoeError(fn, rc)
 
 

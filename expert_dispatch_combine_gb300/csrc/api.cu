@@ -44,7 +44,13 @@ void fill_layout(const Dims& d, moe_layout* L) {
     L->workspace_bytes = make_ws(d).total;
 }
 
-moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+moe_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return MOE_OK;
+    g_last_cuda_error = e;
+    return MOE_ERR_CUDA;
+}
 
 moe_status check_weights(const Dims& d, const moe_expert_weights* w) {
     if (!w || !w->w_gate_up || !w->s_gate_up || !w->w_down || !w->s_down) return MOE_ERR_INVALID_ARG;
@@ -201,22 +207,21 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t
         return MOE_ERR_WORKSPACE;
     const WsLayout wl = make_ws(d);
     cudaStream_t s = (cudaStream_t)stream;
-    if ((launch_route(d, logits, rep_table, n_copies, max_copies, r.topk_idx, r.topk_w,
-                          r.phys_idx, r.expert_counts, s)) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    if ((launch_dispatch(d, x, r.phys_idx, dispatch_buf, L.dispatch_meta_offset,
-                             r.rank_counts, r.expert_offsets, r.expert_rows, workspace, wl, s)) !=
-        cudaSuccess)
-        return MOE_ERR_CUDA;
-    if ((launch_ffn(d, dispatch_buf, L.dispatch_meta_offset, r.expert_offsets, r.expert_rows,
-                        *weights, combine_buf, L.combine_scale_offset, workspace, wl, s)) !=
-        cudaSuccess)
-        return MOE_ERR_CUDA;
-    if ((launch_combine(d, combine_buf, L.combine_scale_offset, r.topk_w, out, s)) !=
-        cudaSuccess)
-        return MOE_ERR_CUDA;
-    return MOE_OK;
+    if ((st = cuda_status(launch_route(d, logits, rep_table, n_copies, max_copies, r.topk_idx,
+                                       r.topk_w, r.phys_idx, r.expert_counts, s))) != MOE_OK)
+        return st;
+    if ((st = cuda_status(launch_dispatch(d, x, r.phys_idx, dispatch_buf, L.dispatch_meta_offset,
+                                          r.rank_counts, r.expert_offsets, r.expert_rows,
+                                          workspace, wl, s))) != MOE_OK)
+        return st;
+    if ((st = cuda_status(launch_ffn(d, dispatch_buf, L.dispatch_meta_offset, r.expert_offsets,
+                                     r.expert_rows, *weights, combine_buf, L.combine_scale_offset,
+                                     workspace, wl, s))) != MOE_OK)
+        return st;
+    return cuda_status(launch_combine(d, combine_buf, L.combine_scale_offset, r.topk_w, out, s));
 }
+
+const char* moe_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
 
 int64_t moe_launch_count(void) { return (int64_t)g_launches.load(std::memory_order_relaxed); }
 

@@ -16,20 +16,23 @@
 //
 // GEMM structure (one CTA per SM, persistent over tiles):
 //   D^T[channel][token] = W[channel][:] . X[token][:]
-//   A operand = weights (128 channel rows): TMA loads int8 tiles into shared
-//     memory; a converter warpgroup turns them into fp16 and stores them in
-//     tensor memory (A-from-TMEM form of tcgen05.mma), so the converted
-//     weights cost no shared-memory bandwidth;
-//   B operand = activations (up to 128 tokens, fp16, K-major, 128B swizzle),
-//     TMA-loaded into shared memory;
-//   D = two 128x128 fp32 accumulators in TMEM (double-buffered across the
-//     1024-K chunks) plus 128 columns of int32 running sums.
-// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
-// warps 2-5 converter / chunk drain / epilogue (one TMEM lane quarter each).
-// The MMA N is the tile's token count rounded up to 16, so small experts do
-// not pay for padding.  Every mbarrier wait is bounded (2 s): on a timeout
-// the kernel records MOE_ERR_TIMEOUT in the workspace status word, waits
-// briefly for its own copies in flight, frees TMEM and returns.
+//   A operand = weights, 128 channel rows per tile: TMA loads int8 tiles into
+//     shared memory; a converter warpgroup turns them into fp16 and stores
+//     them in tensor memory (the A-from-TMEM form of tcgen05.mma), so the
+//     converted weights cost no shared-memory bandwidth;
+//   B operand = activations, up to 256 tokens per tile (fp16, K-major, 128B
+//     swizzle), TMA-loaded in 32-row boxes so that small experts only load
+//     the rows they have; the MMA N is the tile's token count rounded up to 16.
+//   TMEM (512 columns): one 256-column fp32 accumulator, 128 columns of int32
+//     running sums (token columns 0..127; the sums of columns 128..255 live in
+//     registers of the drain warpgroup), and four 32-column A slots.
+// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5
+// converter, warps 6-9 drain (every 1024 K) and epilogue.  Each warpgroup
+// covers the four TMEM lane quarters.  A single 256-wide MMA per 16 K
+// reaches the tensor pipe's full rate, which 128-wide MMAs do not.
+// Every mbarrier wait is bounded (2 s): on a timeout the kernel records
+// MOE_ERR_TIMEOUT in the workspace status word, waits briefly for its own
+// copies in flight, frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -41,24 +44,24 @@
 namespace moe {
 namespace tc {
 
-constexpr int BN = 128;                          // tokens per tile
+constexpr int BN = 256;                          // tokens per tile
 constexpr int BK = 64;                           // K per stage
-constexpr int NS = 8;                            // shared-memory stages
+constexpr int NS = 5;                            // shared-memory stages
 constexpr int NA = 4;                            // TMEM A slots
 constexpr int CK = 16;                           // stages per exact chunk (1024 K)
-constexpr int B_BYTES = BN * BK * 2;             // fp16 activations per stage
-constexpr int A_BYTES = 128 * BK;                // int8 weights per stage
-constexpr int STAGE_BYTES = B_BYTES + A_BYTES;   // 24 KB
-constexpr int XLD = 33;                          // exchange row pitch (floats)
-constexpr int XCH_BYTES = 128 * XLD * 4;
-constexpr int NBARS = 2 * NS + 2 * NA + 4 + 2;
+constexpr int BOX_ROWS = 32;                     // token rows per activation TMA box
+constexpr int BOX_BYTES = BOX_ROWS * BK * 2;     // 4 KB
+constexpr int B_BYTES = BN * BK * 2;             // 32 KB fp16 activations per stage
+constexpr int A_BYTES = 128 * BK;                // 8 KB int8 weights per stage
+constexpr int STAGE_BYTES = B_BYTES + A_BYTES;   // 40 KB
+constexpr int NBARS = 2 * NS + 2 * NA + 2 + 1;
 constexpr uint32_t TM_ACC = 0, TM_SUM = 256, TM_A = 384, TM_COLS = 512;
-constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = NS * STAGE_BYTES + XCH_BYTES + NBARS * 8 + 16 + 1024;
+constexpr int THREADS = 320;                     // producer, MMA, converter WG, drain WG
+constexpr int SMEM_BYTES = NS * STAGE_BYTES + NBARS * 8 + 16 + 1024;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 20000000ull;
 
-enum { EPI_I32 = 0, EPI_SWIGLU = 1, EPI_DOWN_F32 = 2, EPI_DOWN_BF16 = 3 };
+enum { EPI_I32 = 0, EPI_GU = 1, EPI_F32 = 2, EPI_BF16MSG = 3 };
 
 struct Params {
     int G;
@@ -67,15 +70,14 @@ struct Params {
     const int32_t* g2s;          // nullable: weight set of each group
     int K;                       // reduction length, multiple of 64
     int rows_per_set;            // weight rows per set
-    int nout;                    // output channels (h channels for SwiGLU)
+    int nout;                    // output channels per set (EPI_GU: I)
     int mb_count;                // channel blocks per token tile
     int box1_off;                // row offset of the second 64-row weight box
     const float* s_row;          // per token-row scale
     const float* s_ch;           // per-channel weight scales [set][rows_per_set]
     int32_t* c_i32;              // EPI_I32: [M][nout]
-    float* out_f32;              // EPI_SWIGLU: h [M][nout]; EPI_DOWN_F32: y [M][nout]
-    unsigned* rowmax;            // per token-row absmax (float bits)
-    const int32_t* expert_rows;  // EPI_DOWN_BF16: row -> dispatch slot
+    float* out_f32;              // EPI_GU: [M][2I] (gate | up); EPI_F32: [M][nout]
+    const int32_t* expert_rows;  // EPI_BF16MSG: row -> dispatch slot
     const moe_dispatch_meta* meta;
     unsigned char* cbuf;
     long long crow;
@@ -106,20 +108,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* er
     return __all_sync(0xffffffffu, ok);
 }
 
-// Bounded barrier of the four converter warps (an mbarrier with count 4
-// instead of bar.sync, so that a warp that gave up cannot hang the others).
-struct WgBarrier {
-    uint32_t addr;
-    uint32_t phase;
-    __device__ __forceinline__ bool sync(int lane, int* err) {
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(addr);
-        const bool ok = warp_wait(addr, phase & 1, err);
-        ++phase;
-        return ok;
-    }
-};
-
 // Wait without regard to the error word, with a short limit (used only to
 // let copies already in flight land before the CTA exits).
 __device__ __forceinline__ void mbar_wait_quiet(uint32_t bar, uint32_t parity, uint64_t limit) {
@@ -130,84 +118,61 @@ __device__ __forceinline__ void mbar_wait_quiet(uint32_t bar, uint32_t parity, u
 
 // Epilogue for one 32-token slice of a finished tile.  `row` is this
 // thread's TMEM lane (weight channel within the tile), iv[j] the exact int32
-// result for token j0 + j.
+// result for token j0 + j.  Per-token values are loaded once per lane and
+// broadcast with shuffles.
 template <int EPI>
-__device__ __forceinline__ bool epilogue_slice(const Params& P, const TileInfo& ti, int row,
-                                               int j0, const int (&iv)[32], float* xch,
-                                               WgBarrier& wg, int lane) {
+__device__ __forceinline__ void epilogue_slice(const Params& P, const TileInfo& ti, int row,
+                                               int lane, int j0, const int (&iv)[32]) {
+    const bool lane_ok = j0 + lane < ti.nvalid;
     if constexpr (EPI == EPI_I32) {
         const int ch = ti.mb * 128 + row;
         if (ch < P.nout) {
-#pragma unroll 4
+#pragma unroll
             for (int j = 0; j < 32; ++j)
                 if (j0 + j < ti.nvalid) P.c_i32[(long long)(ti.r0 + j0 + j) * P.nout + ch] = iv[j];
         }
-    } else if constexpr (EPI == EPI_SWIGLU) {
-        // rows 0..63: gate of channel i, rows 64..127: up of channel i
-        const int i = ti.mb * 64 + (row & 63);
-        const float* sc = P.s_ch + (long long)ti.set * P.rows_per_set;
-        if (row >= 64) {
-            const float su = sc[P.nout + i];
-#pragma unroll 4
-            for (int j = 0; j < 32; ++j) {
-                const float st = (j0 + j < ti.nvalid) ? P.s_row[ti.r0 + j0 + j] : 0.f;
-                xch[(row - 64) * XLD + j] = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), st), su);
-            }
+    } else if constexpr (EPI == EPI_GU || EPI == EPI_F32) {
+        // EPI_GU: rows 0..63 are gate channels mb*64 + row, rows 64..127 the
+        // matching up channels (stored at I + channel); both scaled outputs go
+        // to a [M][2I] buffer.  EPI_F32: channel mb*128 + row of [M][nout].
+        int col, ld;
+        if constexpr (EPI == EPI_GU) {
+            col = (row < 64) ? ti.mb * 64 + row : P.nout + ti.mb * 64 + (row - 64);
+            ld = 2 * P.nout;
+        } else {
+            col = ti.mb * 128 + row;
+            ld = P.nout;
         }
-        if (!wg.sync(lane, P.err)) return false;
-        if (row < 64) {
-            const float sg = sc[i];
-#pragma unroll 4
-            for (int j = 0; j < 32; ++j) {
-                const bool ok = j0 + j < ti.nvalid;
-                const float st = ok ? P.s_row[ti.r0 + j0 + j] : 0.f;
-                const float g = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), st), sg);
-                const float h = __fmul_rn(silu_spec(g), xch[row * XLD + j]);
-                if (ok) P.out_f32[(long long)(ti.r0 + j0 + j) * P.nout + i] = h;
-                xch[row * XLD + j] = ok ? fabsf(h) : 0.f;
-            }
+        const bool chok = (EPI == EPI_GU) || col < P.nout;
+        const float sc = chok ? P.s_ch[(long long)ti.set * P.rows_per_set + col] : 0.f;
+        const float sr_l = lane_ok ? P.s_row[ti.r0 + j0 + lane] : 0.f;
+        float* out = P.out_f32 + (long long)ti.r0 * ld + col;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float sr = __shfl_sync(0xffffffffu, sr_l, j);
+            const float v = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sc);
+            if (chok && j0 + j < ti.nvalid) out[(long long)(j0 + j) * ld] = v;
         }
-        if (!wg.sync(lane, P.err)) return false;
-        if (row < 32 && j0 + row < ti.nvalid) {
-            float m = 0.f;
-            for (int L = 0; L < 64; ++L) m = fmaxf(m, xch[L * XLD + row]);
-            atomicMax(&P.rowmax[ti.r0 + j0 + row], __float_as_uint(m));
-        }
-        if (!wg.sync(lane, P.err)) return false;
-    } else {
+    } else {  // EPI_BF16MSG: the return message is bf16(y), written in place
         const int ch = ti.mb * 128 + row;
         const bool chok = ch < P.nout;
         const float sd = chok ? P.s_ch[(long long)ti.set * P.rows_per_set + ch] : 0.f;
-        if constexpr (EPI == EPI_DOWN_F32) {
-#pragma unroll 4
-            for (int j = 0; j < 32; ++j) {
-                const bool ok = chok && (j0 + j < ti.nvalid);
-                const float sr = (j0 + j < ti.nvalid) ? P.s_row[ti.r0 + j0 + j] : 0.f;
-                const float y = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sd);
-                if (ok) P.out_f32[(long long)(ti.r0 + j0 + j) * P.nout + ch] = y;
-                xch[row * XLD + j] = ok ? fabsf(y) : 0.f;
-            }
-            if (!wg.sync(lane, P.err)) return false;
-            if (row < 32 && j0 + row < ti.nvalid) {
-                float m = 0.f;
-                for (int L = 0; L < 128; ++L) m = fmaxf(m, xch[L * XLD + row]);
-                atomicMax(&P.rowmax[ti.r0 + j0 + row], __float_as_uint(m));
-            }
-            if (!wg.sync(lane, P.err)) return false;
-        } else {  // EPI_DOWN_BF16: the return message is bf16(y), written in place
-#pragma unroll 2
-            for (int j = 0; j < 32; ++j) {
-                if (j0 + j >= ti.nvalid) break;
-                const int r = ti.r0 + j0 + j;
-                const moe_dispatch_meta m = P.meta[P.expert_rows[r]];
-                const long long tj = ((long long)m.src_rank * P.lb + m.batch_slot) * P.k + m.route_slot;
-                const float y = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), P.s_row[r]), sd);
-                if (chok)
-                    reinterpret_cast<__nv_bfloat16*>(P.cbuf + tj * P.crow)[ch] = __float2bfloat16_rn(y);
-            }
+        const float sr_l = lane_ok ? P.s_row[ti.r0 + j0 + lane] : 0.f;
+        int tj_l = 0;
+        if (lane_ok) {
+            const moe_dispatch_meta m = P.meta[P.expert_rows[ti.r0 + j0 + lane]];
+            tj_l = (m.src_rank * P.lb + m.batch_slot) * P.k + m.route_slot;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float sr = __shfl_sync(0xffffffffu, sr_l, j);
+            const int tj = __shfl_sync(0xffffffffu, tj_l, j);
+            const float y = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sd);
+            if (chok && j0 + j < ti.nvalid)
+                reinterpret_cast<__nv_bfloat16*>(P.cbuf + (long long)tj * P.crow)[ch] =
+                    __float2bfloat16_rn(y);
         }
     }
-    return true;
 }
 
 template <int EPI>
@@ -218,8 +183,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = smem;
-    float* xch = reinterpret_cast<float*>(smem + NS * STAGE_BYTES);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE_BYTES + XCH_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -228,10 +192,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     auto empty = [&](int s) { return bar(NS + s); };
     auto afull = [&](int a) { return bar(2 * NS + a); };
     auto aempty = [&](int a) { return bar(2 * NS + NA + a); };
-    auto accfull = [&](int b) { return bar(2 * NS + 2 * NA + b); };
-    auto accempty = [&](int b) { return bar(2 * NS + 2 * NA + 2 + b); };
-    const uint32_t done_bar = bar(2 * NS + 2 * NA + 4);
-    const uint32_t wg_bar = bar(2 * NS + 2 * NA + 5);
+    const uint32_t accfull = bar(2 * NS + 2 * NA);
+    const uint32_t accempty = bar(2 * NS + 2 * NA + 1);
+    const uint32_t done_bar = bar(2 * NS + 2 * NA + 2);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -242,12 +205,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             ptx::mbar_init(afull(a), 4);
             ptx::mbar_init(aempty(a), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(accfull(b), 1);
-            ptx::mbar_init(accempty(b), 4);
-        }
+        ptx::mbar_init(accfull, 1);
+        ptx::mbar_init(accempty, 4);
         ptx::mbar_init(done_bar, 1);
-        ptx::mbar_init(wg_bar, 4);
         ptx::fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -274,8 +234,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
                 const TileInfo ti = decode(P, tile);
-                const int yw0 = ti.set * P.rows_per_set + (EPI == EPI_SWIGLU ? ti.mb * 64 : ti.mb * 128);
+                const int yw0 = ti.set * P.rows_per_set + (EPI == EPI_GU ? ti.mb * 64 : ti.mb * 128);
                 const int yw1 = yw0 + P.box1_off;
+                const int nb = (ti.nmma + BOX_ROWS - 1) / BOX_ROWS;
+                const uint32_t bytes = A_BYTES + nb * BOX_BYTES;
                 for (int ks = 0; ks < KS; ++ks) {
                     const int s = g % NS;
                     if (!ptx::mbar_wait(empty(s), ((g / NS) & 1) ^ 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
@@ -283,10 +245,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                         break;
                     }
                     const uint32_t st = ptx::smem_addr(stages + s * STAGE_BYTES);
-                    ptx::mbar_expect_tx(full(s), STAGE_BYTES);
-                    ptx::tma_load_2d(st, &tmX, ks * BK, ti.r0, full(s));
+                    ptx::mbar_expect_tx(full(s), bytes);
                     ptx::tma_load_2d(st + B_BYTES, &tmW, ks * BK, yw0, full(s));
                     ptx::tma_load_2d(st + B_BYTES + 4096, &tmW, ks * BK, yw1, full(s));
+                    for (int j = 0; j < nb; ++j)
+                        ptx::tma_load_2d(st + j * BOX_BYTES, &tmX, ks * BK, ti.r0 + j * BOX_ROWS, full(s));
                     ++g;
                 }
             }
@@ -306,9 +269,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 for (int ks = 0; ks < KS; ++ks) {
                     const bool first = (ks % CK) == 0;
                     const bool last = (ks % CK) == CK - 1 || ks == KS - 1;
-                    const uint32_t b = q & 1;
                     if (first) {
-                        if (!ptx::mbar_wait(accempty(b), ((q >> 1) & 1) ^ 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
+                        // the drain must have taken the previous chunk out of TMEM
+                        if (!ptx::mbar_wait(accempty, (q & 1) ^ 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
                             ok = false;
                             break;
                         }
@@ -321,16 +284,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     }
                     ptx::tc_fence_after();
                     const uint32_t bbase = ptx::smem_addr(stages + s * STAGE_BYTES);
-                    const uint32_t d = tmem + TM_ACC + b * 128;
                     const uint32_t abase = tmem + TM_A + a * 32;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        ptx::mma_f16_ts(d, abase + kk * 8, ptx::sdesc_k_sw128(bbase + kk * 32), idesc,
-                                        (first && kk == 0) ? 0u : 1u);
+                        ptx::mma_f16_ts(tmem + TM_ACC, abase + kk * 8, ptx::sdesc_k_sw128(bbase + kk * 32),
+                                        idesc, (first && kk == 0) ? 0u : 1u);
                     ptx::tc_commit(empty(s));
                     ptx::tc_commit(aempty(a));
                     if (last) {
-                        ptx::tc_commit(accfull(b));
+                        ptx::tc_commit(accfull);
                         ++q;
                     }
                     ++g;
@@ -340,52 +302,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             ptx::tc_commit(done_bar);
             mbar_wait_quiet(done_bar, 0, WAIT_NS);
         }
-    } else {
-        // ------------------------- converter / chunk drain / epilogue
+    } else if (warp < 6) {
+        // ------------------------------------------------------- converter
         const int wq = warp & 3;
         const int row = wq * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-        uint32_t g = 0, q = 0;
+        const uint8_t* arow_base = stages + B_BYTES + (row >> 6) * 4096 + (row & 63) * 64;
+        const int sw = (row >> 1) & 3;
+        uint32_t g = 0;
         bool ok = true;
-        WgBarrier wg{wg_bar, 0};
         for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-            const TileInfo ti = decode(P, tile);
-            const int nsl = (ti.nmma + 31) / 32;
-
-            auto drain = [&](int c, bool final_chunk) -> bool {
-                const uint32_t b = q & 1;
-                if (!warp_wait(accfull(b), (q >> 1) & 1, P.err)) return false;
-                ptx::tc_fence_after();
-                const uint32_t accb = tmem + lane_base + TM_ACC + b * 128;
-                const uint32_t sumb = tmem + lane_base + TM_SUM;
-                for (int sl = 0; sl < nsl; ++sl) {
-                    uint32_t v[32], sv[32];
-                    ptx::tmem_ld32(accb + sl * 32, v);
-                    if (c > 0) ptx::tmem_ld32(sumb + sl * 32, sv);
-                    ptx::tmem_wait_ld();
-                    int iv[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        iv[j] = __float2int_rn(__uint_as_float(v[j])) + (c > 0 ? static_cast<int>(sv[j]) : 0);
-                    if (!final_chunk) {
-                        uint32_t w[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) w[j] = static_cast<uint32_t>(iv[j]);
-                        ptx::tmem_st32(sumb + sl * 32, w);
-                    } else if (!epilogue_slice<EPI>(P, ti, row, sl * 32, iv, xch, wg, lane)) {
-                        return false;
-                    }
-                }
-                if (!final_chunk) ptx::tmem_wait_st();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(accempty(b));
-                ++q;
-                return true;
-            };
-
-            int next_drain = 0;
-            for (int ks = 0; ks < KS; ++ks) {
+            for (int ks = 0; ks < KS; ++ks, ++g) {
                 const int s = g % NS, a = g % NA;
                 if (!warp_wait(full(s), (g / NS) & 1, P.err) ||
                     !warp_wait(aempty(a), ((g / NA) & 1) ^ 1, P.err)) {
@@ -393,35 +320,99 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     break;
                 }
                 ptx::tc_fence_after();
-                // this thread's weight row: 64 int8 in 64-byte swizzled rows
-                const uint8_t* arow = stages + s * STAGE_BYTES + B_BYTES + (row >> 6) * 4096 + (row & 63) * 64;
-                const int sw = (row >> 1) & 3;
+                // this thread's weight row: 64 int8 in 64-byte rows, 64B swizzle
+                const uint8_t* arow = arow_base + s * STAGE_BYTES;
+                uint4 w[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ sw) << 4));
                 uint32_t v[32];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(arow + ((c ^ sw) << 4));
-                    s8x4_to_f16x4(w.x, v[8 * c + 0], v[8 * c + 1]);
-                    s8x4_to_f16x4(w.y, v[8 * c + 2], v[8 * c + 3]);
-                    s8x4_to_f16x4(w.z, v[8 * c + 4], v[8 * c + 5]);
-                    s8x4_to_f16x4(w.w, v[8 * c + 6], v[8 * c + 7]);
+                    s8x4_to_f16x4(w[c].x, v[8 * c + 0], v[8 * c + 1]);
+                    s8x4_to_f16x4(w[c].y, v[8 * c + 2], v[8 * c + 3]);
+                    s8x4_to_f16x4(w[c].z, v[8 * c + 4], v[8 * c + 5]);
+                    s8x4_to_f16x4(w[c].w, v[8 * c + 6], v[8 * c + 7]);
                 }
                 ptx::tmem_st32(tmem + lane_base + TM_A + a * 32, v);
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(afull(a));
-                ++g;
-                if (next_drain < nchunks - 1 && ks == (next_drain + 1) * CK + NA - 1) {
-                    if (!drain(next_drain, false)) {
-                        ok = false;
-                        break;
-                    }
-                    ++next_drain;
-                }
             }
-            while (ok && next_drain < nchunks) {
-                if (!drain(next_drain, next_drain == nchunks - 1)) ok = false;
-                ++next_drain;
+        }
+    } else {
+        // ------------------------------------- chunk drain and epilogue
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t accb = tmem + lane_base + TM_ACC;
+        const uint32_t sumb = tmem + lane_base + TM_SUM;
+        int rs[128];  // int32 running sums of token columns 128..255
+        uint32_t q = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+            const TileInfo ti = decode(P, tile);
+            const int nsl = (ti.nmma + 31) / 32;
+            for (int c = 0; c < nchunks; ++c) {
+                if (!warp_wait(accfull, q & 1, P.err)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                // columns 0..127: running sums in TMEM
+#pragma unroll
+                for (int sl = 0; sl < 4; ++sl) {
+                    if (sl < nsl) {
+                        uint32_t v[32], sv[32];
+                        ptx::tmem_ld32(accb + sl * 32, v);
+                        if (c > 0) ptx::tmem_ld32(sumb + sl * 32, sv);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            v[j] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[j])) +
+                                                         (c > 0 ? static_cast<int>(sv[j]) : 0));
+                        ptx::tmem_st32(sumb + sl * 32, v);
+                    }
+                }
+                // columns 128..255: running sums in registers
+#pragma unroll
+                for (int sl = 4; sl < 8; ++sl) {
+                    if (sl < nsl) {
+                        uint32_t v[32];
+                        ptx::tmem_ld32(accb + sl * 32, v);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int x = __float2int_rn(__uint_as_float(v[j]));
+                            rs[(sl - 4) * 32 + j] = (c > 0) ? rs[(sl - 4) * 32 + j] + x : x;
+                        }
+                    }
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(accempty);  // the MMA may overwrite the accumulator
+                ++q;
+                if (c == nchunks - 1) {
+                    // epilogue from the final sums, overlapping the next tile's MMAs
+#pragma unroll
+                    for (int sl = 0; sl < 8; ++sl) {
+                        if (sl < nsl) {
+                            int iv[32];
+                            if (sl < 4) {
+                                uint32_t v[32];
+                                ptx::tmem_ld32(sumb + sl * 32, v);
+                                ptx::tmem_wait_ld();
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) iv[j] = static_cast<int>(v[j]);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) iv[j] = rs[(sl - 4) * 32 + j];
+                            }
+                            epilogue_slice<EPI>(P, ti, row, lane, sl * 32, iv);
+                        }
+                    }
+                }
             }
         }
     }
@@ -457,42 +448,59 @@ assemble_kernel(int K, const int32_t* __restrict__ row_index, const int8_t* __re
     if (meta && threadIdx.x == 0) s_row[r] = meta[g].scale;
 }
 
-// Token-wise requantisation of the SwiGLU output h (absmax already reduced
-// into rowmax): hq as exact fp16 integers, s_h per row.
+template <int NT>
+__device__ __forceinline__ float block_max(float v, float* s_red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = s_red[0];
+#pragma unroll
+    for (int i = 1; i < NT / 32; ++i) r = fmaxf(r, s_red[i]);
+    __syncthreads();
+    return r;
+}
+
+// SwiGLU of one expert row (g | u from the gate/up GEMM) and its token-wise
+// requantisation: hq as exact fp16 integers, s_h per row.
 __global__ void __launch_bounds__(256)
-requant_kernel(int I, const float* __restrict__ h, const unsigned* __restrict__ rowmax,
-               __half* __restrict__ hq, float* __restrict__ sh) {
+swiglu_requant_kernel(int I, const float* __restrict__ gu, __half* __restrict__ hq,
+                      float* __restrict__ sh) {
+    extern __shared__ float s_h[];
+    __shared__ float s_red[8];
     const int r = blockIdx.x;
-    const float s = row_scale(__uint_as_float(rowmax[r]));
-    const float4* src = reinterpret_cast<const float4*>(h + (long long)r * I);
-    uint2* dst = reinterpret_cast<uint2*>(hq + (long long)r * I);
-    for (int c = threadIdx.x; c < I / 4; c += blockDim.x) {
-        const float4 v = src[c];
-        int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-        if (s != 0.f) {
-            q0 = quant1(v.x, s); q1 = quant1(v.y, s); q2 = quant1(v.z, s); q3 = quant1(v.w, s);
-        }
-        __half2 a = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
-        __half2 b = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
-        uint2 o;
-        o.x = *reinterpret_cast<uint32_t*>(&a);
-        o.y = *reinterpret_cast<uint32_t*>(&b);
-        dst[c] = o;
+    const float* g = gu + (long long)r * 2 * I;
+    float amax = 0.f;
+    for (int i = threadIdx.x; i < I; i += blockDim.x) {
+        const float h = __fmul_rn(silu_spec(g[i]), g[I + i]);
+        s_h[i] = h;
+        amax = fmaxf(amax, fabsf(h));
     }
+    amax = block_max<256>(amax, s_red);
+    const float s = row_scale(amax);
+    __half* out = hq + (long long)r * I;
+    for (int i = threadIdx.x; i < I; i += blockDim.x)
+        out[i] = __int2half_rn(s == 0.f ? 0 : quant1(s_h[i], s));
     if (threadIdx.x == 0) sh[r] = s;
 }
 
 // INT8 return message: token-wise codes of y into the combine row (t, j).
 __global__ void __launch_bounds__(256)
 retquant_kernel(int H, int k, int lb, long long crow, const float* __restrict__ y,
-                const unsigned* __restrict__ rowmax, const int32_t* __restrict__ expert_rows,
-                const moe_dispatch_meta* __restrict__ meta, unsigned char* __restrict__ cbuf,
-                float* __restrict__ cscale) {
+                const int32_t* __restrict__ expert_rows, const moe_dispatch_meta* __restrict__ meta,
+                unsigned char* __restrict__ cbuf, float* __restrict__ cscale) {
+    __shared__ float s_red[8];
     const int r = blockIdx.x;
     const moe_dispatch_meta m = meta[expert_rows[r]];
     const long long tj = ((long long)m.src_rank * lb + m.batch_slot) * k + m.route_slot;
-    const float s = row_scale(__uint_as_float(rowmax[r]));
     const float4* src = reinterpret_cast<const float4*>(y + (long long)r * H);
+    float amax = 0.f;
+    for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
+        const float4 v = src[c];
+        amax = fmaxf(fmaxf(amax, fabsf(v.x)), fmaxf(fabsf(v.y), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    amax = block_max<256>(amax, s_red);
+    const float s = row_scale(amax);
     uint32_t* dst = reinterpret_cast<uint32_t*>(cbuf + tj * crow);
     for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
         const float4 v = src[c];
@@ -561,6 +569,15 @@ cudaError_t launch_gemm(const Params& P, const CUtensorMap& w, const CUtensorMap
     return cudaGetLastError();
 }
 
+bool weight_map(CUtensorMap* m, const int8_t* w, int K, uint64_t rows) {
+    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, K, rows, BK, 64, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+bool act_map(CUtensorMap* m, const __half* x, int K, uint64_t rows) {
+    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, rows, BK, BOX_ROWS,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 }  // namespace tc
 
 // Exact grouped int8 GEMM with int32 output on the tensor-core path.
@@ -581,10 +598,7 @@ cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long lo
     assemble_kernel<<<(unsigned)max_rows, 128, 0, st>>>(K, row_index, A, lda, nullptr, a16, nullptr);
     count_launches(1);
     CUtensorMap mw, mx;
-    if (!make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, (uint64_t)n_groups * N, 64, 64,
-                  CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a16, K, (uint64_t)max_rows, 64, BN,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!weight_map(&mw, B, K, (uint64_t)n_groups * N) || !act_map(&mx, a16, K, (uint64_t)max_rows))
         return cudaErrorInvalidValue;
     Params P = {};
     P.G = n_groups; P.offsets = offsets; P.tile_prefix = tp; P.g2s = nullptr;
@@ -592,8 +606,6 @@ cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long lo
     P.c_i32 = C; P.err = err;
     return launch_gemm<EPI_I32>(P, mw, mx, st);
 }
-
-bool ffn_tc_eligible(const Dims& d) { return d.H % 64 == 0 && d.I % 64 == 0; }
 
 cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                           const int32_t* expert_offsets, const int32_t* expert_rows,
@@ -605,12 +617,10 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
         reinterpret_cast<const moe_dispatch_meta*>(static_cast<const char*>(dbuf) + meta_off);
     int* err = ws_ptr<int>(ws, 0);
     int32_t* tp = ws_ptr<int32_t>(ws, wl.tiles);
-    unsigned* hmax = ws_ptr<unsigned>(ws, wl.rowmax);
-    unsigned* ymax = hmax + M;
     float* s_row = ws_ptr<float>(ws, wl.s_row);
     float* sh = ws_ptr<float>(ws, wl.sh);
     __half* a16 = ws_ptr<__half>(ws, wl.a16);
-    float* hbuf = ws_ptr<float>(ws, wl.hbuf);
+    float* gu = ws_ptr<float>(ws, wl.gu);
     __half* hq16 = ws_ptr<__half>(ws, wl.hq16);
     float* ybuf = ws_ptr<float>(ws, wl.ybuf);
     unsigned char* cb = static_cast<unsigned char*>(cbuf);
@@ -619,31 +629,30 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     cudaError_t e;
 
     if ((e = cudaMemsetAsync(err, 0, 256, st)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(hmax, 0, sizeof(unsigned) * 2 * M, st)) != cudaSuccess) return e;
-    count_launches(2);
+    count_launches(1);
     if ((e = launch_tile_prefix(d.E_phys, BN, expert_offsets, tp, st)) != cudaSuccess) return e;
     assemble_kernel<<<(unsigned)M, 128, 0, st>>>(d.H, expert_rows, static_cast<const int8_t*>(dbuf),
                                                  d.drow, meta, a16, s_row);
     count_launches(1);
 
     CUtensorMap mwgu, mx1, mwd, mx2;
-    if (!make_map(&mwgu, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w.w_gate_up, d.H, (uint64_t)E_w * 2 * d.I,
-                  64, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&mx1, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a16, d.H, (uint64_t)M, 64, BN,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mwd, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w.w_down, d.I, (uint64_t)E_w * d.H, 64, 64,
-                  CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&mx2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hq16, d.I, (uint64_t)M, 64, BN,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!weight_map(&mwgu, w.w_gate_up, d.H, (uint64_t)E_w * 2 * d.I) ||
+        !act_map(&mx1, a16, d.H, (uint64_t)M) ||
+        !weight_map(&mwd, w.w_down, d.I, (uint64_t)E_w * d.H) ||
+        !act_map(&mx2, hq16, d.I, (uint64_t)M))
         return cudaErrorInvalidValue;
 
     Params P1 = {};
     P1.G = d.E_phys; P1.offsets = expert_offsets; P1.tile_prefix = tp; P1.g2s = w.phys_to_weight;
     P1.K = d.H; P1.rows_per_set = 2 * d.I; P1.nout = d.I; P1.mb_count = d.I / 64; P1.box1_off = d.I;
-    P1.s_row = s_row; P1.s_ch = w.s_gate_up; P1.out_f32 = hbuf; P1.rowmax = hmax; P1.err = err;
-    if ((e = launch_gemm<EPI_SWIGLU>(P1, mwgu, mx1, st)) != cudaSuccess) return e;
+    P1.s_row = s_row; P1.s_ch = w.s_gate_up; P1.out_f32 = gu; P1.err = err;
+    if ((e = launch_gemm<EPI_GU>(P1, mwgu, mx1, st)) != cudaSuccess) return e;
 
-    requant_kernel<<<(unsigned)M, 256, 0, st>>>(d.I, hbuf, hmax, hq16, sh);
+    if (sizeof(float) * d.I > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(swiglu_requant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)(sizeof(float) * d.I))) != cudaSuccess)
+        return e;
+    swiglu_requant_kernel<<<(unsigned)M, 256, sizeof(float) * d.I, st>>>(d.I, gu, hq16, sh);
     count_launches(1);
 
     Params P2 = {};
@@ -651,14 +660,14 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     P2.K = d.I; P2.rows_per_set = d.H; P2.nout = d.H; P2.mb_count = (d.H + 127) / 128; P2.box1_off = 64;
     P2.s_row = sh; P2.s_ch = w.s_down; P2.err = err;
     if (int8_ret) {
-        P2.out_f32 = ybuf; P2.rowmax = ymax;
-        if ((e = launch_gemm<EPI_DOWN_F32>(P2, mwd, mx2, st)) != cudaSuccess) return e;
-        retquant_kernel<<<(unsigned)M, 256, 0, st>>>(d.H, d.k, d.lb, d.crow, ybuf, ymax, expert_rows,
-                                                     meta, cb, reinterpret_cast<float*>(cb + scale_off));
+        P2.out_f32 = ybuf;
+        if ((e = launch_gemm<EPI_F32>(P2, mwd, mx2, st)) != cudaSuccess) return e;
+        retquant_kernel<<<(unsigned)M, 256, 0, st>>>(d.H, d.k, d.lb, d.crow, ybuf, expert_rows, meta,
+                                                     cb, reinterpret_cast<float*>(cb + scale_off));
         count_launches(1);
     } else {
         P2.expert_rows = expert_rows; P2.meta = meta; P2.cbuf = cb; P2.crow = d.crow; P2.k = d.k; P2.lb = d.lb;
-        if ((e = launch_gemm<EPI_DOWN_BF16>(P2, mwd, mx2, st)) != cudaSuccess) return e;
+        if ((e = launch_gemm<EPI_BF16MSG>(P2, mwd, mx2, st)) != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

@@ -51,10 +51,9 @@ struct WsLayout {
     long long hq;          // int8  [T*k][I]
     long long acc_d;       // int32 [T*k][H]
     // tensor-core expert FFN
-    long long rowmax;      // u32   [2][T*k]  absmax of h and of y (float bits)
     long long s_row;       // f32   [T*k]     dispatch scale of each expert row
     long long a16;         // fp16  [T*k][H]  expert input rows
-    long long hbuf;        // f32   [T*k][I]  SwiGLU output
+    long long gu;          // f32   [T*k][2I] gate | up projections
     long long hq16;        // fp16  [T*k][I]  requantised SwiGLU output
     long long ybuf;        // f32   [T*k][H]  expert output (INT8 return messages only)
     long long total;
@@ -73,10 +72,9 @@ inline WsLayout make_ws(const Dims& d) {
     w.sh = o;         o = align_up(o + 4 * tk, 256);
     w.tc = ffn_uses_tc(d);
     if (w.tc) {
-        w.rowmax = o; o = align_up(o + 8 * tk, 256);
         w.s_row = o;  o = align_up(o + 4 * tk, 256);
         w.a16 = o;    o = align_up(o + 2 * tk * d.H, 256);
-        w.hbuf = o;   o = align_up(o + 4 * tk * d.I, 256);
+        w.gu = o;     o = align_up(o + 8 * tk * d.I, 256);
         w.hq16 = o;   o = align_up(o + 2 * tk * d.I, 256);
         if (d.cfmt == MOE_MSG_INT8) { w.ybuf = o; o = align_up(o + 4 * tk * d.H, 256); }
     } else {

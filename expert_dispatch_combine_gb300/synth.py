@@ -74,6 +74,9 @@ WORKLOADS = {
     "c2_decode_zipf": Workload("c2_decode_zipf", 12288, 7168, 256, 256, 8, 2048, 32, 32, 2, zipf=1.1),
     "c3_eplb": Workload("c3_eplb", 4608, 7168, 256, 288, 8, 2048, 32, 32, 3, zipf=1.2, eplb=True),
     "c4_prefill": Workload("c4_prefill", 16384, 7168, 256, 256, 8, 2048, 32, 32, 4),
+    # profiling case: the DeepSeek-V3 expert shape with 32 experts (1.4 GB of
+    # weights, about 3.5 GB on the device in total) and 1024 rows per expert
+    "prof_e32": Workload("prof_e32", 4096, 7168, 32, 32, 8, 2048, 32, 32, 5),
 }
 
 

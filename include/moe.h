@@ -280,6 +280,10 @@ moe_status moe_grouped_gemm_s8(int32_t n_groups, const int32_t* offsets, int64_t
  * moe_grouped_gemm_s8 call that used this workspace.  Synchronises `stream`. */
 moe_status moe_device_status(const void* workspace, int32_t* status, moe_stream_t stream);
 
+/* Text of the CUDA error behind the last MOE_ERR_CUDA returned on the
+ * calling host thread ("no error" if there was none).  Host only. */
+const char* moe_last_cuda_error(void);
+
 /* Number of GPU operations (kernel launches and memsets) the library has
  * enqueued in this process since it was loaded.  Host only, thread-safe. */
 int64_t moe_launch_count(void);
