@@ -23,9 +23,11 @@
 //   B operand = activations, up to 256 tokens per tile (fp16, K-major, 128B
 //     swizzle), TMA-loaded in 32-row boxes so that small experts only load
 //     the rows they have; the MMA N is the tile's token count rounded up to 16.
-//   TMEM (512 columns): one 256-column fp32 accumulator, 128 columns of int32
-//     running sums (token columns 0..127; the sums of columns 128..255 live in
-//     registers of the drain warpgroup), and four 32-column A slots.
+//   TMEM (512 columns): one 256-column fp32 accumulator, 160 columns of int32
+//     running sums (token columns 0..159; the sums of columns 160..255 live in
+//     registers of the drain warpgroup), and three 32-column A slots.
+//   Epilogue: each 32-token slice is scaled, staged in shared memory and
+//     written with one TMA tensor store (partial slices use plain stores).
 // Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5
 // converter, warps 6-9 drain (every 1024 K) and epilogue.  Each warpgroup
 // covers the four TMEM lane quarters.  A single 256-wide MMA per 16 K
@@ -47,17 +49,21 @@ namespace tc {
 constexpr int BN = 256;                          // tokens per tile
 constexpr int BK = 64;                           // K per stage
 constexpr int NS = 5;                            // shared-memory stages
-constexpr int NA = 4;                            // TMEM A slots
+constexpr int NA = 3;                            // TMEM A slots
 constexpr int CK = 16;                           // stages per exact chunk (1024 K)
 constexpr int BOX_ROWS = 32;                     // token rows per activation TMA box
 constexpr int BOX_BYTES = BOX_ROWS * BK * 2;     // 4 KB
 constexpr int B_BYTES = BN * BK * 2;             // 32 KB fp16 activations per stage
 constexpr int A_BYTES = 128 * BK;                // 8 KB int8 weights per stage
 constexpr int STAGE_BYTES = B_BYTES + A_BYTES;   // 40 KB
-constexpr int NBARS = 2 * NS + 2 * NA + 2 + 1;
-constexpr uint32_t TM_ACC = 0, TM_SUM = 256, TM_A = 384, TM_COLS = 512;
+constexpr int STG_BYTES = 32 * 128 * 4;         // epilogue staging: 32 tokens x 128 channels
+constexpr int NBARS = 2 * NS + 2 * NA + 2 + 2;
+// TMEM columns: accumulator [0, 256); int32 running sums of token columns
+// 0..159 at [256, 416) (those of 160..255 are kept in registers); A slots.
+constexpr uint32_t TM_ACC = 0, TM_SUM = 256, TM_A = 416, TM_COLS = 512;
+constexpr int SUM_SLICES = 5;                    // 32-column slices with TMEM sums
 constexpr int THREADS = 320;                     // producer, MMA, converter WG, drain WG
-constexpr int SMEM_BYTES = NS * STAGE_BYTES + NBARS * 8 + 16 + 1024;
+constexpr int SMEM_BYTES = NS * STAGE_BYTES + STG_BYTES + NBARS * 8 + 16 + 1024;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 20000000ull;
 
@@ -82,6 +88,7 @@ struct Params {
     unsigned char* cbuf;
     long long crow;
     int k, lb;
+    int tma_out;                 // epilogue may use tensor stores for full slices
     int* err;
 };
 
@@ -108,6 +115,20 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* er
     return __all_sync(0xffffffffu, ok);
 }
 
+// Bounded barrier of the four drain warps (an mbarrier with count 4 instead
+// of bar.sync, so that a warp that gave up cannot hang the others).
+struct WgBarrier {
+    uint32_t addr;
+    uint32_t phase;
+    __device__ __forceinline__ bool sync(int lane, int* err) {
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(addr);
+        const bool ok = warp_wait(addr, phase & 1, err);
+        ++phase;
+        return ok;
+    }
+};
+
 // Wait without regard to the error word, with a short limit (used only to
 // let copies already in flight land before the CTA exits).
 __device__ __forceinline__ void mbar_wait_quiet(uint32_t bar, uint32_t parity, uint64_t limit) {
@@ -116,10 +137,11 @@ __device__ __forceinline__ void mbar_wait_quiet(uint32_t bar, uint32_t parity, u
         if (ptx::globaltimer() - t0 > limit) break;
 }
 
-// Epilogue for one 32-token slice of a finished tile.  `row` is this
-// thread's TMEM lane (weight channel within the tile), iv[j] the exact int32
-// result for token j0 + j.  Per-token values are loaded once per lane and
-// broadcast with shuffles.
+// Epilogue for one 32-token slice of a finished tile, plain stores (used for
+// partial slices and for bf16 return messages).  `row` is this thread's TMEM
+// lane (weight channel within the tile), iv[j] the exact int32 result for
+// token j0 + j.  Per-token values are loaded once per lane and broadcast with
+// shuffles.
 template <int EPI>
 __device__ __forceinline__ void epilogue_slice(const Params& P, const TileInfo& ti, int row,
                                                int lane, int j0, const int (&iv)[32]) {
@@ -175,15 +197,63 @@ __device__ __forceinline__ void epilogue_slice(const Params& P, const TileInfo& 
     }
 }
 
+// Epilogue for a full 32-token slice through shared memory and one TMA
+// tensor store (two for EPI_GU: the gate and the up half).  All four drain
+// warps take part; `leader` issues the store.
+template <int EPI>
+__device__ __forceinline__ bool epilogue_slice_tma(const Params& P, const TileInfo& ti, int row,
+                                                   int lane, int j0, const int (&iv)[32],
+                                                   uint8_t* stg, const CUtensorMap* tmO,
+                                                   WgBarrier& wg, bool leader) {
+    const float sr_l = (EPI == EPI_I32) ? 0.f : P.s_row[ti.r0 + j0 + lane];
+    if constexpr (EPI == EPI_I32) {
+        int32_t* o = reinterpret_cast<int32_t*>(stg) + row;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j * 128] = iv[j];
+    } else {
+        int col;
+        float* o;
+        if constexpr (EPI == EPI_GU) {
+            col = (row < 64) ? ti.mb * 64 + row : P.nout + ti.mb * 64 + (row - 64);
+            o = reinterpret_cast<float*>(stg) + (row < 64 ? 0 : 2048) + (row & 63);
+        } else {
+            col = ti.mb * 128 + row;
+            o = reinterpret_cast<float*>(stg) + row;
+        }
+        const bool chok = (EPI == EPI_GU) || col < P.nout;
+        const float sc = chok ? P.s_ch[(long long)ti.set * P.rows_per_set + col] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float sr = __shfl_sync(0xffffffffu, sr_l, j);
+            o[j * (EPI == EPI_GU ? 64 : 128)] = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sc);
+        }
+    }
+    ptx::fence_proxy_async_smem();
+    if (!wg.sync(lane, P.err)) return false;
+    if (leader) {
+        const uint32_t src = ptx::smem_addr(stg);
+        if constexpr (EPI == EPI_GU) {
+            ptx::tma_store_2d(tmO, ti.mb * 64, ti.r0 + j0, src);
+            ptx::tma_store_2d(tmO, P.nout + ti.mb * 64, ti.r0 + j0, src + 8192);
+        } else {
+            ptx::tma_store_2d(tmO, ti.mb * 128, ti.r0 + j0, src);
+        }
+        ptx::bulk_commit();
+        ptx::bulk_wait_read0();
+    }
+    return wg.sync(lane, P.err);  // staging buffer free again
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-               const Params P) {
+               const __grid_constant__ CUtensorMap tmO, const Params P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE_BYTES);
+    uint8_t* stg = smem + NS * STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE_BYTES + STG_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -195,6 +265,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     const uint32_t accfull = bar(2 * NS + 2 * NA);
     const uint32_t accempty = bar(2 * NS + 2 * NA + 1);
     const uint32_t done_bar = bar(2 * NS + 2 * NA + 2);
+    const uint32_t wg_bar = bar(2 * NS + 2 * NA + 3);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -208,11 +279,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         ptx::mbar_init(accfull, 1);
         ptx::mbar_init(accempty, 4);
         ptx::mbar_init(done_bar, 1);
+        ptx::mbar_init(wg_bar, 4);
         ptx::fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmW);
         ptx::prefetch_tmap(&tmX);
+        if (EPI != EPI_BF16MSG) ptx::prefetch_tmap(&tmO);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), TM_COLS);
@@ -344,24 +417,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         // ------------------------------------- chunk drain and epilogue
         const int wq = warp & 3;
         const int row = wq * 32 + lane;
+        const bool leader = (wq == 0) && (lane == 0);
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t accb = tmem + lane_base + TM_ACC;
         const uint32_t sumb = tmem + lane_base + TM_SUM;
-        int rs[128];  // int32 running sums of token columns 128..255
+        constexpr int RS = (8 - SUM_SLICES) * 32;
+        int rs[RS];  // int32 running sums of token columns 32*SUM_SLICES..255
         uint32_t q = 0;
         bool ok = true;
+        WgBarrier wg{wg_bar, 0};
         for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
             const TileInfo ti = decode(P, tile);
             const int nsl = (ti.nmma + 31) / 32;
-            for (int c = 0; c < nchunks; ++c) {
+            for (int c = 0; ok && c < nchunks; ++c) {
                 if (!warp_wait(accfull, q & 1, P.err)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                // columns 0..127: running sums in TMEM
 #pragma unroll
-                for (int sl = 0; sl < 4; ++sl) {
+                for (int sl = 0; sl < SUM_SLICES; ++sl) {
                     if (sl < nsl) {
                         uint32_t v[32], sv[32];
                         ptx::tmem_ld32(accb + sl * 32, v);
@@ -374,9 +449,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                         ptx::tmem_st32(sumb + sl * 32, v);
                     }
                 }
-                // columns 128..255: running sums in registers
 #pragma unroll
-                for (int sl = 4; sl < 8; ++sl) {
+                for (int sl = SUM_SLICES; sl < 8; ++sl) {
                     if (sl < nsl) {
                         uint32_t v[32];
                         ptx::tmem_ld32(accb + sl * 32, v);
@@ -384,7 +458,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             const int x = __float2int_rn(__uint_as_float(v[j]));
-                            rs[(sl - 4) * 32 + j] = (c > 0) ? rs[(sl - 4) * 32 + j] + x : x;
+                            int& r = rs[(sl - SUM_SLICES) * 32 + j];
+                            r = (c > 0) ? r + x : x;
                         }
                     }
                 }
@@ -397,9 +472,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     // epilogue from the final sums, overlapping the next tile's MMAs
 #pragma unroll
                     for (int sl = 0; sl < 8; ++sl) {
-                        if (sl < nsl) {
+                        if (ok && sl < nsl) {
                             int iv[32];
-                            if (sl < 4) {
+                            if (sl < SUM_SLICES) {
                                 uint32_t v[32];
                                 ptx::tmem_ld32(sumb + sl * 32, v);
                                 ptx::tmem_wait_ld();
@@ -407,14 +482,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                                 for (int j = 0; j < 32; ++j) iv[j] = static_cast<int>(v[j]);
                             } else {
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) iv[j] = rs[(sl - 4) * 32 + j];
+                                for (int j = 0; j < 32; ++j) iv[j] = rs[(sl - SUM_SLICES) * 32 + j];
                             }
-                            epilogue_slice<EPI>(P, ti, row, lane, sl * 32, iv);
+                            if (EPI != EPI_BF16MSG && P.tma_out && sl * 32 + 32 <= ti.nvalid) {
+                                if (!epilogue_slice_tma<EPI>(P, ti, row, lane, sl * 32, iv, stg, &tmO, wg,
+                                                             leader))
+                                    ok = false;
+                            } else {
+                                epilogue_slice<EPI>(P, ti, row, lane, sl * 32, iv);
+                            }
                         }
                     }
                 }
             }
         }
+        if (leader) ptx::bulk_wait0();  // every tensor store has landed
     }
 
     // ------------------------------------------------------- teardown
@@ -560,11 +642,12 @@ int sm_count() {
 }
 
 template <int EPI>
-cudaError_t launch_gemm(const Params& P, const CUtensorMap& w, const CUtensorMap& x, cudaStream_t st) {
+cudaError_t launch_gemm(const Params& P, const CUtensorMap& w, const CUtensorMap& x,
+                        const CUtensorMap& o, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    gemm_tc_kernel<EPI><<<sm_count(), THREADS, SMEM_BYTES, st>>>(w, x, P);
+    gemm_tc_kernel<EPI><<<sm_count(), THREADS, SMEM_BYTES, st>>>(w, x, o, P);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -576,6 +659,14 @@ bool weight_map(CUtensorMap* m, const int8_t* w, int K, uint64_t rows) {
 bool act_map(CUtensorMap* m, const __half* x, int K, uint64_t rows) {
     return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, rows, BK, BOX_ROWS,
                     CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Output map of the epilogue's tensor stores: [rows][cols] 32-bit elements,
+// boxes of box_cols x 32 rows, no swizzle.
+bool out_map(CUtensorMap* m, const void* base, bool is_int, uint64_t cols, uint64_t rows,
+             uint32_t box_cols) {
+    return make_map(m, is_int ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                    base, cols, rows, box_cols, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace tc
@@ -597,14 +688,17 @@ cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long lo
     if ((e = launch_tile_prefix(n_groups, BN, offsets, tp, st)) != cudaSuccess) return e;
     assemble_kernel<<<(unsigned)max_rows, 128, 0, st>>>(K, row_index, A, lda, nullptr, a16, nullptr);
     count_launches(1);
-    CUtensorMap mw, mx;
-    if (!weight_map(&mw, B, K, (uint64_t)n_groups * N) || !act_map(&mx, a16, K, (uint64_t)max_rows))
+    CUtensorMap mw, mx, mo;
+    const bool tma_out = N % 128 == 0;
+    if (!weight_map(&mw, B, K, (uint64_t)n_groups * N) || !act_map(&mx, a16, K, (uint64_t)max_rows) ||
+        (tma_out && !out_map(&mo, C, true, N, (uint64_t)max_rows, 128)))
         return cudaErrorInvalidValue;
+    if (!tma_out) mo = mx;  // unused
     Params P = {};
     P.G = n_groups; P.offsets = offsets; P.tile_prefix = tp; P.g2s = nullptr;
     P.K = K; P.rows_per_set = N; P.nout = N; P.mb_count = (N + 127) / 128; P.box1_off = 64;
-    P.c_i32 = C; P.err = err;
-    return launch_gemm<EPI_I32>(P, mw, mx, st);
+    P.c_i32 = C; P.err = err; P.tma_out = tma_out;
+    return launch_gemm<EPI_I32>(P, mw, mx, mo, st);
 }
 
 cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
@@ -635,18 +729,25 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                                                  d.drow, meta, a16, s_row);
     count_launches(1);
 
-    CUtensorMap mwgu, mx1, mwd, mx2;
+    CUtensorMap mwgu, mx1, mo1, mwd, mx2, mo2;
     if (!weight_map(&mwgu, w.w_gate_up, d.H, (uint64_t)E_w * 2 * d.I) ||
         !act_map(&mx1, a16, d.H, (uint64_t)M) ||
+        !out_map(&mo1, gu, false, 2ull * d.I, (uint64_t)M, 64) ||
         !weight_map(&mwd, w.w_down, d.I, (uint64_t)E_w * d.H) ||
         !act_map(&mx2, hq16, d.I, (uint64_t)M))
         return cudaErrorInvalidValue;
+    const bool y_tma = int8_ret && d.H >= 128;
+    if (y_tma) {
+        if (!out_map(&mo2, ybuf, false, (uint64_t)d.H, (uint64_t)M, 128)) return cudaErrorInvalidValue;
+    } else {
+        mo2 = mo1;  // unused
+    }
 
     Params P1 = {};
     P1.G = d.E_phys; P1.offsets = expert_offsets; P1.tile_prefix = tp; P1.g2s = w.phys_to_weight;
     P1.K = d.H; P1.rows_per_set = 2 * d.I; P1.nout = d.I; P1.mb_count = d.I / 64; P1.box1_off = d.I;
-    P1.s_row = s_row; P1.s_ch = w.s_gate_up; P1.out_f32 = gu; P1.err = err;
-    if ((e = launch_gemm<EPI_GU>(P1, mwgu, mx1, st)) != cudaSuccess) return e;
+    P1.s_row = s_row; P1.s_ch = w.s_gate_up; P1.out_f32 = gu; P1.err = err; P1.tma_out = 1;
+    if ((e = launch_gemm<EPI_GU>(P1, mwgu, mx1, mo1, st)) != cudaSuccess) return e;
 
     if (sizeof(float) * d.I > 48 * 1024 &&
         (e = cudaFuncSetAttribute(swiglu_requant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -658,16 +759,16 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     Params P2 = {};
     P2.G = d.E_phys; P2.offsets = expert_offsets; P2.tile_prefix = tp; P2.g2s = w.phys_to_weight;
     P2.K = d.I; P2.rows_per_set = d.H; P2.nout = d.H; P2.mb_count = (d.H + 127) / 128; P2.box1_off = 64;
-    P2.s_row = sh; P2.s_ch = w.s_down; P2.err = err;
+    P2.s_row = sh; P2.s_ch = w.s_down; P2.err = err; P2.tma_out = y_tma;
     if (int8_ret) {
         P2.out_f32 = ybuf;
-        if ((e = launch_gemm<EPI_F32>(P2, mwd, mx2, st)) != cudaSuccess) return e;
+        if ((e = launch_gemm<EPI_F32>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
         retquant_kernel<<<(unsigned)M, 256, 0, st>>>(d.H, d.k, d.lb, d.crow, ybuf, expert_rows, meta,
                                                      cb, reinterpret_cast<float*>(cb + scale_off));
         count_launches(1);
     } else {
         P2.expert_rows = expert_rows; P2.meta = meta; P2.cbuf = cb; P2.crow = d.crow; P2.k = d.k; P2.lb = d.lb;
-        if ((e = launch_gemm<EPI_BF16MSG>(P2, mwd, mx2, st)) != cudaSuccess) return e;
+        if ((e = launch_gemm<EPI_BF16MSG>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
