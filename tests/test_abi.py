@@ -1,0 +1,141 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every
+entry point include/moe.h declares; host-only entry points (buffer formula,
+layout, EPLB planner) match the oracle; argument validation rejects bad
+input before anything is enqueued."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import eplb
+from expert_dispatch_combine_gb300 import binding as B
+from expert_dispatch_combine_gb300 import synth
+from expert_dispatch_combine_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return B.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_symbols_exported(lib):
+    names = _declared()
+    assert len(names) >= 14
+    raw = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+    assert set(B.EXPORTED) <= set(names)
+
+
+def test_status_strings(lib):
+    assert B.moe_status_string(0) == "ok"
+    assert "invalid" in B.moe_status_string(1)
+    assert B.moe_status_string(99) == "unknown status"
+
+
+def test_buffer_formula_matches_page_example(lib):
+    for line in open(os.path.join(GOLDEN, "buffer_formula.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        a = [int(x) for x in line.split()]
+        assert B.moe_static_buffer_bytes(*a[:5]) == a[5]
+    with pytest.raises(B.MoeError):
+        B.moe_static_buffer_bytes(0, 96, 8, 1, 7680)
+    with pytest.raises(B.MoeError):
+        B.moe_static_buffer_bytes(1 << 40, 1 << 20, 8, 8, 1 << 20)  # overflow
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_layout_matches_formula(lib, name):
+    w = synth.WORKLOADS[name]
+    s = B.Shape(w.T, w.H, w.E_log, w.E_phys, w.k, w.I, w.R, w.S)
+    L = B.moe_query_layout(s)
+    assert L["max_tokens"] == w.lb * min(w.k, w.epr)
+    per_rank = B.moe_static_buffer_bytes(w.S, w.lb, w.k, w.epr, w.H + 16)
+    assert L["dispatch_bytes"] >= w.R * per_rank
+    assert L["dispatch_bytes"] - w.R * per_rank < 1024
+    assert L["dispatch_meta_offset"] % 256 == 0
+    assert L["combine_scale_offset"] >= w.T * w.k * w.H
+    assert L["workspace_bytes"] > 0
+
+
+@pytest.mark.parametrize("bad", [
+    dict(T=0), dict(H=24), dict(I=8), dict(k=0), dict(k=17), dict(E_phys=8),
+    dict(n_ranks=3), dict(n_src_ranks=5), dict(dispatch_fmt=2),
+])
+def test_shape_validation(lib, bad):
+    base = dict(T=64, H=256, E_log=16, E_phys=16, k=2, I=128, n_ranks=4, n_src_ranks=4)
+    base.update(bad)
+    with pytest.raises(B.MoeError) as e:
+        B.moe_query_layout(B.Shape(**base))
+    assert e.value.code == 1
+
+
+def test_entry_points_reject_before_enqueue(lib):
+    """Null pointers, misaligned buffers and short buffers are refused on the
+    host (the fake device pointers below are never dereferenced)."""
+    s = B.Shape(64, 256, 16, 16, 2, 128, 4, 4).c()
+    L = B.moe_query_layout(B.Shape(64, 256, 16, 16, 2, 128, 4, 4))
+    P = ctypes.c_void_p
+    fake = 1 << 40  # 256-aligned, never touched
+    rc = lib.moe_dispatch(ctypes.byref(s), P(fake), P(fake), P(fake), L["dispatch_bytes"] - 256,
+                          P(fake), P(fake), P(fake), P(fake), L["workspace_bytes"], None)
+    assert rc == 2  # dispatch buffer too small
+    rc = lib.moe_dispatch(ctypes.byref(s), P(fake), P(fake), P(fake + 8), L["dispatch_bytes"],
+                          P(fake), P(fake), P(fake), P(fake), L["workspace_bytes"], None)
+    assert rc == 1  # misaligned
+    rc = lib.moe_dispatch(ctypes.byref(s), None, P(fake), P(fake), L["dispatch_bytes"],
+                          P(fake), P(fake), P(fake), P(fake), L["workspace_bytes"], None)
+    assert rc == 1  # null input
+    rc = lib.moe_combine(ctypes.byref(s), P(fake), L["combine_bytes"] - 1, P(fake), P(fake), None)
+    assert rc == 2
+    # replicas require a map
+    s2 = B.Shape(64, 256, 16, 24, 2, 128, 4, 4).c()
+    rc = lib.moe_route(ctypes.byref(s2), P(fake), None, None, 0, P(fake), P(fake), P(fake),
+                       P(fake), None)
+    assert rc == 1
+    # grouped GEMM: K not a multiple of 16, short workspace
+    rc = lib.moe_grouped_gemm_s8(2, P(fake), 10, None, P(fake), 40, P(fake), 32, 40, P(fake),
+                                 P(fake), 1 << 20, None)
+    assert rc == 1
+    rc = lib.moe_grouped_gemm_s8(2, P(fake), 10, None, P(fake), 64, P(fake), 32, 64, P(fake),
+                                 P(fake), 16, None)
+    assert rc == 2
+
+
+@pytest.mark.parametrize("E,R,E_phys,slices,seed", [
+    (16, 4, 24, 1, 0), (16, 4, 24, 3, 1), (256, 32, 288, 1, 2), (32, 8, 48, 4, 3), (8, 2, 8, 1, 4),
+])
+def test_eplb_planner_matches_oracle(lib, E, R, E_phys, slices, seed):
+    rng = np.random.default_rng(seed)
+    load = (rng.zipf(1.3, size=(slices, E)) * rng.integers(1, 50, size=(slices, E))).astype(np.float64)
+    rep, nc, p2l = B.moe_eplb_plan(load, E_phys, R)
+    rep_o, nc_o, p2l_o = eplb.plan(load, E_phys, R)
+    assert (nc == nc_o).all()
+    assert (p2l == p2l_o).all()
+    assert (rep == rep_o[:, :rep.shape[1]]).all()
+
+
+def test_eplb_planner_on_workload_counts(lib):
+    w = synth.WORKLOADS["c3_eplb"]
+    _, _, _, cnt = oracle.route(synth.logits(w), w.k)
+    rep, nc, p2l = B.moe_eplb_plan(cnt.astype(np.float64), w.E_phys, w.R)
+    rep_o, nc_o, p2l_o = eplb.plan(cnt[None, :].astype(np.float64), w.E_phys, w.R)
+    assert (p2l == p2l_o).all() and (nc == nc_o).all()
+    assert nc.sum() == w.E_phys
+    # the hottest expert got the most copies
+    assert nc[np.argmax(cnt)] == nc.max() > 1
