@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import argparse
 import datetime
+import hashlib
 import json
 import os
 import statistics
@@ -44,6 +45,28 @@ def _peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+FFN_TC_SRC = os.path.join(ROOT, "expert_dispatch_combine_gb300", "csrc", "ffn_tc.cu")
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch of the gate/up GEMM kernel from the committed ncu
+    summary, if it was taken on this workload with the current kernel source
+    (else None)."""
+    path = os.path.join(ROOT, "profiles", "gemm_tc_gate_up_" + workload + ".md")
+    try:
+        txt = open(path).read()
+        src = hashlib.sha1(open(FFN_TC_SRC, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    kv = dict(l.split(":", 1) for l in txt.splitlines() if l.startswith(("source_sha1:", "traffic_bytes_per_launch:")))
+    if kv.get("source_sha1", "").strip() != src:
+        return None
+    try:
+        return int(kv["traffic_bytes_per_launch"].strip())
+    except (KeyError, ValueError):
+        return None
+
+
 # ------------------------------------------------------------- bookkeeping
 def algorithmic(w: synth.Workload) -> dict:
     """Algorithmic bytes / ops per step of each stage (INT8 messages, msg = H+16)."""
@@ -52,7 +75,9 @@ def algorithmic(w: synth.Workload) -> dict:
     dispatch = T * 2 * H + T * k * (H + 16) + T * k * 4 * 2      # read x, write msgs + rows
     combine = T * k * (H + 4) + T * k * 4 + T * 2 * H            # read msgs + w, write out
     ffn_ops = T * k * 6 * H * I                                   # 2 flops x 3 H*I MACs
-    return dict(route_bytes=route, dispatch_bytes=dispatch, combine_bytes=combine, ffn_ops=ffn_ops)
+    gate_up_ops = T * k * 4 * H * I                               # gate|up GEMM alone
+    return dict(route_bytes=route, dispatch_bytes=dispatch, combine_bytes=combine, ffn_ops=ffn_ops,
+                gate_up_ops=gate_up_ops, down_ops=ffn_ops - gate_up_ops)
 
 
 class ClockSampler:
@@ -248,7 +273,9 @@ def run_ours(args, rank: int, world: int):
     r = b.routing
     names = ["route", "dispatch", "ffn", "combine"]
     acc = {n: 0.0 for n in names}
+    kern = {"gemm_gate_up": 0.0, "gemm_down": 0.0}
     reps = max(1, min(args.steps, 5))
+    B.moe_profile_enable(True)
     for _ in range(reps):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         evs[0].record(stream)
@@ -266,6 +293,10 @@ def run_ours(args, rank: int, world: int):
         torch.cuda.synchronize()
         for i, n in enumerate(names):
             acc[n] += evs[i].elapsed_time(evs[i + 1]) / reps
+        gu_ms, dn_ms = B.moe_profile_read()
+        kern["gemm_gate_up"] += gu_ms / reps
+        kern["gemm_down"] += dn_ms / reps
+    B.moe_profile_enable(False)
     alg = algorithmic(w)
     peaks, peak_kind = _peaks()
     hbm = peaks["hbm_gbs"]
@@ -281,11 +312,22 @@ def run_ours(args, rank: int, world: int):
     dc_s = (acc["dispatch"] + acc["combine"]) / 1000
     stages["dispatch_combine_hbm_frac"] = dc_bytes / dc_s / 1e9 / hbm
     ffn_tflops = alg["ffn_ops"] / (acc["ffn"] / 1000) / 1e12
+    stages["ffn_tflops"] = ffn_tflops
     peak_tc = peaks["bf16_tflops_sustained"]
-    roofline = {"bound": "tensor", "achieved": ffn_tflops, "peak": peak_tc, "unit": "TFLOP/s",
-                "frac": ffn_tflops / peak_tc, "traffic": None,
-                "kernel": "moe_expert_ffn (grouped W8A8 SwiGLU experts)",
-                "peak_source": f"{peak_kind} bf16 sustained (exact int8 runs on the bf16/fp16 path)"}
+    if kern["gemm_gate_up"] > 0:
+        # dominant kernel: the gate|up expert GEMM, timed by CUDA events on its stream
+        gu_tflops = alg["gate_up_ops"] / (kern["gemm_gate_up"] / 1000) / 1e12
+        stages["gemm_gate_up_us"] = 1000 * kern["gemm_gate_up"]
+        stages["gemm_down_us"] = 1000 * kern["gemm_down"]
+        stages["gemm_down_tflops"] = alg["down_ops"] / (kern["gemm_down"] / 1000) / 1e12
+        roofline = {"bound": "tensor", "achieved": gu_tflops, "peak": peak_tc, "unit": "TFLOP/s",
+                    "frac": gu_tflops / peak_tc, "traffic": measured_traffic(w.name),
+                    "kernel": "gemm_tc_kernel<gate|up> (exact int8 on tcgen05 kind::f16)",
+                    "algorithmic_ops_per_launch": alg["gate_up_ops"],
+                    "peak_source": f"{peak_kind} bf16 sustained (exact int8 runs on the fp16 tensor path)"}
+    else:  # CUDA-core expert path (shapes the tensor-core kernel does not take)
+        roofline = {"bound": "alu", "achieved": ffn_tflops, "peak": None, "unit": "TFLOP/s",
+                    "frac": None, "traffic": None, "kernel": "moe_expert_ffn (dp4a path)"}
 
     # ---- end to end through the public API with host buffers
     lg_pin = torch.from_numpy(lg_h).pin_memory()

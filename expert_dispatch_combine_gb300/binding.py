@@ -55,7 +55,7 @@ class moe_routing(ctypes.Structure):
 EXPORTED = ("moe_status_string", "moe_static_buffer_bytes", "moe_query_layout", "moe_eplb_plan",
             "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_layer",
             "moe_gemm_workspace_bytes", "moe_grouped_gemm_s8", "moe_launch_count",
-            "moe_device_status", "moe_last_cuda_error")
+            "moe_device_status", "moe_last_cuda_error", "moe_profile_enable", "moe_profile_read")
 
 _lib = None
 
@@ -87,6 +87,8 @@ def load(path: str = LIB_PATH):
         "moe_device_status": ([P, ctypes.POINTER(i32), P], ctypes.c_int),
         "moe_launch_count": ([], i64),
         "moe_last_cuda_error": ([], ctypes.c_char_p),
+        "moe_profile_enable": ([i32], ctypes.c_int),
+        "moe_profile_read": ([P, i32], ctypes.c_int),
         "moe_grouped_gemm_s8": ([i32, P, i64, P, P, i64, P, i32, i32, P, P, i64, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
@@ -225,6 +227,17 @@ def moe_layer(shape: Shape, logits, x, w_gate_up, s_gate_up, w_down, s_down, rou
         ctypes.byref(w), ctypes.byref(r), _ptr(dispatch_buf), dispatch_buf.numel(),
         _ptr(combine_buf), combine_buf.numel(), _ptr(workspace), workspace.numel(), _ptr(out),
         _stream(stream)))
+
+
+def moe_profile_enable(on: bool) -> None:
+    _check("moe_profile_enable", load().moe_profile_enable(1 if on else 0))
+
+
+def moe_profile_read() -> tuple[float, float]:
+    """(gate/up GEMM ms, down GEMM ms) of the most recent expert FFN."""
+    ms = (ctypes.c_float * 2)()
+    _check("moe_profile_read", load().moe_profile_read(ctypes.cast(ms, ctypes.c_void_p), 2))
+    return float(ms[0]), float(ms[1])
 
 
 def moe_launch_count() -> int:

@@ -11,6 +11,10 @@ using namespace moe;
 namespace moe {
 static std::atomic<long long> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+static bool g_prof_on = false;
+static cudaEvent_t g_prof_ev[kProfSlots][2] = {};
+cudaEvent_t prof_event(int slot, int end) { return g_prof_on ? g_prof_ev[slot][end] : nullptr; }
 }  // namespace moe
 
 namespace {
@@ -219,6 +223,30 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t
                                      workspace, wl, s))) != MOE_OK)
         return st;
     return cuda_status(launch_combine(d, combine_buf, L.combine_scale_offset, r.topk_w, out, s));
+}
+
+moe_status moe_profile_enable(int32_t on) {
+    if (on && !g_prof_on) {
+        for (int s = 0; s < kProfSlots; ++s)
+            for (int e = 0; e < 2; ++e)
+                if (!g_prof_ev[s][e] && cudaEventCreate(&g_prof_ev[s][e]) != cudaSuccess)
+                    return cuda_status(cudaGetLastError());
+    }
+    g_prof_on = on != 0;
+    return MOE_OK;
+}
+
+moe_status moe_profile_read(float* ms, int32_t n) {
+    if (!ms || n < 1) return MOE_ERR_INVALID_ARG;
+    for (int s = 0; s < kProfSlots && s < n; ++s) {
+        ms[s] = -1.f;
+        if (!g_prof_ev[s][0] || !g_prof_ev[s][1]) continue;
+        if (cudaEventSynchronize(g_prof_ev[s][1]) != cudaSuccess) return cuda_status(cudaGetLastError());
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, g_prof_ev[s][0], g_prof_ev[s][1]) == cudaSuccess) ms[s] = t;
+        else cudaGetLastError();
+    }
+    return MOE_OK;
 }
 
 const char* moe_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }

@@ -647,7 +647,10 @@ cudaError_t launch_gemm(const Params& P, const CUtensorMap& w, const CUtensorMap
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    const int slot = EPI == EPI_GU ? 0 : 1;
+    if (cudaEvent_t ev = prof_event(slot, 0)) cudaEventRecord(ev, st);
     gemm_tc_kernel<EPI><<<sm_count(), THREADS, SMEM_BYTES, st>>>(w, x, o, P);
+    if (cudaEvent_t ev = prof_event(slot, 1)) cudaEventRecord(ev, st);
     count_launches(1);
     return cudaGetLastError();
 }

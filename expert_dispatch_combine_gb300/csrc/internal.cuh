@@ -97,6 +97,11 @@ inline T* ws_ptr(void* ws, long long off) { return reinterpret_cast<T*>(static_c
 // Number of kernels (and memsets) this library has enqueued in this process.
 void count_launches(int n);
 
+// Optional kernel timing: when enabled, the expert GEMM launches are
+// bracketed by CUDA events (slot 0: gate/up GEMM, slot 1: down GEMM).
+constexpr int kProfSlots = 2;
+cudaEvent_t prof_event(int slot, int end);  // nullptr when profiling is off
+
 // Kernel launchers (each returns cudaGetLastError() after its launches).
 cudaError_t launch_route(const Dims& d, const float* logits, const int32_t* rep_table,
                          const int32_t* n_copies, int max_copies, int32_t* topk_idx,

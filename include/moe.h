@@ -284,6 +284,13 @@ moe_status moe_device_status(const void* workspace, int32_t* status, moe_stream_
  * calling host thread ("no error" if there was none).  Host only. */
 const char* moe_last_cuda_error(void);
 
+/* Optional kernel timing for benchmarks (host only).  While enabled, each
+ * tensor-core expert GEMM launch is bracketed by CUDA events on its stream;
+ * moe_profile_read synchronises on them and returns the durations (ms) of
+ * the most recent gate/up GEMM (ms[0]) and down GEMM (ms[1]), -1 if none. */
+moe_status moe_profile_enable(int32_t on);
+moe_status moe_profile_read(float* ms, int32_t n);
+
 /* Number of GPU operations (kernel launches and memsets) the library has
  * enqueued in this process since it was loaded.  Host only, thread-safe. */
 int64_t moe_launch_count(void);
