@@ -55,7 +55,8 @@ class moe_routing(ctypes.Structure):
 EXPORTED = ("moe_status_string", "moe_static_buffer_bytes", "moe_query_layout", "moe_eplb_plan",
             "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_layer",
             "moe_gemm_workspace_bytes", "moe_grouped_gemm_s8", "moe_launch_count",
-            "moe_device_status", "moe_last_cuda_error", "moe_profile_enable", "moe_profile_read")
+            "moe_device_status", "moe_last_cuda_error", "moe_profile_enable", "moe_profile_read",
+            "moe_dispatch_noalloc", "moe_dispatch_noalloc_max_scratch")
 
 _lib = None
 
@@ -88,6 +89,8 @@ def load(path: str = LIB_PATH):
         "moe_launch_count": ([], i64),
         "moe_last_cuda_error": ([], ctypes.c_char_p),
         "moe_profile_enable": ([i32], ctypes.c_int),
+        "moe_dispatch_noalloc": ([PS, P, P, P, i64, P, P, P, P], ctypes.c_int),
+        "moe_dispatch_noalloc_max_scratch": ([], i64),
         "moe_profile_read": ([P, i32], ctypes.c_int),
         "moe_grouped_gemm_s8": ([i32, P, i64, P, P, i64, P, i32, i32, P, P, i64, P], ctypes.c_int),
     }
@@ -191,6 +194,20 @@ def moe_dispatch(shape: Shape, x, phys_idx, dispatch_buf, rank_counts, expert_of
         ctypes.byref(cs), _ptr(x), _ptr(phys_idx), _ptr(dispatch_buf), dispatch_buf.numel(),
         _ptr(rank_counts), _ptr(expert_offsets), _ptr(expert_rows), _ptr(workspace),
         workspace.numel(), _stream(stream)))
+
+
+def moe_dispatch_noalloc(shape: Shape, x, phys_idx, dispatch_buf, rank_counts, expert_offsets,
+                         expert_rows, stream=None):
+    """moe_dispatch for callers that cannot allocate a workspace (the scratch is a
+    fixed device array inside the library; see include/moe.h)."""
+    cs = shape.c()
+    _check("moe_dispatch_noalloc", load().moe_dispatch_noalloc(
+        ctypes.byref(cs), _ptr(x), _ptr(phys_idx), _ptr(dispatch_buf), dispatch_buf.numel(),
+        _ptr(rank_counts), _ptr(expert_offsets), _ptr(expert_rows), _stream(stream)))
+
+
+def moe_dispatch_noalloc_max_scratch() -> int:
+    return int(load().moe_dispatch_noalloc_max_scratch())
 
 
 def _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight=None) -> moe_expert_weights:

@@ -274,6 +274,32 @@ moe_status moe_grouped_gemm_s8(int32_t n_groups, const int32_t* offsets, int64_t
                                const int8_t* B, int32_t N, int32_t K, int32_t* C,
                                void* workspace, int64_t workspace_bytes, moe_stream_t stream);
 
+/* FusedDispatch without a workspace.  The pages have no counterpart to this
+ * entry point: it exists for callers that cannot call cudaMalloc at all --
+ * an engine whose allocator has reserved all device memory and forbids any
+ * allocation outside its pool, a latency-critical decode loop that must not
+ * risk the synchronisation an allocation or free can bring, a plug-in inside
+ * a host process that owns every device-memory decision.
+ * Same arguments, definitions and outputs as moe_dispatch, minus the
+ * workspace: its scratch (slot/rank arrays and per-source histograms) lives
+ * in a file-scope device array of moe_dispatch_noalloc_max_scratch() bytes
+ * (4 MiB) that every GPU loading this library holds until the process exits.
+ * Allocates nothing and calls no allocating routine.
+ *   - A shape whose dispatch scratch exceeds that size (about
+ *     8*T*k + 8*n_src_ranks*E_phys + 256 bytes) returns MOE_ERR_WORKSPACE
+ *     before anything is enqueued.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it needs clearing: every word is written before it is
+ *     read).  Calls that overlap on the GPU -- several streams, or several
+ *     host threads -- race on it; serialise them. */
+moe_status moe_dispatch_noalloc(const moe_shape* shape, const uint16_t* x, const int32_t* phys_idx,
+                                void* dispatch_buf, int64_t dispatch_bytes, int32_t* rank_counts,
+                                int32_t* expert_offsets, int32_t* expert_rows, moe_stream_t stream);
+int64_t moe_dispatch_noalloc_max_scratch(void);
+
 /* Reads the device status word that the library's kernels keep at the start
  * of `workspace` (device): MOE_OK, or MOE_ERR_TIMEOUT if a bounded device
  * wait gave up during the last moe_expert_ffn / moe_layer /
