@@ -20,18 +20,20 @@
 //     shared memory; a converter warpgroup turns them into fp16 and stores
 //     them in tensor memory (the A-from-TMEM form of tcgen05.mma), so the
 //     converted weights cost no shared-memory bandwidth;
-//   B operand = activations, up to 256 tokens per tile (fp16, K-major, 128B
+//   B operand = activations, up to 224 tokens per tile (fp16, K-major, 128B
 //     swizzle), TMA-loaded in 32-row boxes so that small experts only load
 //     the rows they have; the MMA N is the tile's token count rounded up to 16.
-//   TMEM (512 columns): one 256-column fp32 accumulator, 160 columns of int32
-//     running sums (token columns 0..159; the sums of columns 160..255 live in
-//     registers of the drain warpgroup), and three 32-column A slots.
-//   Epilogue: each 32-token slice is scaled, staged in shared memory and
-//     written with one TMA tensor store (partial slices use plain stores).
-// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5
-// converter, warps 6-9 drain (every 1024 K) and epilogue.  Each warpgroup
-// covers the four TMEM lane quarters.  A single 256-wide MMA per 16 K
-// reaches the tensor pipe's full rate, which 128-wide MMAs do not.
+//   TMEM (512 columns): two 224-column fp32 accumulators, so that the drain
+//     of one 1024-K chunk overlaps the MMAs of the next, and two 32-column A
+//     slots.  The int32 running sums live in registers of two drain
+//     warpgroups (112 token columns each).
+//   Epilogue: each 16-token group is scaled, staged in shared memory and
+//     written with one TMA tensor store (partial groups use plain stores).
+// Warp roles (16 warps): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
+// warps 4-7 converter, warps 8-15 two drain/epilogue warpgroups.  Register
+// budgets are moved between warpgroups with setmaxnreg (the totals stay
+// within the launch allocation).  Each warpgroup covers the four TMEM lane
+// quarters.
 // Every mbarrier wait is bounded (2 s): on a timeout the kernel records
 // MOE_ERR_TIMEOUT in the workspace status word, waits briefly for its own
 // copies in flight, frees TMEM and returns.
@@ -46,26 +48,30 @@
 namespace moe {
 namespace tc {
 
-constexpr int BN = 256;                          // tokens per tile
+constexpr int BN = 224;                          // tokens per tile
 constexpr int BK = 64;                           // K per stage
 constexpr int NS = 5;                            // shared-memory stages
-constexpr int NA = 3;                            // TMEM A slots
+constexpr int NA = 2;                            // TMEM A slots
 constexpr int CK = 16;                           // stages per exact chunk (1024 K)
 constexpr int BOX_ROWS = 32;                     // token rows per activation TMA box
 constexpr int BOX_BYTES = BOX_ROWS * BK * 2;     // 4 KB
-constexpr int B_BYTES = BN * BK * 2;             // 32 KB fp16 activations per stage
+constexpr int B_BYTES = BN * BK * 2;             // 28 KB fp16 activations per stage
 constexpr int A_BYTES = 128 * BK;                // 8 KB int8 weights per stage
-constexpr int STAGE_BYTES = B_BYTES + A_BYTES;   // 40 KB
-constexpr int STG_BYTES = 32 * 128 * 4;         // epilogue staging: 32 tokens x 128 channels
-constexpr int NBARS = 2 * NS + 2 * NA + 2 + 2;
-// TMEM columns: accumulator [0, 256); int32 running sums of token columns
-// 0..159 at [256, 416) (those of 160..255 are kept in registers); A slots.
-constexpr uint32_t TM_ACC = 0, TM_SUM = 256, TM_A = 416, TM_COLS = 512;
-constexpr int SUM_SLICES = 5;                    // 32-column slices with TMEM sums
-constexpr int THREADS = 320;                     // producer, MMA, converter WG, drain WG
-constexpr int SMEM_BYTES = NS * STAGE_BYTES + STG_BYTES + NBARS * 8 + 16 + 1024;
+constexpr int STAGE_BYTES = B_BYTES + A_BYTES;   // 36 KB
+constexpr int GT = 16;                           // tokens per epilogue group
+constexpr int HALF = BN / 2;                     // token columns per drain warpgroup
+constexpr int NGRP = HALF / GT;                  // 7 groups
+constexpr int STG_BYTES = GT * 128 * 4;          // 8 KB staging per drain warpgroup
+constexpr int NBARS = 2 * NS + 2 * NA + 4 + 1 + 2;
+constexpr uint32_t TM_ACC = 0, TM_A = 2 * BN, TM_COLS = 512;
+constexpr int THREADS = 512;
+constexpr int SMEM_BYTES = NS * STAGE_BYTES + 2 * STG_BYTES + NBARS * 8 + 16 + 1024;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 20000000ull;
+// per-thread register budgets after setmaxnreg: 128 threads each at
+// 48 (producer/MMA) + 80 (converter) + 2 x 184 (drains) = 63,488 <= 512 x 128
+constexpr uint32_t REG_CTRL = 48, REG_CONV = 80, REG_DRAIN = 184;
+static_assert(128 * (REG_CTRL + REG_CONV + 2 * REG_DRAIN) <= THREADS * 128, "register split");
 
 enum { EPI_I32 = 0, EPI_GU = 1, EPI_F32 = 2, EPI_BF16MSG = 3 };
 
@@ -88,7 +94,7 @@ struct Params {
     unsigned char* cbuf;
     long long crow;
     int k, lb;
-    int tma_out;                 // epilogue may use tensor stores for full slices
+    int tma_out;                 // epilogue may use tensor stores for full groups
     int* err;
 };
 
@@ -115,8 +121,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* er
     return __all_sync(0xffffffffu, ok);
 }
 
-// Bounded barrier of the four drain warps (an mbarrier with count 4 instead
-// of bar.sync, so that a warp that gave up cannot hang the others).
+// Bounded barrier of the four warps of one warpgroup (an mbarrier with count
+// 4 instead of bar.sync, so that a warp that gave up cannot hang the others).
 struct WgBarrier {
     uint32_t addr;
     uint32_t phase;
@@ -137,26 +143,32 @@ __device__ __forceinline__ void mbar_wait_quiet(uint32_t bar, uint32_t parity, u
         if (ptx::globaltimer() - t0 > limit) break;
 }
 
-// Epilogue for one 32-token slice of a finished tile, plain stores (used for
-// partial slices and for bf16 return messages).  `row` is this thread's TMEM
-// lane (weight channel within the tile), iv[j] the exact int32 result for
-// token j0 + j.  Per-token values are loaded once per lane and broadcast with
-// shuffles.
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Epilogue for one 16-token group of a finished tile with plain stores (used
+// for partial groups and for bf16 return messages).  `row` is this thread's
+// TMEM lane (weight channel within the tile), iv[j] the exact int32 result
+// for token j0 + j.  Per-token values are loaded once per lane and broadcast
+// with shuffles.
 template <int EPI>
-__device__ __forceinline__ void epilogue_slice(const Params& P, const TileInfo& ti, int row,
-                                               int lane, int j0, const int (&iv)[32]) {
-    const bool lane_ok = j0 + lane < ti.nvalid;
+__device__ __forceinline__ void epilogue_direct(const Params& P, const TileInfo& ti, int row,
+                                                int lane, int j0, const int (&iv)[GT]) {
+    const bool lane_ok = lane < GT && j0 + lane < ti.nvalid;
     if constexpr (EPI == EPI_I32) {
         const int ch = ti.mb * 128 + row;
         if (ch < P.nout) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
+            for (int j = 0; j < GT; ++j)
                 if (j0 + j < ti.nvalid) P.c_i32[(long long)(ti.r0 + j0 + j) * P.nout + ch] = iv[j];
         }
     } else if constexpr (EPI == EPI_GU || EPI == EPI_F32) {
-        // EPI_GU: rows 0..63 are gate channels mb*64 + row, rows 64..127 the
-        // matching up channels (stored at I + channel); both scaled outputs go
-        // to a [M][2I] buffer.  EPI_F32: channel mb*128 + row of [M][nout].
         int col, ld;
         if constexpr (EPI == EPI_GU) {
             col = (row < 64) ? ti.mb * 64 + row : P.nout + ti.mb * 64 + (row - 64);
@@ -170,7 +182,7 @@ __device__ __forceinline__ void epilogue_slice(const Params& P, const TileInfo& 
         const float sr_l = lane_ok ? P.s_row[ti.r0 + j0 + lane] : 0.f;
         float* out = P.out_f32 + (long long)ti.r0 * ld + col;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < GT; ++j) {
             const float sr = __shfl_sync(0xffffffffu, sr_l, j);
             const float v = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sc);
             if (chok && j0 + j < ti.nvalid) out[(long long)(j0 + j) * ld] = v;
@@ -186,7 +198,7 @@ __device__ __forceinline__ void epilogue_slice(const Params& P, const TileInfo& 
             tj_l = (m.src_rank * P.lb + m.batch_slot) * P.k + m.route_slot;
         }
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < GT; ++j) {
             const float sr = __shfl_sync(0xffffffffu, sr_l, j);
             const int tj = __shfl_sync(0xffffffffu, tj_l, j);
             const float y = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sd);
@@ -197,25 +209,24 @@ __device__ __forceinline__ void epilogue_slice(const Params& P, const TileInfo& 
     }
 }
 
-// Epilogue for a full 32-token slice through shared memory and one TMA
-// tensor store (two for EPI_GU: the gate and the up half).  All four drain
-// warps take part; `leader` issues the store.
+// Epilogue for a full 16-token group through shared memory and one TMA
+// tensor store (two for EPI_GU: the gate half and the up half).  All four
+// warps of the drain warpgroup take part; `leader` issues the store.
 template <int EPI>
-__device__ __forceinline__ bool epilogue_slice_tma(const Params& P, const TileInfo& ti, int row,
-                                                   int lane, int j0, const int (&iv)[32],
-                                                   uint8_t* stg, const CUtensorMap* tmO,
-                                                   WgBarrier& wg, bool leader) {
-    const float sr_l = (EPI == EPI_I32) ? 0.f : P.s_row[ti.r0 + j0 + lane];
+__device__ __forceinline__ bool epilogue_tma(const Params& P, const TileInfo& ti, int row,
+                                             int lane, int j0, const int (&iv)[GT], uint8_t* stg,
+                                             const CUtensorMap* tmO, WgBarrier& wg, bool leader) {
     if constexpr (EPI == EPI_I32) {
         int32_t* o = reinterpret_cast<int32_t*>(stg) + row;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) o[j * 128] = iv[j];
+        for (int j = 0; j < GT; ++j) o[j * 128] = iv[j];
     } else {
+        const float sr_l = lane < GT ? P.s_row[ti.r0 + j0 + lane] : 0.f;
         int col;
         float* o;
         if constexpr (EPI == EPI_GU) {
             col = (row < 64) ? ti.mb * 64 + row : P.nout + ti.mb * 64 + (row - 64);
-            o = reinterpret_cast<float*>(stg) + (row < 64 ? 0 : 2048) + (row & 63);
+            o = reinterpret_cast<float*>(stg) + (row < 64 ? 0 : GT * 64) + (row & 63);
         } else {
             col = ti.mb * 128 + row;
             o = reinterpret_cast<float*>(stg) + row;
@@ -223,7 +234,7 @@ __device__ __forceinline__ bool epilogue_slice_tma(const Params& P, const TileIn
         const bool chok = (EPI == EPI_GU) || col < P.nout;
         const float sc = chok ? P.s_ch[(long long)ti.set * P.rows_per_set + col] : 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < GT; ++j) {
             const float sr = __shfl_sync(0xffffffffu, sr_l, j);
             o[j * (EPI == EPI_GU ? 64 : 128)] = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sc);
         }
@@ -234,7 +245,7 @@ __device__ __forceinline__ bool epilogue_slice_tma(const Params& P, const TileIn
         const uint32_t src = ptx::smem_addr(stg);
         if constexpr (EPI == EPI_GU) {
             ptx::tma_store_2d(tmO, ti.mb * 64, ti.r0 + j0, src);
-            ptx::tma_store_2d(tmO, P.nout + ti.mb * 64, ti.r0 + j0, src + 8192);
+            ptx::tma_store_2d(tmO, P.nout + ti.mb * 64, ti.r0 + j0, src + GT * 64 * 4);
         } else {
             ptx::tma_store_2d(tmO, ti.mb * 128, ti.r0 + j0, src);
         }
@@ -253,7 +264,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = smem;
     uint8_t* stg = smem + NS * STAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE_BYTES + STG_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE_BYTES + 2 * STG_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -262,10 +273,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     auto empty = [&](int s) { return bar(NS + s); };
     auto afull = [&](int a) { return bar(2 * NS + a); };
     auto aempty = [&](int a) { return bar(2 * NS + NA + a); };
-    const uint32_t accfull = bar(2 * NS + 2 * NA);
-    const uint32_t accempty = bar(2 * NS + 2 * NA + 1);
-    const uint32_t done_bar = bar(2 * NS + 2 * NA + 2);
-    const uint32_t wg_bar = bar(2 * NS + 2 * NA + 3);
+    auto accfull = [&](int b) { return bar(2 * NS + 2 * NA + b); };
+    auto accempty = [&](int b) { return bar(2 * NS + 2 * NA + 2 + b); };
+    const uint32_t done_bar = bar(2 * NS + 2 * NA + 4);
+    auto wg_bar = [&](int h) { return bar(2 * NS + 2 * NA + 5 + h); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -276,10 +287,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             ptx::mbar_init(afull(a), 4);
             ptx::mbar_init(aempty(a), 1);
         }
-        ptx::mbar_init(accfull, 1);
-        ptx::mbar_init(accempty, 4);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(accfull(b), 1);
+            ptx::mbar_init(accempty(b), 8);
+        }
         ptx::mbar_init(done_bar, 1);
-        ptx::mbar_init(wg_bar, 4);
+        ptx::mbar_init(wg_bar(0), 4);
+        ptx::mbar_init(wg_bar(1), 4);
         ptx::fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -299,10 +313,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     const int total_tiles = P.tile_prefix[P.G] * P.mb_count;
     const int KS = P.K / BK;
     const int nchunks = (KS + CK - 1) / CK;
+    const int wgi = warp >> 2;
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
+    if (wgi == 0) {
+        reg_dealloc<REG_CTRL>();
+        if (warp == 0 && lane == 0) {
+            // -------------------------------------------- TMA producer
             uint32_t g = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
@@ -330,10 +346,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 for (uint32_t j = (g > NS ? g - NS : 0); j < g; ++j)
                     mbar_wait_quiet(full(j % NS), (j / NS) & 1, DRAIN_NS);
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
+            // --------------------------------------------- MMA issuer
             uint32_t g = 0, q = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
@@ -342,9 +356,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 for (int ks = 0; ks < KS; ++ks) {
                     const bool first = (ks % CK) == 0;
                     const bool last = (ks % CK) == CK - 1 || ks == KS - 1;
+                    const uint32_t b = q & 1;
                     if (first) {
-                        // the drain must have taken the previous chunk out of TMEM
-                        if (!ptx::mbar_wait(accempty, (q & 1) ^ 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
+                        // the drains must have taken this buffer's previous chunk
+                        if (!ptx::mbar_wait(accempty(b), ((q >> 1) & 1) ^ 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
                             ok = false;
                             break;
                         }
@@ -358,14 +373,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     ptx::tc_fence_after();
                     const uint32_t bbase = ptx::smem_addr(stages + s * STAGE_BYTES);
                     const uint32_t abase = tmem + TM_A + a * 32;
+                    const uint32_t d = tmem + TM_ACC + b * BN;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        ptx::mma_f16_ts(tmem + TM_ACC, abase + kk * 8, ptx::sdesc_k_sw128(bbase + kk * 32),
-                                        idesc, (first && kk == 0) ? 0u : 1u);
+                        ptx::mma_f16_ts(d, abase + kk * 8, ptx::sdesc_k_sw128(bbase + kk * 32), idesc,
+                                        (first && kk == 0) ? 0u : 1u);
                     ptx::tc_commit(empty(s));
                     ptx::tc_commit(aempty(a));
                     if (last) {
-                        ptx::tc_commit(accfull);
+                        ptx::tc_commit(accfull(b));
                         ++q;
                     }
                     ++g;
@@ -375,8 +391,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             ptx::tc_commit(done_bar);
             mbar_wait_quiet(done_bar, 0, WAIT_NS);
         }
-    } else if (warp < 6) {
+    } else if (wgi == 1) {
         // ------------------------------------------------------- converter
+        reg_dealloc<REG_CONV>();
         const int wq = warp & 3;
         const int row = wq * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
@@ -414,82 +431,62 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             }
         }
     } else {
-        // ------------------------------------- chunk drain and epilogue
+        // ---------------------------- chunk drain and epilogue (2 groups)
+        reg_alloc<REG_DRAIN>();
+        const int h = wgi - 2;                 // token columns [h*HALF, h*HALF + HALF)
         const int wq = warp & 3;
         const int row = wq * 32 + lane;
         const bool leader = (wq == 0) && (lane == 0);
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t accb = tmem + lane_base + TM_ACC;
-        const uint32_t sumb = tmem + lane_base + TM_SUM;
-        constexpr int RS = (8 - SUM_SLICES) * 32;
-        int rs[RS];  // int32 running sums of token columns 32*SUM_SLICES..255
+        uint8_t* my_stg = stg + h * STG_BYTES;
+        int rs[NGRP * GT];                     // int32 running sums of this group's columns
         uint32_t q = 0;
         bool ok = true;
-        WgBarrier wg{wg_bar, 0};
+        WgBarrier wgb{wg_bar(h), 0};
         for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
             const TileInfo ti = decode(P, tile);
-            const int nsl = (ti.nmma + 31) / 32;
+            const int tok0 = h * HALF;
+            const int ng = max(0, min(NGRP, (ti.nmma - tok0 + GT - 1) / GT));
             for (int c = 0; ok && c < nchunks; ++c) {
-                if (!warp_wait(accfull, q & 1, P.err)) {
+                const uint32_t b = q & 1;
+                if (!warp_wait(accfull(b), (q >> 1) & 1, P.err)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
+                const uint32_t accb = tmem + lane_base + TM_ACC + b * BN + tok0;
 #pragma unroll
-                for (int sl = 0; sl < SUM_SLICES; ++sl) {
-                    if (sl < nsl) {
-                        uint32_t v[32], sv[32];
-                        ptx::tmem_ld32(accb + sl * 32, v);
-                        if (c > 0) ptx::tmem_ld32(sumb + sl * 32, sv);
+                for (int gi = 0; gi < NGRP; ++gi) {
+                    if (gi < ng) {
+                        uint32_t v[GT];
+                        ptx::tmem_ld16(accb + gi * GT, v);
                         ptx::tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            v[j] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[j])) +
-                                                         (c > 0 ? static_cast<int>(sv[j]) : 0));
-                        ptx::tmem_st32(sumb + sl * 32, v);
-                    }
-                }
-#pragma unroll
-                for (int sl = SUM_SLICES; sl < 8; ++sl) {
-                    if (sl < nsl) {
-                        uint32_t v[32];
-                        ptx::tmem_ld32(accb + sl * 32, v);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
+                        for (int j = 0; j < GT; ++j) {
                             const int x = __float2int_rn(__uint_as_float(v[j]));
-                            int& r = rs[(sl - SUM_SLICES) * 32 + j];
+                            int& r = rs[gi * GT + j];
                             r = (c > 0) ? r + x : x;
                         }
                     }
                 }
-                ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(accempty);  // the MMA may overwrite the accumulator
+                if (lane == 0) ptx::mbar_arrive(accempty(b));  // buffer free for the MMA
                 ++q;
                 if (c == nchunks - 1) {
-                    // epilogue from the final sums, overlapping the next tile's MMAs
+                    // epilogue from the final sums, overlapping the next chunks' MMAs
 #pragma unroll
-                    for (int sl = 0; sl < 8; ++sl) {
-                        if (ok && sl < nsl) {
-                            int iv[32];
-                            if (sl < SUM_SLICES) {
-                                uint32_t v[32];
-                                ptx::tmem_ld32(sumb + sl * 32, v);
-                                ptx::tmem_wait_ld();
+                    for (int gi = 0; gi < NGRP; ++gi) {
+                        if (ok && gi < ng) {
+                            int iv[GT];
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) iv[j] = static_cast<int>(v[j]);
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 32; ++j) iv[j] = rs[(sl - SUM_SLICES) * 32 + j];
-                            }
-                            if (EPI != EPI_BF16MSG && P.tma_out && sl * 32 + 32 <= ti.nvalid) {
-                                if (!epilogue_slice_tma<EPI>(P, ti, row, lane, sl * 32, iv, stg, &tmO, wg,
-                                                             leader))
+                            for (int j = 0; j < GT; ++j) iv[j] = rs[gi * GT + j];
+                            const int j0 = tok0 + gi * GT;
+                            if (EPI != EPI_BF16MSG && P.tma_out && j0 + GT <= ti.nvalid) {
+                                if (!epilogue_tma<EPI>(P, ti, row, lane, j0, iv, my_stg, &tmO, wgb, leader))
                                     ok = false;
                             } else {
-                                epilogue_slice<EPI>(P, ti, row, lane, sl * 32, iv);
+                                epilogue_direct<EPI>(P, ti, row, lane, j0, iv);
                             }
                         }
                     }
@@ -665,11 +662,11 @@ bool act_map(CUtensorMap* m, const __half* x, int K, uint64_t rows) {
 }
 
 // Output map of the epilogue's tensor stores: [rows][cols] 32-bit elements,
-// boxes of box_cols x 32 rows, no swizzle.
+// boxes of box_cols x GT rows, no swizzle.
 bool out_map(CUtensorMap* m, const void* base, bool is_int, uint64_t cols, uint64_t rows,
              uint32_t box_cols) {
     return make_map(m, is_int ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
-                    base, cols, rows, box_cols, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+                    base, cols, rows, box_cols, GT, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace tc
