@@ -272,7 +272,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     auto full = [&](int s) { return bar(s); };
     auto empty = [&](int s) { return bar(NS + s); };
     auto afull = [&](int a) { return bar(2 * NS + a); };
-    auto aempty = [&](int a) { return bar(2 * NS + NA + a); };
     auto accfull = [&](int b) { return bar(2 * NS + 2 * NA + b); };
     auto accempty = [&](int b) { return bar(2 * NS + 2 * NA + 2 + b); };
     const uint32_t done_bar = bar(2 * NS + 2 * NA + 4);
@@ -283,10 +282,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             ptx::mbar_init(full(s), 1);
             ptx::mbar_init(empty(s), 1);
         }
-        for (int a = 0; a < NA; ++a) {
-            ptx::mbar_init(afull(a), 4);
-            ptx::mbar_init(aempty(a), 1);
-        }
+        for (int a = 0; a < NA; ++a) ptx::mbar_init(afull(a), 4);
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accfull(b), 1);
             ptx::mbar_init(accempty(b), 8);
@@ -378,8 +374,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     for (int kk = 0; kk < BK / 16; ++kk)
                         ptx::mma_f16_ts(d, abase + kk * 8, ptx::sdesc_k_sw128(bbase + kk * 32), idesc,
                                         (first && kk == 0) ? 0u : 1u);
-                    ptx::tc_commit(empty(s));
-                    ptx::tc_commit(aempty(a));
+                    ptx::tc_commit(empty(s));  // stage s and A slot a are consumed
                     if (last) {
                         ptx::tc_commit(accfull(b));
                         ++q;
@@ -404,8 +399,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
             for (int ks = 0; ks < KS; ++ks, ++g) {
                 const int s = g % NS, a = g % NA;
+                // A slot a was last read by the MMAs of K step g - NA, whose
+                // commit completes the `empty` phase of that step's stage
                 if (!warp_wait(full(s), (g / NS) & 1, P.err) ||
-                    !warp_wait(aempty(a), ((g / NA) & 1) ^ 1, P.err)) {
+                    (g >= NA && !warp_wait(empty((g - NA) % NS), ((g - NA) / NS) & 1, P.err))) {
                     ok = false;
                     break;
                 }
