@@ -28,7 +28,8 @@ namespace {
 // tile_prefix[g] = sum_{g' < g} ceil(M_g' / BM), g = 0..G (one block).
 __global__ void __launch_bounds__(1024)
 tile_prefix_kernel(int G, int BM, const int32_t* __restrict__ offsets,
-                   int32_t* __restrict__ tile_prefix) {
+                   int32_t* __restrict__ tile_prefix, int4* __restrict__ table,
+                   const int32_t* __restrict__ g2s) {
     __shared__ int s_warp[32];
     __shared__ int s_carry;
     if (threadIdx.x == 0) s_carry = 0;
@@ -60,7 +61,15 @@ tile_prefix_kernel(int G, int BM, const int32_t* __restrict__ offsets,
         }
         __syncthreads();
         int incl = v + (w > 0 ? s_warp[w - 1] : 0) + s_carry;
-        if (g < G) tile_prefix[g] = incl - n;
+        if (g < G) {
+            tile_prefix[g] = incl - n;
+            if (table) {
+                const int r0 = offsets[g], m = offsets[g + 1] - r0;
+                const int set = g2s ? g2s[g] : g;
+                for (int j = 0; j < n; ++j)
+                    table[incl - n + j] = make_int4(set, r0 + j * BM, min(BM, m - j * BM), g);
+            }
+        }
         __syncthreads();
         if (threadIdx.x == 1023) s_carry = incl;
         __syncthreads();
@@ -235,8 +244,8 @@ cudaError_t set_smem(const void* fn, size_t bytes) {
 }  // namespace
 
 cudaError_t launch_tile_prefix(int G, int BM, const int32_t* offsets, int32_t* tile_prefix,
-                               cudaStream_t st) {
-    tile_prefix_kernel<<<1, 1024, 0, st>>>(G, BM, offsets, tile_prefix);
+                               cudaStream_t st, int4* table, const int32_t* g2s) {
+    tile_prefix_kernel<<<1, 1024, 0, st>>>(G, BM, offsets, tile_prefix, table, g2s);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -20,13 +20,17 @@
 //     shared memory; a converter warpgroup turns them into fp16 and stores
 //     them in tensor memory (the A-from-TMEM form of tcgen05.mma), so the
 //     converted weights cost no shared-memory bandwidth;
-//   B operand = activations, up to 224 tokens per tile (fp16, K-major, 128B
+//   B operand = activations, up to 192 tokens per tile (fp16, K-major, 128B
 //     swizzle), TMA-loaded in 32-row boxes so that small experts only load
 //     the rows they have; the MMA N is the tile's token count rounded up to 16.
-//   TMEM (512 columns): two 224-column fp32 accumulators, so that the drain
-//     of one 1024-K chunk overlaps the MMAs of the next, and two 32-column A
+//   TMEM (512 columns): two 192-column fp32 accumulators, so that the drain
+//     of one 1024-K chunk overlaps the MMAs of the next, and four 32-column A
 //     slots.  The int32 running sums live in registers of two drain
-//     warpgroups (112 token columns each).
+//     warpgroups (96 token columns each).
+//   Issue: the single MMA thread waits once per PAIR of 64-K stages (8 MMAs):
+//     each wait costs the issuing thread a few hundred cycles, which 4 MMAs
+//     of N <= 224 do not cover but 8 do.  The converter fills the A slots of
+//     one pair while the MMAs of the other run.
 //   Epilogue: each 16-token group is scaled, staged in shared memory and
 //     written with one TMA tensor store (partial groups use plain stores).
 // Warp roles (16 warps): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
@@ -48,30 +52,32 @@
 namespace moe {
 namespace tc {
 
-constexpr int BN = 224;                          // tokens per tile
+constexpr int BN = kTcTileRows;                  // tokens per tile (192)
 constexpr int BK = 64;                           // K per stage
-constexpr int NS = 5;                            // shared-memory stages
-constexpr int NA = 2;                            // TMEM A slots
+constexpr int NS = 6;                            // shared-memory stages
+constexpr int NA = 4;                            // TMEM A slots (two pairs)
 constexpr int CK = 16;                           // stages per exact chunk (1024 K)
 constexpr int BOX_ROWS = 32;                     // token rows per activation TMA box
 constexpr int BOX_BYTES = BOX_ROWS * BK * 2;     // 4 KB
-constexpr int B_BYTES = BN * BK * 2;             // 28 KB fp16 activations per stage
+constexpr int B_BYTES = BN * BK * 2;             // 24 KB fp16 activations per stage
 constexpr int A_BYTES = 128 * BK;                // 8 KB int8 weights per stage
-constexpr int STAGE_BYTES = B_BYTES + A_BYTES;   // 36 KB
+constexpr int STAGE_BYTES = B_BYTES + A_BYTES;   // 32 KB
 constexpr int GT = 16;                           // tokens per epilogue group
 constexpr int HALF = BN / 2;                     // token columns per drain warpgroup
-constexpr int NGRP = HALF / GT;                  // 7 groups
-constexpr int STG_BYTES = GT * 128 * 4;          // 8 KB staging per drain warpgroup
-constexpr int NBARS = 2 * NS + 2 * NA + 4 + 1 + 2;
+constexpr int NGRP = HALF / GT;                  // 6 groups
+constexpr int STG_BYTES = GT * 128 * 4;          // 8 KB staging buffer; two per drain warpgroup
+constexpr int NBARS = 2 * NS + 2 + 4 + 1 + 2;
 constexpr uint32_t TM_ACC = 0, TM_A = 2 * BN, TM_COLS = 512;
 constexpr int THREADS = 512;
-constexpr int SMEM_BYTES = NS * STAGE_BYTES + 2 * STG_BYTES + NBARS * 8 + 16 + 1024;
+constexpr int SMEM_BYTES = NS * STAGE_BYTES + 4 * STG_BYTES + NBARS * 8 + 16 + 1024;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 20000000ull;
 // per-thread register budgets after setmaxnreg: 128 threads each at
 // 48 (producer/MMA) + 80 (converter) + 2 x 184 (drains) = 63,488 <= 512 x 128
 constexpr uint32_t REG_CTRL = 48, REG_CONV = 80, REG_DRAIN = 184;
 static_assert(128 * (REG_CTRL + REG_CONV + 2 * REG_DRAIN) <= THREADS * 128, "register split");
+static_assert(SMEM_BYTES <= 227 * 1024, "dynamic shared memory per CTA");
+static_assert(NA == 4 && TM_A + NA * 32 <= TM_COLS, "two accumulators and two pairs of A slots in TMEM");
 
 enum { EPI_I32 = 0, EPI_GU = 1, EPI_F32 = 2, EPI_BF16MSG = 3 };
 
@@ -79,6 +85,7 @@ struct Params {
     int G;
     const int32_t* offsets;      // [G+1] token rows per group
     const int32_t* tile_prefix;  // [G+1] token tiles per group
+    const int4* ttab;            // per token tile: (weight set, first row, rows, group)
     const int32_t* g2s;          // nullable: weight set of each group
     int K;                       // reduction length, multiple of 64
     int rows_per_set;            // weight rows per set
@@ -88,7 +95,8 @@ struct Params {
     const float* s_row;          // per token-row scale
     const float* s_ch;           // per-channel weight scales [set][rows_per_set]
     int32_t* c_i32;              // EPI_I32: [M][nout]
-    float* out_f32;              // EPI_GU: [M][2I] (gate | up); EPI_F32: [M][nout]
+    float* out_f32;              // EPI_GU: h [M][I]; EPI_F32: y [M][nout]
+    unsigned* rowmax;            // EPI_GU / EPI_F32: per-row absmax of the output (float bits)
     const int32_t* expert_rows;  // EPI_BF16MSG: row -> dispatch slot
     const moe_dispatch_meta* meta;
     unsigned char* cbuf;
@@ -99,18 +107,22 @@ struct Params {
 };
 
 struct TileInfo {
-    int p, set, r0, nvalid, nmma, mb;
+    int set, r0, nvalid, nmma, mb;
 };
 
-__device__ __forceinline__ TileInfo decode(const Params& P, int tile) {
+// Tile t covers token tile t / mb_count and channel block t % mb_count.  Each
+// role loads the table entry of its next tile one tile ahead, so the load's
+// latency hides behind the current tile.
+__device__ __forceinline__ int4 tile_entry(const Params& P, int tile, int total_tiles) {
+    return tile < total_tiles ? __ldg(P.ttab + tile / P.mb_count) : make_int4(0, 0, 0, 0);
+}
+__device__ __forceinline__ TileInfo decode(const Params& P, int tile, const int4& e) {
     TileInfo t;
-    const int nt = tile / P.mb_count;
-    t.mb = tile - nt * P.mb_count;
-    t.p = find_group(P.tile_prefix, P.G, nt);
-    t.r0 = P.offsets[t.p] + (nt - P.tile_prefix[t.p]) * BN;
-    t.nvalid = min(BN, P.offsets[t.p + 1] - t.r0);
+    t.mb = tile % P.mb_count;
+    t.set = e.x;
+    t.r0 = e.y;
+    t.nvalid = e.z;
     t.nmma = (t.nvalid + 15) & ~15;
-    t.set = P.g2s ? P.g2s[t.p] : t.p;
     return t;
 }
 
@@ -255,34 +267,139 @@ __device__ __forceinline__ bool epilogue_tma(const Params& P, const TileInfo& ti
     return wg.sync(lane, P.err);  // staging buffer free again
 }
 
+// Epilogue of the expert FFN for one 16-token group, staged in shared memory.
+//   EPI_GU: rows 0..63 hold the gate projection g of the tile's 64 channels,
+//     rows 64..127 the up projection u of the same channels; the group's
+//     h = SiLU(g) * u is formed in shared memory (8 values per thread).
+//   EPI_F32: y of the tile's 128 output channels.
+// The per-row absolute maximum of this tile's outputs goes to `rowmax` with
+// an atomic max (the token-wise requantisation needs the whole row); the
+// values go out with one TMA tensor store for a full group, plain stores for
+// a partial one.  All four warps of the drain warpgroup take part.
+// Groups alternate between two staging buffers.  Two warpgroup barriers per
+// group suffice: every thread's reads of a buffer precede its arrival at the
+// next group's first barrier, and the leader waits for the previous group's
+// tensor store to have read its buffer before the second barrier, so a buffer
+// is free again when the group after next starts writing it.
+template <int EPI>
+__device__ __forceinline__ bool epilogue_staged(const Params& P, const TileInfo& ti, int row,
+                                                int lane, int j0, const int (&iv)[GT], float* stg,
+                                                const CUtensorMap* tmO, WgBarrier& wg, bool leader) {
+    const int nv = min(GT, ti.nvalid - j0);  // valid tokens in this group (>= 1)
+    const float sr_l = lane < nv ? P.s_row[ti.r0 + j0 + lane] : 0.f;
+    if constexpr (EPI == EPI_GU) {
+        const int c = row & 63;
+        const int colw = (row < 64) ? ti.mb * 64 + c : P.nout + ti.mb * 64 + c;
+        const float sc = P.s_ch[(long long)ti.set * P.rows_per_set + colw];
+        float* o = stg + (row < 64 ? 0 : GT * 64) + c;
+#pragma unroll
+        for (int j = 0; j < GT; ++j) {
+            const float sr = __shfl_sync(0xffffffffu, sr_l, j);
+            o[j * 64] = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sc);
+        }
+        if (!wg.sync(lane, P.err)) return false;
+        // h for channel c and tokens tb .. tb+7
+        const int tb = (row >> 6) * 8;
+        float hv[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+            hv[jj] = __fmul_rn(silu_fast(stg[(tb + jj) * 64 + c]), stg[GT * 64 + (tb + jj) * 64 + c]);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) stg[(tb + jj) * 64 + c] = hv[jj];
+        ptx::fence_proxy_async_smem();
+        if (leader) ptx::bulk_wait_read0();  // previous group's store has read the other buffer
+        if (!wg.sync(lane, P.err)) return false;
+        {  // token row / 8 = row >> 3 of the group; this thread's 8 channels
+            const int j = row >> 3, p = row & 7;
+            const float4 a = *reinterpret_cast<const float4*>(stg + j * 64 + 4 * p);
+            const float4 b = *reinterpret_cast<const float4*>(stg + j * 64 + 32 + 4 * p);
+            float m = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                            fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            if (p == 0 && j < nv) atomicMax(&P.rowmax[ti.r0 + j0 + j], __float_as_uint(m));
+        }
+        if (nv == GT && P.tma_out) {
+            if (leader) {
+                ptx::tma_store_2d(tmO, ti.mb * 64, ti.r0 + j0, ptx::smem_addr(stg));
+                ptx::bulk_commit();
+            }
+        } else {
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int j = tb + jj;
+                if (j < nv) P.out_f32[(long long)(ti.r0 + j0 + j) * P.nout + ti.mb * 64 + c] = hv[jj];
+            }
+        }
+    } else {  // EPI_F32
+        const int col = ti.mb * 128 + row;
+        const bool chok = col < P.nout;
+        const float sd = chok ? P.s_ch[(long long)ti.set * P.rows_per_set + col] : 0.f;
+#pragma unroll
+        for (int j = 0; j < GT; ++j) {
+            const float sr = __shfl_sync(0xffffffffu, sr_l, j);
+            stg[j * 128 + row] = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sd);  // 0 off the edge
+        }
+        ptx::fence_proxy_async_smem();
+        if (leader) ptx::bulk_wait_read0();  // previous group's store has read the other buffer
+        if (!wg.sync(lane, P.err)) return false;
+        {  // token row >> 3 of the group; this thread's 16 channels
+            const int j = row >> 3, p = row & 7;
+            float m = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 a = *reinterpret_cast<const float4*>(stg + j * 128 + 32 * q + 4 * p);
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+            }
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            if (p == 0 && j < nv) atomicMax(&P.rowmax[ti.r0 + j0 + j], __float_as_uint(m));
+        }
+        if (nv == GT && P.tma_out) {
+            if (leader) {
+                ptx::tma_store_2d(tmO, ti.mb * 128, ti.r0 + j0, ptx::smem_addr(stg));
+                ptx::bulk_commit();
+            }
+        } else if (chok) {
+#pragma unroll
+            for (int j = 0; j < GT; ++j)
+                if (j < nv) P.out_f32[(long long)(ti.r0 + j0 + j) * P.nout + col] = stg[j * 128 + row];
+        }
+    }
+    return true;
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+               const __grid_constant__ CUtensorMap tmXb,
                const __grid_constant__ CUtensorMap tmO, const Params P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = smem;
     uint8_t* stg = smem + NS * STAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE_BYTES + 2 * STG_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE_BYTES + 4 * STG_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
     auto full = [&](int s) { return bar(s); };
     auto empty = [&](int s) { return bar(NS + s); };
-    auto afull = [&](int a) { return bar(2 * NS + a); };
-    auto accfull = [&](int b) { return bar(2 * NS + 2 * NA + b); };
-    auto accempty = [&](int b) { return bar(2 * NS + 2 * NA + 2 + b); };
-    const uint32_t done_bar = bar(2 * NS + 2 * NA + 4);
-    auto wg_bar = [&](int h) { return bar(2 * NS + 2 * NA + 5 + h); };
+    auto afull = [&](int p) { return bar(2 * NS + p); };  // A slots of a stage pair converted
+    auto accfull = [&](int b) { return bar(2 * NS + 2 + b); };
+    auto accempty = [&](int b) { return bar(2 * NS + 2 + 2 + b); };
+    const uint32_t done_bar = bar(2 * NS + 2 + 4);
+    auto wg_bar = [&](int h) { return bar(2 * NS + 2 + 5 + h); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(full(s), 1);
             ptx::mbar_init(empty(s), 1);
         }
-        for (int a = 0; a < NA; ++a) ptx::mbar_init(afull(a), 4);
+        for (int p = 0; p < 2; ++p) ptx::mbar_init(afull(p), 4);
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accfull(b), 1);
             ptx::mbar_init(accempty(b), 8);
@@ -295,6 +412,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmW);
         ptx::prefetch_tmap(&tmX);
+        ptx::prefetch_tmap(&tmXb);
         if (EPI != EPI_BF16MSG) ptx::prefetch_tmap(&tmO);
     }
     if (warp == 1) {
@@ -317,24 +435,40 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             // -------------------------------------------- TMA producer
             uint32_t g = 0;
             bool ok = true;
+            int4 e_next = tile_entry(P, blockIdx.x, total_tiles);
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const TileInfo ti = decode(P, tile);
+                const TileInfo ti = decode(P, tile, e_next);
+                e_next = tile_entry(P, tile + gridDim.x, total_tiles);
                 const int yw0 = ti.set * P.rows_per_set + (EPI == EPI_GU ? ti.mb * 64 : ti.mb * 128);
                 const int yw1 = yw0 + P.box1_off;
+                // nearly full tiles take their activations in one BN-row box
+                // (same shared-memory image as the 32-row boxes), ragged ones
+                // only the 32-row boxes they need
                 const int nb = (ti.nmma + BOX_ROWS - 1) / BOX_ROWS;
+                const bool one_box = nb == BN / BOX_ROWS;
                 const uint32_t bytes = A_BYTES + nb * BOX_BYTES;
                 for (int ks = 0; ks < KS; ++ks) {
                     const int s = g % NS;
-                    if (!ptx::mbar_wait(empty(s), ((g / NS) & 1) ^ 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
-                        ok = false;
-                        break;
+                    // once per stage pair: the MMAs complete in order, so the
+                    // release of the pair's later stage implies the earlier one
+                    if ((ks & 1) == 0) {
+                        const uint32_t gl = ks + 1 < KS ? g + 1 : g;
+                        if (!ptx::mbar_wait(empty(gl % NS), ((gl / NS) & 1) ^ 1, P.err, WAIT_NS,
+                                            MOE_ERR_TIMEOUT)) {
+                            ok = false;
+                            break;
+                        }
                     }
                     const uint32_t st = ptx::smem_addr(stages + s * STAGE_BYTES);
                     ptx::mbar_expect_tx(full(s), bytes);
                     ptx::tma_load_2d(st + B_BYTES, &tmW, ks * BK, yw0, full(s));
                     ptx::tma_load_2d(st + B_BYTES + 4096, &tmW, ks * BK, yw1, full(s));
-                    for (int j = 0; j < nb; ++j)
-                        ptx::tma_load_2d(st + j * BOX_BYTES, &tmX, ks * BK, ti.r0 + j * BOX_ROWS, full(s));
+                    if (one_box) {
+                        ptx::tma_load_2d(st, &tmXb, ks * BK, ti.r0, full(s));
+                    } else {
+                        for (int j = 0; j < nb; ++j)
+                            ptx::tma_load_2d(st + j * BOX_BYTES, &tmX, ks * BK, ti.r0 + j * BOX_ROWS, full(s));
+                    }
                     ++g;
                 }
             }
@@ -344,10 +478,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             }
         } else if (warp == 1 && lane == 0) {
             // --------------------------------------------- MMA issuer
-            uint32_t g = 0, q = 0;
+            uint32_t g = 0, q = 0, pg = 0;
             bool ok = true;
+            int4 e_next = tile_entry(P, blockIdx.x, total_tiles);
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const TileInfo ti = decode(P, tile);
+                const TileInfo ti = decode(P, tile, e_next);
+                e_next = tile_entry(P, tile + gridDim.x, total_tiles);
                 const uint32_t idesc = ptx::idesc_f16_f32(128, ti.nmma);
                 for (int ks = 0; ks < KS; ++ks) {
                     const bool first = (ks % CK) == 0;
@@ -360,9 +496,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                             break;
                         }
                     }
-                    const int s = g % NS, a = g % NA;
-                    if (!ptx::mbar_wait(full(s), (g / NS) & 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT) ||
-                        !ptx::mbar_wait(afull(a), (g / NA) & 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
+                    const int s = g % NS, a = (pg & 1) * 2 + (ks & 1);
+                    // One wait per stage pair (ks, ks+1) of the tile; a tile
+                    // with an odd stage count ends with a single-stage pair.
+                    // The converter arrives on afull only after it has seen
+                    // full(s) of both stages complete, so this wait also
+                    // covers their activation tiles.
+                    if ((ks & 1) == 0 &&
+                        !ptx::mbar_wait(afull(pg & 1), (pg >> 1) & 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
                         ok = false;
                         break;
                     }
@@ -379,6 +520,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                         ptx::tc_commit(accfull(b));
                         ++q;
                     }
+                    if ((ks & 1) == 1 || ks == KS - 1) ++pg;
                     ++g;
                 }
             }
@@ -394,15 +536,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const uint8_t* arow_base = stages + B_BYTES + (row >> 6) * 4096 + (row & 63) * 64;
         const int sw = (row >> 1) & 3;
-        uint32_t g = 0;
+        uint32_t g = 0, pg = 0;
+        uint32_t pair_last0 = 0, pair_last1 = 0;  // last K step of the latest pair on each slot pair
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
             for (int ks = 0; ks < KS; ++ks, ++g) {
-                const int s = g % NS, a = g % NA;
-                // A slot a was last read by the MMAs of K step g - NA, whose
-                // commit completes the `empty` phase of that step's stage
+                const int s = g % NS, a = (pg & 1) * 2 + (ks & 1);
+                // The slots of pair pg were last read by the MMAs of pair
+                // pg - 2; the commit after its last K step completes the
+                // `empty` phase of that step's stage.
+                const uint32_t pl = (pg & 1) ? pair_last1 : pair_last0;
                 if (!warp_wait(full(s), (g / NS) & 1, P.err) ||
-                    (g >= NA && !warp_wait(empty((g - NA) % NS), ((g - NA) / NS) & 1, P.err))) {
+                    ((ks & 1) == 0 && pg >= 2 && !warp_wait(empty(pl % NS), (pl / NS) & 1, P.err))) {
                     ok = false;
                     break;
                 }
@@ -422,9 +567,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 }
                 ptx::tmem_st32(tmem + lane_base + TM_A + a * 32, v);
                 ptx::tmem_wait_st();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(afull(a));
+                if ((ks & 1) == 1 || ks == KS - 1) {  // the stage pair is converted
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(afull(pg & 1));
+                    if (pg & 1) pair_last1 = g; else pair_last0 = g;
+                    ++pg;
+                }
             }
         }
     } else {
@@ -435,13 +584,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         const int row = wq * 32 + lane;
         const bool leader = (wq == 0) && (lane == 0);
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-        uint8_t* my_stg = stg + h * STG_BYTES;
+        uint8_t* my_stg = stg + h * 2 * STG_BYTES;
+        uint32_t ngrp_done = 0;                // staged groups so far (buffer = parity)
         int rs[NGRP * GT];                     // int32 running sums of this group's columns
         uint32_t q = 0;
         bool ok = true;
         WgBarrier wgb{wg_bar(h), 0};
+        int4 e_next = tile_entry(P, blockIdx.x, total_tiles);
         for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-            const TileInfo ti = decode(P, tile);
+            const TileInfo ti = decode(P, tile, e_next);
+            e_next = tile_entry(P, tile + gridDim.x, total_tiles);
             const int tok0 = h * HALF;
             const int ng = max(0, min(NGRP, (ti.nmma - tok0 + GT - 1) / GT));
             for (int c = 0; ok && c < nchunks; ++c) {
@@ -472,14 +624,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 ++q;
                 if (c == nchunks - 1) {
                     // epilogue from the final sums, overlapping the next chunks' MMAs
+#pragma unroll 1
+                    for (int gi = 0; gi < ng; ++gi) {
+                        if (ok) {
+                            int iv[GT];  // this group's sums (predicated moves keep rs in registers)
 #pragma unroll
-                    for (int gi = 0; gi < NGRP; ++gi) {
-                        if (ok && gi < ng) {
-                            int iv[GT];
+                            for (int g2 = 0; g2 < NGRP; ++g2)
+                                if (g2 == gi) {
 #pragma unroll
-                            for (int j = 0; j < GT; ++j) iv[j] = rs[gi * GT + j];
+                                    for (int j = 0; j < GT; ++j) iv[j] = rs[g2 * GT + j];
+                                }
                             const int j0 = tok0 + gi * GT;
-                            if (EPI != EPI_BF16MSG && P.tma_out && j0 + GT <= ti.nvalid) {
+                            if constexpr (EPI == EPI_GU || EPI == EPI_F32) {
+                                float* buf = reinterpret_cast<float*>(my_stg + (ngrp_done & 1) * STG_BYTES);
+                                if (!epilogue_staged<EPI>(P, ti, row, lane, j0, iv, buf, &tmO, wgb, leader))
+                                    ok = false;
+                                ++ngrp_done;
+                            } else if (EPI == EPI_I32 && P.tma_out && j0 + GT <= ti.nvalid) {
                                 if (!epilogue_tma<EPI>(P, ti, row, lane, j0, iv, my_stg, &tmO, wgb, leader))
                                     ok = false;
                             } else {
@@ -537,46 +698,43 @@ __device__ __forceinline__ float block_max(float v, float* s_red) {
     return r;
 }
 
-// SwiGLU of one expert row (g | u from the gate/up GEMM) and its token-wise
-// requantisation: hq as exact fp16 integers, s_h per row.
+// Token-wise requantisation of the SwiGLU output h (its row absmax was
+// reduced by the gate/up GEMM's epilogue): hq as exact fp16 integers, s_h.
 __global__ void __launch_bounds__(256)
-swiglu_requant_kernel(int I, const float* __restrict__ gu, __half* __restrict__ hq,
-                      float* __restrict__ sh) {
-    extern __shared__ float s_h[];
-    __shared__ float s_red[8];
+requant_kernel(int I, const float* __restrict__ h, const unsigned* __restrict__ rowmax,
+               __half* __restrict__ hq, float* __restrict__ sh) {
     const int r = blockIdx.x;
-    const float* g = gu + (long long)r * 2 * I;
-    float amax = 0.f;
-    for (int i = threadIdx.x; i < I; i += blockDim.x) {
-        const float h = __fmul_rn(silu_spec(g[i]), g[I + i]);
-        s_h[i] = h;
-        amax = fmaxf(amax, fabsf(h));
+    const float s = row_scale(__uint_as_float(rowmax[r]));
+    const float4* src = reinterpret_cast<const float4*>(h + (long long)r * I);
+    uint2* dst = reinterpret_cast<uint2*>(hq + (long long)r * I);
+    for (int c = threadIdx.x; c < I / 4; c += blockDim.x) {
+        const float4 v = src[c];
+        int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+        if (s != 0.f) {
+            q0 = quant1(v.x, s); q1 = quant1(v.y, s); q2 = quant1(v.z, s); q3 = quant1(v.w, s);
+        }
+        __half2 a = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+        __half2 b = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
+        uint2 o;
+        o.x = *reinterpret_cast<uint32_t*>(&a);
+        o.y = *reinterpret_cast<uint32_t*>(&b);
+        dst[c] = o;
     }
-    amax = block_max<256>(amax, s_red);
-    const float s = row_scale(amax);
-    __half* out = hq + (long long)r * I;
-    for (int i = threadIdx.x; i < I; i += blockDim.x)
-        out[i] = __int2half_rn(s == 0.f ? 0 : quant1(s_h[i], s));
     if (threadIdx.x == 0) sh[r] = s;
 }
 
-// INT8 return message: token-wise codes of y into the combine row (t, j).
+// INT8 return message: token-wise codes of y (row absmax reduced by the down
+// GEMM's epilogue) into the combine row (t, j).
 __global__ void __launch_bounds__(256)
 retquant_kernel(int H, int k, int lb, long long crow, const float* __restrict__ y,
-                const int32_t* __restrict__ expert_rows, const moe_dispatch_meta* __restrict__ meta,
-                unsigned char* __restrict__ cbuf, float* __restrict__ cscale) {
-    __shared__ float s_red[8];
+                const unsigned* __restrict__ rowmax, const int32_t* __restrict__ expert_rows,
+                const moe_dispatch_meta* __restrict__ meta, unsigned char* __restrict__ cbuf,
+                float* __restrict__ cscale) {
     const int r = blockIdx.x;
     const moe_dispatch_meta m = meta[expert_rows[r]];
     const long long tj = ((long long)m.src_rank * lb + m.batch_slot) * k + m.route_slot;
+    const float s = row_scale(__uint_as_float(rowmax[r]));
     const float4* src = reinterpret_cast<const float4*>(y + (long long)r * H);
-    float amax = 0.f;
-    for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
-        const float4 v = src[c];
-        amax = fmaxf(fmaxf(amax, fabsf(v.x)), fmaxf(fabsf(v.y), fmaxf(fabsf(v.z), fabsf(v.w))));
-    }
-    amax = block_max<256>(amax, s_red);
-    const float s = row_scale(amax);
     uint32_t* dst = reinterpret_cast<uint32_t*>(cbuf + tj * crow);
     for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
         const float4 v = src[c];
@@ -636,14 +794,14 @@ int sm_count() {
 }
 
 template <int EPI>
-cudaError_t launch_gemm(const Params& P, const CUtensorMap& w, const CUtensorMap& x,
+cudaError_t launch_gemm(const Params& P, const CUtensorMap& w, const CUtensorMap (&x)[2],
                         const CUtensorMap& o, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int slot = EPI == EPI_GU ? 0 : 1;
     if (cudaEvent_t ev = prof_event(slot, 0)) cudaEventRecord(ev, st);
-    gemm_tc_kernel<EPI><<<sm_count(), THREADS, SMEM_BYTES, st>>>(w, x, o, P);
+    gemm_tc_kernel<EPI><<<sm_count(), THREADS, SMEM_BYTES, st>>>(w, x[0], x[1], o, P);
     if (cudaEvent_t ev = prof_event(slot, 1)) cudaEventRecord(ev, st);
     count_launches(1);
     return cudaGetLastError();
@@ -653,8 +811,11 @@ bool weight_map(CUtensorMap* m, const int8_t* w, int K, uint64_t rows) {
     return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, K, rows, BK, 64, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-bool act_map(CUtensorMap* m, const __half* x, int K, uint64_t rows) {
-    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, rows, BK, BOX_ROWS,
+// Activation maps: [0] boxes of BOX_ROWS rows, [1] boxes of BN rows.
+bool act_map(CUtensorMap (&m)[2], const __half* x, int K, uint64_t rows) {
+    return make_map(&m[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, rows, BK, BOX_ROWS,
+                    CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(&m[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, rows, BK, BN,
                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -678,21 +839,24 @@ cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long lo
     char* w = static_cast<char*>(ws);
     int* err = reinterpret_cast<int*>(w);
     int32_t* tp = reinterpret_cast<int32_t*>(w + 256);
-    __half* a16 = reinterpret_cast<__half*>(w + 256 + align_up(4LL * (n_groups + 1), 256));
+    int4* ttab = reinterpret_cast<int4*>(w + 256 + align_up(4LL * (n_groups + 1), 256));
+    __half* a16 = reinterpret_cast<__half*>(
+        w + 256 + align_up(4LL * (n_groups + 1), 256) +
+        align_up(16LL * tile_table_entries(n_groups, max_rows, BN), 256));
     cudaError_t e = cudaMemsetAsync(err, 0, 256, st);
     if (e != cudaSuccess) return e;
     count_launches(1);
-    if ((e = launch_tile_prefix(n_groups, BN, offsets, tp, st)) != cudaSuccess) return e;
+    if ((e = launch_tile_prefix(n_groups, BN, offsets, tp, st, ttab)) != cudaSuccess) return e;
     assemble_kernel<<<(unsigned)max_rows, 128, 0, st>>>(K, row_index, A, lda, nullptr, a16, nullptr);
     count_launches(1);
-    CUtensorMap mw, mx, mo;
+    CUtensorMap mw, mx[2], mo;
     const bool tma_out = N % 128 == 0;
-    if (!weight_map(&mw, B, K, (uint64_t)n_groups * N) || !act_map(&mx, a16, K, (uint64_t)max_rows) ||
+    if (!weight_map(&mw, B, K, (uint64_t)n_groups * N) || !act_map(mx, a16, K, (uint64_t)max_rows) ||
         (tma_out && !out_map(&mo, C, true, N, (uint64_t)max_rows, 128)))
         return cudaErrorInvalidValue;
-    if (!tma_out) mo = mx;  // unused
+    if (!tma_out) mo = mx[0];  // unused
     Params P = {};
-    P.G = n_groups; P.offsets = offsets; P.tile_prefix = tp; P.g2s = nullptr;
+    P.G = n_groups; P.offsets = offsets; P.tile_prefix = tp; P.ttab = ttab; P.g2s = nullptr;
     P.K = K; P.rows_per_set = N; P.nout = N; P.mb_count = (N + 127) / 128; P.box1_off = 64;
     P.c_i32 = C; P.err = err; P.tma_out = tma_out;
     return launch_gemm<EPI_I32>(P, mw, mx, mo, st);
@@ -708,10 +872,13 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
         reinterpret_cast<const moe_dispatch_meta*>(static_cast<const char*>(dbuf) + meta_off);
     int* err = ws_ptr<int>(ws, 0);
     int32_t* tp = ws_ptr<int32_t>(ws, wl.tiles);
+    int4* ttab = ws_ptr<int4>(ws, wl.ttab);
     float* s_row = ws_ptr<float>(ws, wl.s_row);
     float* sh = ws_ptr<float>(ws, wl.sh);
     __half* a16 = ws_ptr<__half>(ws, wl.a16);
-    float* gu = ws_ptr<float>(ws, wl.gu);
+    float* hbuf = ws_ptr<float>(ws, wl.hbuf);
+    unsigned* hmax = ws_ptr<unsigned>(ws, wl.rowmax);
+    unsigned* ymax = hmax + M;
     __half* hq16 = ws_ptr<__half>(ws, wl.hq16);
     float* ybuf = ws_ptr<float>(ws, wl.ybuf);
     unsigned char* cb = static_cast<unsigned char*>(cbuf);
@@ -720,18 +887,21 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     cudaError_t e;
 
     if ((e = cudaMemsetAsync(err, 0, 256, st)) != cudaSuccess) return e;
-    count_launches(1);
-    if ((e = launch_tile_prefix(d.E_phys, BN, expert_offsets, tp, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(hmax, 0, sizeof(unsigned) * 2 * M, st)) != cudaSuccess) return e;
+    count_launches(2);
+    if ((e = launch_tile_prefix(d.E_phys, BN, expert_offsets, tp, st, ttab, w.phys_to_weight)) !=
+        cudaSuccess)
+        return e;
     assemble_kernel<<<(unsigned)M, 128, 0, st>>>(d.H, expert_rows, static_cast<const int8_t*>(dbuf),
                                                  d.drow, meta, a16, s_row);
     count_launches(1);
 
-    CUtensorMap mwgu, mx1, mo1, mwd, mx2, mo2;
+    CUtensorMap mwgu, mx1[2], mo1, mwd, mx2[2], mo2;
     if (!weight_map(&mwgu, w.w_gate_up, d.H, (uint64_t)E_w * 2 * d.I) ||
-        !act_map(&mx1, a16, d.H, (uint64_t)M) ||
-        !out_map(&mo1, gu, false, 2ull * d.I, (uint64_t)M, 64) ||
+        !act_map(mx1, a16, d.H, (uint64_t)M) ||
+        !out_map(&mo1, hbuf, false, (uint64_t)d.I, (uint64_t)M, 64) ||
         !weight_map(&mwd, w.w_down, d.I, (uint64_t)E_w * d.H) ||
-        !act_map(&mx2, hq16, d.I, (uint64_t)M))
+        !act_map(mx2, hq16, d.I, (uint64_t)M))
         return cudaErrorInvalidValue;
     const bool y_tma = int8_ret && d.H >= 128;
     if (y_tma) {
@@ -741,27 +911,26 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     }
 
     Params P1 = {};
-    P1.G = d.E_phys; P1.offsets = expert_offsets; P1.tile_prefix = tp; P1.g2s = w.phys_to_weight;
+    P1.G = d.E_phys; P1.offsets = expert_offsets; P1.tile_prefix = tp; P1.ttab = ttab;
+    P1.g2s = w.phys_to_weight;
     P1.K = d.H; P1.rows_per_set = 2 * d.I; P1.nout = d.I; P1.mb_count = d.I / 64; P1.box1_off = d.I;
-    P1.s_row = s_row; P1.s_ch = w.s_gate_up; P1.out_f32 = gu; P1.err = err; P1.tma_out = 1;
+    P1.s_row = s_row; P1.s_ch = w.s_gate_up; P1.out_f32 = hbuf; P1.rowmax = hmax; P1.err = err;
+    P1.tma_out = 1;
     if ((e = launch_gemm<EPI_GU>(P1, mwgu, mx1, mo1, st)) != cudaSuccess) return e;
 
-    if (sizeof(float) * d.I > 48 * 1024 &&
-        (e = cudaFuncSetAttribute(swiglu_requant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)(sizeof(float) * d.I))) != cudaSuccess)
-        return e;
-    swiglu_requant_kernel<<<(unsigned)M, 256, sizeof(float) * d.I, st>>>(d.I, gu, hq16, sh);
+    requant_kernel<<<(unsigned)M, 256, 0, st>>>(d.I, hbuf, hmax, hq16, sh);
     count_launches(1);
 
     Params P2 = {};
-    P2.G = d.E_phys; P2.offsets = expert_offsets; P2.tile_prefix = tp; P2.g2s = w.phys_to_weight;
+    P2.G = d.E_phys; P2.offsets = expert_offsets; P2.tile_prefix = tp; P2.ttab = ttab;
+    P2.g2s = w.phys_to_weight;
     P2.K = d.I; P2.rows_per_set = d.H; P2.nout = d.H; P2.mb_count = (d.H + 127) / 128; P2.box1_off = 64;
     P2.s_row = sh; P2.s_ch = w.s_down; P2.err = err; P2.tma_out = y_tma;
     if (int8_ret) {
-        P2.out_f32 = ybuf;
+        P2.out_f32 = ybuf; P2.rowmax = ymax;
         if ((e = launch_gemm<EPI_F32>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
-        retquant_kernel<<<(unsigned)M, 256, 0, st>>>(d.H, d.k, d.lb, d.crow, ybuf, expert_rows, meta,
-                                                     cb, reinterpret_cast<float*>(cb + scale_off));
+        retquant_kernel<<<(unsigned)M, 256, 0, st>>>(d.H, d.k, d.lb, d.crow, ybuf, ymax, expert_rows,
+                                                     meta, cb, reinterpret_cast<float*>(cb + scale_off));
         count_launches(1);
     } else {
         P2.expert_rows = expert_rows; P2.meta = meta; P2.cbuf = cb; P2.crow = d.crow; P2.k = d.k; P2.lb = d.lb;

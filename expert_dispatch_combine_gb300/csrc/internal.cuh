@@ -37,6 +37,15 @@ inline long long align_up(long long v, long long a) { return (v + a - 1) / a * a
 // The tensor-core expert FFN needs K multiples of 64 for both GEMMs.
 inline bool ffn_uses_tc(const Dims& d) { return d.H % 64 == 0 && d.I % 64 == 0; }
 
+// Token rows per tile of the tensor-core grouped GEMM.
+constexpr int kTcTileRows = 192;
+
+// Token tiles of a grouped GEMM over n_groups groups and max_rows rows, at
+// most bm rows per tile (each group adds at most one partial tile).
+inline long long tile_table_entries(int n_groups, long long max_rows, int bm) {
+    return max_rows / bm + n_groups + 1;
+}
+
 // Workspace carve-up.  Every region is 256-byte aligned; offset 0 holds the
 // int32 device status word (MOE_OK or MOE_ERR_TIMEOUT).
 struct WsLayout {
@@ -45,15 +54,17 @@ struct WsLayout {
     long long hist;        // int32 [S][E_phys]
     long long src_base;    // int32 [S][E_phys]
     long long tiles;       // int32 [E_phys + 1]  grouped-GEMM tile prefix
+    long long ttab;        // int4  [tile_table_entries]  (set, first row, rows, group) per token tile
     long long sh;          // f32   [T*k]   requantisation scale of h
     // SIMT expert FFN
     long long acc_gu;      // int32 [T*k][2I]
     long long hq;          // int8  [T*k][I]
     long long acc_d;       // int32 [T*k][H]
     // tensor-core expert FFN
+    long long rowmax;      // u32   [2][T*k]  absmax of h and of y (float bits)
     long long s_row;       // f32   [T*k]     dispatch scale of each expert row
     long long a16;         // fp16  [T*k][H]  expert input rows
-    long long gu;          // f32   [T*k][2I] gate | up projections
+    long long hbuf;        // f32   [T*k][I]  SwiGLU output h
     long long hq16;        // fp16  [T*k][I]  requantised SwiGLU output
     long long ybuf;        // f32   [T*k][H]  expert output (INT8 return messages only)
     long long total;
@@ -69,12 +80,14 @@ inline WsLayout make_ws(const Dims& d) {
     w.hist = o;       o = align_up(o + 4LL * d.S * d.E_phys, 256);
     w.src_base = o;   o = align_up(o + 4LL * d.S * d.E_phys, 256);
     w.tiles = o;      o = align_up(o + 4LL * (d.E_phys + 1), 256);
+    w.ttab = o;       o = align_up(o + 16LL * tile_table_entries(d.E_phys, tk, kTcTileRows), 256);
     w.sh = o;         o = align_up(o + 4 * tk, 256);
     w.tc = ffn_uses_tc(d);
     if (w.tc) {
+        w.rowmax = o; o = align_up(o + 8 * tk, 256);
         w.s_row = o;  o = align_up(o + 4 * tk, 256);
         w.a16 = o;    o = align_up(o + 2 * tk * d.H, 256);
-        w.gu = o;     o = align_up(o + 8 * tk * d.I, 256);
+        w.hbuf = o;   o = align_up(o + 4 * tk * d.I, 256);
         w.hq16 = o;   o = align_up(o + 2 * tk * d.I, 256);
         if (d.cfmt == MOE_MSG_INT8) { w.ybuf = o; o = align_up(o + 4 * tk * d.H, 256); }
     } else {
@@ -86,9 +99,11 @@ inline WsLayout make_ws(const Dims& d) {
     return w;
 }
 
-// Workspace of moe_grouped_gemm_s8: [status][tile prefix][fp16 A rows].
+// Workspace of moe_grouped_gemm_s8: [status][tile prefix][tile table][fp16 A rows].
 inline long long gemm_ws_bytes(int n_groups, long long max_rows, int K) {
-    return 256 + align_up(4LL * (n_groups + 1), 256) + align_up(2LL * max_rows * K, 256);
+    return 256 + align_up(4LL * (n_groups + 1), 256) +
+           align_up(16LL * tile_table_entries(n_groups, max_rows, kTcTileRows), 256) +
+           align_up(2LL * max_rows * K, 256);
 }
 
 template <typename T>
@@ -118,8 +133,11 @@ cudaError_t launch_grouped_gemm_s8(int n_groups, const int32_t* offsets, long lo
                                    const int8_t* B, long long b_group_stride,
                                    const int32_t* group_to_set, int N, int K, int32_t* C,
                                    int32_t* tile_prefix, cudaStream_t st);
+// Exclusive prefix of the token tiles (at most BM rows) of each of G groups,
+// tile_prefix[G] = their total; with a non-null `table`, also one entry per
+// token tile: (weight set = g2s[g] or g, first row, rows, group g).
 cudaError_t launch_tile_prefix(int G, int BM, const int32_t* offsets, int32_t* tile_prefix,
-                               cudaStream_t st);
+                               cudaStream_t st, int4* table = nullptr, const int32_t* g2s = nullptr);
 cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long long max_rows,
                                    const int32_t* row_index, const int8_t* A, long long lda,
                                    const int8_t* B, int N, int K, int32_t* C, void* ws,

@@ -203,6 +203,29 @@ def test_grouped_gemm_exact_worst_case(K, N):
     assert B.moe_device_status(ws) == 0
 
 
+@pytest.mark.parametrize("K", [64, 192, 320])
+def test_grouped_gemm_odd_stage_counts_many_tiles(K):
+    """1, 3 or 5 K stages of 64 per tile, and several tiles per CTA, so that
+    stage pairs of one element follow each other across tiles."""
+    rng = np.random.default_rng(K + 1)
+    G, N = 4, 512
+    sizes = np.array([6000, 5999, 6100, 5901])
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    M = int(offs[-1])
+    A = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    Bw = rng.integers(-127, 128, size=(G, N, K)).astype(np.int8)
+    ref = np.empty((M, N), np.int64)
+    for g in range(G):
+        ref[offs[g]:offs[g + 1]] = A[offs[g]:offs[g + 1]].astype(np.int64) @ Bw[g].astype(np.int64).T
+    ws = torch.empty(B.moe_gemm_workspace_bytes(G, M, K), dtype=torch.uint8, device="cuda")
+    C = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    B.moe_grouped_gemm_s8(torch.from_numpy(offs).cuda(), M, torch.from_numpy(A).cuda(), K,
+                          torch.from_numpy(Bw).cuda(), C, ws)
+    torch.cuda.synchronize()
+    assert (_np(C).astype(np.int64) == ref).all()
+    assert B.moe_device_status(ws) == 0
+
+
 @pytest.mark.parametrize("N,K,lda", [(48, 96, 112), (144, 128, 160), (16, 1024, 1024)])
 def test_grouped_gemm_gather_rows(N, K, lda):
     rng = np.random.default_rng(1)
