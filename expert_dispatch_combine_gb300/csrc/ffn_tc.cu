@@ -34,7 +34,8 @@
 //   Epilogue: each 16-token group is scaled, staged in shared memory and
 //     written with one TMA tensor store (partial groups use plain stores).
 // Warp roles (16 warps): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
-// warps 4-7 converter, warps 8-15 two drain/epilogue warpgroups.  Register
+// warp 2 L2 prefetcher, warps 4-7 converter, warps 8-15 two drain/epilogue
+// warpgroups.  Register
 // budgets are moved between warpgroups with setmaxnreg (the totals stay
 // within the launch allocation).  Each warpgroup covers the four TMEM lane
 // quarters.
@@ -66,15 +67,18 @@ constexpr int GT = 16;                           // tokens per epilogue group
 constexpr int HALF = BN / 2;                     // token columns per drain warpgroup
 constexpr int NGRP = HALF / GT;                  // 6 groups
 constexpr int STG_BYTES = GT * 128 * 4;          // 8 KB staging buffer; two per drain warpgroup
-constexpr int NBARS = 2 * NS + 2 + 4 + 1 + 2;
+constexpr int NP = NS / 2;                       // stage pairs in shared memory
+constexpr int CKP = CK / 2;                      // stage pairs per exact chunk
+constexpr int NBARS = 2 * NP + 2 + 4 + 1 + 2;
 constexpr uint32_t TM_ACC = 0, TM_A = 2 * BN, TM_COLS = 512;
 constexpr int THREADS = 512;
 constexpr int SMEM_BYTES = NS * STAGE_BYTES + 4 * STG_BYTES + NBARS * 8 + 16 + 1024;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 20000000ull;
+constexpr uint32_t PF_AHEAD = 4;                 // L2 prefetch distance, stage pairs beyond the producer
 // per-thread register budgets after setmaxnreg: 128 threads each at
-// 48 (producer/MMA) + 80 (converter) + 2 x 184 (drains) = 63,488 <= 512 x 128
-constexpr uint32_t REG_CTRL = 48, REG_CONV = 80, REG_DRAIN = 184;
+// 56 (producer/MMA) + 80 (converter) + 2 x 184 (drains) = 64,512 <= 512 x 128
+constexpr uint32_t REG_CTRL = 56, REG_CONV = 80, REG_DRAIN = 184;
 static_assert(128 * (REG_CTRL + REG_CONV + 2 * REG_DRAIN) <= THREADS * 128, "register split");
 static_assert(SMEM_BYTES <= 227 * 1024, "dynamic shared memory per CTA");
 static_assert(NA == 4 && TM_A + NA * 32 <= TM_COLS, "two accumulators and two pairs of A slots in TMEM");
@@ -383,21 +387,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     uint8_t* stg = smem + NS * STAGE_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE_BYTES + 4 * STG_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+    volatile uint32_t* prod_progress = tmem_slot + 1;  // K stages the producer has issued
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
-    auto full = [&](int s) { return bar(s); };
-    auto empty = [&](int s) { return bar(NS + s); };
-    auto afull = [&](int p) { return bar(2 * NS + p); };  // A slots of a stage pair converted
-    auto accfull = [&](int b) { return bar(2 * NS + 2 + b); };
-    auto accempty = [&](int b) { return bar(2 * NS + 2 + 2 + b); };
-    const uint32_t done_bar = bar(2 * NS + 2 + 4);
-    auto wg_bar = [&](int h) { return bar(2 * NS + 2 + 5 + h); };
+    auto fullp = [&](int sp) { return bar(sp); };        // both stages of pair slot sp loaded
+    auto emptyp = [&](int sp) { return bar(NP + sp); };  // pair slot sp consumed by the MMAs
+    auto afull = [&](int p) { return bar(2 * NP + p); };  // A slots of a stage pair converted
+    auto accfull = [&](int b) { return bar(2 * NP + 2 + b); };
+    auto accempty = [&](int b) { return bar(2 * NP + 2 + 2 + b); };
+    const uint32_t done_bar = bar(2 * NP + 2 + 4);
+    auto wg_bar = [&](int h) { return bar(2 * NP + 2 + 5 + h); };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            ptx::mbar_init(full(s), 1);
-            ptx::mbar_init(empty(s), 1);
+        *prod_progress = 0;
+        for (int sp = 0; sp < NP; ++sp) {
+            ptx::mbar_init(fullp(sp), 1);
+            ptx::mbar_init(emptyp(sp), 1);
         }
         for (int p = 0; p < 2; ++p) ptx::mbar_init(afull(p), 4);
         for (int b = 0; b < 2; ++b) {
@@ -425,15 +431,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     const uint32_t tmem = *tmem_slot;
 
     const int total_tiles = P.tile_prefix[P.G] * P.mb_count;
-    const int KS = P.K / BK;
-    const int nchunks = (KS + CK - 1) / CK;
+    // K stages in pairs; an odd count gets one more stage entirely beyond K,
+    // which TMA fills with zeros (it adds nothing to the sums)
+    const int KSP = (P.K / BK + 1) / 2;
+    const int nchunks = (2 * KSP + CK - 1) / CK;
     const int wgi = warp >> 2;
 
     if (wgi == 0) {
         reg_dealloc<REG_CTRL>();
         if (warp == 0 && lane == 0) {
             // -------------------------------------------- TMA producer
-            uint32_t g = 0;
+            // One pair of stages per step: one wait for the pair slot, one
+            // expect_tx for both stages' bytes, then the loads of both.
+            uint32_t pr = 0;  // stage pairs issued
             bool ok = true;
             int4 e_next = tile_entry(P, blockIdx.x, total_tiles);
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
@@ -446,48 +456,97 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 // only the 32-row boxes they need
                 const int nb = (ti.nmma + BOX_ROWS - 1) / BOX_ROWS;
                 const bool one_box = nb == BN / BOX_ROWS;
-                const uint32_t bytes = A_BYTES + nb * BOX_BYTES;
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int s = g % NS;
-                    // once per stage pair: the MMAs complete in order, so the
-                    // release of the pair's later stage implies the earlier one
-                    if ((ks & 1) == 0) {
-                        const uint32_t gl = ks + 1 < KS ? g + 1 : g;
-                        if (!ptx::mbar_wait(empty(gl % NS), ((gl / NS) & 1) ^ 1, P.err, WAIT_NS,
-                                            MOE_ERR_TIMEOUT)) {
-                            ok = false;
-                            break;
+                const uint32_t bytes = 2 * (A_BYTES + nb * BOX_BYTES);
+                for (int kp = 0; kp < KSP; ++kp, ++pr) {
+                    const int sp = pr % NP;
+                    if (!ptx::mbar_wait(emptyp(sp), ((pr / NP) & 1) ^ 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_expect_tx(fullp(sp), bytes);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const uint32_t st = ptx::smem_addr(stages + (2 * sp + j) * STAGE_BYTES);
+                        const int x = (2 * kp + j) * BK;  // beyond K (padding stage): zero fill
+                        ptx::tma_load_2d(st + B_BYTES, &tmW, x, yw0, fullp(sp));
+                        ptx::tma_load_2d(st + B_BYTES + 4096, &tmW, x, yw1, fullp(sp));
+                        if (one_box) {
+                            ptx::tma_load_2d(st, &tmXb, x, ti.r0, fullp(sp));
+                        } else {
+                            for (int b = 0; b < nb; ++b)
+                                ptx::tma_load_2d(st + b * BOX_BYTES, &tmX, x, ti.r0 + b * BOX_ROWS, fullp(sp));
                         }
                     }
-                    const uint32_t st = ptx::smem_addr(stages + s * STAGE_BYTES);
-                    ptx::mbar_expect_tx(full(s), bytes);
-                    ptx::tma_load_2d(st + B_BYTES, &tmW, ks * BK, yw0, full(s));
-                    ptx::tma_load_2d(st + B_BYTES + 4096, &tmW, ks * BK, yw1, full(s));
-                    if (one_box) {
-                        ptx::tma_load_2d(st, &tmXb, ks * BK, ti.r0, full(s));
-                    } else {
-                        for (int j = 0; j < nb; ++j)
-                            ptx::tma_load_2d(st + j * BOX_BYTES, &tmX, ks * BK, ti.r0 + j * BOX_ROWS, full(s));
-                    }
-                    ++g;
+                    *prod_progress = pr + 1;
                 }
             }
             if (!ok) {  // let the loads already issued land before leaving
-                for (uint32_t j = (g > NS ? g - NS : 0); j < g; ++j)
-                    mbar_wait_quiet(full(j % NS), (j / NS) & 1, DRAIN_NS);
+                for (uint32_t j = (pr > NP ? pr - NP : 0); j < pr; ++j)
+                    mbar_wait_quiet(fullp(j % NP), (j / NP) & 1, DRAIN_NS);
+            }
+        } else if (warp == 2 && lane == 0) {
+            // ------------------------------------------------- L2 prefetcher
+            // Walks the producer's sequence of stage pairs and asks L2 for
+            // each one up to PF_AHEAD pairs before the producer loads it, so
+            // that a weight block's first reader does not wait on DRAM latency
+            // with only NS stages in flight.  It paces itself on the
+            // producer's progress word (no barrier phases) and stops on an
+            // error or when the producer makes no progress for WAIT_NS.
+            uint32_t hp = 0, seen = 0;
+            uint64_t t_last = ptx::globaltimer();
+            bool live = true;
+            int4 e_next = tile_entry(P, blockIdx.x, total_tiles);
+            for (int tile = blockIdx.x; live && tile < total_tiles; tile += gridDim.x) {
+                const TileInfo ti = decode(P, tile, e_next);
+                e_next = tile_entry(P, tile + gridDim.x, total_tiles);
+                const int yw0 = ti.set * P.rows_per_set + (EPI == EPI_GU ? ti.mb * 64 : ti.mb * 128);
+                const int yw1 = yw0 + P.box1_off;
+                const int nb = (ti.nmma + BOX_ROWS - 1) / BOX_ROWS;
+                for (int kp = 0; live && kp < KSP; ++kp, ++hp) {
+                    for (;;) {
+                        const uint32_t pg = *prod_progress;
+                        if (hp < pg + PF_AHEAD) break;
+                        const uint64_t now = ptx::globaltimer();
+                        if (pg != seen) {
+                            seen = pg;
+                            t_last = now;
+                        }
+                        if (*reinterpret_cast<volatile int*>(P.err) != 0 || now - t_last > WAIT_NS) {
+                            live = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    if (!live) break;
+                    for (int j = 0; j < 2; ++j) {
+                        const int x = (2 * kp + j) * BK;
+                        if (x >= P.K) break;
+                        ptx::tma_prefetch_2d(&tmW, x, yw0);
+                        ptx::tma_prefetch_2d(&tmW, x, yw1);
+                        if (nb == BN / BOX_ROWS) {
+                            ptx::tma_prefetch_2d(&tmXb, x, ti.r0);
+                        } else {
+                            for (int b = 0; b < nb; ++b) ptx::tma_prefetch_2d(&tmX, x, ti.r0 + b * BOX_ROWS);
+                        }
+                    }
+                }
             }
         } else if (warp == 1 && lane == 0) {
             // --------------------------------------------- MMA issuer
-            uint32_t g = 0, q = 0, pg = 0;
+            // Per stage pair: one wait (converted weights, which the converter
+            // signals only after it has seen the pair's loads land), 8 MMAs at
+            // constant descriptor offsets, one commit that releases the pair.
+            uint32_t pr = 0, q = 0;
             bool ok = true;
+            const uint64_t bdesc0 = ptx::sdesc_k_sw128(ptx::smem_addr(stages));
             int4 e_next = tile_entry(P, blockIdx.x, total_tiles);
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
                 const TileInfo ti = decode(P, tile, e_next);
                 e_next = tile_entry(P, tile + gridDim.x, total_tiles);
                 const uint32_t idesc = ptx::idesc_f16_f32(128, ti.nmma);
-                for (int ks = 0; ks < KS; ++ks) {
-                    const bool first = (ks % CK) == 0;
-                    const bool last = (ks % CK) == CK - 1 || ks == KS - 1;
+                for (int kp = 0; kp < KSP; ++kp, ++pr) {
+                    const bool first = (kp % CKP) == 0;
+                    const bool last = (kp % CKP) == CKP - 1 || kp == KSP - 1;
                     const uint32_t b = q & 1;
                     if (first) {
                         // the drains must have taken this buffer's previous chunk
@@ -496,32 +555,25 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                             break;
                         }
                     }
-                    const int s = g % NS, a = (pg & 1) * 2 + (ks & 1);
-                    // One wait per stage pair (ks, ks+1) of the tile; a tile
-                    // with an odd stage count ends with a single-stage pair.
-                    // The converter arrives on afull only after it has seen
-                    // full(s) of both stages complete, so this wait also
-                    // covers their activation tiles.
-                    if ((ks & 1) == 0 &&
-                        !ptx::mbar_wait(afull(pg & 1), (pg >> 1) & 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
+                    if (!ptx::mbar_wait(afull(pr & 1), (pr >> 1) & 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t bbase = ptx::smem_addr(stages + s * STAGE_BYTES);
-                    const uint32_t abase = tmem + TM_A + a * 32;
+                    const int sp = pr % NP;
+                    const uint64_t bd = bdesc0 + static_cast<uint64_t>((2 * sp * STAGE_BYTES) >> 4);
+                    const uint32_t abase = tmem + TM_A + (pr & 1) * 64;
                     const uint32_t d = tmem + TM_ACC + b * BN;
+                    ptx::mma_f16_ts(d, abase, bd, idesc, first ? 0u : 1u);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        ptx::mma_f16_ts(d, abase + kk * 8, ptx::sdesc_k_sw128(bbase + kk * 32), idesc,
-                                        (first && kk == 0) ? 0u : 1u);
-                    ptx::tc_commit(empty(s));  // stage s and A slot a are consumed
+                    for (int kk = 1; kk < 2 * BK / 16; ++kk)
+                        ptx::mma_f16_ts(d, abase + kk * 8,
+                                        bd + (kk >> 2) * (STAGE_BYTES >> 4) + (kk & 3) * 2, idesc, 1u);
+                    ptx::tc_commit(emptyp(sp));  // both stages and their A slots are consumed
                     if (last) {
                         ptx::tc_commit(accfull(b));
                         ++q;
                     }
-                    if ((ks & 1) == 1 || ks == KS - 1) ++pg;
-                    ++g;
                 }
             }
             // every MMA issued above must be complete before TMEM is freed
@@ -536,44 +588,41 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const uint8_t* arow_base = stages + B_BYTES + (row >> 6) * 4096 + (row & 63) * 64;
         const int sw = (row >> 1) & 3;
-        uint32_t g = 0, pg = 0;
-        uint32_t pair_last0 = 0, pair_last1 = 0;  // last K step of the latest pair on each slot pair
+        uint32_t pr = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-            for (int ks = 0; ks < KS; ++ks, ++g) {
-                const int s = g % NS, a = (pg & 1) * 2 + (ks & 1);
-                // The slots of pair pg were last read by the MMAs of pair
-                // pg - 2; the commit after its last K step completes the
-                // `empty` phase of that step's stage.
-                const uint32_t pl = (pg & 1) ? pair_last1 : pair_last0;
-                if (!warp_wait(full(s), (g / NS) & 1, P.err) ||
-                    ((ks & 1) == 0 && pg >= 2 && !warp_wait(empty(pl % NS), (pl / NS) & 1, P.err))) {
+            for (int kp = 0; kp < KSP; ++kp, ++pr) {
+                const int sp = pr % NP;
+                // The A slots of pair pr were last read by the MMAs of pair
+                // pr - 2, whose commit completed the `empty` phase of its slot.
+                const uint32_t pq = pr - 2;
+                if (!warp_wait(fullp(sp), (pr / NP) & 1, P.err) ||
+                    (pr >= 2 && !warp_wait(emptyp(pq % NP), (pq / NP) & 1, P.err))) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                // this thread's weight row: 64 int8 in 64-byte rows, 64B swizzle
-                const uint8_t* arow = arow_base + s * STAGE_BYTES;
-                uint4 w[4];
+#pragma unroll 1
+                for (int j = 0; j < 2; ++j) {
+                    // this thread's weight row: 64 int8 in 64-byte rows, 64B swizzle
+                    const uint8_t* arow = arow_base + (2 * sp + j) * STAGE_BYTES;
+                    uint4 w[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ sw) << 4));
-                uint32_t v[32];
+                    for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ sw) << 4));
+                    uint32_t v[32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    s8x4_to_f16x4(w[c].x, v[8 * c + 0], v[8 * c + 1]);
-                    s8x4_to_f16x4(w[c].y, v[8 * c + 2], v[8 * c + 3]);
-                    s8x4_to_f16x4(w[c].z, v[8 * c + 4], v[8 * c + 5]);
-                    s8x4_to_f16x4(w[c].w, v[8 * c + 6], v[8 * c + 7]);
+                    for (int c = 0; c < 4; ++c) {
+                        s8x4_to_f16x4(w[c].x, v[8 * c + 0], v[8 * c + 1]);
+                        s8x4_to_f16x4(w[c].y, v[8 * c + 2], v[8 * c + 3]);
+                        s8x4_to_f16x4(w[c].z, v[8 * c + 4], v[8 * c + 5]);
+                        s8x4_to_f16x4(w[c].w, v[8 * c + 6], v[8 * c + 7]);
+                    }
+                    ptx::tmem_st32(tmem + lane_base + TM_A + (pr & 1) * 64 + j * 32, v);
+                    ptx::tmem_wait_st();
                 }
-                ptx::tmem_st32(tmem + lane_base + TM_A + a * 32, v);
-                ptx::tmem_wait_st();
-                if ((ks & 1) == 1 || ks == KS - 1) {  // the stage pair is converted
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(afull(pg & 1));
-                    if (pg & 1) pair_last1 = g; else pair_last0 = g;
-                    ++pg;
-                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(afull(pr & 1));
             }
         }
     } else {
