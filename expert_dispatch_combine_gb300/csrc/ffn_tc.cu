@@ -34,8 +34,7 @@
 //   Epilogue: each 16-token group is scaled, staged in shared memory and
 //     written with one TMA tensor store (partial groups use plain stores).
 // Warp roles (16 warps): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
-// warp 2 L2 prefetcher, warps 4-7 converter, warps 8-15 two drain/epilogue
-// warpgroups.  Register
+// warps 4-7 converter, warps 8-15 two drain/epilogue warpgroups.  Register
 // budgets are moved between warpgroups with setmaxnreg (the totals stay
 // within the launch allocation).  Each warpgroup covers the four TMEM lane
 // quarters.
@@ -75,7 +74,6 @@ constexpr int THREADS = 512;
 constexpr int SMEM_BYTES = NS * STAGE_BYTES + 4 * STG_BYTES + NBARS * 8 + 16 + 1024;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 20000000ull;
-constexpr uint32_t PF_AHEAD = 4;                 // L2 prefetch distance, stage pairs beyond the producer
 // per-thread register budgets after setmaxnreg: 128 threads each at
 // 56 (producer/MMA) + 80 (converter) + 2 x 184 (drains) = 64,512 <= 512 x 128
 constexpr uint32_t REG_CTRL = 56, REG_CONV = 80, REG_DRAIN = 184;
@@ -387,7 +385,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     uint8_t* stg = smem + NS * STAGE_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE_BYTES + 4 * STG_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
-    volatile uint32_t* prod_progress = tmem_slot + 1;  // K stages the producer has issued
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
@@ -400,7 +397,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     auto wg_bar = [&](int h) { return bar(2 * NP + 2 + 5 + h); };
 
     if (threadIdx.x == 0) {
-        *prod_progress = 0;
         for (int sp = 0; sp < NP; ++sp) {
             ptx::mbar_init(fullp(sp), 1);
             ptx::mbar_init(emptyp(sp), 1);
@@ -477,59 +473,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                                 ptx::tma_load_2d(st + b * BOX_BYTES, &tmX, x, ti.r0 + b * BOX_ROWS, fullp(sp));
                         }
                     }
-                    *prod_progress = pr + 1;
                 }
             }
             if (!ok) {  // let the loads already issued land before leaving
                 for (uint32_t j = (pr > NP ? pr - NP : 0); j < pr; ++j)
                     mbar_wait_quiet(fullp(j % NP), (j / NP) & 1, DRAIN_NS);
-            }
-        } else if (warp == 2 && lane == 0) {
-            // ------------------------------------------------- L2 prefetcher
-            // Walks the producer's sequence of stage pairs and asks L2 for
-            // each one up to PF_AHEAD pairs before the producer loads it, so
-            // that a weight block's first reader does not wait on DRAM latency
-            // with only NS stages in flight.  It paces itself on the
-            // producer's progress word (no barrier phases) and stops on an
-            // error or when the producer makes no progress for WAIT_NS.
-            uint32_t hp = 0, seen = 0;
-            uint64_t t_last = ptx::globaltimer();
-            bool live = true;
-            int4 e_next = tile_entry(P, blockIdx.x, total_tiles);
-            for (int tile = blockIdx.x; live && tile < total_tiles; tile += gridDim.x) {
-                const TileInfo ti = decode(P, tile, e_next);
-                e_next = tile_entry(P, tile + gridDim.x, total_tiles);
-                const int yw0 = ti.set * P.rows_per_set + (EPI == EPI_GU ? ti.mb * 64 : ti.mb * 128);
-                const int yw1 = yw0 + P.box1_off;
-                const int nb = (ti.nmma + BOX_ROWS - 1) / BOX_ROWS;
-                for (int kp = 0; live && kp < KSP; ++kp, ++hp) {
-                    for (;;) {
-                        const uint32_t pg = *prod_progress;
-                        if (hp < pg + PF_AHEAD) break;
-                        const uint64_t now = ptx::globaltimer();
-                        if (pg != seen) {
-                            seen = pg;
-                            t_last = now;
-                        }
-                        if (*reinterpret_cast<volatile int*>(P.err) != 0 || now - t_last > WAIT_NS) {
-                            live = false;
-                            break;
-                        }
-                        __nanosleep(64);
-                    }
-                    if (!live) break;
-                    for (int j = 0; j < 2; ++j) {
-                        const int x = (2 * kp + j) * BK;
-                        if (x >= P.K) break;
-                        ptx::tma_prefetch_2d(&tmW, x, yw0);
-                        ptx::tma_prefetch_2d(&tmW, x, yw1);
-                        if (nb == BN / BOX_ROWS) {
-                            ptx::tma_prefetch_2d(&tmXb, x, ti.r0);
-                        } else {
-                            for (int b = 0; b < nb; ++b) ptx::tma_prefetch_2d(&tmX, x, ti.r0 + b * BOX_ROWS);
-                        }
-                    }
-                }
             }
         } else if (warp == 1 && lane == 0) {
             // --------------------------------------------- MMA issuer
