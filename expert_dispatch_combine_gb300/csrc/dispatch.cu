@@ -22,6 +22,7 @@
 //                  codes into shared memory, then k bulk asynchronous copies
 //                  (shared -> global) of the code row into the k slots, plus
 //                  the 16-byte metadata and the expert row list entries.
+#include "device_math.cuh"
 #include "internal.cuh"
 
 namespace moe {
@@ -155,15 +156,9 @@ __device__ __forceinline__ void bulk_store_s2g(void* gdst, const void* ssrc, uns
 __device__ __forceinline__ float bf16_lo(unsigned w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(unsigned w) { return __uint_as_float(w & 0xffff0000u); }
 
-__device__ __forceinline__ unsigned quant4(float a, float b, float c, float d, float s) {
-    int q0 = __float2int_rn(__fdiv_rn(a, s));
-    int q1 = __float2int_rn(__fdiv_rn(b, s));
-    int q2 = __float2int_rn(__fdiv_rn(c, s));
-    int q3 = __float2int_rn(__fdiv_rn(d, s));
-    q0 = max(-127, min(127, q0));
-    q1 = max(-127, min(127, q1));
-    q2 = max(-127, min(127, q2));
-    q3 = max(-127, min(127, q3));
+__device__ __forceinline__ unsigned quant4(float a, float b, float c, float d, float s, float rs) {
+    const int q0 = quant1_row(a, s, rs), q1 = quant1_row(b, s, rs);
+    const int q2 = quant1_row(c, s, rs), q3 = quant1_row(d, s, rs);
     return (unsigned)(q0 & 0xff) | ((unsigned)(q1 & 0xff) << 8) | ((unsigned)(q2 & 0xff) << 16) |
            ((unsigned)(q3 & 0xff) << 24);
 }
@@ -216,14 +211,15 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
         }
         __syncthreads();
         scale = s_scale;
+        const float rscale = quant_rcp(scale);
         for (int c = threadIdx.x; c < nch; c += kScatterThreads) {
             uint4 v = srow[c];
             uint2 q;
             if (scale == 0.f) {
                 q.x = 0u; q.y = 0u;
             } else {
-                q.x = quant4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y), scale);
-                q.y = quant4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w), scale);
+                q.x = quant4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y), scale, rscale);
+                q.y = quant4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w), scale, rscale);
             }
             scode[c] = q;
         }

@@ -702,13 +702,15 @@ requant_kernel(int I, const float* __restrict__ h, const unsigned* __restrict__ 
                __half* __restrict__ hq, float* __restrict__ sh) {
     const int r = blockIdx.x;
     const float s = row_scale(__uint_as_float(rowmax[r]));
+    const float rs = quant_rcp(s);
     const float4* src = reinterpret_cast<const float4*>(h + (long long)r * I);
     uint2* dst = reinterpret_cast<uint2*>(hq + (long long)r * I);
     for (int c = threadIdx.x; c < I / 4; c += blockDim.x) {
         const float4 v = src[c];
         int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
         if (s != 0.f) {
-            q0 = quant1(v.x, s); q1 = quant1(v.y, s); q2 = quant1(v.z, s); q3 = quant1(v.w, s);
+            q0 = quant1_row(v.x, s, rs); q1 = quant1_row(v.y, s, rs);
+            q2 = quant1_row(v.z, s, rs); q3 = quant1_row(v.w, s, rs);
         }
         __half2 a = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
         __half2 b = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
@@ -731,14 +733,16 @@ retquant_kernel(int H, int k, int lb, long long crow, const float* __restrict__ 
     const moe_dispatch_meta m = meta[expert_rows[r]];
     const long long tj = ((long long)m.src_rank * lb + m.batch_slot) * k + m.route_slot;
     const float s = row_scale(__uint_as_float(rowmax[r]));
+    const float rs = quant_rcp(s);
     const float4* src = reinterpret_cast<const float4*>(y + (long long)r * H);
     uint32_t* dst = reinterpret_cast<uint32_t*>(cbuf + tj * crow);
     for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
         const float4 v = src[c];
         uint32_t w = 0;
         if (s != 0.f) {
-            w = (uint32_t)(quant1(v.x, s) & 0xff) | ((uint32_t)(quant1(v.y, s) & 0xff) << 8) |
-                ((uint32_t)(quant1(v.z, s) & 0xff) << 16) | ((uint32_t)(quant1(v.w, s) & 0xff) << 24);
+            w = (uint32_t)(quant1_row(v.x, s, rs) & 0xff) | ((uint32_t)(quant1_row(v.y, s, rs) & 0xff) << 8) |
+                ((uint32_t)(quant1_row(v.z, s, rs) & 0xff) << 16) |
+                ((uint32_t)(quant1_row(v.w, s, rs) & 0xff) << 24);
         }
         dst[c] = w;
     }

@@ -1,7 +1,11 @@
-"""The SiLU of the gate/up GEMM epilogue (branch-free, FMA-based division)
-against the straightforward form (IEEE division) on every binary32 input, and
-both, with the exp behind them, against the oracle on a strided sample of bit
-patterns plus the special values."""
+"""Device arithmetic of the library against its straightforward forms:
+
+- the SiLU of the gate/up GEMM epilogue (branch-free, FMA-based division)
+  against the IEEE-division form on every binary32 input, and both, with the
+  exp behind them, against the oracle on a strided sample plus special values;
+- the reciprocal form of the token-wise INT8 code against the IEEE-division
+  form on 2^30 random (row absmax, value) pairs, half of them next to a
+  half-integer quotient."""
 import ctypes
 import os
 import subprocess
@@ -22,14 +26,16 @@ CSRC = os.path.join(ROOT, "expert_dispatch_combine_gb300", "csrc")
 def helper():
     out_dir = os.path.join(HERE, "_build")
     os.makedirs(out_dir, exist_ok=True)
-    so = os.path.join(out_dir, "silu_check.so")
+    so = os.path.join(out_dir, "device_math_check.so")
     subprocess.run([os.environ.get("NVCC", "nvcc"), "-O3", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
                     "-gencode", "arch=compute_103a,code=sm_103a", "-I", CSRC,
-                    os.path.join(HERE, "cuda", "silu_check.cu"), "-o", so], check=True)
+                    os.path.join(HERE, "cuda", "device_math_check.cu"), "-o", so], check=True)
     lib = ctypes.CDLL(so)
     P = ctypes.c_void_p
     lib.silu_check_all.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.POINTER(ctypes.c_uint)]
     lib.silu_eval.argtypes = [P, P, P, P, ctypes.c_int]
+    U64P = ctypes.POINTER(ctypes.c_ulonglong)
+    lib.quant_check.argtypes = [ctypes.c_ulonglong, U64P, U64P, ctypes.POINTER(ctypes.c_uint)]
     return lib
 
 
@@ -61,3 +67,13 @@ def test_device_silu_and_exp_match_oracle_sample(helper):
     assert same(spec, ref_s).all()
     assert same(fast, ref_s).all()
     assert same(ex, ref_e).all()
+
+
+def test_reciprocal_quantisation_equals_division_form(helper):
+    m = ctypes.c_ulonglong(0)
+    nh = ctypes.c_ulonglong(0)
+    first = ctypes.c_uint(0)
+    n = 1 << 30
+    assert helper.quant_check(n, ctypes.byref(m), ctypes.byref(nh), ctypes.byref(first)) == 0
+    assert nh.value > n // 4  # the near-half-integer draws happened
+    assert m.value == 0, f"{m.value} mismatches, first at draw {first.value}"
