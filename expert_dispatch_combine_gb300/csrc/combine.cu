@@ -8,10 +8,11 @@
 // 的 All-to-All" (COMBINE procedure: result[token] += value * gate_weight).
 //
 // On one GPU "all contributions are in" is the kernel boundary after the
-// expert FFN.  One block per token; each thread owns 8 consecutive hidden
-// elements at a time, reads them from the k messages (8-byte code loads or
-// 16-byte bf16 loads), accumulates in binary32 in ascending route slot
-// (product and sum rounded separately) and stores 8 bf16 values (16 bytes).
+// expert FFN.  One block per token; each thread owns 16 consecutive hidden
+// elements at a time, reads them from the k messages (16-byte code loads or
+// 32-byte bf16 loads, all issued before the arithmetic), accumulates in
+// binary32 in ascending route slot (product and sum rounded separately) and
+// stores 16 bf16 values (32 bytes).
 #include <cuda_bf16.h>
 
 #include "internal.cuh"
@@ -31,11 +32,48 @@ __device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi) {
     return (unsigned)__bfloat16_as_ushort(a) | ((unsigned)__bfloat16_as_ushort(b) << 16);
 }
 
+// 16 consecutive hidden elements of route message j, dequantised.
+template <bool kInt8>
+__device__ __forceinline__ void load16(const unsigned char* __restrict__ row, int c, uint4 (&q)[2]) {
+    if (kInt8) {
+        q[0] = __ldg(reinterpret_cast<const uint4*>(row) + c);
+    } else {
+        q[0] = __ldg(reinterpret_cast<const uint4*>(row) + 2 * c);
+        q[1] = __ldg(reinterpret_cast<const uint4*>(row) + 2 * c + 1);
+    }
+}
+
+template <bool kInt8>
+__device__ __forceinline__ void accumulate16(const uint4 (&q)[2], float w, float s, float (&acc)[16]) {
+    float v[16];
+    if (kInt8) {
+        const unsigned u[4] = {q[0].x, q[0].y, q[0].z, q[0].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) v[4 * i + b] = __fmul_rn(s8_to_f(u[i], b), s);
+    } else {
+        const unsigned u[8] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[2 * i] = __uint_as_float(u[i] << 16);
+            v[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(w, v[i]));
+}
+
+// One block per token.  Each thread owns 16 consecutive hidden elements at a
+// time and loads them from the first kUnroll messages before any arithmetic
+// (k 16-byte or 32-byte loads in flight per thread); messages beyond
+// kUnroll follow one at a time.  Accumulation is in ascending route slot.
 template <bool kInt8>
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(int H, int k, long long crow, const unsigned char* __restrict__ cbuf,
                const float* __restrict__ cscale, const float* __restrict__ topk_w,
                uint16_t* __restrict__ out) {
+    constexpr int kUnroll = 8;
     __shared__ float s_w[kMaxK], s_s[kMaxK];
     const int t = blockIdx.x;
     const long long tk = (long long)t * k;
@@ -44,40 +82,34 @@ combine_kernel(int H, int k, long long crow, const unsigned char* __restrict__ c
         s_s[threadIdx.x] = kInt8 ? cscale[tk + threadIdx.x] : 0.f;
     }
     __syncthreads();
-    const int nch = H / 8;
+    const int nch = H / 16;
+    const unsigned char* rows = cbuf + tk * crow;
     uint4* orow = reinterpret_cast<uint4*>(out + (long long)t * H);
     for (int c = threadIdx.x; c < nch; c += kCombineThreads) {
-        float acc[8];
+        uint4 q[kUnroll][2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const unsigned char* row = cbuf + (tk + j) * crow;
-            const float w = s_w[j];
-            float v[8];
-            if (kInt8) {
-                uint2 q = __ldg(reinterpret_cast<const uint2*>(row) + c);
-                const float s = s_s[j];
+        for (int j = 0; j < kUnroll; ++j)
+            if (j < k) load16<kInt8>(rows + j * crow, c, q[j]);
+        float acc[16];
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    v[b] = __fmul_rn(s8_to_f(q.x, b), s);
-                    v[4 + b] = __fmul_rn(s8_to_f(q.y, b), s);
-                }
-            } else {
-                uint4 q = __ldg(reinterpret_cast<const uint4*>(row) + c);
-                v[0] = __uint_as_float(q.x << 16); v[1] = __uint_as_float(q.x & 0xffff0000u);
-                v[2] = __uint_as_float(q.y << 16); v[3] = __uint_as_float(q.y & 0xffff0000u);
-                v[4] = __uint_as_float(q.z << 16); v[5] = __uint_as_float(q.z & 0xffff0000u);
-                v[6] = __uint_as_float(q.w << 16); v[7] = __uint_as_float(q.w & 0xffff0000u);
-            }
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(w, v[i]));
+        for (int j = 0; j < kUnroll; ++j)
+            if (j < k) accumulate16<kInt8>(q[j], s_w[j], s_s[j], acc);
+        for (int j = kUnroll; j < k; ++j) {
+            uint4 r[2];
+            load16<kInt8>(rows + j * crow, c, r);
+            accumulate16<kInt8>(r, s_w[j], s_s[j], acc);
         }
-        uint4 o;
-        o.x = pack_bf16x2(acc[0], acc[1]);
-        o.y = pack_bf16x2(acc[2], acc[3]);
-        o.z = pack_bf16x2(acc[4], acc[5]);
-        o.w = pack_bf16x2(acc[6], acc[7]);
-        orow[c] = o;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint4 o;
+            o.x = pack_bf16x2(acc[8 * h + 0], acc[8 * h + 1]);
+            o.y = pack_bf16x2(acc[8 * h + 2], acc[8 * h + 3]);
+            o.z = pack_bf16x2(acc[8 * h + 4], acc[8 * h + 5]);
+            o.w = pack_bf16x2(acc[8 * h + 6], acc[8 * h + 7]);
+            orow[2 * c + h] = o;
+        }
     }
 }
 
