@@ -695,58 +695,100 @@ __device__ __forceinline__ float block_max(float v, float* s_red) {
     return r;
 }
 
+// The row kernels below take 16 consecutive values per thread and chunk and
+// issue the loads of two chunks (eight 16-byte loads) before quantising.
+constexpr int kRowThreads = 128;
+
+__device__ __forceinline__ void load_chunk16(const float4* __restrict__ src, int c, int nch,
+                                             float4 (&v)[4]) {
+    if (c < nch) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = __ldg(src + 4 * c + i);
+    }
+}
+
 // Token-wise requantisation of the SwiGLU output h (its row absmax was
 // reduced by the gate/up GEMM's epilogue): hq as exact fp16 integers, s_h.
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kRowThreads)
 requant_kernel(int I, const float* __restrict__ h, const unsigned* __restrict__ rowmax,
                __half* __restrict__ hq, float* __restrict__ sh) {
     const int r = blockIdx.x;
-    const float s = row_scale(__uint_as_float(rowmax[r]));
-    const float rs = quant_rcp(s);
+    const int nch = I / 16;
     const float4* src = reinterpret_cast<const float4*>(h + (long long)r * I);
-    uint2* dst = reinterpret_cast<uint2*>(hq + (long long)r * I);
-    for (int c = threadIdx.x; c < I / 4; c += blockDim.x) {
-        const float4 v = src[c];
-        int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-        if (s != 0.f) {
-            q0 = quant1_row(v.x, s, rs); q1 = quant1_row(v.y, s, rs);
-            q2 = quant1_row(v.z, s, rs); q3 = quant1_row(v.w, s, rs);
+    uint4* dst = reinterpret_cast<uint4*>(hq + (long long)r * I);
+    for (int c0 = threadIdx.x; c0 < nch; c0 += 2 * kRowThreads) {
+        float4 v[2][4];
+        load_chunk16(src, c0, nch, v[0]);
+        load_chunk16(src, c0 + kRowThreads, nch, v[1]);
+        const float s = row_scale(__uint_as_float(rowmax[r]));
+        const float rs = quant_rcp(s);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int c = c0 + u * kRowThreads;
+            if (c >= nch) break;
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float x[4] = {v[u][i].x, v[u][i].y, v[u][i].z, v[u][i].w};
+                int q[4] = {0, 0, 0, 0};
+                if (s != 0.f) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) q[e] = quant1_row(x[e], s, rs);
+                }
+                __half2 a = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[1]));
+                __half2 b = __halves2half2(__int2half_rn(q[2]), __int2half_rn(q[3]));
+                o[2 * i] = *reinterpret_cast<uint32_t*>(&a);
+                o[2 * i + 1] = *reinterpret_cast<uint32_t*>(&b);
+            }
+            dst[2 * c] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
-        __half2 a = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
-        __half2 b = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
-        uint2 o;
-        o.x = *reinterpret_cast<uint32_t*>(&a);
-        o.y = *reinterpret_cast<uint32_t*>(&b);
-        dst[c] = o;
     }
-    if (threadIdx.x == 0) sh[r] = s;
+    if (threadIdx.x == 0) sh[r] = row_scale(__uint_as_float(rowmax[r]));
 }
 
 // INT8 return message: token-wise codes of y (row absmax reduced by the down
 // GEMM's epilogue) into the combine row (t, j).
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kRowThreads)
 retquant_kernel(int H, int k, int lb, long long crow, const float* __restrict__ y,
                 const unsigned* __restrict__ rowmax, const int32_t* __restrict__ expert_rows,
                 const moe_dispatch_meta* __restrict__ meta, unsigned char* __restrict__ cbuf,
                 float* __restrict__ cscale) {
     const int r = blockIdx.x;
-    const moe_dispatch_meta m = meta[expert_rows[r]];
-    const long long tj = ((long long)m.src_rank * lb + m.batch_slot) * k + m.route_slot;
-    const float s = row_scale(__uint_as_float(rowmax[r]));
-    const float rs = quant_rcp(s);
+    const int nch = H / 16;
     const float4* src = reinterpret_cast<const float4*>(y + (long long)r * H);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(cbuf + tj * crow);
-    for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
-        const float4 v = src[c];
-        uint32_t w = 0;
-        if (s != 0.f) {
-            w = (uint32_t)(quant1_row(v.x, s, rs) & 0xff) | ((uint32_t)(quant1_row(v.y, s, rs) & 0xff) << 8) |
-                ((uint32_t)(quant1_row(v.z, s, rs) & 0xff) << 16) |
-                ((uint32_t)(quant1_row(v.w, s, rs) & 0xff) << 24);
+    for (int c0 = threadIdx.x; c0 < nch; c0 += 2 * kRowThreads) {
+        float4 v[2][4];
+        load_chunk16(src, c0, nch, v[0]);
+        load_chunk16(src, c0 + kRowThreads, nch, v[1]);
+        const moe_dispatch_meta m = meta[expert_rows[r]];
+        const long long tj = ((long long)m.src_rank * lb + m.batch_slot) * k + m.route_slot;
+        uint4* dst = reinterpret_cast<uint4*>(cbuf + tj * crow);
+        const float s = row_scale(__uint_as_float(rowmax[r]));
+        const float rs = quant_rcp(s);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int c = c0 + u * kRowThreads;
+            if (c >= nch) break;
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float x[4] = {v[u][i].x, v[u][i].y, v[u][i].z, v[u][i].w};
+                uint32_t word = 0;
+                if (s != 0.f) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) word |= (uint32_t)(quant1_row(x[e], s, rs) & 0xff) << (8 * e);
+                }
+                w[i] = word;
+            }
+            dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        dst[c] = w;
     }
-    if (threadIdx.x == 0) cscale[tj] = s;
+    if (threadIdx.x == 0) {
+        const moe_dispatch_meta m = meta[expert_rows[r]];
+        cscale[((long long)m.src_rank * lb + m.batch_slot) * k + m.route_slot] =
+            row_scale(__uint_as_float(rowmax[r]));
+    }
 }
 
 // ---------------------------------------------------------------- host
@@ -919,7 +961,7 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     P1.tma_out = 1;
     if ((e = launch_gemm<EPI_GU>(P1, mwgu, mx1, mo1, st)) != cudaSuccess) return e;
 
-    requant_kernel<<<(unsigned)M, 256, 0, st>>>(d.I, hbuf, hmax, hq16, sh);
+    requant_kernel<<<(unsigned)M, kRowThreads, 0, st>>>(d.I, hbuf, hmax, hq16, sh);
     count_launches(1);
 
     Params P2 = {};
@@ -930,7 +972,7 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     if (int8_ret) {
         P2.out_f32 = ybuf; P2.rowmax = ymax;
         if ((e = launch_gemm<EPI_F32>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
-        retquant_kernel<<<(unsigned)M, 256, 0, st>>>(d.H, d.k, d.lb, d.crow, ybuf, ymax, expert_rows,
+        retquant_kernel<<<(unsigned)M, kRowThreads, 0, st>>>(d.H, d.k, d.lb, d.crow, ybuf, ymax, expert_rows,
                                                      meta, cb, reinterpret_cast<float*>(cb + scale_off));
         count_launches(1);
     } else {
