@@ -56,7 +56,8 @@ EXPORTED = ("moe_status_string", "moe_static_buffer_bytes", "moe_query_layout", 
             "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_layer",
             "moe_gemm_workspace_bytes", "moe_grouped_gemm_s8", "moe_launch_count",
             "moe_device_status", "moe_last_cuda_error", "moe_profile_enable", "moe_profile_read",
-            "moe_dispatch_noalloc", "moe_dispatch_noalloc_max_scratch")
+            "moe_dispatch_noalloc", "moe_dispatch_noalloc_max_scratch", "moe_layer_graph_create",
+            "moe_graph_launch", "moe_graph_destroy")
 
 _lib = None
 
@@ -93,6 +94,11 @@ def load(path: str = LIB_PATH):
         "moe_dispatch_noalloc_max_scratch": ([], i64),
         "moe_profile_read": ([P, i32], ctypes.c_int),
         "moe_grouped_gemm_s8": ([i32, P, i64, P, P, i64, P, i32, i32, P, P, i64, P], ctypes.c_int),
+        "moe_layer_graph_create": ([PS, P, P, P, P, i32, ctypes.POINTER(moe_expert_weights),
+                                    ctypes.POINTER(moe_routing), P, i64, P, i64, P, i64, P, P,
+                                    ctypes.POINTER(P)], ctypes.c_int),
+        "moe_graph_launch": ([P, P], ctypes.c_int),
+        "moe_graph_destroy": ([P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -244,6 +250,33 @@ def moe_layer(shape: Shape, logits, x, w_gate_up, s_gate_up, w_down, s_down, rou
         ctypes.byref(w), ctypes.byref(r), _ptr(dispatch_buf), dispatch_buf.numel(),
         _ptr(combine_buf), combine_buf.numel(), _ptr(workspace), workspace.numel(), _ptr(out),
         _stream(stream)))
+
+
+def moe_layer_graph_create(shape: Shape, logits, x, w_gate_up, s_gate_up, w_down, s_down,
+                           routing: dict, dispatch_buf, combine_buf, workspace, out,
+                           capture_stream, rep_table=None, n_copies=None, phys_to_weight=None) -> int:
+    """Captures moe_layer with these arguments on capture_stream (a
+    torch.cuda.Stream other than the legacy default stream); returns the
+    graph handle for moe_graph_launch / moe_graph_destroy."""
+    cs = shape.c()
+    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight)
+    r = moe_routing(*[_ptr(routing[n]) for n, _ in moe_routing._fields_])
+    mc = int(rep_table.shape[1]) if rep_table is not None else 0
+    h = ctypes.c_void_p(None)
+    _check("moe_layer_graph_create", load().moe_layer_graph_create(
+        ctypes.byref(cs), _ptr(logits), _ptr(x), _ptr(rep_table), _ptr(n_copies), mc,
+        ctypes.byref(w), ctypes.byref(r), _ptr(dispatch_buf), dispatch_buf.numel(),
+        _ptr(combine_buf), combine_buf.numel(), _ptr(workspace), workspace.numel(), _ptr(out),
+        _stream(capture_stream), ctypes.byref(h)))
+    return h.value
+
+
+def moe_graph_launch(graph: int, stream=None) -> None:
+    _check("moe_graph_launch", load().moe_graph_launch(graph, _stream(stream)))
+
+
+def moe_graph_destroy(graph: int) -> None:
+    _check("moe_graph_destroy", load().moe_graph_destroy(graph))
 
 
 def moe_profile_enable(on: bool) -> None:

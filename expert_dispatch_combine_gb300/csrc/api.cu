@@ -292,3 +292,7 @@ moe_status moe_grouped_gemm_s8(int32_t n_groups, const int32_t* offsets, int64_t
 }
 
 }  // extern "C"
+
+// Status for a CUDA error raised outside this file (records it for
+// moe_last_cuda_error like every entry point here).
+moe_status moe::record_cuda_status(cudaError_t e) { return cuda_status(e); }

@@ -111,6 +111,9 @@ inline T* ws_ptr(void* ws, long long off) { return reinterpret_cast<T*>(static_c
 
 // Number of kernels (and memsets) this library has enqueued in this process.
 void count_launches(int n);
+// MOE_OK for cudaSuccess, else MOE_ERR_CUDA with the error kept for
+// moe_last_cuda_error.
+moe_status record_cuda_status(cudaError_t e);
 
 // Optional kernel timing: when enabled, the expert GEMM launches are
 // bracketed by CUDA events (slot 0: gate/up GEMM, slot 1: down GEMM).

@@ -78,3 +78,48 @@ class MoELayer:
                     b.out, rep_table=self.rep_table, n_copies=self.n_copies,
                     phys_to_weight=self.phys_to_weight, stream=stream)
         return b.out
+
+
+class GraphedLayer:
+    """The decode layer replayed from CUDA graphs over `n_sets` static buffer
+    sets (two: double buffering).  Step i copies its inputs into set
+    i % n_sets, launches that set's graph (one moe_layer captured by
+    moe_layer_graph_create) and returns that set's output buffer, so two
+    consecutive steps never share dispatch, combine or output buffers."""
+
+    def __init__(self, layer: MoELayer, n_sets: int = 2, device="cuda"):
+        s = layer.shape
+        self.layer = layer
+        self.sets = []
+        self.next = 0
+        cap = torch.cuda.Stream(device=device)
+        dev = torch.device(device)
+        for _ in range(n_sets):
+            buf = LayerBuffers(s, device)
+            lg = torch.zeros((s.T, s.E_log), dtype=torch.float32, device=dev)
+            x = torch.zeros((s.T, s.H), dtype=torch.bfloat16, device=dev)
+            g = B.moe_layer_graph_create(s, lg, x, *layer.w, buf.routing, buf.dispatch, buf.combine,
+                                         buf.workspace, buf.out, cap, rep_table=layer.rep_table,
+                                         n_copies=layer.n_copies, phys_to_weight=layer.phys_to_weight)
+            self.sets.append((buf, lg, x, g))
+
+    def step(self, logits: torch.Tensor, x: torch.Tensor, stream=None) -> torch.Tensor:
+        buf, lg, xs, g = self.sets[self.next]
+        self.next = (self.next + 1) % len(self.sets)
+        st = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(st):
+            lg.copy_(logits)
+            xs.copy_(x)
+        B.moe_graph_launch(g, st)
+        return buf.out
+
+    def close(self) -> None:
+        for _, _, _, g in self.sets:
+            B.moe_graph_destroy(g)
+        self.sets = []
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

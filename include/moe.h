@@ -254,6 +254,38 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t
                      int64_t combine_bytes, void* workspace, int64_t workspace_bytes,
                      uint16_t* out, moe_stream_t stream);
 
+/* The decode layer as a CUDA graph ([C] "EP320：token 去找专家": the static
+ * dispatch/combine buffers are allocated once, reused by every decode step
+ * and double-buffered so that one step's combine cannot overwrite dispatch
+ * data another step still uses).
+ *   moe_layer_graph_create captures one moe_layer call with exactly these
+ *   arguments on `capture_stream` and instantiates it; nothing runs during
+ *   the call.  Each moe_graph_launch then replays the whole layer on
+ *   `stream` with the same buffers, reading whatever `logits` and `x` hold
+ *   when it runs and writing the same outputs moe_layer writes.  Double
+ *   buffering is two graphs over two buffer sets, launched in turn.
+ *   - capture_stream (a cudaStream_t) must not be NULL (the legacy default
+ *     stream cannot be captured) and must not be capturing already; the
+ *     capture uses cudaStreamCaptureModeThreadLocal.
+ *   - Argument errors are those of moe_layer and are reported before
+ *     anything is captured; *graph is NULL on any error.
+ *   - The handle owns the driver's executable graph (host-side objects; no
+ *     device buffer is allocated) until moe_graph_destroy.  Buffers passed
+ *     here must stay valid while the graph exists.
+ *   - Replays of one graph on several streams at once race on its buffers.
+ *   - Profiling (moe_profile_enable) should be off while capturing. */
+typedef struct moe_graph_s* moe_graph;
+moe_status moe_layer_graph_create(const moe_shape* shape, const float* logits, const uint16_t* x,
+                                  const int32_t* rep_table, const int32_t* n_copies,
+                                  int32_t max_copies, const moe_expert_weights* weights,
+                                  const moe_routing* routing, void* dispatch_buf,
+                                  int64_t dispatch_bytes, void* combine_buf, int64_t combine_bytes,
+                                  void* workspace, int64_t workspace_bytes, uint16_t* out,
+                                  moe_stream_t capture_stream, moe_graph* graph);
+moe_status moe_graph_launch(moe_graph graph, moe_stream_t stream);
+/* NULL is accepted and ignored. */
+moe_status moe_graph_destroy(moe_graph graph);
+
 /* Exact grouped INT8 GEMM with int32 output -- the contraction inside
  * moe_expert_ffn ([X] P085: sum_k q(x_ik) q(w_jk)), exposed on its own.
  * With K % 64 == 0 it runs the same tensor-core kernel as moe_expert_ffn

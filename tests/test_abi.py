@@ -115,6 +115,13 @@ def test_entry_points_reject_before_enqueue(lib):
     rc = lib.moe_grouped_gemm_s8(2, P(fake), 10, None, P(fake), 64, P(fake), 32, 64, P(fake),
                                  P(fake), 16, None)
     assert rc == 2
+    # graph capture: the legacy default stream cannot be captured; no handle is returned
+    h = ctypes.c_void_p(12345)
+    rc = lib.moe_layer_graph_create(ctypes.byref(s), P(fake), P(fake), None, None, 0, None, None,
+                                    P(fake), L["dispatch_bytes"], P(fake), L["combine_bytes"],
+                                    P(fake), L["workspace_bytes"], P(fake), None, ctypes.byref(h))
+    assert rc == 1 and not h.value
+    assert lib.moe_graph_destroy(None) == 0
 
 
 @pytest.mark.parametrize("E,R,E_phys,slices,seed", [
