@@ -52,34 +52,44 @@
 namespace moe {
 namespace tc {
 
-constexpr int BN = kTcTileRows;                  // tokens per tile (192)
 constexpr int BK = 64;                           // K per stage
-constexpr int NS = 6;                            // shared-memory stages
 constexpr int NA = 4;                            // TMEM A slots (two pairs)
 constexpr int CK = 16;                           // stages per exact chunk (1024 K)
+constexpr int CKP = CK / 2;                      // stage pairs per exact chunk
 constexpr int BOX_ROWS = 32;                     // token rows per activation TMA box
 constexpr int BOX_BYTES = BOX_ROWS * BK * 2;     // 4 KB
-constexpr int B_BYTES = BN * BK * 2;             // 24 KB fp16 activations per stage
 constexpr int A_BYTES = 128 * BK;                // 8 KB int8 weights per stage
-constexpr int STAGE_BYTES = B_BYTES + A_BYTES;   // 32 KB
 constexpr int GT = 16;                           // tokens per epilogue group
-constexpr int HALF = BN / 2;                     // token columns per drain warpgroup
-constexpr int NGRP = HALF / GT;                  // 6 groups
 constexpr int STG_BYTES = GT * 128 * 4;          // 8 KB staging buffer; two per drain warpgroup
-constexpr int NP = NS / 2;                       // stage pairs in shared memory
-constexpr int CKP = CK / 2;                      // stage pairs per exact chunk
-constexpr int NBARS = 2 * NP + 2 + 4 + 1 + 2;
-constexpr uint32_t TM_ACC = 0, TM_A = 2 * BN, TM_COLS = 512;
+constexpr uint32_t TM_ACC = 0, TM_COLS = 512;
 constexpr int THREADS = 512;
-constexpr int SMEM_BYTES = NS * STAGE_BYTES + 4 * STG_BYTES + NBARS * 8 + 16 + 1024;
+
+// Shapes that depend on the tile's token count BN: 192 for batches with
+// many rows per expert, 64 for decode-sized batches, where the smaller
+// activation region buys twice the stages (weight bytes in flight).
+template <int BNV>
+struct Tile {
+    static constexpr int BN = BNV;                            // tokens per tile
+    static constexpr int B_BYTES = BN * BK * 2;               // fp16 activations per stage
+    static constexpr int STAGE_BYTES = B_BYTES + A_BYTES;     // 32 KB or 16 KB
+    static constexpr int NS = BN == 192 ? 6 : 12;             // shared-memory stages
+    static constexpr int NP = NS / 2;                         // stage pairs
+    static constexpr int HALF = BN / 2;                       // token columns per drain warpgroup
+    static constexpr int NGRP = HALF / GT;                    // epilogue groups per drain warpgroup
+    static constexpr int NBARS = 2 * NP + 2 + 4 + 1 + 2;
+    static constexpr uint32_t TM_A = 2 * BN;                  // after the two accumulators
+    static constexpr int SMEM_BYTES = NS * STAGE_BYTES + 4 * STG_BYTES + NBARS * 8 + 16 + 1024;
+    static_assert(BN % 32 == 0 && HALF % GT == 0 && NS % 2 == 0, "tile shape");
+    static_assert(SMEM_BYTES <= 227 * 1024, "dynamic shared memory per CTA");
+    static_assert(NA == 4 && TM_A + NA * 32 <= TM_COLS, "two accumulators and two pairs of A slots in TMEM");
+};
+constexpr int BN_LARGE = kTcTileRows, BN_DECODE = kTcMinTileRows;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 20000000ull;
 // per-thread register budgets after setmaxnreg: 128 threads each at
 // 56 (producer/MMA) + 80 (converter) + 2 x 184 (drains) = 64,512 <= 512 x 128
 constexpr uint32_t REG_CTRL = 56, REG_CONV = 80, REG_DRAIN = 184;
 static_assert(128 * (REG_CTRL + REG_CONV + 2 * REG_DRAIN) <= THREADS * 128, "register split");
-static_assert(SMEM_BYTES <= 227 * 1024, "dynamic shared memory per CTA");
-static_assert(NA == 4 && TM_A + NA * 32 <= TM_COLS, "two accumulators and two pairs of A slots in TMEM");
 
 enum { EPI_I32 = 0, EPI_GU = 1, EPI_F32 = 2, EPI_BF16MSG = 3 };
 
@@ -373,11 +383,15 @@ __device__ __forceinline__ bool epilogue_staged(const Params& P, const TileInfo&
     return true;
 }
 
-template <int EPI>
+template <int EPI, int BNV>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                const __grid_constant__ CUtensorMap tmXb,
                const __grid_constant__ CUtensorMap tmO, const Params P) {
+    using TL = Tile<BNV>;
+    constexpr int BN = TL::BN, NS = TL::NS, NP = TL::NP, HALF = TL::HALF, NGRP = TL::NGRP;
+    constexpr int B_BYTES = TL::B_BYTES, STAGE_BYTES = TL::STAGE_BYTES, NBARS = TL::NBARS;
+    constexpr uint32_t TM_A = TL::TM_A;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -836,15 +850,16 @@ int sm_count() {
     return cached[dev];
 }
 
-template <int EPI>
+template <int EPI, int BNV>
 cudaError_t launch_gemm(const Params& P, const CUtensorMap& w, const CUtensorMap (&x)[2],
                         const CUtensorMap& o, cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    constexpr int smem = Tile<BNV>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, BNV>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int slot = EPI == EPI_GU ? 0 : 1;
     if (cudaEvent_t ev = prof_event(slot, 0)) cudaEventRecord(ev, st);
-    gemm_tc_kernel<EPI><<<sm_count(), THREADS, SMEM_BYTES, st>>>(w, x[0], x[1], o, P);
+    gemm_tc_kernel<EPI, BNV><<<sm_count(), THREADS, smem, st>>>(w, x[0], x[1], o, P);
     if (cudaEvent_t ev = prof_event(slot, 1)) cudaEventRecord(ev, st);
     count_launches(1);
     return cudaGetLastError();
@@ -854,11 +869,11 @@ bool weight_map(CUtensorMap* m, const int8_t* w, int K, uint64_t rows) {
     return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, K, rows, BK, 64, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-// Activation maps: [0] boxes of BOX_ROWS rows, [1] boxes of BN rows.
-bool act_map(CUtensorMap (&m)[2], const __half* x, int K, uint64_t rows) {
+// Activation maps: [0] boxes of BOX_ROWS rows, [1] boxes of bn rows (a tile).
+bool act_map(CUtensorMap (&m)[2], const __half* x, int K, uint64_t rows, int bn) {
     return make_map(&m[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, rows, BK, BOX_ROWS,
                     CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_map(&m[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, rows, BK, BN,
+           make_map(&m[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, rows, BK, (uint32_t)bn,
                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -879,22 +894,20 @@ cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long lo
                                    const int8_t* B, int N, int K, int32_t* C, void* ws,
                                    cudaStream_t st) {
     using namespace tc;
-    char* w = static_cast<char*>(ws);
-    int* err = reinterpret_cast<int*>(w);
-    int32_t* tp = reinterpret_cast<int32_t*>(w + 256);
-    int4* ttab = reinterpret_cast<int4*>(w + 256 + align_up(4LL * (n_groups + 1), 256));
-    __half* a16 = reinterpret_cast<__half*>(
-        w + 256 + align_up(4LL * (n_groups + 1), 256) +
-        align_up(16LL * tile_table_entries(n_groups, max_rows, BN), 256));
+    const GemmWs gw = gemm_ws(n_groups, max_rows, K);
+    int* err = ws_ptr<int>(ws, 0);
+    int32_t* tp = ws_ptr<int32_t>(ws, gw.tiles);
+    int4* ttab = ws_ptr<int4>(ws, gw.ttab);
+    __half* a16 = ws_ptr<__half>(ws, gw.a16);
     cudaError_t e = cudaMemsetAsync(err, 0, 256, st);
     if (e != cudaSuccess) return e;
     count_launches(1);
-    if ((e = launch_tile_prefix(n_groups, BN, offsets, tp, st, ttab)) != cudaSuccess) return e;
+    if ((e = launch_tile_prefix(n_groups, BN_LARGE, offsets, tp, st, ttab)) != cudaSuccess) return e;
     assemble_kernel<<<(unsigned)max_rows, 128, 0, st>>>(K, row_index, A, lda, nullptr, a16, nullptr);
     count_launches(1);
     CUtensorMap mw, mx[2], mo;
     const bool tma_out = N % 128 == 0;
-    if (!weight_map(&mw, B, K, (uint64_t)n_groups * N) || !act_map(mx, a16, K, (uint64_t)max_rows) ||
+    if (!weight_map(&mw, B, K, (uint64_t)n_groups * N) || !act_map(mx, a16, K, (uint64_t)max_rows, BN_LARGE) ||
         (tma_out && !out_map(&mo, C, true, N, (uint64_t)max_rows, 128)))
         return cudaErrorInvalidValue;
     if (!tma_out) mo = mx[0];  // unused
@@ -902,14 +915,16 @@ cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long lo
     P.G = n_groups; P.offsets = offsets; P.tile_prefix = tp; P.ttab = ttab; P.g2s = nullptr;
     P.K = K; P.rows_per_set = N; P.nout = N; P.mb_count = (N + 127) / 128; P.box1_off = 64;
     P.c_i32 = C; P.err = err; P.tma_out = tma_out;
-    return launch_gemm<EPI_I32>(P, mw, mx, mo, st);
+    return launch_gemm<EPI_I32, BN_LARGE>(P, mw, mx, mo, st);
 }
 
-cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
-                          const int32_t* expert_offsets, const int32_t* expert_rows,
-                          const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                          const WsLayout& wl, cudaStream_t st) {
-    using namespace tc;
+namespace tc {
+
+template <int BNV>
+cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
+                   const int32_t* expert_offsets, const int32_t* expert_rows,
+                   const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
+                   const WsLayout& wl, cudaStream_t st) {
     const long long M = (long long)d.T * d.k;
     const moe_dispatch_meta* meta =
         reinterpret_cast<const moe_dispatch_meta*>(static_cast<const char*>(dbuf) + meta_off);
@@ -932,7 +947,7 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     if ((e = cudaMemsetAsync(err, 0, 256, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(hmax, 0, sizeof(unsigned) * 2 * M, st)) != cudaSuccess) return e;
     count_launches(2);
-    if ((e = launch_tile_prefix(d.E_phys, BN, expert_offsets, tp, st, ttab, w.phys_to_weight)) !=
+    if ((e = launch_tile_prefix(d.E_phys, BNV, expert_offsets, tp, st, ttab, w.phys_to_weight)) !=
         cudaSuccess)
         return e;
     assemble_kernel<<<(unsigned)M, 128, 0, st>>>(d.H, expert_rows, static_cast<const int8_t*>(dbuf),
@@ -941,10 +956,10 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
 
     CUtensorMap mwgu, mx1[2], mo1, mwd, mx2[2], mo2;
     if (!weight_map(&mwgu, w.w_gate_up, d.H, (uint64_t)E_w * 2 * d.I) ||
-        !act_map(mx1, a16, d.H, (uint64_t)M) ||
+        !act_map(mx1, a16, d.H, (uint64_t)M, BNV) ||
         !out_map(&mo1, hbuf, false, (uint64_t)d.I, (uint64_t)M, 64) ||
         !weight_map(&mwd, w.w_down, d.I, (uint64_t)E_w * d.H) ||
-        !act_map(mx2, hq16, d.I, (uint64_t)M))
+        !act_map(mx2, hq16, d.I, (uint64_t)M, BNV))
         return cudaErrorInvalidValue;
     const bool y_tma = int8_ret && d.H >= 128;
     if (y_tma) {
@@ -959,7 +974,7 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     P1.K = d.H; P1.rows_per_set = 2 * d.I; P1.nout = d.I; P1.mb_count = d.I / 64; P1.box1_off = d.I;
     P1.s_row = s_row; P1.s_ch = w.s_gate_up; P1.out_f32 = hbuf; P1.rowmax = hmax; P1.err = err;
     P1.tma_out = 1;
-    if ((e = launch_gemm<EPI_GU>(P1, mwgu, mx1, mo1, st)) != cudaSuccess) return e;
+    if ((e = launch_gemm<EPI_GU, BNV>(P1, mwgu, mx1, mo1, st)) != cudaSuccess) return e;
 
     requant_kernel<<<(unsigned)M, kRowThreads, 0, st>>>(d.I, hbuf, hmax, hq16, sh);
     count_launches(1);
@@ -971,15 +986,32 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     P2.s_row = sh; P2.s_ch = w.s_down; P2.err = err; P2.tma_out = y_tma;
     if (int8_ret) {
         P2.out_f32 = ybuf; P2.rowmax = ymax;
-        if ((e = launch_gemm<EPI_F32>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
+        if ((e = launch_gemm<EPI_F32, BNV>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
         retquant_kernel<<<(unsigned)M, kRowThreads, 0, st>>>(d.H, d.k, d.lb, d.crow, ybuf, ymax, expert_rows,
                                                      meta, cb, reinterpret_cast<float*>(cb + scale_off));
         count_launches(1);
     } else {
         P2.expert_rows = expert_rows; P2.meta = meta; P2.cbuf = cb; P2.crow = d.crow; P2.k = d.k; P2.lb = d.lb;
-        if ((e = launch_gemm<EPI_BF16MSG>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
+        if ((e = launch_gemm<EPI_BF16MSG, BNV>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
     }
     return cudaGetLastError();
+}
+
+}  // namespace tc
+
+// Decode-sized batches (at most 32 routed rows per expert on average) take
+// 64-token tiles: their tiles are mostly weight streaming, and the smaller
+// activation region doubles the stages in flight.
+cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
+                          const int32_t* expert_offsets, const int32_t* expert_rows,
+                          const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
+                          const WsLayout& wl, cudaStream_t st) {
+    const long long M = (long long)d.T * d.k;
+    if (M <= 32LL * d.E_phys)
+        return tc::ffn_tc<tc::BN_DECODE>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
+                                         scale_off, ws, wl, st);
+    return tc::ffn_tc<tc::BN_LARGE>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
+                                    scale_off, ws, wl, st);
 }
 
 }  // namespace moe

@@ -39,6 +39,8 @@ inline bool ffn_uses_tc(const Dims& d) { return d.H % 64 == 0 && d.I % 64 == 0; 
 
 // Token rows per tile of the tensor-core grouped GEMM.
 constexpr int kTcTileRows = 192;
+// Token rows per tile of its decode variant (few rows per expert).
+constexpr int kTcMinTileRows = 64;
 
 // Token tiles of a grouped GEMM over n_groups groups and max_rows rows, at
 // most bm rows per tile (each group adds at most one partial tile).
@@ -80,7 +82,7 @@ inline WsLayout make_ws(const Dims& d) {
     w.hist = o;       o = align_up(o + 4LL * d.S * d.E_phys, 256);
     w.src_base = o;   o = align_up(o + 4LL * d.S * d.E_phys, 256);
     w.tiles = o;      o = align_up(o + 4LL * (d.E_phys + 1), 256);
-    w.ttab = o;       o = align_up(o + 16LL * tile_table_entries(d.E_phys, tk, kTcTileRows), 256);
+    w.ttab = o;       o = align_up(o + 16LL * tile_table_entries(d.E_phys, tk, kTcMinTileRows), 256);
     w.sh = o;         o = align_up(o + 4 * tk, 256);
     w.tc = ffn_uses_tc(d);
     if (w.tc) {
@@ -100,10 +102,19 @@ inline WsLayout make_ws(const Dims& d) {
 }
 
 // Workspace of moe_grouped_gemm_s8: [status][tile prefix][tile table][fp16 A rows].
+struct GemmWs {
+    long long tiles, ttab, a16, total;
+};
+inline GemmWs gemm_ws(int n_groups, long long max_rows, int K) {
+    GemmWs w;
+    w.tiles = 256;
+    w.ttab = w.tiles + align_up(4LL * (n_groups + 1), 256);
+    w.a16 = w.ttab + align_up(16LL * tile_table_entries(n_groups, max_rows, kTcMinTileRows), 256);
+    w.total = w.a16 + align_up(2LL * max_rows * K, 256);
+    return w;
+}
 inline long long gemm_ws_bytes(int n_groups, long long max_rows, int K) {
-    return 256 + align_up(4LL * (n_groups + 1), 256) +
-           align_up(16LL * tile_table_entries(n_groups, max_rows, kTcTileRows), 256) +
-           align_up(2LL * max_rows * K, 256);
+    return gemm_ws(n_groups, max_rows, K).total;
 }
 
 template <typename T>

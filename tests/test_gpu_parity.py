@@ -124,6 +124,7 @@ def test_layer_tiny_full(cfmt):
     dict(T=130, H=128, E_log=16, k=2, I=64, R=16, S=2),   # epr = 1, ragged token tiles
     dict(T=40, H=1088, E_log=12, k=3, I=192, R=3, S=5),   # K = 17 stages (2 exact chunks), partial channel block
     dict(T=300, H=256, E_log=4, k=4, I=128, R=2, S=3),    # k = E: 300 rows per expert, 3 token tiles
+    dict(T=512, H=256, E_log=64, k=4, I=128, R=8, S=4, zipf=1.5),  # decode tiles, hot experts span several
     # CUDA-core expert path (H or I not a multiple of 64)
     dict(T=1, H=16, E_log=4, k=1, I=16, R=1),             # one token
     dict(T=31, H=48, E_log=8, k=8, I=32, R=2, S=1),       # k = E, ragged
