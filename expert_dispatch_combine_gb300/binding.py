@@ -57,7 +57,7 @@ EXPORTED = ("moe_status_string", "moe_static_buffer_bytes", "moe_query_layout", 
             "moe_gemm_workspace_bytes", "moe_grouped_gemm_s8", "moe_launch_count",
             "moe_device_status", "moe_last_cuda_error", "moe_profile_enable", "moe_profile_read",
             "moe_dispatch_noalloc", "moe_dispatch_noalloc_max_scratch", "moe_layer_graph_create",
-            "moe_graph_launch", "moe_graph_destroy")
+            "moe_graph_launch", "moe_graph_destroy", "moe_eplb_collect")
 
 _lib = None
 
@@ -99,6 +99,7 @@ def load(path: str = LIB_PATH):
                                     ctypes.POINTER(P)], ctypes.c_int),
         "moe_graph_launch": ([P, P], ctypes.c_int),
         "moe_graph_destroy": ([P], ctypes.c_int),
+        "moe_eplb_collect": ([i32, i32, P, P, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -169,9 +170,11 @@ def moe_query_layout(shape: Shape) -> dict:
     return {n: getattr(L, n) for n, _ in moe_layout._fields_}
 
 
-def moe_eplb_plan(token_count: np.ndarray, E_phys: int, n_ranks: int, max_copies: int | None = None):
+def moe_eplb_plan(token_count: np.ndarray, E_phys: int, n_ranks: int, max_copies: int | None = None,
+                  trim: bool = True):
     """Host planner.  token_count [n_slices, E_log] (or [E_log]).
-    Returns (rep_table [E_log, max_copies], n_copies [E_log], phys_to_logical [E_phys])."""
+    Returns (rep_table [E_log, max_copies], n_copies [E_log], phys_to_logical [E_phys]);
+    with trim the table keeps only the columns the plan uses."""
     tc = np.ascontiguousarray(np.atleast_2d(token_count), dtype=np.float64)
     ns, E = tc.shape
     mc = max_copies or (E_phys - E + 1)
@@ -180,8 +183,18 @@ def moe_eplb_plan(token_count: np.ndarray, E_phys: int, n_ranks: int, max_copies
     p2l = np.empty(E_phys, np.int32)
     _check("moe_eplb_plan", load().moe_eplb_plan(ns, E, E_phys, n_ranks, tc.ctypes.data, mc,
                                                  rep.ctypes.data, nc.ctypes.data, p2l.ctypes.data))
+    if not trim:
+        return rep, nc, p2l
     used = max(1, int(nc.max()))
     return np.ascontiguousarray(rep[:, :used]), nc, p2l
+
+
+def moe_eplb_collect(expert_counts, logical_load, phys_to_logical=None, stream=None) -> None:
+    """logical_load[e] += expert_counts summed over the physical copies of logical
+    expert e (device int32 [E_phys] counts, device int64 [E_log] loads)."""
+    _check("moe_eplb_collect", load().moe_eplb_collect(
+        int(logical_load.numel()), int(expert_counts.numel()), _ptr(expert_counts),
+        _ptr(phys_to_logical), _ptr(logical_load), _stream(stream)))
 
 
 def moe_route(shape: Shape, logits, topk_idx, topk_w, phys_idx, expert_counts,

@@ -152,6 +152,18 @@ moe_status moe_eplb_plan(int32_t n_slices, int32_t E_log, int32_t E_phys, int32_
                          const double* token_count, int32_t max_copies,
                          int32_t* rep_table, int32_t* n_copies, int32_t* phys_to_logical);
 
+/* Load aggregation of the EPLB loop ([X] "专家负载均衡" P068: the Collect
+ * kernel's counts, summed over a time window for the planner).
+ *   load[e] += sum of expert_counts[p] over the physical experts p with
+ *   phys_to_logical[p] == e, for e in [0, E_log).
+ *   expert_counts (device) int32 [E_phys], as moe_route writes it;
+ *   phys_to_logical (device) int32 [E_phys], or NULL when E_phys == E_log
+ *   (identity); load (device) int64 [E_log], accumulated, never cleared here.
+ * Integer sums, so the result does not depend on the order of additions.
+ * One small kernel on `stream`; no workspace. */
+moe_status moe_eplb_collect(int32_t E_log, int32_t E_phys, const int32_t* expert_counts,
+                            const int32_t* phys_to_logical, int64_t* load, moe_stream_t stream);
+
 /* Gate top-k ([X] P038) with renormalised softmax weights and the EPLB map
  * ([X] P078-P079), plus per-physical-expert counts (the Collect kernel of
  * [X] P068).
