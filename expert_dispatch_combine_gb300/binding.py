@@ -57,7 +57,7 @@ EXPORTED = ("moe_status_string", "moe_static_buffer_bytes", "moe_query_layout", 
             "moe_gemm_workspace_bytes", "moe_grouped_gemm_s8", "moe_launch_count",
             "moe_device_status", "moe_last_cuda_error", "moe_profile_enable", "moe_profile_read",
             "moe_dispatch_noalloc", "moe_dispatch_noalloc_max_scratch", "moe_layer_graph_create",
-            "moe_graph_launch", "moe_graph_destroy", "moe_eplb_collect")
+            "moe_graph_launch", "moe_graph_destroy", "moe_eplb_collect", "moe_expert_ffn_combine")
 
 _lib = None
 
@@ -100,6 +100,8 @@ def load(path: str = LIB_PATH):
         "moe_graph_launch": ([P, P], ctypes.c_int),
         "moe_graph_destroy": ([P], ctypes.c_int),
         "moe_eplb_collect": ([i32, i32, P, P, P, P], ctypes.c_int),
+        "moe_expert_ffn_combine": ([PS, P, i64, P, P, ctypes.POINTER(moe_expert_weights), P, P, i64,
+                                    P, P, i64, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -242,6 +244,17 @@ def moe_expert_ffn(shape: Shape, dispatch_buf, expert_offsets, expert_rows, w_ga
         ctypes.byref(cs), _ptr(dispatch_buf), dispatch_buf.numel(), _ptr(expert_offsets),
         _ptr(expert_rows), ctypes.byref(w), _ptr(combine_buf), combine_buf.numel(),
         _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def moe_expert_ffn_combine(shape: Shape, dispatch_buf, expert_offsets, expert_rows, w_gate_up,
+                           s_gate_up, w_down, s_down, topk_w, combine_buf, out, workspace,
+                           phys_to_weight=None, stream=None):
+    cs = shape.c()
+    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight)
+    _check("moe_expert_ffn_combine", load().moe_expert_ffn_combine(
+        ctypes.byref(cs), _ptr(dispatch_buf), dispatch_buf.numel(), _ptr(expert_offsets),
+        _ptr(expert_rows), ctypes.byref(w), _ptr(topk_w), _ptr(combine_buf), combine_buf.numel(),
+        _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def moe_combine(shape: Shape, combine_buf, topk_w, out, stream=None):

@@ -165,6 +165,35 @@ moe_status moe_expert_ffn(const moe_shape* shape, const void* dispatch_buf,
                                   workspace, make_ws(d), (cudaStream_t)stream));
 }
 
+moe_status moe_expert_ffn_combine(const moe_shape* shape, const void* dispatch_buf,
+                                  int64_t dispatch_bytes, const int32_t* expert_offsets,
+                                  const int32_t* expert_rows, const moe_expert_weights* weights,
+                                  const float* topk_w, void* combine_buf, int64_t combine_bytes,
+                                  uint16_t* out, void* workspace, int64_t workspace_bytes,
+                                  moe_stream_t stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (shape->dispatch_fmt != MOE_MSG_INT8) return MOE_ERR_UNSUPPORTED;
+    if (!dispatch_buf || !expert_offsets || !expert_rows || !combine_buf || !workspace || !topk_w ||
+        !out)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(dispatch_buf, 256) || !aligned(combine_buf, 256) || !aligned(workspace, 256) ||
+        !aligned(out, 16))
+        return MOE_ERR_INVALID_ARG;
+    Dims d = make_dims(*shape);
+    const WsLayout wl = make_ws(d);
+    if (!ffn_fuses_combine(d, wl)) return MOE_ERR_UNSUPPORTED;
+    if ((st = check_weights(d, weights)) != MOE_OK) return st;
+    moe_layout L;
+    fill_layout(d, &L);
+    if (dispatch_bytes < L.dispatch_bytes || combine_bytes < L.combine_bytes ||
+        workspace_bytes < L.workspace_bytes)
+        return MOE_ERR_WORKSPACE;
+    return cuda_status(launch_ffn(d, dispatch_buf, L.dispatch_meta_offset, expert_offsets,
+                                  expert_rows, *weights, combine_buf, L.combine_scale_offset,
+                                  workspace, wl, (cudaStream_t)stream, FusedCombine{topk_w, out}));
+}
+
 moe_status moe_combine(const moe_shape* shape, const void* combine_buf, int64_t combine_bytes,
                        const float* topk_w, uint16_t* out, moe_stream_t stream) {
     moe_status st = check_shape(shape);

@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "combine_math.cuh"
 #include "device_math.cuh"
 #include "internal.cuh"
 #include "tc_ptx.cuh"
@@ -763,11 +764,21 @@ requant_kernel(int I, const float* __restrict__ h, const unsigned* __restrict__ 
 
 // INT8 return message: token-wise codes of y (row absmax reduced by the down
 // GEMM's epilogue) into the combine row (t, j).
+// With kFuse (moe_layer) it also performs FusedCombine as the pages' fused
+// path does: once all k contributions of token t are in ("CloudMatrix384 LLM
+// Serving", "EP320" fused_moe listing; "xDeepServe", COMBINE procedure).  Each
+// block publishes its message (stores, fence, then an atomic increment of the
+// token's readiness counter); the block that brings the counter to k reads
+// the token's k messages back through L2 and writes out[t], with the
+// arithmetic of the combine kernel.  Nothing waits: the last contributor does
+// the work.
+template <bool kFuse>
 __global__ void __launch_bounds__(kRowThreads)
 retquant_kernel(int H, int k, int lb, long long crow, const float* __restrict__ y,
                 const unsigned* __restrict__ rowmax, const int32_t* __restrict__ expert_rows,
                 const moe_dispatch_meta* __restrict__ meta, unsigned char* __restrict__ cbuf,
-                float* __restrict__ cscale) {
+                float* __restrict__ cscale, const float* __restrict__ topk_w, int* __restrict__ ready,
+                uint16_t* __restrict__ out) {
     const int r = blockIdx.x;
     const int nch = H / 16;
     const float4* src = reinterpret_cast<const float4*>(y + (long long)r * H);
@@ -802,6 +813,53 @@ retquant_kernel(int H, int k, int lb, long long crow, const float* __restrict__ 
         const moe_dispatch_meta m = meta[expert_rows[r]];
         cscale[((long long)m.src_rank * lb + m.batch_slot) * k + m.route_slot] =
             row_scale(__uint_as_float(rowmax[r]));
+    }
+    if constexpr (kFuse) {
+        constexpr int kMaxK = 32;
+        __shared__ int s_last;
+        __shared__ float s_w[kMaxK], s_s[kMaxK];
+        const moe_dispatch_meta m = meta[expert_rows[r]];
+        const long long t = (long long)m.src_rank * lb + m.batch_slot;
+        __threadfence();  // this thread's message stores, device-wide, before the count
+        __syncthreads();
+        if (threadIdx.x == 0) s_last = atomicAdd(ready + t, 1) == k - 1;
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();  // the other contributors' messages are visible from here on
+        if (threadIdx.x < k) {
+            s_w[threadIdx.x] = topk_w[t * k + threadIdx.x];
+            s_s[threadIdx.x] = __ldcg(cscale + t * k + threadIdx.x);
+        }
+        __syncthreads();
+        constexpr int kUnroll = 8;
+        const unsigned char* rows = cbuf + t * k * crow;
+        uint4* orow = reinterpret_cast<uint4*>(out + t * H);
+        for (int c = threadIdx.x; c < nch; c += kRowThreads) {
+            uint4 q[kUnroll][2];
+#pragma unroll
+            for (int j = 0; j < kUnroll; ++j)
+                if (j < k) load16<true, true>(rows + j * crow, c, q[j]);
+            float acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll
+            for (int j = 0; j < kUnroll; ++j)
+                if (j < k) accumulate16<true>(q[j], s_w[j], s_s[j], acc);
+            for (int j = kUnroll; j < k; ++j) {
+                uint4 q2[2];
+                load16<true, true>(rows + j * crow, c, q2);
+                accumulate16<true>(q2, s_w[j], s_s[j], acc);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint4 o;
+                o.x = pack_bf16x2(acc[8 * h + 0], acc[8 * h + 1]);
+                o.y = pack_bf16x2(acc[8 * h + 2], acc[8 * h + 3]);
+                o.z = pack_bf16x2(acc[8 * h + 4], acc[8 * h + 5]);
+                o.w = pack_bf16x2(acc[8 * h + 6], acc[8 * h + 7]);
+                orow[2 * c + h] = o;
+            }
+        }
     }
 }
 
@@ -924,7 +982,7 @@ template <int BNV>
 cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                    const int32_t* expert_offsets, const int32_t* expert_rows,
                    const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                   const WsLayout& wl, cudaStream_t st) {
+                   const WsLayout& wl, cudaStream_t st, const FusedCombine& fc) {
     const long long M = (long long)d.T * d.k;
     const moe_dispatch_meta* meta =
         reinterpret_cast<const moe_dispatch_meta*>(static_cast<const char*>(dbuf) + meta_off);
@@ -947,6 +1005,12 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     if ((e = cudaMemsetAsync(err, 0, 256, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(hmax, 0, sizeof(unsigned) * 2 * M, st)) != cudaSuccess) return e;
     count_launches(2);
+    const bool fuse = fc.out != nullptr && int8_ret;
+    int* ready = ws_ptr<int>(ws, wl.ready);
+    if (fuse) {
+        if ((e = cudaMemsetAsync(ready, 0, sizeof(int) * d.T, st)) != cudaSuccess) return e;
+        count_launches(1);
+    }
     if ((e = launch_tile_prefix(d.E_phys, BNV, expert_offsets, tp, st, ttab, w.phys_to_weight)) !=
         cudaSuccess)
         return e;
@@ -987,8 +1051,14 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     if (int8_ret) {
         P2.out_f32 = ybuf; P2.rowmax = ymax;
         if ((e = launch_gemm<EPI_F32, BNV>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
-        retquant_kernel<<<(unsigned)M, kRowThreads, 0, st>>>(d.H, d.k, d.lb, d.crow, ybuf, ymax, expert_rows,
-                                                     meta, cb, reinterpret_cast<float*>(cb + scale_off));
+        if (fuse)
+            retquant_kernel<true><<<(unsigned)M, kRowThreads, 0, st>>>(
+                d.H, d.k, d.lb, d.crow, ybuf, ymax, expert_rows, meta, cb,
+                reinterpret_cast<float*>(cb + scale_off), fc.topk_w, ready, fc.out);
+        else
+            retquant_kernel<false><<<(unsigned)M, kRowThreads, 0, st>>>(
+                d.H, d.k, d.lb, d.crow, ybuf, ymax, expert_rows, meta, cb,
+                reinterpret_cast<float*>(cb + scale_off), nullptr, nullptr, nullptr);
         count_launches(1);
     } else {
         P2.expert_rows = expert_rows; P2.meta = meta; P2.cbuf = cb; P2.crow = d.crow; P2.k = d.k; P2.lb = d.lb;
@@ -1005,13 +1075,13 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
 cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                           const int32_t* expert_offsets, const int32_t* expert_rows,
                           const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                          const WsLayout& wl, cudaStream_t st) {
+                          const WsLayout& wl, cudaStream_t st, const FusedCombine& fc) {
     const long long M = (long long)d.T * d.k;
     if (M <= 32LL * d.E_phys)
         return tc::ffn_tc<tc::BN_DECODE>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
-                                         scale_off, ws, wl, st);
+                                         scale_off, ws, wl, st, fc);
     return tc::ffn_tc<tc::BN_LARGE>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
-                                    scale_off, ws, wl, st);
+                                    scale_off, ws, wl, st, fc);
 }
 
 }  // namespace moe

@@ -58,6 +58,7 @@ struct WsLayout {
     long long tiles;       // int32 [E_phys + 1]  grouped-GEMM tile prefix
     long long ttab;        // int4  [tile_table_entries]  (set, first row, rows, group) per token tile
     long long sh;          // f32   [T*k]   requantisation scale of h
+    long long ready;       // int32 [T]     return messages in per token (fused combine)
     // SIMT expert FFN
     long long acc_gu;      // int32 [T*k][2I]
     long long hq;          // int8  [T*k][I]
@@ -84,6 +85,7 @@ inline WsLayout make_ws(const Dims& d) {
     w.tiles = o;      o = align_up(o + 4LL * (d.E_phys + 1), 256);
     w.ttab = o;       o = align_up(o + 16LL * tile_table_entries(d.E_phys, tk, kTcMinTileRows), 256);
     w.sh = o;         o = align_up(o + 4 * tk, 256);
+    w.ready = o;      o = align_up(o + 4LL * d.T, 256);
     w.tc = ffn_uses_tc(d);
     if (w.tc) {
         w.rowmax = o; o = align_up(o + 8 * tk, 256);
@@ -160,16 +162,27 @@ cudaError_t launch_ffn_simt(const Dims& d, const void* dbuf, long long meta_off,
                             const int32_t* expert_offsets, const int32_t* expert_rows,
                             const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
                             const WsLayout& wl, cudaStream_t st);
+// FusedCombine folded into the expert FFN (moe_layer, INT8 return messages,
+// tensor-core path): gate weights and the output.  Null members: no fusion.
+struct FusedCombine {
+    const float* topk_w;  // [T][k]
+    uint16_t* out;        // bf16 [T][H]
+};
 cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                           const int32_t* expert_offsets, const int32_t* expert_rows,
                           const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                          const WsLayout& wl, cudaStream_t st);
+                          const WsLayout& wl, cudaStream_t st, const FusedCombine& fc);
+// Whether launch_ffn performs the combine itself for this shape.
+inline bool ffn_fuses_combine(const Dims& d, const WsLayout& wl) {
+    return wl.tc && d.cfmt == MOE_MSG_INT8;
+}
 inline cudaError_t launch_ffn(const Dims& d, const void* dbuf, long long meta_off,
                               const int32_t* expert_offsets, const int32_t* expert_rows,
                               const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                              const WsLayout& wl, cudaStream_t st) {
+                              const WsLayout& wl, cudaStream_t st,
+                              const FusedCombine& fc = FusedCombine{nullptr, nullptr}) {
     return wl.tc ? launch_ffn_tc(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf, scale_off,
-                                 ws, wl, st)
+                                 ws, wl, st, fc)
                  : launch_ffn_simt(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
                                    scale_off, ws, wl, st);
 }

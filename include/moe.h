@@ -245,6 +245,28 @@ moe_status moe_expert_ffn(const moe_shape* shape, const void* dispatch_buf,
 moe_status moe_combine(const moe_shape* shape, const void* combine_buf, int64_t combine_bytes,
                        const float* topk_w, uint16_t* out, moe_stream_t stream);
 
+/* moe_expert_ffn and moe_combine in one pass, with the combine of each token
+ * done as soon as its k return messages are in ([C] "EP320" fused_moe
+ * listing; [X] COMBINE procedure): every message writer publishes its message
+ * (stores, device-scope fence, atomic increment of the token's readiness
+ * counter in the workspace) and the writer that completes the count reads
+ * the token's k messages back and writes out[t].  Nothing waits on a flag:
+ * the last contributor does the work.  Same outputs as moe_expert_ffn
+ * followed by moe_combine, bit for bit (combine_buf holds the messages too).
+ *   Arguments: those of moe_expert_ffn plus topk_w and out of moe_combine.
+ *   UNSUPPORTED unless combine_fmt is MOE_MSG_INT8 and the tensor-core path
+ *   applies (H and I multiples of 64).
+ * On the GB300 measurements (c2_decode_zipf, c4_prefill) the two separate
+ * calls are faster: the k messages of a token come from rows spread over the
+ * whole launch, so the completing writers arrive late and unevenly.  moe_layer
+ * therefore uses the separate calls. */
+moe_status moe_expert_ffn_combine(const moe_shape* shape, const void* dispatch_buf,
+                                  int64_t dispatch_bytes, const int32_t* expert_offsets,
+                                  const int32_t* expert_rows, const moe_expert_weights* weights,
+                                  const float* topk_w, void* combine_buf, int64_t combine_bytes,
+                                  uint16_t* out, void* workspace, int64_t workspace_bytes,
+                                  moe_stream_t stream);
+
 /* Routing arrays produced inside moe_layer (all device, caller-owned). */
 typedef struct {
     int32_t* topk_idx;       /* [T][k] */

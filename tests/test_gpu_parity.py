@@ -254,3 +254,32 @@ def test_weights_generated_on_device_equal_host():
     a = synth.int8_tensor_torch(w.seed, 17, synth.GATE_UP, (2 * w.I, w.H), device="cuda")
     b = synth.int8_tensor_np(w.seed, 17, synth.GATE_UP, (2 * w.I, w.H))
     assert (_np(a) == b).all()
+
+
+@pytest.mark.parametrize("w", [
+    synth.WORKLOADS["c0_tiny"],
+    synth.custom(seed=6, T=300, H=256, E_log=4, k=4, I=128, R=2, S=3),
+    synth.custom(seed=8, T=64, H=128, E_log=16, k=12, I=64, R=4, S=4),
+    synth.WORKLOADS["c1_decode"],
+], ids=["c0_tiny", "tc_300x256", "k12", "c1_decode"])
+def test_fused_ffn_combine_equals_separate_steps(w):
+    """moe_expert_ffn_combine (combine per token once its k messages are in,
+    readiness counters) gives the messages and output of moe_expert_ffn
+    followed by moe_combine, bit for bit."""
+    layer = make_layer(w)
+    lg = torch.from_numpy(synth.logits(w)).cuda()
+    x = bits_to_bf16_tensor(synth.hidden_bits(w))
+    ref = layer.forward(lg, x).clone()
+    ref_rows = layer.buf.combine_rows().clone()
+    ref_scales = layer.buf.combine_scales().clone()
+    b, r, s = layer.buf, layer.buf.routing, layer.shape
+    w_gu, s_gu, w_d, s_d = layer.w
+    b.combine.zero_()
+    out = torch.empty_like(ref)
+    for _ in range(2):  # the readiness counters start from zero on every call
+        B.moe_expert_ffn_combine(s, b.dispatch, r["expert_offsets"], r["expert_rows"], w_gu, s_gu,
+                                 w_d, s_d, r["topk_w"], b.combine, out, b.workspace)
+        torch.cuda.synchronize()
+        assert torch.equal(ref_rows, b.combine_rows())
+        assert torch.equal(ref_scales, b.combine_scales())
+        assert torch.equal(ref, out)
