@@ -1,0 +1,51 @@
+"""Failure detection without a GPU fault: the bounded mbarrier wait that
+every wait of the tensor-core GEMM uses gives up after its limit on a barrier
+nothing arrives on, records MOE_ERR_TIMEOUT in the status word and returns;
+when another thread has already posted an error it gives up at once and
+leaves that error in place.  The kernel ends normally in both cases."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+PKG = os.path.join(ROOT, "expert_dispatch_combine_gb300", "csrc")
+MOE_ERR_TIMEOUT = 5
+
+
+@pytest.fixture(scope="module")
+def helper():
+    out_dir = os.path.join(HERE, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    so = os.path.join(out_dir, "wait_check.so")
+    subprocess.run([os.environ.get("NVCC", "nvcc"), "-O3", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
+                    "-gencode", "arch=compute_103a,code=sm_103a", "-I", PKG, "-I",
+                    os.path.join(ROOT, "include"), os.path.join(HERE, "cuda", "wait_check.cu"),
+                    "-o", so, "-lcuda"], check=True)
+    lib = ctypes.CDLL(so)
+    lib.wait_check.argtypes = [ctypes.c_ulonglong, ctypes.c_int, ctypes.c_void_p]
+    return lib
+
+
+def _run(helper, limit_ns, preset):
+    out = (ctypes.c_longlong * 3)()
+    assert helper.wait_check(limit_ns, preset, ctypes.cast(out, ctypes.c_void_p)) == 0
+    return int(out[0]), int(out[1]), int(out[2])
+
+
+def test_wait_times_out_and_records_status(helper):
+    ok, status, ns = _run(helper, 1_000_000, 0)  # 1 ms limit
+    assert ok == 0
+    assert status == MOE_ERR_TIMEOUT
+    assert 1_000_000 <= ns < 1_000_000_000
+
+
+def test_wait_gives_up_on_posted_error(helper):
+    ok, status, ns = _run(helper, 1_000_000_000, 3)  # 1 s limit, error already posted
+    assert ok == 0
+    assert status == 3  # left as posted
+    assert ns < 100_000_000
