@@ -185,7 +185,7 @@ def oracle_sample_fixed(w, n):
         if w.eplb:
             _, _, _, cnt = oracle.route(synth.logits(w), w.k)
             from oracle import eplb
-            rep, nc, p2l = eplb.plan(cnt[None, :].astype(np.float64), w.E_phys, w.R)
+            rep, nc, p2l = eplb.plan(cnt[None, :].astype(np.float64), w.E_phys, w.placement_ranks)
         _, _, pidx, _ = oracle.route(lg, w.k, w.E_phys, rep, nc)
         need = set(int(p2l[p]) if p2l is not None else int(p) for p in np.unique(pidx))
         weights = {e: synth.expert_weights_np(w, e) for e in need}
@@ -218,14 +218,14 @@ def run_ours(args, rank: int, world: int):
     if w.eplb:
         # Collect step: per-expert loads of the unreplicated routing (moe_route),
         # then the host planner (moe_eplb_plan) builds the replica map.
-        s0 = B.Shape(w.T, w.H, w.E_log, w.E_log, w.k, w.I, w.R, w.S)
+        s0 = B.Shape(w.T, w.H, w.E_log, w.E_log, w.k, w.I, w.placement_ranks, w.S)
         lg0 = torch.from_numpy(synth.logits(w)).to(dev)
         ti = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
         tw = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
         tp = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
         cnt = torch.empty(w.E_log, dtype=torch.int32, device=dev)
         B.moe_route(s0, lg0, ti, tw, tp, cnt)
-        r_, n_, p_ = B.moe_eplb_plan(cnt.cpu().numpy().astype(np.float64), w.E_phys, w.R)
+        r_, n_, p_ = B.moe_eplb_plan(cnt.cpu().numpy().astype(np.float64), w.E_phys, w.placement_ranks)
         rep, nc, p2l = (torch.from_numpy(a).to(dev) for a in (r_, n_, p_))
     layer = MoELayer(shape, w_gu, s_gu, w_d, s_d, rep_table=rep, n_copies=nc, phys_to_weight=p2l,
                      device=dev)
@@ -297,6 +297,21 @@ def run_ours(args, rank: int, world: int):
         kern["gemm_gate_up"] += gu_ms / reps
         kern["gemm_down"] += dn_ms / reps
     B.moe_profile_enable(False)
+    tramp_us = None
+    if w.S < w.R:
+        # trampoline forward (A2E + A2E'): same outputs as moe_dispatch, two hops
+        tbuf = torch.empty(B.moe_trampoline_bytes(shape), dtype=torch.uint8, device=dev)
+        t_ms = 0.0
+        for _ in range(reps):
+            ta, tb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ta.record(stream)
+            B.moe_dispatch_trampoline(shape, x, r["phys_idx"], tbuf, b.dispatch, r["rank_counts"],
+                                      r["expert_offsets"], r["expert_rows"], b.workspace)
+            tb.record(stream)
+            torch.cuda.synchronize()
+            t_ms += ta.elapsed_time(tb) / reps
+        tramp_us = 1000 * t_ms
+        del tbuf
     alg = algorithmic(w)
     # gate|up kernel bytes: int8 gate/up rows of the weight sets this step touches, the
     # fp16 expert rows it reads and the f32 h it writes
@@ -316,6 +331,8 @@ def run_ours(args, rank: int, world: int):
         "dispatch_gbs": alg["dispatch_bytes"] / (acc["dispatch"] / 1000) / 1e9,
         "combine_gbs": alg["combine_bytes"] / (acc["combine"] / 1000) / 1e9,
     }
+    if tramp_us is not None:
+        stages["dispatch_trampoline_us"] = tramp_us
     dc_bytes = alg["dispatch_bytes"] + alg["combine_bytes"]
     dc_s = (acc["dispatch"] + acc["combine"]) / 1000
     stages["dispatch_combine_hbm_frac"] = dc_bytes / dc_s / 1e9 / hbm

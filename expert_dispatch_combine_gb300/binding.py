@@ -57,7 +57,8 @@ EXPORTED = ("moe_status_string", "moe_static_buffer_bytes", "moe_query_layout", 
             "moe_gemm_workspace_bytes", "moe_grouped_gemm_s8", "moe_launch_count",
             "moe_device_status", "moe_last_cuda_error", "moe_profile_enable", "moe_profile_read",
             "moe_dispatch_noalloc", "moe_dispatch_noalloc_max_scratch", "moe_layer_graph_create",
-            "moe_graph_launch", "moe_graph_destroy", "moe_eplb_collect", "moe_expert_ffn_combine")
+            "moe_graph_launch", "moe_graph_destroy", "moe_eplb_collect", "moe_expert_ffn_combine",
+            "moe_trampoline_bytes", "moe_dispatch_trampoline")
 
 _lib = None
 
@@ -100,6 +101,8 @@ def load(path: str = LIB_PATH):
         "moe_graph_launch": ([P, P], ctypes.c_int),
         "moe_graph_destroy": ([P], ctypes.c_int),
         "moe_eplb_collect": ([i32, i32, P, P, P, P], ctypes.c_int),
+        "moe_trampoline_bytes": ([PS, ctypes.POINTER(i64)], ctypes.c_int),
+        "moe_dispatch_trampoline": ([PS, P, P, P, i64, P, i64, P, P, P, P, i64, P], ctypes.c_int),
         "moe_expert_ffn_combine": ([PS, P, i64, P, P, ctypes.POINTER(moe_expert_weights), P, P, i64,
                                     P, P, i64, P], ctypes.c_int),
     }
@@ -244,6 +247,21 @@ def moe_expert_ffn(shape: Shape, dispatch_buf, expert_offsets, expert_rows, w_ga
         ctypes.byref(cs), _ptr(dispatch_buf), dispatch_buf.numel(), _ptr(expert_offsets),
         _ptr(expert_rows), ctypes.byref(w), _ptr(combine_buf), combine_buf.numel(),
         _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def moe_trampoline_bytes(shape: Shape) -> int:
+    v = ctypes.c_int64(0)
+    _check("moe_trampoline_bytes", load().moe_trampoline_bytes(ctypes.byref(shape.c()), ctypes.byref(v)))
+    return v.value
+
+
+def moe_dispatch_trampoline(shape: Shape, x, phys_idx, trampoline_buf, dispatch_buf, rank_counts,
+                            expert_offsets, expert_rows, workspace, stream=None):
+    cs = shape.c()
+    _check("moe_dispatch_trampoline", load().moe_dispatch_trampoline(
+        ctypes.byref(cs), _ptr(x), _ptr(phys_idx), _ptr(trampoline_buf), trampoline_buf.numel(),
+        _ptr(dispatch_buf), dispatch_buf.numel(), _ptr(rank_counts), _ptr(expert_offsets),
+        _ptr(expert_rows), _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def moe_expert_ffn_combine(shape: Shape, dispatch_buf, expert_offsets, expert_rows, w_gate_up,

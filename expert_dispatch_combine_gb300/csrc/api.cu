@@ -141,6 +141,40 @@ moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, const int32_t
                                        make_ws(d), (cudaStream_t)stream));
 }
 
+moe_status moe_trampoline_bytes(const moe_shape* shape, int64_t* bytes) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (!bytes || shape->n_src_ranks > shape->n_ranks) return MOE_ERR_INVALID_ARG;
+    *bytes = trampoline_layout(make_dims(*shape)).total;
+    return MOE_OK;
+}
+
+moe_status moe_dispatch_trampoline(const moe_shape* shape, const uint16_t* x, const int32_t* phys_idx,
+                                   void* trampoline_buf, int64_t trampoline_bytes,
+                                   void* dispatch_buf, int64_t dispatch_bytes, int32_t* rank_counts,
+                                   int32_t* expert_offsets, int32_t* expert_rows, void* workspace,
+                                   int64_t workspace_bytes, moe_stream_t stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (shape->n_src_ranks > shape->n_ranks) return MOE_ERR_INVALID_ARG;
+    if (!x || !phys_idx || !trampoline_buf || !dispatch_buf || !rank_counts || !expert_offsets ||
+        !expert_rows || !workspace)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(trampoline_buf, 256) || !aligned(dispatch_buf, 256) ||
+        !aligned(workspace, 256))
+        return MOE_ERR_INVALID_ARG;
+    Dims d = make_dims(*shape);
+    moe_layout L;
+    fill_layout(d, &L);
+    if (dispatch_bytes < L.dispatch_bytes || workspace_bytes < L.workspace_bytes ||
+        trampoline_bytes < trampoline_layout(d).total)
+        return MOE_ERR_WORKSPACE;
+    return cuda_status(launch_dispatch_trampoline(d, x, phys_idx, trampoline_buf, dispatch_buf,
+                                                  L.dispatch_meta_offset, rank_counts,
+                                                  expert_offsets, expert_rows, workspace,
+                                                  make_ws(d), (cudaStream_t)stream));
+}
+
 moe_status moe_expert_ffn(const moe_shape* shape, const void* dispatch_buf,
                           int64_t dispatch_bytes, const int32_t* expert_offsets,
                           const int32_t* expert_rows, const moe_expert_weights* weights,

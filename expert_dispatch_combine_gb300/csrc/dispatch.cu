@@ -165,13 +165,26 @@ __device__ __forceinline__ unsigned quant4(float a, float b, float c, float d, f
 
 constexpr int kScatterThreads = 128;
 
+// Dispatch modes of the scatter kernel:
+//   kDirect: quantise token t and write its k messages into the owners'
+//            static areas (FusedDispatch);
+//   kHop1:   quantise token t and write it once, with its k physical expert
+//            ids, into its trampoline's area (the first hop of the
+//            trampoline forward, "xDeepServe", P045);
+//   kHop2:   read token t back from the trampoline area and write its k
+//            messages exactly as kDirect does (the second hop).
+enum { kDirect = 0, kHop1 = 1, kHop2 = 2 };
+
+template <int MODE>
 __global__ void __launch_bounds__(kScatterThreads)
 scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int8_msgs,
                long long drow, const uint16_t* __restrict__ x,
                const int32_t* __restrict__ phys_idx, const int32_t* __restrict__ slot_local,
                const int32_t* __restrict__ erank, const int32_t* __restrict__ src_base,
                const int32_t* __restrict__ expert_offsets, char* __restrict__ dbuf,
-               moe_dispatch_meta* __restrict__ meta, int32_t* __restrict__ expert_rows) {
+               moe_dispatch_meta* __restrict__ meta, int32_t* __restrict__ expert_rows,
+               char* __restrict__ trows, moe_dispatch_meta* __restrict__ tmeta,
+               int32_t* __restrict__ troutes) {
     extern __shared__ __align__(128) unsigned char sm[];
     uint4* srow = reinterpret_cast<uint4*>(sm);                 // bf16 row, 2H bytes
     uint2* scode = reinterpret_cast<uint2*>(sm + 2 * (size_t)H);  // H codes
@@ -181,6 +194,41 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
     const int t = blockIdx.x;
     const int src = t / lb, bs = t - src * lb;
     const int nch = H / 8;  // 16-byte chunks of 8 bf16
+    const long long tk = (long long)t * k;
+    if constexpr (MODE == kHop2) {
+        // the token as the trampoline holds it: the message row, its scale and routes
+        const uint4* tr = reinterpret_cast<const uint4*>(trows + (long long)t * drow);
+        uint4* dstm = reinterpret_cast<uint4*>(sm);
+        for (int c = threadIdx.x; c < (int)(drow / 16); c += kScatterThreads) dstm[c] = tr[c];
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        __syncthreads();
+        const float scale = tmeta[t].scale;
+        if (threadIdx.x == 0) {
+            for (int j = 0; j < k; ++j) {
+                int p = troutes[tk + j];
+                int dst = p / epr;
+                long long g = ((long long)dst * S + src) * mt + slot_local[tk + j];
+                bulk_store_s2g(dbuf + g * drow, sm, (unsigned)drow);
+            }
+            asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+        }
+        if (threadIdx.x >= 32 && threadIdx.x < 32 + k) {
+            int j = threadIdx.x - 32;
+            int p = troutes[tk + j];
+            int dst = p / epr;
+            long long g = ((long long)dst * S + src) * mt + slot_local[tk + j];
+            moe_dispatch_meta m;
+            m.scale = scale;
+            m.src_rank = src;
+            m.batch_slot = bs;
+            m.route_slot = j;
+            meta[g] = m;
+            expert_rows[expert_offsets[p] + src_base[(long long)src * E_phys + p] + erank[tk + j]] =
+                (int32_t)g;
+        }
+        if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+        return;
+    }
     const uint4* xr = reinterpret_cast<const uint4*>(x + (long long)t * H);
     float amax = 0.f;
     for (int c = threadIdx.x; c < nch; c += kScatterThreads) {
@@ -228,7 +276,22 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
     // generic-proxy shared writes -> visible to the bulk-copy (async) proxy
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     __syncthreads();
-    const long long tk = (long long)t * k;
+    if constexpr (MODE == kHop1) {
+        // one copy of the token, its scale and its routes to the trampoline
+        if (threadIdx.x == 0) {
+            bulk_store_s2g(trows + (long long)t * drow, src_row, (unsigned)drow);
+            asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+            moe_dispatch_meta m;
+            m.scale = scale;
+            m.src_rank = src;
+            m.batch_slot = bs;
+            m.route_slot = k;  // the k routes follow in troutes
+            tmeta[t] = m;
+        }
+        if (threadIdx.x >= 32 && threadIdx.x < 32 + k) troutes[tk + threadIdx.x - 32] = phys_idx[tk + threadIdx.x - 32];
+        if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+        return;
+    }
     if (threadIdx.x == 0) {
         for (int j = 0; j < k; ++j) {
             int p = phys_idx[tk + j];
@@ -257,10 +320,12 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
 
 }  // namespace
 
-cudaError_t launch_dispatch(const Dims& d, const uint16_t* x, const int32_t* phys_idx,
-                            void* dbuf, long long meta_off, int32_t* rank_counts,
-                            int32_t* expert_offsets, int32_t* expert_rows, void* ws,
-                            const WsLayout& wl, cudaStream_t st) {
+namespace {
+
+// The two layout kernels: per-(destination, source) slots, per-expert counts,
+// offsets and the per-source bases of the expert row lists.
+cudaError_t launch_layout(const Dims& d, const int32_t* phys_idx, int32_t* rank_counts,
+                          int32_t* expert_offsets, void* ws, const WsLayout& wl, cudaStream_t st) {
     int32_t* slot_local = ws_ptr<int32_t>(ws, wl.slot_local);
     int32_t* erank = ws_ptr<int32_t>(ws, wl.erank);
     int32_t* hist = ws_ptr<int32_t>(ws, wl.hist);
@@ -270,19 +335,70 @@ cudaError_t launch_dispatch(const Dims& d, const uint16_t* x, const int32_t* phy
                                                              d.S, phys_idx, slot_local, erank,
                                                              rank_counts, hist);
     layout_expert_kernel<<<1, 1024, 0, st>>>(d.S, d.E_phys, hist, src_base, expert_offsets);
+    count_launches(2);
+    return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_scatter(const Dims& d, const uint16_t* x, const int32_t* phys_idx, void* dbuf,
+                           long long meta_off, int32_t* expert_offsets, int32_t* expert_rows,
+                           void* ws, const WsLayout& wl, char* trows, moe_dispatch_meta* tmeta,
+                           int32_t* troutes, cudaStream_t st) {
     size_t smem3 = (size_t)d.H * 2 + (d.dfmt == MOE_MSG_INT8 ? (size_t)d.H : 0);
     if (smem3 > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(scatter_kernel,
+        cudaError_t e = cudaFuncSetAttribute(scatter_kernel<MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem3);
         if (e != cudaSuccess) return e;
     }
-    scatter_kernel<<<d.T, kScatterThreads, smem3, st>>>(
+    scatter_kernel<MODE><<<d.T, kScatterThreads, smem3, st>>>(
         d.H, d.k, d.lb, d.epr, d.S, d.mt, d.E_phys, d.dfmt == MOE_MSG_INT8 ? 1 : 0, d.drow, x,
-        phys_idx, slot_local, erank, src_base, expert_offsets, static_cast<char*>(dbuf),
-        reinterpret_cast<moe_dispatch_meta*>(static_cast<char*>(dbuf) + meta_off), expert_rows);
-    count_launches(3);
+        phys_idx, ws_ptr<int32_t>(ws, wl.slot_local), ws_ptr<int32_t>(ws, wl.erank),
+        ws_ptr<int32_t>(ws, wl.src_base), expert_offsets, static_cast<char*>(dbuf),
+        reinterpret_cast<moe_dispatch_meta*>(static_cast<char*>(dbuf) + meta_off), expert_rows,
+        trows, tmeta, troutes);
+    count_launches(1);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const Dims& d, const uint16_t* x, const int32_t* phys_idx,
+                            void* dbuf, long long meta_off, int32_t* rank_counts,
+                            int32_t* expert_offsets, int32_t* expert_rows, void* ws,
+                            const WsLayout& wl, cudaStream_t st) {
+    cudaError_t e = launch_layout(d, phys_idx, rank_counts, expert_offsets, ws, wl, st);
+    if (e != cudaSuccess) return e;
+    return launch_scatter<kDirect>(d, x, phys_idx, dbuf, meta_off, expert_offsets, expert_rows, ws,
+                                   wl, nullptr, nullptr, nullptr, st);
+}
+
+TrampolineLayout trampoline_layout(const Dims& d) {
+    TrampolineLayout t;
+    t.rows = 0;
+    t.meta = align_up((long long)d.T * d.drow, 256);
+    t.routes = align_up(t.meta + 16LL * d.T, 256);
+    t.total = align_up(t.routes + 4LL * d.T * d.k, 256);
+    return t;
+}
+
+cudaError_t launch_dispatch_trampoline(const Dims& d, const uint16_t* x, const int32_t* phys_idx,
+                                       void* tbuf, void* dbuf, long long meta_off,
+                                       int32_t* rank_counts, int32_t* expert_offsets,
+                                       int32_t* expert_rows, void* ws, const WsLayout& wl,
+                                       cudaStream_t st) {
+    const TrampolineLayout tl = trampoline_layout(d);
+    char* tb = static_cast<char*>(tbuf);
+    char* trows = tb + tl.rows;
+    moe_dispatch_meta* tmeta = reinterpret_cast<moe_dispatch_meta*>(tb + tl.meta);
+    int32_t* troutes = reinterpret_cast<int32_t*>(tb + tl.routes);
+    cudaError_t e = launch_scatter<kHop1>(d, x, phys_idx, dbuf, meta_off, expert_offsets,
+                                          expert_rows, ws, wl, trows, tmeta, troutes, st);
+    if (e != cudaSuccess) return e;
+    if ((e = launch_layout(d, phys_idx, rank_counts, expert_offsets, ws, wl, st)) != cudaSuccess)
+        return e;
+    return launch_scatter<kHop2>(d, nullptr, nullptr, dbuf, meta_off, expert_offsets, expert_rows,
+                                 ws, wl, trows, tmeta, troutes, st);
 }
 
 }  // namespace moe

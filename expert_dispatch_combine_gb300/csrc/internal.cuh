@@ -124,6 +124,19 @@ inline T* ws_ptr(void* ws, long long off) { return reinterpret_cast<T*>(static_c
 
 // Number of kernels (and memsets) this library has enqueued in this process.
 void count_launches(int n);
+// Trampoline area of the two-hop dispatch: [T][drow] message rows, [T]
+// moe_dispatch_meta (route_slot = k: the routes follow), [T][k] int32
+// physical expert ids.  Trampoline s holds the rows of source rank s's tokens.
+struct TrampolineLayout {
+    long long rows, meta, routes, total;
+};
+TrampolineLayout trampoline_layout(const Dims& d);
+cudaError_t launch_dispatch_trampoline(const Dims& d, const uint16_t* x, const int32_t* phys_idx,
+                                       void* tbuf, void* dbuf, long long meta_off,
+                                       int32_t* rank_counts, int32_t* expert_offsets,
+                                       int32_t* expert_rows, void* ws, const WsLayout& wl,
+                                       cudaStream_t st);
+
 // MOE_OK for cudaSuccess, else MOE_ERR_CUDA with the error kept for
 // moe_last_cuda_error.
 moe_status record_cuda_status(cudaError_t e);

@@ -54,6 +54,11 @@ class Workload:
     seed: int
     zipf: float = 0.0
     eplb: bool = False
+    plan_ranks: int = 0  # ranks the replica planner places over (0: R)
+
+    @property
+    def placement_ranks(self) -> int:
+        return self.plan_ranks or self.R
 
     @property
     def lb(self) -> int:
@@ -77,13 +82,19 @@ WORKLOADS = {
     # profiling case: the DeepSeek-V3 expert shape with 32 experts (1.4 GB of
     # weights, about 3.5 GB on the device in total) and 1024 rows per expert
     "prof_e32": Workload("prof_e32", 4096, 7168, 32, 32, 8, 2048, 32, 32, 5),
+    # trampoline forward ("xDeepServe", P044-P047): one DP domain of 160
+    # attention ranks x 96 tokens (the pages' global batch 46,080 is three such
+    # domains) sent to 288 expert ranks, one physical expert each (256 routed
+    # experts + 32 redundant copies, placed over 32 groups of 9 slots)
+    "tr_domain": Workload("tr_domain", 15360, 7168, 256, 288, 8, 2048, 288, 160, 10, zipf=1.2,
+                          eplb=True, plan_ranks=32),
 }
 
 
 def custom(name="custom", T=64, H=256, E_log=16, E_phys=None, k=2, I=128, R=4, S=None,
-           seed=0, zipf=0.0, eplb=False) -> Workload:
+           seed=0, zipf=0.0, eplb=False, plan_ranks=0) -> Workload:
     return Workload(name, T, H, E_log, E_phys if E_phys else E_log, k, I, R,
-                    S if S else R, seed, zipf, eplb)
+                    S if S else R, seed, zipf, eplb, plan_ranks)
 
 
 # ------------------------------------------------------------------ floats

@@ -340,6 +340,30 @@ moe_status moe_grouped_gemm_s8(int32_t n_groups, const int32_t* offsets, int64_t
                                const int8_t* B, int32_t N, int32_t K, int32_t* C,
                                void* workspace, int64_t workspace_bytes, moe_stream_t stream);
 
+/* FusedDispatch by trampoline forward ([X] "合设 MoE-Attention 的
+ * All-to-All" P044-P045, P109: with fewer attention ranks than expert ranks,
+ * as many expert ranks as there are attention ranks first receive all of an
+ * attention rank's data and forward it to the other expert ranks).  Source
+ * rank s (an attention rank) uses expert rank s as its trampoline:
+ *   hop 1 (A2E):  every token of s is written once into trampoline s's area:
+ *                 its message row (INT8 codes + scale, or bf16), its
+ *                 batch_slot and its k physical expert ids;
+ *   hop 2 (A2E'): the trampoline writes one message per (token, route) into
+ *                 the owner's static area.
+ * The outputs (dispatch buffer rows and meta, rank_counts, expert_offsets,
+ * expert_rows) are those of moe_dispatch, bit for bit.  Requires
+ * n_src_ranks <= n_ranks.
+ *   trampoline_buf (device, 256-byte aligned) of moe_trampoline_bytes bytes:
+ *   rows [T][row bytes], then meta [T] (moe_dispatch_meta, route_slot = k),
+ *   then routes [T][k] int32, each region 256-byte aligned.  Caller-owned;
+ *   its contents after the call are the trampolines' receive areas. */
+moe_status moe_trampoline_bytes(const moe_shape* shape, int64_t* bytes);
+moe_status moe_dispatch_trampoline(const moe_shape* shape, const uint16_t* x, const int32_t* phys_idx,
+                                   void* trampoline_buf, int64_t trampoline_bytes,
+                                   void* dispatch_buf, int64_t dispatch_bytes, int32_t* rank_counts,
+                                   int32_t* expert_offsets, int32_t* expert_rows, void* workspace,
+                                   int64_t workspace_bytes, moe_stream_t stream);
+
 /* FusedDispatch without a workspace.  The pages have no counterpart to this
  * entry point: it exists for callers that cannot call cudaMalloc at all --
  * an engine whose allocator has reserved all device memory and forbids any

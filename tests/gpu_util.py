@@ -43,7 +43,7 @@ def eplb_map(w: synth.Workload):
     lg = synth.logits(w)
     _, _, _, cnt = oracle.route(lg, w.k)
     from oracle import eplb
-    rep, nc, p2l = eplb.plan(cnt[None, :].astype(np.float64), w.E_phys, w.R)
+    rep, nc, p2l = eplb.plan(cnt[None, :].astype(np.float64), w.E_phys, w.placement_ranks)
     return rep, nc, p2l
 
 
