@@ -88,8 +88,8 @@ constexpr int BN_LARGE = kTcTileRows, BN_DECODE = kTcMinTileRows;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 20000000ull;
 // per-thread register budgets after setmaxnreg: 128 threads each at
-// 56 (producer/MMA) + 96 (converter) + 2 x 176 (drains) = 64,512 <= 512 x 128
-constexpr uint32_t REG_CTRL = 56, REG_CONV = 96, REG_DRAIN = 176;
+// 48 (producer/MMA) + 96 (converter) + 2 x 184 (drains) = 65,536 <= 512 x 128
+constexpr uint32_t REG_CTRL = 48, REG_CONV = 96, REG_DRAIN = 184;
 static_assert(128 * (REG_CTRL + REG_CONV + 2 * REG_DRAIN) <= THREADS * 128, "register split");
 
 enum { EPI_I32 = 0, EPI_GU = 1, EPI_F32 = 2, EPI_BF16MSG = 3 };
