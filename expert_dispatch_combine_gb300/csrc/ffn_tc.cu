@@ -196,7 +196,8 @@ __device__ __forceinline__ void epilogue_direct(const Params& P, const TileInfo&
     } else if constexpr (EPI == EPI_GU || EPI == EPI_F32) {
         int col, ld;
         if constexpr (EPI == EPI_GU) {
-            col = (row < 64) ? ti.mb * 64 + row : P.nout + ti.mb * 64 + (row - 64);
+            // gate channel c in lane 2c, up channel c in lane 2c + 1 (converter)
+            col = (row & 1) ? P.nout + ti.mb * 64 + (row >> 1) : ti.mb * 64 + (row >> 1);
             ld = 2 * P.nout;
         } else {
             col = ti.mb * 128 + row;
@@ -250,8 +251,8 @@ __device__ __forceinline__ bool epilogue_tma(const Params& P, const TileInfo& ti
         int col;
         float* o;
         if constexpr (EPI == EPI_GU) {
-            col = (row < 64) ? ti.mb * 64 + row : P.nout + ti.mb * 64 + (row - 64);
-            o = reinterpret_cast<float*>(stg) + (row < 64 ? 0 : GT * 64) + (row & 63);
+            col = (row & 1) ? P.nout + ti.mb * 64 + (row >> 1) : ti.mb * 64 + (row >> 1);
+            o = reinterpret_cast<float*>(stg) + ((row & 1) ? GT * 64 : 0) + (row >> 1);
         } else {
             col = ti.mb * 128 + row;
             o = reinterpret_cast<float*>(stg) + row;
@@ -281,19 +282,20 @@ __device__ __forceinline__ bool epilogue_tma(const Params& P, const TileInfo& ti
 }
 
 // Epilogue of the expert FFN for one 16-token group, staged in shared memory.
-//   EPI_GU: rows 0..63 hold the gate projection g of the tile's 64 channels,
-//     rows 64..127 the up projection u of the same channels; the group's
-//     h = SiLU(g) * u is formed in shared memory (8 values per thread).
+//   EPI_GU: lane 2c holds the gate projection g of the tile's channel c and
+//     lane 2c + 1 the up projection u of the same channel; the two lanes
+//     swap halves through a shuffle and each forms h = SiLU(g) * u for 8 of
+//     the group's tokens, which it stores into the staging buffer.
 //   EPI_F32: y of the tile's 128 output channels.
 // The per-row absolute maximum of this tile's outputs goes to `rowmax` with
 // an atomic max (the token-wise requantisation needs the whole row); the
 // values go out with one TMA tensor store for a full group, plain stores for
 // a partial one.  All four warps of the drain warpgroup take part.
-// Groups alternate between two staging buffers.  Two warpgroup barriers per
-// group suffice: every thread's reads of a buffer precede its arrival at the
-// next group's first barrier, and the leader waits for the previous group's
-// tensor store to have read its buffer before the second barrier, so a buffer
-// is free again when the group after next starts writing it.
+// Groups alternate between two staging buffers, with one warpgroup barrier
+// per group: every thread's reads of a buffer precede its arrival at the next
+// group's barrier, and before that barrier the leader waits for the previous
+// group's tensor store to have read its buffer, so a buffer is free again
+// when the group after next writes it.
 template <int EPI>
 __device__ __forceinline__ bool epilogue_staged(const Params& P, const TileInfo& ti, int row,
                                                 int lane, int j0, const int (&iv)[GT], float* stg,
@@ -301,22 +303,30 @@ __device__ __forceinline__ bool epilogue_staged(const Params& P, const TileInfo&
     const int nv = min(GT, ti.nvalid - j0);  // valid tokens in this group (>= 1)
     const float sr_l = lane < nv ? P.s_row[ti.r0 + j0 + lane] : 0.f;
     if constexpr (EPI == EPI_GU) {
-        const int c = row & 63;
-        const int colw = (row < 64) ? ti.mb * 64 + c : P.nout + ti.mb * 64 + c;
+        // lane 2c holds the gate projection g of channel c, lane 2c + 1 the up
+        // projection u (see the converter); the even lane forms h for tokens
+        // 0..7 of the group, the odd lane for tokens 8..15, after swapping
+        // the other half through a shuffle
+        const int c = row >> 1;
+        const bool up = row & 1;
+        const int colw = up ? P.nout + ti.mb * 64 + c : ti.mb * 64 + c;
         const float sc = P.s_ch[(long long)ti.set * P.rows_per_set + colw];
-        float* o = stg + (row < 64 ? 0 : GT * 64) + c;
+        float v[GT];
 #pragma unroll
         for (int j = 0; j < GT; ++j) {
             const float sr = __shfl_sync(0xffffffffu, sr_l, j);
-            o[j * 64] = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sc);
+            v[j] = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sc);
         }
-        if (!wg.sync(lane, P.err)) return false;
-        // h for channel c and tokens tb .. tb+7
-        const int tb = (row >> 6) * 8;
+        const int tb = up ? 8 : 0;  // this thread's tokens tb .. tb+7
         float hv[8];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
-            hv[jj] = __fmul_rn(silu_fast(stg[(tb + jj) * 64 + c]), stg[GT * 64 + (tb + jj) * 64 + c]);
+        for (int jj = 0; jj < 8; ++jj) {
+            // even lane sends g of tokens 8..15, odd lane u of tokens 0..7
+            const float o = __shfl_xor_sync(0xffffffffu, up ? v[jj] : v[8 + jj], 1);
+            const float g = up ? o : v[jj];
+            const float u = up ? v[8 + jj] : o;
+            hv[jj] = __fmul_rn(silu_fast(g), u);
+        }
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) stg[(tb + jj) * 64 + c] = hv[jj];
         ptx::fence_proxy_async_smem();
@@ -549,8 +559,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         const int wq = warp & 3;
         const int row = wq * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-        const uint8_t* arow_base = stages + B_BYTES + (row >> 6) * 4096 + (row & 63) * 64;
-        const int sw = (row >> 1) & 3;
+        // EPI_GU: TMEM lane 2c takes gate channel c (shared-memory row c), lane
+        // 2c + 1 the matching up channel (row 64 + c), so that the epilogue
+        // finds g and u of one channel in neighbouring lanes
+        const int srow = EPI == EPI_GU ? ((row & 1) << 6) | (row >> 1) : row;
+        const uint8_t* arow_base = stages + B_BYTES + (srow >> 6) * 4096 + (srow & 63) * 64;
+        const int sw = (srow >> 1) & 3;
+        // EPI_GU: a gate lane and its up lane read the same bank positions of
+        // their two boxes; the up lane takes its chunks in the order c ^ 2,
+        // which keeps every 8-lane phase of the loads free of bank conflicts
+        const int rot = EPI == EPI_GU ? (row & 1) << 1 : 0;
         uint32_t pr = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
@@ -571,7 +589,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     const uint8_t* arow = arow_base + (2 * sp + j) * STAGE_BYTES;
                     uint4 w[4];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ sw) << 4));
+                    for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ rot ^ sw) << 4));
+                    if (EPI == EPI_GU && rot) {  // back to chunk order
+                        const uint4 t0 = w[0], t1 = w[1];
+                        w[0] = w[2]; w[1] = w[3]; w[2] = t0; w[3] = t1;
+                    }
                     uint32_t v[32];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
