@@ -20,17 +20,18 @@
 //     shared memory; a converter warpgroup turns them into fp16 and stores
 //     them in tensor memory (the A-from-TMEM form of tcgen05.mma), so the
 //     converted weights cost no shared-memory bandwidth;
-//   B operand = activations, up to 192 tokens per tile (fp16, K-major, 128B
+//   B operand = activations, up to BN tokens per tile (fp16, K-major, 128B
 //     swizzle), TMA-loaded in 32-row boxes so that small experts only load
 //     the rows they have; the MMA N is the tile's token count rounded up to 16.
-//   TMEM (512 columns): two 192-column fp32 accumulators, so that the drain
-//     of one 1024-K chunk overlaps the MMAs of the next, and four 32-column A
-//     slots.  The int32 running sums live in registers of two drain
-//     warpgroups (96 token columns each).
+//   TMEM (512 columns): two BN-column fp32 accumulators, so that the drain
+//     of one 1024-K chunk overlaps the MMAs of the next, and the rest in
+//     pairs of 32-column A slots (two pairs at BN = 192, three at 160).  The
+//     int32 running sums live in registers of two drain warpgroups (BN / 2
+//     token columns each).
 //   Issue: the single MMA thread waits once per PAIR of 64-K stages (8 MMAs):
 //     each wait costs the issuing thread a few hundred cycles, which 4 MMAs
 //     of N <= 224 do not cover but 8 do.  The converter fills the A slots of
-//     one pair while the MMAs of the other run.
+//     one pair while the MMAs of the others run.
 //   Epilogue: each 16-token group is scaled, staged in shared memory and
 //     written with one TMA tensor store (partial groups use plain stores).
 // Warp roles (16 warps): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
@@ -54,7 +55,6 @@ namespace moe {
 namespace tc {
 
 constexpr int BK = 64;                           // K per stage
-constexpr int NA = 4;                            // TMEM A slots (two pairs)
 constexpr int CK = 16;                           // stages per exact chunk (1024 K)
 constexpr int CKP = CK / 2;                      // stage pairs per exact chunk
 constexpr int BOX_ROWS = 32;                     // token rows per activation TMA box
@@ -65,26 +65,34 @@ constexpr int STG_BYTES = GT * 128 * 4;          // 8 KB staging buffer; two per
 constexpr uint32_t TM_ACC = 0, TM_COLS = 512;
 constexpr int THREADS = 512;
 
-// Shapes that depend on the tile's token count BN: 192 for batches with
-// many rows per expert, 64 for decode-sized batches, where the smaller
+// Shapes that depend on the tile's token count BN: 192 or 160 for batches
+// with many rows per expert, 64 for decode-sized batches, where the smaller
 // activation region buys twice the stages (weight bytes in flight).
+// The TMEM columns after the two accumulators hold NAP pairs of A slots
+// (64 columns per stage pair): the converter can fill pair p while the MMAs
+// of pairs p - NAP + 1 .. p - 1 run.  More A pairs than shared-memory pairs
+// would never be used.
 template <int BNV>
 struct Tile {
     static constexpr int BN = BNV;                            // tokens per tile
     static constexpr int B_BYTES = BN * BK * 2;               // fp16 activations per stage
-    static constexpr int STAGE_BYTES = B_BYTES + A_BYTES;     // 32 KB or 16 KB
-    static constexpr int NS = BN == 192 ? 6 : 12;             // shared-memory stages
+    static constexpr int STAGE_BYTES = B_BYTES + A_BYTES;     // 32, 28 or 16 KB
+    static constexpr int NS = BN == 64 ? 12 : 6;              // shared-memory stages
     static constexpr int NP = NS / 2;                         // stage pairs
+    static constexpr uint32_t TM_A = 2 * BN;                  // after the two accumulators
+    static constexpr int NAP_FIT = (TM_COLS - TM_A) / 64;     // A-slot pairs that fit in TMEM
+    static constexpr int NAP = NAP_FIT < NP ? NAP_FIT : NP;   // A-slot pairs used
     static constexpr int HALF = BN / 2;                       // token columns per drain warpgroup
     static constexpr int NGRP = HALF / GT;                    // epilogue groups per drain warpgroup
-    static constexpr int NBARS = 2 * NP + 2 + 4 + 1 + 2;
-    static constexpr uint32_t TM_A = 2 * BN;                  // after the two accumulators
+    static constexpr int NBARS = 2 * NP + NAP + 4 + 1 + 2;
     static constexpr int SMEM_BYTES = NS * STAGE_BYTES + 4 * STG_BYTES + NBARS * 8 + 16 + 1024;
     static_assert(BN % 32 == 0 && HALF % GT == 0 && NS % 2 == 0, "tile shape");
+    static_assert(STAGE_BYTES % 1024 == 0, "stages start on 128B-swizzle atoms");
     static_assert(SMEM_BYTES <= 227 * 1024, "dynamic shared memory per CTA");
-    static_assert(NA == 4 && TM_A + NA * 32 <= TM_COLS, "two accumulators and two pairs of A slots in TMEM");
+    static_assert(NAP >= 2 && TM_A + NAP * 64 <= TM_COLS, "two accumulators and two or more A-slot pairs in TMEM");
 };
 constexpr int BN_LARGE = kTcTileRows, BN_DECODE = kTcMinTileRows;
+constexpr int BN_MID = 160;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 20000000ull;
 // per-thread register budgets after setmaxnreg: 128 threads each at
@@ -400,7 +408,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                const __grid_constant__ CUtensorMap tmXb,
                const __grid_constant__ CUtensorMap tmO, const Params P) {
     using TL = Tile<BNV>;
-    constexpr int BN = TL::BN, NS = TL::NS, NP = TL::NP, HALF = TL::HALF, NGRP = TL::NGRP;
+    constexpr int BN = TL::BN, NS = TL::NS, NP = TL::NP, NAP = TL::NAP, HALF = TL::HALF, NGRP = TL::NGRP;
     constexpr int B_BYTES = TL::B_BYTES, STAGE_BYTES = TL::STAGE_BYTES, NBARS = TL::NBARS;
     constexpr uint32_t TM_A = TL::TM_A;
     extern __shared__ uint8_t smem_raw[];
@@ -415,18 +423,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
     auto fullp = [&](int sp) { return bar(sp); };        // both stages of pair slot sp loaded
     auto emptyp = [&](int sp) { return bar(NP + sp); };  // pair slot sp consumed by the MMAs
-    auto afull = [&](int p) { return bar(2 * NP + p); };  // A slots of a stage pair converted
-    auto accfull = [&](int b) { return bar(2 * NP + 2 + b); };
-    auto accempty = [&](int b) { return bar(2 * NP + 2 + 2 + b); };
-    const uint32_t done_bar = bar(2 * NP + 2 + 4);
-    auto wg_bar = [&](int h) { return bar(2 * NP + 2 + 5 + h); };
+    auto afull = [&](int p) { return bar(2 * NP + p); };  // A-slot pair p converted
+    auto accfull = [&](int b) { return bar(2 * NP + NAP + b); };
+    auto accempty = [&](int b) { return bar(2 * NP + NAP + 2 + b); };
+    const uint32_t done_bar = bar(2 * NP + NAP + 4);
+    auto wg_bar = [&](int h) { return bar(2 * NP + NAP + 5 + h); };
 
     if (threadIdx.x == 0) {
         for (int sp = 0; sp < NP; ++sp) {
             ptx::mbar_init(fullp(sp), 1);
             ptx::mbar_init(emptyp(sp), 1);
         }
-        for (int p = 0; p < 2; ++p) ptx::mbar_init(afull(p), 4);
+        for (int p = 0; p < NAP; ++p) ptx::mbar_init(afull(p), 4);
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accfull(b), 1);
             ptx::mbar_init(accempty(b), 8);
@@ -528,14 +536,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                             break;
                         }
                     }
-                    if (!ptx::mbar_wait(afull(pr & 1), (pr >> 1) & 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
+                    if (!ptx::mbar_wait(afull(pr % NAP), (pr / NAP) & 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
                     const int sp = pr % NP;
                     const uint64_t bd = bdesc0 + static_cast<uint64_t>((2 * sp * STAGE_BYTES) >> 4);
-                    const uint32_t abase = tmem + TM_A + (pr & 1) * 64;
+                    const uint32_t abase = tmem + TM_A + (pr % NAP) * 64;
                     const uint32_t d = tmem + TM_ACC + b * BN;
                     ptx::mma_f16_ts(d, abase, bd, idesc, first ? 0u : 1u);
 #pragma unroll
@@ -575,10 +583,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             for (int kp = 0; kp < KSP; ++kp, ++pr) {
                 const int sp = pr % NP;
                 // The A slots of pair pr were last read by the MMAs of pair
-                // pr - 2, whose commit completed the `empty` phase of its slot.
-                const uint32_t pq = pr - 2;
+                // pr - NAP, whose commit completed the `empty` phase of its
+                // shared-memory slot.  With as many A pairs as shared-memory
+                // pairs that phase also let the producer load pair pr, so
+                // the data wait covers it.
+                const uint32_t pq = pr - NAP;
                 if (!warp_wait(fullp(sp), (pr / NP) & 1, P.err) ||
-                    (pr >= 2 && !warp_wait(emptyp(pq % NP), (pq / NP) & 1, P.err))) {
+                    (NAP < NP && pr >= NAP && !warp_wait(emptyp(pq % NP), (pq / NP) & 1, P.err))) {
                     ok = false;
                     break;
                 }
@@ -602,12 +613,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                         s8x4_to_f16x4(w[c].z, v[8 * c + 4], v[8 * c + 5]);
                         s8x4_to_f16x4(w[c].w, v[8 * c + 6], v[8 * c + 7]);
                     }
-                    ptx::tmem_st32(tmem + lane_base + TM_A + (pr & 1) * 64 + j * 32, v);
+                    ptx::tmem_st32(tmem + lane_base + TM_A + (pr % NAP) * 64 + j * 32, v);
                     ptx::tmem_wait_st();
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(afull(pr & 1));
+                if (lane == 0) ptx::mbar_arrive(afull(pr % NAP));
             }
         }
     } else {
