@@ -46,16 +46,18 @@ def _peaks():
 
 
 FFN_TC_SRC = os.path.join(ROOT, "expert_dispatch_combine_gb300", "csrc", "ffn_tc.cu")
+FFN_GEMV_SRC = os.path.join(ROOT, "expert_dispatch_combine_gb300", "csrc", "ffn_gemv.cu")
 
 
-def measured_traffic(workload: str):
-    """DRAM bytes per launch of the gate/up GEMM kernel from the committed ncu
-    summary, if it was taken on this workload with the current kernel source
-    (else None)."""
-    path = os.path.join(ROOT, "profiles", "gemm_tc_gate_up_" + workload + ".md")
+def measured_traffic(workload: str, gemv: bool = False):
+    """DRAM bytes per launch of the gate/up kernel (tensor-core GEMM, or the
+    decode matrix-vector kernel) from the committed ncu summary, if it was
+    taken on this workload with the current kernel source (else None)."""
+    prefix, src_file = ("gemv_gate_up_", FFN_GEMV_SRC) if gemv else ("gemm_tc_gate_up_", FFN_TC_SRC)
+    path = os.path.join(ROOT, "profiles", prefix + workload + ".md")
     try:
         txt = open(path).read()
-        src = hashlib.sha1(open(FFN_TC_SRC, "rb").read()).hexdigest()
+        src = hashlib.sha1(open(src_file, "rb").read()).hexdigest()
     except OSError:
         return None
     kv = dict(l.split(":", 1) for l in txt.splitlines() if l.startswith(("source_sha1:", "traffic_bytes_per_launch:")))
@@ -319,7 +321,11 @@ def run_ours(args, rank: int, world: int):
     touched = np.nonzero(cnt_h)[0]
     if p2l is not None:
         touched = np.unique(p2l.cpu().numpy()[touched])
-    alg["gate_up_bytes"] = (len(touched) * 2 * w.I * w.H + w.T * w.k * w.H * 2
+    ffn_path = B.moe_expert_ffn_path(shape)
+    # the tensor-core GEMM reads the expert rows as fp16 codes, the decode
+    # matrix-vector kernel reads the int8 dispatch rows
+    act_bytes = 1 if ffn_path == B.MOE_FFN_GEMV else 2
+    alg["gate_up_bytes"] = (len(touched) * 2 * w.I * w.H + w.T * w.k * w.H * act_bytes
                             + w.T * w.k * w.I * 4)
     peaks, peak_kind = _peaks()
     hbm = peaks["hbm_gbs"]
@@ -339,6 +345,8 @@ def run_ours(args, rank: int, world: int):
     ffn_tflops = alg["ffn_ops"] / (acc["ffn"] / 1000) / 1e12
     stages["ffn_tflops"] = ffn_tflops
     peak_tc = peaks["bf16_tflops_sustained"]
+    gu_name = ("gemv_kernel<gate|up> (int8 dp4a weight streaming)" if ffn_path == B.MOE_FFN_GEMV
+               else "gemm_tc_kernel<gate|up> (exact int8 on tcgen05 kind::f16)")
     if kern["gemm_gate_up"] > 0:
         # dominant kernel: the gate|up expert GEMM, timed by CUDA events on its stream
         gu_tflops = alg["gate_up_ops"] / (kern["gemm_gate_up"] / 1000) / 1e12
@@ -350,16 +358,16 @@ def run_ours(args, rank: int, world: int):
         ridge = peak_tc * 1e12 / (hbm * 1e9)
         if intensity >= ridge:
             roofline = {"bound": "tensor", "achieved": gu_tflops, "peak": peak_tc, "unit": "TFLOP/s",
-                        "frac": gu_tflops / peak_tc, "traffic": measured_traffic(w.name),
-                        "kernel": "gemm_tc_kernel<gate|up> (exact int8 on tcgen05 kind::f16)",
+                        "frac": gu_tflops / peak_tc, "traffic": measured_traffic(w.name, ffn_path == B.MOE_FFN_GEMV),
+                        "kernel": gu_name,
                         "algorithmic_ops_per_launch": alg["gate_up_ops"],
                         "algorithmic_bytes_per_launch": alg["gate_up_bytes"],
                         "peak_source": f"{peak_kind} bf16 sustained (exact int8 runs on the fp16 tensor path)"}
         else:  # decode-sized batches stream the weights: HBM-bound
             gu_gbs = alg["gate_up_bytes"] / (kern["gemm_gate_up"] / 1000) / 1e9
             roofline = {"bound": "hbm", "achieved": gu_gbs, "peak": hbm, "unit": "GB/s",
-                        "frac": gu_gbs / hbm, "traffic": measured_traffic(w.name),
-                        "kernel": "gemm_tc_kernel<gate|up> (exact int8 on tcgen05 kind::f16)",
+                        "frac": gu_gbs / hbm, "traffic": measured_traffic(w.name, ffn_path == B.MOE_FFN_GEMV),
+                        "kernel": gu_name,
                         "algorithmic_ops_per_launch": alg["gate_up_ops"],
                         "algorithmic_bytes_per_launch": alg["gate_up_bytes"],
                         "peak_source": f"{peak_kind} HBM copy bandwidth"}
@@ -367,31 +375,62 @@ def run_ours(args, rank: int, world: int):
         roofline = {"bound": "alu", "achieved": ffn_tflops, "peak": None, "unit": "TFLOP/s",
                     "frac": None, "traffic": None, "kernel": "moe_expert_ffn (dp4a path)"}
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers.  A serving loop
+    # double-buffers: while step i runs on the compute stream, the copy stream
+    # moves step i+1's inputs in and step i-1's output out, so each step has
+    # its own layer buffers (two MoELayer objects over the same weights).
     lg_pin = torch.from_numpy(lg_h).pin_memory()
     x_pin = torch.from_numpy(x_h.view(np.int16)).pin_memory()
     out_pin = torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()
-    lg_d = torch.empty_like(logits)
-    x_d = torch.empty((w.T, w.H), dtype=torch.int16, device=dev)
-    e_steps = max(1, min(args.steps, 5))
+    layers = [layer, MoELayer(shape, w_gu, s_gu, w_d, s_d, rep_table=rep, n_copies=nc,
+                              phys_to_weight=p2l, device=dev)]
+    lg_d = [torch.empty_like(logits) for _ in range(2)]
+    x_d = [torch.empty((w.T, w.H), dtype=torch.int16, device=dev) for _ in range(2)]
+    cstream = torch.cuda.Stream(device=dev)
+    e_steps = max(2, min(args.steps, 6))
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of the set copied in
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # layer of the set finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # output of the set copied out
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e_steps):
-        lg_d.copy_(lg_pin, non_blocking=True)
-        x_d.copy_(x_pin, non_blocking=True)
-        out = layer.forward(lg_d, x_d.view(torch.bfloat16))
-        out_pin.copy_(out.view(torch.int16), non_blocking=True)
+    cstream.wait_event(e0)
+    with torch.cuda.stream(cstream):
+        lg_d[0].copy_(lg_pin, non_blocking=True)
+        x_d[0].copy_(x_pin, non_blocking=True)
+        ev_in[0].record(cstream)
+    for i in range(e_steps):
+        s_, n_ = i % 2, (i + 1) % 2
+        stream.wait_event(ev_in[s_])
+        if i >= 2:
+            stream.wait_event(ev_out[s_])  # this set's previous output has been read back
+        out = layers[s_].forward(lg_d[s_], x_d[s_].view(torch.bfloat16), stream=stream)
+        ev_done[s_].record(stream)
+        with torch.cuda.stream(cstream):
+            if i + 1 < e_steps:
+                if i >= 1:
+                    cstream.wait_event(ev_done[n_])  # step i-1 has consumed that set's inputs
+                lg_d[n_].copy_(lg_pin, non_blocking=True)
+                x_d[n_].copy_(x_pin, non_blocking=True)
+                ev_in[n_].record(cstream)
+            cstream.wait_event(ev_done[s_])
+            out_pin.copy_(out.view(torch.int16), non_blocking=True)
+            ev_out[s_].record(cstream)
+    stream.wait_stream(cstream)
     e1.record(stream)
     torch.cuda.synchronize()
+    del layers[1]
     e_ms = e0.elapsed_time(e1) / e_steps
     if world > 1:
         t = torch.tensor([e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e_ms = float(t.item())
     e2e = {"value": world * w.T / (e_ms / 1000.0), "unit": UNIT,
-           "h2d_bytes_per_step": lg_h.nbytes + x_h.nbytes, "d2h_bytes_per_step": w.T * w.H * 2}
+           "h2d_bytes_per_step": lg_h.nbytes + x_h.nbytes, "d2h_bytes_per_step": w.T * w.H * 2,
+           "steps": e_steps,
+           "pipelining": "two buffer sets: step i+1's inputs copied in and step i's output "
+                         "copied out on a second stream while the next layer runs"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -408,7 +447,9 @@ def run_ours(args, rank: int, world: int):
             "config": {"workload": w.name, "T": w.T, "H": w.H, "E_log": w.E_log, "E_phys": w.E_phys,
                        "k": w.k, "I": w.I, "ranks": w.R, "src_ranks": w.S,
                        "messages": "int8 dispatch, int8 combine",
-                       "l2": "inputs larger than L2: 11.3 GB int8 weights and 176 MB hidden read per step",
+                       "l2": (f"inputs larger than L2: {3 * w.E_log * w.H * w.I / 1e9:.2f} GB of int8 "
+                              f"expert weights (the touched experts' streamed every step) and "
+                              f"{2 * w.T * w.H / 1e6:.1f} MB of bf16 hidden per step"),
                        "parallelism": f"replicas x{world}"},
             "stages": stages,
             "roofline": roofline,

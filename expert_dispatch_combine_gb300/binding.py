@@ -58,7 +58,7 @@ EXPORTED = ("moe_status_string", "moe_static_buffer_bytes", "moe_query_layout", 
             "moe_device_status", "moe_last_cuda_error", "moe_profile_enable", "moe_profile_read",
             "moe_dispatch_noalloc", "moe_dispatch_noalloc_max_scratch", "moe_layer_graph_create",
             "moe_graph_launch", "moe_graph_destroy", "moe_eplb_collect", "moe_expert_ffn_combine",
-            "moe_trampoline_bytes", "moe_dispatch_trampoline")
+            "moe_trampoline_bytes", "moe_dispatch_trampoline", "moe_expert_ffn_path")
 
 _lib = None
 
@@ -78,6 +78,7 @@ def load(path: str = LIB_PATH):
         "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "moe_static_buffer_bytes": ([i64, i64, i64, i64, i64, ctypes.POINTER(i64)], ctypes.c_int),
         "moe_query_layout": ([PS, ctypes.POINTER(moe_layout)], ctypes.c_int),
+        "moe_expert_ffn_path": ([PS, ctypes.POINTER(i32)], ctypes.c_int),
         "moe_eplb_plan": ([i32, i32, i32, i32, P, i32, P, P, P], ctypes.c_int),
         "moe_route": ([PS, P, P, P, i32, P, P, P, P, P], ctypes.c_int),
         "moe_dispatch": ([PS, P, P, P, i64, P, P, P, P, i64, P], ctypes.c_int),
@@ -173,6 +174,18 @@ def moe_query_layout(shape: Shape) -> dict:
     cs = shape.c()
     _check("moe_query_layout", load().moe_query_layout(ctypes.byref(cs), ctypes.byref(L)))
     return {n: getattr(L, n) for n, _ in moe_layout._fields_}
+
+
+MOE_FFN_CUDA_CORE, MOE_FFN_TENSOR_CORE, MOE_FFN_GEMV = 0, 1, 2
+
+
+def moe_expert_ffn_path(shape: Shape) -> int:
+    """Which kernels run the expert FFN of moe_expert_ffn / moe_layer for
+    `shape`: MOE_FFN_CUDA_CORE, MOE_FFN_TENSOR_CORE or MOE_FFN_GEMV."""
+    out = ctypes.c_int32(0)
+    cs = shape.c()
+    _check("moe_expert_ffn_path", load().moe_expert_ffn_path(ctypes.byref(cs), ctypes.byref(out)))
+    return out.value
 
 
 def moe_eplb_plan(token_count: np.ndarray, E_phys: int, n_ranks: int, max_copies: int | None = None,

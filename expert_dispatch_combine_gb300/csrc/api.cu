@@ -103,6 +103,16 @@ moe_status moe_query_layout(const moe_shape* shape, moe_layout* layout) {
     return MOE_OK;
 }
 
+moe_status moe_expert_ffn_path(const moe_shape* shape, int32_t* path) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (!path) return MOE_ERR_INVALID_ARG;
+    const Dims d = make_dims(*shape);
+    const WsLayout wl = make_ws(d);
+    *path = !wl.tc ? MOE_FFN_CUDA_CORE : ffn_gemv_fits(d) ? MOE_FFN_GEMV : MOE_FFN_TENSOR_CORE;
+    return MOE_OK;
+}
+
 moe_status moe_route(const moe_shape* shape, const float* logits, const int32_t* rep_table,
                      const int32_t* n_copies, int32_t max_copies, int32_t* topk_idx,
                      float* topk_w, int32_t* phys_idx, int32_t* expert_counts,

@@ -92,7 +92,6 @@ struct Tile {
     static_assert(NAP >= 2 && TM_A + NAP * 64 <= TM_COLS, "two accumulators and two or more A-slot pairs in TMEM");
 };
 constexpr int BN_LARGE = kTcTileRows, BN_DECODE = kTcMinTileRows;
-constexpr int BN_MID = 160;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 20000000ull;
 // per-thread register budgets after setmaxnreg: 128 threads each at
@@ -1101,6 +1100,22 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
 }
 
 }  // namespace tc
+
+cudaError_t launch_requant_rows(int I, long long M, const float* h, const unsigned* rowmax, void* hq16,
+                                float* sh, cudaStream_t st) {
+    tc::requant_kernel<<<(unsigned)M, tc::kRowThreads, 0, st>>>(I, h, rowmax, static_cast<__half*>(hq16), sh);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_retquant_rows(const Dims& d, long long M, const float* y, const unsigned* rowmax,
+                                 const int32_t* expert_rows, const moe_dispatch_meta* meta,
+                                 unsigned char* cbuf, float* cscale, cudaStream_t st) {
+    tc::retquant_kernel<false><<<(unsigned)M, tc::kRowThreads, 0, st>>>(
+        d.H, d.k, d.lb, d.crow, y, rowmax, expert_rows, meta, cbuf, cscale, nullptr, nullptr, nullptr);
+    count_launches(1);
+    return cudaGetLastError();
+}
 
 // Decode-sized batches (at most 32 routed rows per expert on average) take
 // 64-token tiles: their tiles are mostly weight streaming, and the smaller

@@ -41,6 +41,9 @@ inline bool ffn_uses_tc(const Dims& d) { return d.H % 64 == 0 && d.I % 64 == 0; 
 constexpr int kTcTileRows = 192;
 // Token rows per tile of its decode variant (few rows per expert).
 constexpr int kTcMinTileRows = 64;
+// Routed rows per expert (on average) up to which the expert FFN streams the
+// weights through CUDA-core matrix-vector products instead of the tensor cores.
+constexpr int kGemvRowsPerExpert = 4;
 
 // Token tiles of a grouped GEMM over n_groups groups and max_rows rows, at
 // most bm rows per tile (each group adds at most one partial tile).
@@ -185,6 +188,22 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                           const int32_t* expert_offsets, const int32_t* expert_rows,
                           const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
                           const WsLayout& wl, cudaStream_t st, const FusedCombine& fc);
+// The token-wise requantisation of h (row kernel of the tensor-core path):
+// hq as exact fp16 integers and the scales s_h, from h and its row maxima.
+cudaError_t launch_requant_rows(int I, long long M, const float* h, const unsigned* rowmax, void* hq16,
+                                float* sh, cudaStream_t st);
+// INT8 return messages from y and its row maxima into the combine rows.
+cudaError_t launch_retquant_rows(const Dims& d, long long M, const float* y, const unsigned* rowmax,
+                                 const int32_t* expert_rows, const moe_dispatch_meta* meta,
+                                 unsigned char* cbuf, float* cscale, cudaStream_t st);
+// Decode batches (at most kGemvRowsPerExpert routed rows per expert on
+// average, INT8 return messages, H and I multiples of 512): the expert FFN
+// by streamed CUDA-core matrix-vector products, same outputs as launch_ffn_tc.
+bool ffn_gemv_fits(const Dims& d);
+cudaError_t launch_ffn_gemv(const Dims& d, const void* dbuf, long long meta_off,
+                            const int32_t* expert_offsets, const int32_t* expert_rows,
+                            const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
+                            const WsLayout& wl, cudaStream_t st);
 // Whether launch_ffn performs the combine itself for this shape.
 inline bool ffn_fuses_combine(const Dims& d, const WsLayout& wl) {
     return wl.tc && d.cfmt == MOE_MSG_INT8;
@@ -194,10 +213,14 @@ inline cudaError_t launch_ffn(const Dims& d, const void* dbuf, long long meta_of
                               const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
                               const WsLayout& wl, cudaStream_t st,
                               const FusedCombine& fc = FusedCombine{nullptr, nullptr}) {
-    return wl.tc ? launch_ffn_tc(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf, scale_off,
-                                 ws, wl, st, fc)
-                 : launch_ffn_simt(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
-                                   scale_off, ws, wl, st);
+    if (!wl.tc)
+        return launch_ffn_simt(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf, scale_off, ws,
+                               wl, st);
+    if (fc.out == nullptr && ffn_gemv_fits(d))
+        return launch_ffn_gemv(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf, scale_off, ws,
+                               wl, st);
+    return launch_ffn_tc(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf, scale_off, ws, wl,
+                         st, fc);
 }
 
 }  // namespace moe

@@ -82,6 +82,9 @@ WORKLOADS = {
     # profiling case: the DeepSeek-V3 expert shape with 32 experts (1.4 GB of
     # weights, about 3.5 GB on the device in total) and 1024 rows per expert
     "prof_e32": Workload("prof_e32", 4096, 7168, 32, 32, 8, 2048, 32, 32, 5),
+    # profiling case of the decode matrix-vector path: the same expert shape,
+    # 32 experts (1.4 GB of weights), 16 tokens x top-8 = 4 rows per expert
+    "prof_decode_e32": Workload("prof_decode_e32", 16, 7168, 32, 32, 8, 2048, 32, 16, 6),
     # trampoline forward ("xDeepServe", P044-P047): one DP domain of 160
     # attention ranks x 96 tokens (the pages' global batch 46,080 is three such
     # domains) sent to 288 expert ranks, one physical expert each (256 routed

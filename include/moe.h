@@ -120,6 +120,19 @@ typedef struct {
     int64_t workspace_bytes;      /* scratch bytes */
 } moe_layout;
 
+/* Which kernels moe_expert_ffn and moe_layer run the expert FFN with for
+ * `shape` (host only; moe_expert_ffn_combine always takes the tensor-core
+ * GEMMs where the shape allows them).  The choice depends on the shape alone:
+ *   MOE_FFN_CUDA_CORE    H or I not a multiple of 64: dp4a grouped GEMMs;
+ *   MOE_FFN_TENSOR_CORE  the exact-int8 tcgen05 grouped GEMMs;
+ *   MOE_FFN_GEMV         decode batches (INT8 return messages, H and I
+ *                        multiples of 512, T*k at most 4 rows per physical
+ *                        expert): weight-streaming matrix-vector products.
+ * All three give the same outputs bit for bit.  INVALID_ARG for a bad shape
+ * or a null `path`. */
+enum { MOE_FFN_CUDA_CORE = 0, MOE_FFN_TENSOR_CORE = 1, MOE_FFN_GEMV = 2 };
+moe_status moe_expert_ffn_path(const moe_shape* shape, int32_t* path);
+
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(moe_status s);
 
@@ -401,9 +414,10 @@ moe_status moe_device_status(const void* workspace, int32_t* status, moe_stream_
 const char* moe_last_cuda_error(void);
 
 /* Optional kernel timing for benchmarks (host only).  While enabled, each
- * tensor-core expert GEMM launch is bracketed by CUDA events on its stream;
+ * tensor-core expert GEMM launch (or matrix-vector kernel of the decode
+ * path, see moe_expert_ffn_path) is bracketed by CUDA events on its stream;
  * moe_profile_read synchronises on them and returns the durations (ms) of
- * the most recent gate/up GEMM (ms[0]) and down GEMM (ms[1]), -1 if none. */
+ * the most recent gate/up kernel (ms[0]) and down kernel (ms[1]), -1 if none. */
 moe_status moe_profile_enable(int32_t on);
 moe_status moe_profile_read(float* ms, int32_t n);
 

@@ -73,6 +73,26 @@ def test_layout_matches_formula(lib, name):
     assert L["workspace_bytes"] > 0
 
 
+def test_expert_ffn_path_choice(lib):
+    """The FFN kernel family follows the shape: dp4a GEMMs off the 64 grid,
+    matrix-vector products for decode batches (at most 4 routed rows per
+    physical expert, INT8 return messages, H and I multiples of 512), the
+    tensor-core GEMMs otherwise."""
+    def path(**kw):
+        base = dict(T=64, H=256, E_log=16, E_phys=16, k=2, I=128, n_ranks=4, n_src_ranks=4)
+        base.update(kw)
+        return B.moe_expert_ffn_path(B.Shape(**base))
+    assert path(H=48) == B.MOE_FFN_CUDA_CORE
+    assert path() == B.MOE_FFN_TENSOR_CORE                     # H = 256: not a multiple of 512
+    dec = dict(T=96, H=7168, E_log=256, E_phys=256, k=8, I=2048, n_ranks=32, n_src_ranks=32)
+    assert path(**dec) == B.MOE_FFN_GEMV                        # 768 rows over 256 experts
+    assert path(**dict(dec, T=128)) == B.MOE_FFN_GEMV           # exactly 4 rows per expert
+    assert path(**dict(dec, T=160)) == B.MOE_FFN_TENSOR_CORE    # 5 rows per expert
+    assert path(**dict(dec, combine_fmt=B.MOE_MSG_BF16)) == B.MOE_FFN_TENSOR_CORE
+    with pytest.raises(B.MoeError):
+        path(T=0)
+
+
 @pytest.mark.parametrize("bad", [
     dict(T=0), dict(H=24), dict(I=8), dict(k=0), dict(k=17), dict(E_phys=8),
     dict(n_ranks=3), dict(n_src_ranks=5), dict(dispatch_fmt=2),

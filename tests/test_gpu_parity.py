@@ -125,6 +125,9 @@ def test_layer_tiny_full(cfmt):
     dict(T=40, H=1088, E_log=12, k=3, I=192, R=3, S=5),   # K = 17 stages (2 exact chunks), partial channel block
     dict(T=300, H=256, E_log=4, k=4, I=128, R=2, S=3),    # k = E: 300 rows per expert, 3 token tiles
     dict(T=512, H=256, E_log=64, k=4, I=128, R=8, S=4, zipf=1.5),  # decode tiles, hot experts span several
+    # decode path: CUDA-core matrix-vector products (<= 4 rows per expert, H and I multiples of 512)
+    dict(T=48, H=1024, E_log=32, k=2, I=512, R=8, S=4),   # 1-6 rows per expert, empty experts
+    dict(T=40, H=512, E_log=64, k=4, I=1024, R=4, S=5, zipf=1.5),  # hot experts above 8 rows: several passes
     # CUDA-core expert path (H or I not a multiple of 64)
     dict(T=1, H=16, E_log=4, k=1, I=16, R=1),             # one token
     dict(T=31, H=48, E_log=8, k=8, I=32, R=2, S=1),       # k = E, ragged
@@ -137,6 +140,13 @@ def test_layer_edge_shapes(cfg):
 
 def test_layer_eplb_tiny():
     w = synth.custom("eplb_tiny", T=96, H=128, E_log=16, E_phys=24, k=2, I=64, R=8, seed=3,
+                     zipf=1.2, eplb=True)
+    _full_layer_check(w, B.MOE_MSG_INT8)
+
+
+def test_layer_eplb_decode_path():
+    # replicas alias their logical expert's weights on the decode (matrix-vector) path
+    w = synth.custom("eplb_decode", T=32, H=512, E_log=16, E_phys=24, k=2, I=512, R=8, seed=4,
                      zipf=1.2, eplb=True)
     _full_layer_check(w, B.MOE_MSG_INT8)
 
