@@ -22,33 +22,38 @@
 //                  codes into shared memory, then k bulk asynchronous copies
 //                  (shared -> global) of the code row into the k slots, plus
 //                  the 16-byte metadata and the expert row list entries.
+#include <algorithm>
+
 #include "device_math.cuh"
 #include "internal.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kLayoutWarps = 4;
+// Up to kLayoutMaxWarps warps per source rank, each taking a contiguous run
+// of 32-message rounds, so a source's lb*k messages take a few rounds per warp.
+constexpr int kLayoutMaxWarps = 16;
 
-__global__ void __launch_bounds__(kLayoutWarps * 32)
+__global__ void __launch_bounds__(kLayoutMaxWarps * 32)
 layout_src_kernel(int lb, int k, int epr, int R, int E_phys, int S,
                   const int32_t* __restrict__ phys_idx, int32_t* __restrict__ slot_local,
                   int32_t* __restrict__ erank, int32_t* __restrict__ rank_counts,
                   int32_t* __restrict__ hist) {
     extern __shared__ int smem[];
-    int* cntD = smem;                          // [W][R]
-    int* cntE = cntD + kLayoutWarps * R;       // [W][E_phys]
-    int* totD = cntE + kLayoutWarps * E_phys;  // [R]
+    const int W = blockDim.x >> 5;
+    int* cntD = smem;                // [W][R]
+    int* cntE = cntD + W * R;        // [W][E_phys]
+    int* totD = cntE + W * E_phys;   // [R]
     int* totE = totD + R;                      // [E_phys]
     const int src = blockIdx.x;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int N = lb * k;
     const long long base = (long long)src * N;
-    for (int i = threadIdx.x; i < kLayoutWarps * (R + E_phys); i += blockDim.x) smem[i] = 0;
+    for (int i = threadIdx.x; i < W * (R + E_phys); i += blockDim.x) smem[i] = 0;
     __syncthreads();
 
     const int rounds = (N + 31) / 32;
-    const int rpw = (rounds + kLayoutWarps - 1) / kLayoutWarps;
+    const int rpw = (rounds + W - 1) / W;
     const int r0 = w * rpw, r1 = min(rounds, r0 + rpw);
     const unsigned lt = (1u << lane) - 1u;
 
@@ -66,7 +71,7 @@ layout_src_kernel(int lb, int k, int epr, int R, int E_phys, int S,
     __syncthreads();
     for (int b = threadIdx.x; b < R; b += blockDim.x) {
         int run = 0;
-        for (int ww = 0; ww < kLayoutWarps; ++ww) {
+        for (int ww = 0; ww < W; ++ww) {
             int c = cntD[ww * R + b];
             cntD[ww * R + b] = run;
             run += c;
@@ -75,7 +80,7 @@ layout_src_kernel(int lb, int k, int epr, int R, int E_phys, int S,
     }
     for (int b = threadIdx.x; b < E_phys; b += blockDim.x) {
         int run = 0;
-        for (int ww = 0; ww < kLayoutWarps; ++ww) {
+        for (int ww = 0; ww < W; ++ww) {
             int c = cntE[ww * E_phys + b];
             cntE[ww * E_phys + b] = run;
             run += c;
@@ -330,10 +335,21 @@ cudaError_t launch_layout(const Dims& d, const int32_t* phys_idx, int32_t* rank_
     int32_t* erank = ws_ptr<int32_t>(ws, wl.erank);
     int32_t* hist = ws_ptr<int32_t>(ws, wl.hist);
     int32_t* src_base = ws_ptr<int32_t>(ws, wl.src_base);
-    size_t smem1 = sizeof(int) * (size_t)(kLayoutWarps + 1) * (d.R + d.E_phys);
-    layout_src_kernel<<<d.S, kLayoutWarps * 32, smem1, st>>>(d.lb, d.k, d.epr, d.R, d.E_phys,
-                                                             d.S, phys_idx, slot_local, erank,
-                                                             rank_counts, hist);
+    // warps per source: one per 32-message round, between 4 (the per-rank and
+    // per-expert passes use every thread of the block) and kLayoutMaxWarps;
+    // fewer if their per-warp counters would not fit in shared memory
+    const long long rounds = ((long long)d.lb * d.k + 31) / 32;
+    const size_t per_warp = sizeof(int) * (size_t)(d.R + d.E_phys);
+    int W = (int)std::min<long long>(kLayoutMaxWarps, std::max<long long>(4, rounds));
+    while (W > 1 && (size_t)(W + 1) * per_warp > 48 * 1024) --W;
+    const size_t smem1 = (size_t)(W + 1) * per_warp;
+    if (smem1 > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(layout_src_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem1);
+        if (e != cudaSuccess) return e;
+    }
+    layout_src_kernel<<<d.S, W * 32, smem1, st>>>(d.lb, d.k, d.epr, d.R, d.E_phys, d.S, phys_idx,
+                                                  slot_local, erank, rank_counts, hist);
     layout_expert_kernel<<<1, 1024, 0, st>>>(d.S, d.E_phys, hist, src_base, expert_offsets);
     count_launches(2);
     return cudaGetLastError();

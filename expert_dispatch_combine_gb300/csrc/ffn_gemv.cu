@@ -20,9 +20,11 @@
 // (down); requant_rows and retquant_rows take it from there.
 //
 // Block (256 threads, 8 warps) = one expert and 32 gate/up channel pairs
-// (gate/up), or one expert and 64 output channels (down).  Warp w takes 8
-// weight rows: gate channels 4w..4w+3 of the block and the matching up
-// channels, or output channels 8w..8w+7.  A lane reads 16 bytes of each row
+// (gate/up), or one expert and 4 groups of 64 output channels (down: its
+// rows are only I = 2048 bytes long, so a block takes 256 of them to spread
+// the staging of its token rows over 512 KB of weights).  Warp w takes 8
+// weight rows at a time: gate channels 4w..4w+3 of the block and the matching
+// up channels, or output channels 8w..8w+7 of each down group.  A lane reads 16 bytes of each row
 // per 512-byte step of K.  Experts with more than 8 rows are done 8 at a time.
 // After the K loop the warp's 64 partial sums (8 rows x 8 tokens) are reduced
 // over the lanes by a reduce-scatter of shuffles (62 exchanges), which leaves
@@ -40,6 +42,7 @@ constexpr int ROWS = 8;      // weight rows per warp
 constexpr int WARPS = 8;
 constexpr int THREADS = 32 * WARPS;
 constexpr int KSTEP = 512;   // K bytes per warp step (32 lanes x 16 bytes)
+constexpr int DOWN_GROUPS = 4;  // 64-channel groups per down block (256 channels)
 
 enum { GATE_UP = 0, DOWN = 1 };
 
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(THREADS, 2) gemv_kernel(const Params P) {
             wrow[r] = P.w + wr * K + lane * 16;
         }
     } else {
-        ch0 = blockIdx.x * 64 + warp * 8;
+        ch0 = blockIdx.x * 64 * DOWN_GROUPS + warp * 8;
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) wrow[r] = P.w + ((long long)set * P.nout + ch0 + r) * K + lane * 16;
     }
@@ -146,83 +149,86 @@ __global__ void __launch_bounds__(THREADS, 2) gemv_kernel(const Params P) {
         }
         __syncthreads();
 
-        int acc[ROWS * NT];
+        for (int g = 0; g < (KIND == DOWN ? DOWN_GROUPS : 1); ++g) {
+            const long long goff = (long long)g * 64 * K;  // down: rows of group g
+            int acc[ROWS * NT];
 #pragma unroll
-        for (int i = 0; i < ROWS * NT; ++i) acc[i] = 0;
+            for (int i = 0; i < ROWS * NT; ++i) acc[i] = 0;
 #pragma unroll 2
-        for (int k = 0; k < K; k += KSTEP) {
-            int4 wv[ROWS];
+            for (int k = 0; k < K; k += KSTEP) {
+                int4 wv[ROWS];
 #pragma unroll
-            for (int r = 0; r < ROWS; ++r) wv[r] = ld_stream(wrow[r] + k);
+                for (int r = 0; r < ROWS; ++r) wv[r] = ld_stream(wrow[r] + goff + k);
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                if (t < n) {
-                    const int4 x = *reinterpret_cast<const int4*>(xs + t * K + k + lane * 16);
+                for (int t = 0; t < NT; ++t) {
+                    if (t < n) {
+                        const int4 x = *reinterpret_cast<const int4*>(xs + t * K + k + lane * 16);
 #pragma unroll
-                    for (int r = 0; r < ROWS; ++r) {
-                        int& s = acc[r * NT + t];
-                        s = __dp4a(wv[r].x, x.x, s);
-                        s = __dp4a(wv[r].y, x.y, s);
-                        s = __dp4a(wv[r].z, x.z, s);
-                        s = __dp4a(wv[r].w, x.w, s);
+                        for (int r = 0; r < ROWS; ++r) {
+                            int& s = acc[r * NT + t];
+                            s = __dp4a(wv[r].x, x.x, s);
+                            s = __dp4a(wv[r].y, x.y, s);
+                            s = __dp4a(wv[r].z, x.z, s);
+                            s = __dp4a(wv[r].w, x.w, s);
+                        }
                     }
                 }
             }
-        }
-        reduce_scatter64(acc, lane);
-        // lane L: row L >> 2, tokens tl and tl + 1
-        const int row = lane >> 2, tl = 2 * (lane & 3);
-        if constexpr (KIND == GATE_UP) {
-            // lanes 0..15 hold gate rows, lanes 16..31 the up rows of the same
-            // channels and tokens
-            const int c = ch0 + (row & 3);
-            const int up0 = __shfl_xor_sync(0xffffffffu, acc[0], 16);
-            const int up1 = __shfl_xor_sync(0xffffffffu, acc[1], 16);
-            float mx[2] = {0.f, 0.f};
-            if (lane < 16) {
-                const float sg = P.s_ch[(long long)set * 2 * P.nout + c];
-                const float su = P.s_ch[(long long)set * 2 * P.nout + P.nout + c];
+            reduce_scatter64(acc, lane);
+            // lane L: row L >> 2, tokens tl and tl + 1
+            const int row = lane >> 2, tl = 2 * (lane & 3);
+            if constexpr (KIND == GATE_UP) {
+                // lanes 0..15 hold gate rows, lanes 16..31 the up rows of the same
+                // channels and tokens
+                const int c = ch0 + (row & 3);
+                const int up0 = __shfl_xor_sync(0xffffffffu, acc[0], 16);
+                const int up1 = __shfl_xor_sync(0xffffffffu, acc[1], 16);
+                float mx[2] = {0.f, 0.f};
+                if (lane < 16) {
+                    const float sg = P.s_ch[(long long)set * 2 * P.nout + c];
+                    const float su = P.s_ch[(long long)set * 2 * P.nout + P.nout + c];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int t = tl + u;
+                        if (t < n) {
+                            const float st = s_tok[t];
+                            const float g = __fmul_rn(__fmul_rn(__int2float_rn(acc[u]), st), sg);
+                            const float uv = __fmul_rn(__fmul_rn(__int2float_rn(u ? up1 : up0), st), su);
+                            const float h = __fmul_rn(silu_fast(g), uv);
+                            P.out[(long long)(t0 + t) * P.nout + c] = h;
+                            mx[u] = fabsf(h);
+                        }
+                    }
+                }
+                // per-token maximum over the warp's 4 channels (lane bits 2 and 3)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    float m = mx[u];
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                    if (lane < 4 && tl + u < n) atomicMax(&P.rowmax[t0 + tl + u], __float_as_uint(m));
+                }
+            } else {
+                const int c = ch0 + g * 64 + row;
+                const float sd = P.s_ch[(long long)set * P.nout + c];
+                float mx[2] = {0.f, 0.f};
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int t = tl + u;
                     if (t < n) {
-                        const float st = s_tok[t];
-                        const float g = __fmul_rn(__fmul_rn(__int2float_rn(acc[u]), st), sg);
-                        const float uv = __fmul_rn(__fmul_rn(__int2float_rn(u ? up1 : up0), st), su);
-                        const float h = __fmul_rn(silu_fast(g), uv);
-                        P.out[(long long)(t0 + t) * P.nout + c] = h;
-                        mx[u] = fabsf(h);
+                        const float y = __fmul_rn(__fmul_rn(__int2float_rn(acc[u]), s_tok[t]), sd);
+                        P.out[(long long)(t0 + t) * P.nout + c] = y;
+                        mx[u] = fabsf(y);
                     }
                 }
-            }
-            // per-token maximum over the warp's 4 channels (lane bits 2 and 3)
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                float m = mx[u];
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                if (lane < 4 && tl + u < n) atomicMax(&P.rowmax[t0 + tl + u], __float_as_uint(m));
-            }
-        } else {
-            const int c = ch0 + row;
-            const float sd = P.s_ch[(long long)set * P.nout + c];
-            float mx[2] = {0.f, 0.f};
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int t = tl + u;
-                if (t < n) {
-                    const float y = __fmul_rn(__fmul_rn(__int2float_rn(acc[u]), s_tok[t]), sd);
-                    P.out[(long long)(t0 + t) * P.nout + c] = y;
-                    mx[u] = fabsf(y);
+                for (int u = 0; u < 2; ++u) {
+                    float m = mx[u];
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                    if (row == 0 && tl + u < n) atomicMax(&P.rowmax[t0 + tl + u], __float_as_uint(m));
                 }
-            }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                float m = mx[u];
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                if (row == 0 && tl + u < n) atomicMax(&P.rowmax[t0 + tl + u], __float_as_uint(m));
             }
         }
     }
@@ -283,7 +289,7 @@ cudaError_t launch_ffn_gemv(const Dims& d, const void* dbuf, long long meta_off,
     P2.hq16 = hq16; P2.s_h = sh;
     P2.out = ybuf; P2.rowmax = ymax;
     if (cudaEvent_t ev = prof_event(1, 0)) cudaEventRecord(ev, st);
-    if ((e = gv::launch<gv::DOWN>(P2, d.E_phys, d.H / 64, st)) != cudaSuccess) return e;
+    if ((e = gv::launch<gv::DOWN>(P2, d.E_phys, d.H / (64 * gv::DOWN_GROUPS), st)) != cudaSuccess) return e;
     if (cudaEvent_t ev = prof_event(1, 1)) cudaEventRecord(ev, st);
 
     return launch_retquant_rows(d, M, ybuf, ymax, expert_rows, meta, static_cast<unsigned char*>(cbuf),
