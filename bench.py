@@ -280,6 +280,10 @@ def run_ours(args, rank: int, world: int):
     B.moe_profile_enable(True)
     for _ in range(reps):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        # keep the GPU busy for about 2 ms so that the host has enqueued all
+        # four calls before the first event: the stage times then hold device
+        # time only, not the host's launch latency of a call on an idle GPU
+        torch.cuda._sleep(4_000_000)
         evs[0].record(stream)
         B.moe_route(shape, logits, r["topk_idx"], r["topk_w"], r["phys_idx"], r["expert_counts"],
                     rep, nc)
@@ -306,6 +310,7 @@ def run_ours(args, rank: int, world: int):
         t_ms = 0.0
         for _ in range(reps):
             ta, tb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(4_000_000)
             ta.record(stream)
             B.moe_dispatch_trampoline(shape, x, r["phys_idx"], tbuf, b.dispatch, r["rank_counts"],
                                       r["expert_offsets"], r["expert_rows"], b.workspace)

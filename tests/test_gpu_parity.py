@@ -72,11 +72,13 @@ def test_route_ties_and_k_equals_e():
 
 
 # -------------------------------------------------------------- whole layer
-def _full_layer_check(w, cfmt):
-    """Every intermediate and the output of moe_layer against the oracle."""
+def _full_layer_check(w, cfmt, xb=None):
+    """Every intermediate and the output of moe_layer against the oracle
+    (hidden rows from the workload's generator unless xb, bf16 bits, is given)."""
     layer = make_layer(w, cfmt)
     lg = synth.logits(w)
-    xb = synth.hidden_bits(w)
+    if xb is None:
+        xb = synth.hidden_bits(w)
     out = layer.forward(torch.from_numpy(lg).cuda(), bits_to_bf16_tensor(xb))
     torch.cuda.synchronize()
     rep = nc = p2l = None
@@ -136,6 +138,43 @@ def test_layer_tiny_full(cfmt):
 ])
 def test_layer_edge_shapes(cfg):
     _full_layer_check(synth.custom(seed=5, **cfg), B.MOE_MSG_INT8)
+
+
+def _special_rows(w):
+    """Hidden rows for the degenerate cases of token-wise quantisation: +0 and
+    -0 rows (scale 0, codes 0, and then h = 0 and y = 0 down the whole FFN),
+    a single non-zero at the first index, the absmax at the last index,
+    quotients on half-integers (round-half-even decides 62.5 -> 62, -2.5 -> -2),
+    tiny and large magnitudes, a constant row (every code 127), and rows
+    whose scales (of x, or of h further on) are binary32 subnormals."""
+    xb = synth.hidden_bits(w).copy()
+    f = synth.bf16_bits_to_f32(xb)
+    H = w.H
+    f[0] = 0.0
+    f[2] = 0.0
+    f[2, 0] = 3.0
+    f[3, -1] = -8.0 * np.abs(f[3]).max()
+    f[4] = 0.0
+    f[4, :5] = [127.0, 62.5, -0.5, 1.5, -2.5]
+    f[5] *= 1e-30
+    f[6] *= 1e4
+    f[7] = 0.75
+    f[8] *= 1e-20   # h lands in the binary32 subnormals: subnormal scale s_h
+    f[9] *= 1e-37   # subnormal dispatch scale absmax / 127
+    xb = synth.f32_to_bf16_bits(f)
+    xb[1] = 0x8000  # -0.0
+    assert H >= 5
+    return xb
+
+
+@pytest.mark.parametrize("dims", [
+    dict(T=64, H=256, E_log=16, k=2, I=128, R=4),            # tensor-core expert path
+    dict(T=16, H=512, E_log=16, k=2, I=512, R=4, S=2),       # decode matrix-vector path
+    dict(T=16, H=48, E_log=8, k=2, I=32, R=2),               # CUDA-core expert path
+])
+def test_layer_special_rows(dims):
+    w = synth.custom("special_rows", seed=7, **dims)
+    _full_layer_check(w, B.MOE_MSG_INT8, xb=_special_rows(w))
 
 
 def test_layer_eplb_tiny():
