@@ -55,6 +55,7 @@ class Workload:
     zipf: float = 0.0
     eplb: bool = False
     plan_ranks: int = 0  # ranks the replica planner places over (0: R)
+    msg_formats: bool = False  # also time dispatch/combine alone with bf16 and INT8 messages
 
     @property
     def placement_ranks(self) -> int:
@@ -78,7 +79,7 @@ WORKLOADS = {
     "c1_decode": Workload("c1_decode", 96, 7168, 256, 256, 8, 2048, 32, 32, 1),
     "c2_decode_zipf": Workload("c2_decode_zipf", 12288, 7168, 256, 256, 8, 2048, 32, 32, 2, zipf=1.1),
     "c3_eplb": Workload("c3_eplb", 4608, 7168, 256, 288, 8, 2048, 32, 32, 3, zipf=1.2, eplb=True),
-    "c4_prefill": Workload("c4_prefill", 16384, 7168, 256, 256, 8, 2048, 32, 32, 4),
+    "c4_prefill": Workload("c4_prefill", 16384, 7168, 256, 256, 8, 2048, 32, 32, 4, msg_formats=True),
     # profiling case: the DeepSeek-V3 expert shape with 32 experts (1.4 GB of
     # weights, about 3.5 GB on the device in total) and 1024 rows per expert
     "prof_e32": Workload("prof_e32", 4096, 7168, 32, 32, 8, 2048, 32, 32, 5),
