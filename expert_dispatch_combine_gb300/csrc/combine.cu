@@ -22,26 +22,28 @@ namespace moe {
 namespace {
 
 constexpr int kCombineThreads = 128;
-constexpr int kMaxK = 32;
 
 // One block per token.  Each thread owns 16 consecutive hidden elements at a
 // time and loads them from the first kUnroll messages before any arithmetic
 // (k 16-byte or 32-byte loads in flight per thread); messages beyond
 // kUnroll follow one at a time.  Accumulation is in ascending route slot.
 template <bool kInt8>
-__global__ void __launch_bounds__(kCombineThreads)
+__global__ void __launch_bounds__(kCombineThreads, kInt8 ? 6 : 4)
 combine_kernel(int H, int k, long long crow, const unsigned char* __restrict__ cbuf,
                const float* __restrict__ cscale, const float* __restrict__ topk_w,
                uint16_t* __restrict__ out) {
     constexpr int kUnroll = 8;
-    __shared__ float s_w[kMaxK], s_s[kMaxK];
     const int t = blockIdx.x;
     const long long tk = (long long)t * k;
-    if (threadIdx.x < k) {
-        s_w[threadIdx.x] = topk_w[tk + threadIdx.x];
-        s_s[threadIdx.x] = kInt8 ? cscale[tk + threadIdx.x] : 0.f;
+    // every thread reads the first kUnroll gate weights and message scales
+    // itself (the same words for the whole block, served by L1): no barrier
+    // holds the message loads back behind them
+    float w_r[kUnroll], s_r[kUnroll];
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+        w_r[j] = j < k ? __ldg(topk_w + tk + j) : 0.f;
+        s_r[j] = (kInt8 && j < k) ? __ldg(cscale + tk + j) : 0.f;
     }
-    __syncthreads();
     const int nch = H / 16;
     const unsigned char* rows = cbuf + tk * crow;
     uint4* orow = reinterpret_cast<uint4*>(out + (long long)t * H);
@@ -55,11 +57,11 @@ combine_kernel(int H, int k, long long crow, const unsigned char* __restrict__ c
         for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll
         for (int j = 0; j < kUnroll; ++j)
-            if (j < k) accumulate16<kInt8>(q[j], s_w[j], s_s[j], acc);
+            if (j < k) accumulate16<kInt8>(q[j], w_r[j], s_r[j], acc);
         for (int j = kUnroll; j < k; ++j) {
             uint4 r[2];
             load16<kInt8>(rows + j * crow, c, r);
-            accumulate16<kInt8>(r, s_w[j], s_s[j], acc);
+            accumulate16<kInt8>(r, __ldg(topk_w + tk + j), kInt8 ? __ldg(cscale + tk + j) : 0.f, acc);
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {

@@ -169,6 +169,8 @@ __device__ __forceinline__ unsigned quant4(float a, float b, float c, float d, f
 }
 
 constexpr int kScatterThreads = 128;
+constexpr int kLoadUnroll = 8;
+constexpr int kMaxRoutes = 32;  // k <= 32 (checked by every entry point)
 
 // Dispatch modes of the scatter kernel:
 //   kDirect: quantise token t and write its k messages into the owners'
@@ -195,6 +197,7 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
     uint2* scode = reinterpret_cast<uint2*>(sm + 2 * (size_t)H);  // H codes
     __shared__ float s_red[kScatterThreads / 32];
     __shared__ float s_scale;
+    __shared__ long long s_slot[kMaxRoutes];  // kDirect: message slot of each route
 
     const int t = blockIdx.x;
     const int src = t / lb, bs = t - src * lb;
@@ -234,20 +237,44 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
         if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
         return;
     }
+    // kDirect: the route threads look up their message slots and expert row
+    // positions now, so that these dependent loads overlap the row's loads
+    // instead of following the quantisation
+    long long my_slot = 0;
+    int my_erow = 0;
+    if (MODE == kDirect && threadIdx.x >= 32 && threadIdx.x < 32 + k) {
+        const int j = threadIdx.x - 32;
+        const int p = phys_idx[tk + j];
+        my_slot = ((long long)(p / epr) * S + src) * mt + slot_local[tk + j];
+        my_erow = expert_offsets[p] + src_base[(long long)src * E_phys + p] + erank[tk + j];
+        s_slot[j] = my_slot;
+    }
     const uint4* xr = reinterpret_cast<const uint4*>(x + (long long)t * H);
     float amax = 0.f;
-    for (int c = threadIdx.x; c < nch; c += kScatterThreads) {
-        uint4 v = __ldg(xr + c);
-        srow[c] = v;
-        if (int8_msgs) {
-            amax = fmaxf(amax, fabsf(bf16_lo(v.x)));
-            amax = fmaxf(amax, fabsf(bf16_hi(v.x)));
-            amax = fmaxf(amax, fabsf(bf16_lo(v.y)));
-            amax = fmaxf(amax, fabsf(bf16_hi(v.y)));
-            amax = fmaxf(amax, fabsf(bf16_lo(v.z)));
-            amax = fmaxf(amax, fabsf(bf16_hi(v.z)));
-            amax = fmaxf(amax, fabsf(bf16_lo(v.w)));
-            amax = fmaxf(amax, fabsf(bf16_hi(v.w)));
+    // up to kLoadUnroll 16-byte loads of the row in flight per thread
+    for (int c0 = threadIdx.x; c0 < nch; c0 += kLoadUnroll * kScatterThreads) {
+        uint4 v[kLoadUnroll];
+#pragma unroll
+        for (int u = 0; u < kLoadUnroll; ++u) {
+            const int c = c0 + u * kScatterThreads;
+            if (c < nch) v[u] = __ldg(xr + c);
+        }
+#pragma unroll
+        for (int u = 0; u < kLoadUnroll; ++u) {
+            const int c = c0 + u * kScatterThreads;
+            if (c < nch) {
+                srow[c] = v[u];
+                if (int8_msgs) {
+                    amax = fmaxf(amax, fabsf(bf16_lo(v[u].x)));
+                    amax = fmaxf(amax, fabsf(bf16_hi(v[u].x)));
+                    amax = fmaxf(amax, fabsf(bf16_lo(v[u].y)));
+                    amax = fmaxf(amax, fabsf(bf16_hi(v[u].y)));
+                    amax = fmaxf(amax, fabsf(bf16_lo(v[u].z)));
+                    amax = fmaxf(amax, fabsf(bf16_hi(v[u].z)));
+                    amax = fmaxf(amax, fabsf(bf16_lo(v[u].w)));
+                    amax = fmaxf(amax, fabsf(bf16_hi(v[u].w)));
+                }
+            }
         }
     }
     const unsigned char* src_row = sm;
@@ -298,27 +325,17 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
         return;
     }
     if (threadIdx.x == 0) {
-        for (int j = 0; j < k; ++j) {
-            int p = phys_idx[tk + j];
-            int dst = p / epr;
-            long long g = ((long long)dst * S + src) * mt + slot_local[tk + j];
-            bulk_store_s2g(dbuf + g * drow, src_row, (unsigned)drow);
-        }
+        for (int j = 0; j < k; ++j) bulk_store_s2g(dbuf + s_slot[j] * drow, src_row, (unsigned)drow);
         asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
     }
     if (threadIdx.x >= 32 && threadIdx.x < 32 + k) {
-        int j = threadIdx.x - 32;
-        int p = phys_idx[tk + j];
-        int dst = p / epr;
-        long long g = ((long long)dst * S + src) * mt + slot_local[tk + j];
         moe_dispatch_meta m;
         m.scale = scale;
         m.src_rank = src;
         m.batch_slot = bs;
-        m.route_slot = j;
-        meta[g] = m;
-        expert_rows[expert_offsets[p] + src_base[(long long)src * E_phys + p] + erank[tk + j]] =
-            (int32_t)g;
+        m.route_slot = threadIdx.x - 32;
+        meta[my_slot] = m;
+        expert_rows[my_erow] = (int32_t)my_slot;
     }
     if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
 }

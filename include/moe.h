@@ -252,8 +252,10 @@ moe_status moe_expert_ffn(const moe_shape* shape, const void* dispatch_buf,
 
 /* FusedCombine ([C] fused_moe listing; [X] COMBINE procedure):
  *   out[t][h] = bf16_rne( sum_{j=0..k-1} topk_w[t][j] * v[t][j][h] )
- * with v = code * scale (INT8, one binary32 product) or the bf16 value, the
- * sum taken in binary32 in ascending j (product and sum rounded separately).
+ * with v = code * scale (INT8) or the bf16 value, the sum taken in binary32
+ * in ascending j: for INT8 each term adds RN(topk_w * scale) * code by one
+ * fused multiply-add; for bf16 the product and the sum are rounded
+ * separately.
  *   topk_w (device) f32 [T][k]; out (device) bf16 [T][H].  No workspace. */
 moe_status moe_combine(const moe_shape* shape, const void* combine_buf, int64_t combine_bytes,
                        const float* topk_w, uint16_t* out, moe_stream_t stream);
