@@ -329,40 +329,6 @@ def run_ours(args, rank: int, world: int):
             t_ms += ta.elapsed_time(tb) / reps
         tramp_us = 1000 * t_ms
         del tbuf
-    formats = None
-    if w.msg_formats:
-        # FusedDispatch and FusedCombine alone, with bf16 (unquantised) and with
-        # INT8 + scale messages, on this step's routing
-        formats = {}
-        for fname, fmt in (("int8", B.MOE_MSG_INT8), ("bf16", B.MOE_MSG_BF16)):
-            fs = B.Shape(w.T, w.H, w.E_log, w.E_phys, w.k, w.I, w.R, w.S, fmt, fmt)
-            fb = b if fmt == B.MOE_MSG_INT8 else LayerBuffers(fs, dev)
-            if fmt == B.MOE_MSG_BF16:
-                # return messages: any bf16 values (the combine's time does not depend on them)
-                fb.combine_rows().view(torch.bfloat16).copy_(
-                    torch.randn((w.T, w.k, w.H), device=dev).to(torch.bfloat16))
-            d_ms = c_ms = 0.0
-            for _ in range(reps):
-                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-                torch.cuda._sleep(4_000_000)
-                e[0].record(stream)
-                B.moe_dispatch(fs, x, r["phys_idx"], fb.dispatch, fb.routing["rank_counts"],
-                               fb.routing["expert_offsets"], fb.routing["expert_rows"], fb.workspace)
-                e[1].record(stream)
-                B.moe_combine(fs, fb.combine, r["topk_w"], fb.out)
-                e[2].record(stream)
-                torch.cuda.synchronize()
-                d_ms += e[0].elapsed_time(e[1]) / reps
-                c_ms += e[1].elapsed_time(e[2]) / reps
-            db, cb = message_bytes(w, fmt == B.MOE_MSG_BF16)
-            hbm_gbs = _peaks()[0]["hbm_gbs"]
-            formats[fname] = {"dispatch_us": 1000 * d_ms, "combine_us": 1000 * c_ms,
-                              "dispatch_gbs": db / (d_ms / 1000) / 1e9,
-                              "combine_gbs": cb / (c_ms / 1000) / 1e9,
-                              "dispatch_combine_hbm_frac": (db + cb) / ((d_ms + c_ms) / 1000) / 1e9 / hbm_gbs}
-            if fb is not b:
-                del fb
-        torch.cuda.synchronize()
     alg = algorithmic(w)
     # gate|up kernel bytes: int8 gate/up rows of the weight sets this step touches, the
     # fp16 expert rows it reads and the f32 h it writes
@@ -388,8 +354,6 @@ def run_ours(args, rank: int, world: int):
     }
     if tramp_us is not None:
         stages["dispatch_trampoline_us"] = tramp_us
-    if formats is not None:
-        stages["standalone_messages"] = formats
     dc_bytes = alg["dispatch_bytes"] + alg["combine_bytes"]
     dc_s = (acc["dispatch"] + acc["combine"]) / 1000
     stages["dispatch_combine_hbm_frac"] = dc_bytes / dc_s / 1e9 / hbm
@@ -482,6 +446,43 @@ def run_ours(args, rank: int, world: int):
            "steps": e_steps,
            "pipelining": "two buffer sets: step i+1's inputs copied in and step i's output "
                          "copied out on a second stream while the next layer runs"}
+    formats = None
+    if w.msg_formats:
+        # FusedDispatch and FusedCombine alone, with bf16 (unquantised) and with
+        # INT8 + scale messages, on this step's routing
+        formats = {}
+        for fname, fmt in (("int8", B.MOE_MSG_INT8), ("bf16", B.MOE_MSG_BF16)):
+            fs = B.Shape(w.T, w.H, w.E_log, w.E_phys, w.k, w.I, w.R, w.S, fmt, fmt)
+            fb = b if fmt == B.MOE_MSG_INT8 else LayerBuffers(fs, dev)
+            if fmt == B.MOE_MSG_BF16:
+                # return messages: any bf16 values (the combine's time does not depend on them)
+                fb.combine_rows().view(torch.bfloat16).copy_(
+                    torch.randn((w.T, w.k, w.H), device=dev).to(torch.bfloat16))
+            d_ms = c_ms = 0.0
+            for _ in range(reps):
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                torch.cuda._sleep(4_000_000)
+                e[0].record(stream)
+                B.moe_dispatch(fs, x, r["phys_idx"], fb.dispatch, fb.routing["rank_counts"],
+                               fb.routing["expert_offsets"], fb.routing["expert_rows"], fb.workspace)
+                e[1].record(stream)
+                B.moe_combine(fs, fb.combine, r["topk_w"], fb.out)
+                e[2].record(stream)
+                torch.cuda.synchronize()
+                d_ms += e[0].elapsed_time(e[1]) / reps
+                c_ms += e[1].elapsed_time(e[2]) / reps
+            db, cb = message_bytes(w, fmt == B.MOE_MSG_BF16)
+            hbm_gbs = _peaks()[0]["hbm_gbs"]
+            formats[fname] = {"dispatch_us": 1000 * d_ms, "combine_us": 1000 * c_ms,
+                              "dispatch_gbs": db / (d_ms / 1000) / 1e9,
+                              "combine_gbs": cb / (c_ms / 1000) / 1e9,
+                              "dispatch_combine_hbm_frac": (db + cb) / ((d_ms + c_ms) / 1000) / 1e9 / hbm_gbs}
+            if fb is not b:
+                del fb
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    if formats is not None:
+        stages["standalone_messages"] = formats
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
