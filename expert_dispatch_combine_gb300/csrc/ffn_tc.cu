@@ -782,10 +782,8 @@ requant_kernel(int I, const float* __restrict__ h, const unsigned* __restrict__ 
 #pragma unroll
                     for (int e = 0; e < 4; ++e) q[e] = quant1_row(x[e], s, rs);
                 }
-                __half2 a = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[1]));
-                __half2 b = __halves2half2(__int2half_rn(q[2]), __int2half_rn(q[3]));
-                o[2 * i] = *reinterpret_cast<uint32_t*>(&a);
-                o[2 * i + 1] = *reinterpret_cast<uint32_t*>(&b);
+                o[2 * i] = codes_to_f16x2(q[0], q[1]);
+                o[2 * i + 1] = codes_to_f16x2(q[2], q[3]);
             }
             dst[2 * c] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
