@@ -92,6 +92,21 @@ def message_bytes(w: synth.Workload, bf16: bool) -> tuple[int, int]:
     return dispatch, combine
 
 
+def replica_aggregate(ms: float, units: int, world: int, device=None) -> tuple[float, float]:
+    """Whole-job figure of N independent replicas (one per rank, no
+    data-path collective): the slowest rank's time per step (max over ranks)
+    and the units all ranks processed per second.  The reduction runs in the
+    process group's backend on `device` (a CUDA device with NCCL, the CPU
+    with gloo)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * units / (ms / 1000.0)
+
+
 class ClockSampler:
     """nvidia-smi clocks/throttle sampling during the timed region."""
 
@@ -273,12 +288,7 @@ def run_ours(args, rank: int, world: int):
     launches = B.moe_launch_count() - n0
     clocks = sampler.stop(wall0, wall1)
     ms = ev0.elapsed_time(ev1) / args.steps
-    ms_all = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_all = float(t.item())
-    value = world * w.T / (ms_all / 1000.0)
+    ms_all, value = replica_aggregate(ms, w.T, world, dev)
 
     # ---- per-stage timing (same stream, CUDA events between the four calls)
     b = layer.buf
@@ -436,12 +446,8 @@ def run_ours(args, rank: int, world: int):
     e1.record(stream)
     torch.cuda.synchronize()
     del layers[1]
-    e_ms = e0.elapsed_time(e1) / e_steps
-    if world > 1:
-        t = torch.tensor([e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
-    e2e = {"value": world * w.T / (e_ms / 1000.0), "unit": UNIT,
+    e_ms, e_value = replica_aggregate(e0.elapsed_time(e1) / e_steps, w.T, world, dev)
+    e2e = {"value": e_value, "unit": UNIT,
            "h2d_bytes_per_step": lg_h.nbytes + x_h.nbytes, "d2h_bytes_per_step": w.T * w.H * 2,
            "steps": e_steps,
            "pipelining": "two buffer sets: step i+1's inputs copied in and step i's output "
