@@ -161,9 +161,7 @@ __device__ __forceinline__ void bulk_store_s2g(void* gdst, const void* ssrc, uns
 __device__ __forceinline__ float bf16_lo(unsigned w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(unsigned w) { return __uint_as_float(w & 0xffff0000u); }
 
-__device__ __forceinline__ unsigned quant4(float a, float b, float c, float d, float s, float rs) {
-    const int q0 = quant1_row(a, s, rs), q1 = quant1_row(b, s, rs);
-    const int q2 = quant1_row(c, s, rs), q3 = quant1_row(d, s, rs);
+__device__ __forceinline__ unsigned pack4(int q0, int q1, int q2, int q3) {
     return (unsigned)(q0 & 0xff) | ((unsigned)(q1 & 0xff) << 8) | ((unsigned)(q2 & 0xff) << 16) |
            ((unsigned)(q3 & 0xff) << 24);
 }
@@ -298,8 +296,12 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
             if (scale == 0.f) {
                 q.x = 0u; q.y = 0u;
             } else {
-                q.x = quant4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y), scale, rscale);
-                q.y = quant4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w), scale, rscale);
+                const float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                                    bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+                int c8[8];
+                quant_row_n<8>(x, scale, rscale, c8);
+                q.x = pack4(c8[0], c8[1], c8[2], c8[3]);
+                q.y = pack4(c8[4], c8[5], c8[6], c8[7]);
             }
             scode[c] = q;
         }

@@ -784,18 +784,19 @@ requant_kernel(int I, const float* __restrict__ h, const unsigned* __restrict__ 
         for (int u = 0; u < 2; ++u) {
             const int c = c0 + u * nt;
             if (c >= nch) break;
+            const float x[16] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y,
+                                 v[u][1].z, v[u][1].w, v[u][2].x, v[u][2].y, v[u][2].z, v[u][2].w,
+                                 v[u][3].x, v[u][3].y, v[u][3].z, v[u][3].w};
+            int q[16];
+            if (s != 0.f) {
+                quant_row_n<16>(x, s, rs, q);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) q[e] = 0;
+            }
             uint32_t o[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float x[4] = {v[u][i].x, v[u][i].y, v[u][i].z, v[u][i].w};
-                int q[4] = {0, 0, 0, 0};
-                if (s != 0.f) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) q[e] = quant1_row(x[e], s, rs);
-                }
-                o[2 * i] = codes_to_f16x2(q[0], q[1]);
-                o[2 * i + 1] = codes_to_f16x2(q[2], q[3]);
-            }
+            for (int i = 0; i < 8; ++i) o[i] = codes_to_f16x2(q[2 * i], q[2 * i + 1]);
             dst[2 * c] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
@@ -837,17 +838,21 @@ retquant_kernel(int H, int k, int lb, long long crow, const float* __restrict__ 
         for (int u = 0; u < 2; ++u) {
             const int c = c0 + u * nt;
             if (c >= nch) break;
+            const float x[16] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y,
+                                 v[u][1].z, v[u][1].w, v[u][2].x, v[u][2].y, v[u][2].z, v[u][2].w,
+                                 v[u][3].x, v[u][3].y, v[u][3].z, v[u][3].w};
+            int q[16];
+            if (s != 0.f) {
+                quant_row_n<16>(x, s, rs, q);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) q[e] = 0;
+            }
             uint32_t w[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float x[4] = {v[u][i].x, v[u][i].y, v[u][i].z, v[u][i].w};
-                uint32_t word = 0;
-                if (s != 0.f) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) word |= (uint32_t)(quant1_row(x[e], s, rs) & 0xff) << (8 * e);
-                }
-                w[i] = word;
-            }
+            for (int i = 0; i < 4; ++i)
+                w[i] = (uint32_t)(q[4 * i] & 0xff) | ((uint32_t)(q[4 * i + 1] & 0xff) << 8) |
+                       ((uint32_t)(q[4 * i + 2] & 0xff) << 16) | ((uint32_t)(q[4 * i + 3] & 0xff) << 24);
             dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }

@@ -3,7 +3,8 @@
 //   - the expert-FFN SiLU, straightforward form (silu_spec, IEEE division)
 //     against the branch-free form (silu_fast) of the gate/up GEMM epilogue;
 //   - token-wise INT8 codes, IEEE-division form (quant1) against the
-//     reciprocal form (quant1_row) of the dispatch and requantisation kernels.
+//     reciprocal form (quant1_row) and its 16-value group form (quant_row_n)
+//     of the dispatch and requantisation kernels.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -75,7 +76,71 @@ __global__ void compare_quant(unsigned long long n, unsigned long long* mismatch
     atomicAdd(near_half, nh);
 }
 
+// n random rows of 16 values (absmax a as above, each value next to a
+// half-integer quotient with probability 1/8, else uniform in [-a, a]):
+// quant_row_n<16> of the row against quant1 of each value.  Counts the rows
+// holding a value drawn next to a half-integer quotient.
+__global__ void compare_quant_rows(unsigned long long n, unsigned long long* mismatches,
+                                   unsigned long long* slow_rows, unsigned* first_bad) {
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    unsigned long long bad = 0, ns = 0;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const uint32_t h1 = mix32((uint32_t)i * 2u + 0x51ed27u);
+        const int ex = (int)(h1 >> 23) % 250 - 125;
+        const float a = ldexpf(1.0f + (float)(h1 & 0x7fffffu) * 0x1p-23f, ex);
+        const float s = moe::row_scale(a);
+        if (s == 0.f) continue;
+        const float rs = moe::quant_rcp(s);
+        float v[16];
+        bool near_any = false;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const uint32_t h2 = mix32(h1 ^ (uint32_t)(i >> 32) ^ (0x9e3779b9u * (uint32_t)(e + 1)));
+            float x;
+            if ((h2 & 7u) == 0u) {
+                const int c = (int)((h2 >> 3) % 254u) - 127;
+                x = __fmul_rn((float)c + 0.5f, s);
+                const int d = (int)((h2 >> 11) % 9u) - 4;
+                x = __int_as_float(__float_as_int(x) + d);
+                near_any = true;
+            } else {
+                x = __fmul_rn(a, (float)(h2 >> 1) * 0x1p-30f - 1.0f);
+            }
+            v[e] = fabsf(x) <= a ? x : 0.0f;
+        }
+        int q[16];
+        moe::quant_row_n<16>(v, s, rs, q);
+        bool row_bad = false;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) row_bad |= q[e] != moe::quant1(v[e], s);
+        if (row_bad) {
+            ++bad;
+            atomicMin(first_bad, (unsigned)i);
+        }
+        ns += near_any;
+    }
+    if (bad) atomicAdd(mismatches, bad);
+    atomicAdd(slow_rows, ns);
+}
+
 }  // namespace
+
+// Rows (of n random 16-value rows) whose quant_row_n<16> codes differ from
+// quant1's, and how many rows held a value drawn next to a half-integer.
+extern "C" int quant_rows_check(unsigned long long n, unsigned long long* mismatches,
+                                unsigned long long* near_rows, unsigned* first_bad) {
+    unsigned long long* d = nullptr;
+    if (cudaMalloc(&d, 3 * sizeof(unsigned long long)) != cudaSuccess) return 1;
+    cudaMemset(d, 0, 2 * sizeof(unsigned long long));
+    cudaMemset(d + 2, 0xff, sizeof(unsigned long long));
+    compare_quant_rows<<<152 * 8, 256>>>(n, d, d + 1, reinterpret_cast<unsigned*>(d + 2));
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaMemcpy(mismatches, d, sizeof(*d), cudaMemcpyDeviceToHost);
+    cudaMemcpy(near_rows, d + 1, sizeof(*d), cudaMemcpyDeviceToHost);
+    cudaMemcpy(first_bad, d + 2, sizeof(unsigned), cudaMemcpyDeviceToHost);
+    cudaFree(d);
+    return e == cudaSuccess ? 0 : 2;
+}
 
 // Mismatching codes among n random (absmax, value) pairs, and how many of the
 // pairs were drawn next to a half-integer quotient.

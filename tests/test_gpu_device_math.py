@@ -5,7 +5,8 @@
   exp behind them, against the oracle on a strided sample plus special values;
 - the reciprocal form of the token-wise INT8 code against the IEEE-division
   form on 2^30 random (row absmax, value) pairs, half of them next to a
-  half-integer quotient."""
+  half-integer quotient, and the 16-value group form of the row kernels on
+  2^26 rows."""
 import ctypes
 import os
 import subprocess
@@ -36,6 +37,7 @@ def helper():
     lib.silu_eval.argtypes = [P, P, P, P, ctypes.c_int]
     U64P = ctypes.POINTER(ctypes.c_ulonglong)
     lib.quant_check.argtypes = [ctypes.c_ulonglong, U64P, U64P, ctypes.POINTER(ctypes.c_uint)]
+    lib.quant_rows_check.argtypes = [ctypes.c_ulonglong, U64P, U64P, ctypes.POINTER(ctypes.c_uint)]
     return lib
 
 
@@ -77,3 +79,16 @@ def test_reciprocal_quantisation_equals_division_form(helper):
     assert helper.quant_check(n, ctypes.byref(m), ctypes.byref(nh), ctypes.byref(first)) == 0
     assert nh.value > n // 4  # the near-half-integer draws happened
     assert m.value == 0, f"{m.value} mismatches, first at draw {first.value}"
+
+
+def test_group_quantisation_equals_division_form(helper):
+    """The 16-value group form of the row kernels (the correctly rounded
+    quotient from the reciprocal by Markstein's correction, no division and no
+    branch per value) on 2^26 rows of 16 values, most of them holding a value
+    next to a half-integer quotient."""
+    n = 1 << 26
+    m, nr = ctypes.c_ulonglong(0), ctypes.c_ulonglong(0)
+    first = ctypes.c_uint(0)
+    assert helper.quant_rows_check(n, ctypes.byref(m), ctypes.byref(nr), ctypes.byref(first)) == 0
+    assert nr.value > n // 2  # most rows hold a value next to a half-integer quotient
+    assert m.value == 0, f"{m.value} rows differ, first at row {first.value}"
