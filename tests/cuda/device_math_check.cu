@@ -3,8 +3,8 @@
 //   - the expert-FFN SiLU, straightforward form (silu_spec, IEEE division)
 //     against the branch-free form (silu_fast) of the gate/up GEMM epilogue;
 //   - token-wise INT8 codes, IEEE-division form (quant1) against the
-//     reciprocal form (quant1_row) and its 16-value group form (quant_row_n)
-//     of the dispatch and requantisation kernels.
+//     reciprocal form with Markstein's correction (quant_row_n, one value and
+//     groups of 16) of the dispatch and requantisation kernels.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -67,7 +67,10 @@ __global__ void compare_quant(unsigned long long n, unsigned long long* mismatch
             v = __fmul_rn(a, (float)(h2 >> 1) * 0x1p-30f - 1.0f);
         }
         if (!(fabsf(v) <= a)) continue;
-        if (moe::quant1_row(v, s, rs) != moe::quant1(v, s)) {
+        const float v1[1] = {v};
+        int q1[1];
+        moe::quant_row_n<1>(v1, s, rs, q1);
+        if (q1[0] != moe::quant1(v, s)) {
             ++bad;
             atomicMin(first_bad, (unsigned)i);
         }

@@ -3,10 +3,10 @@
 - the SiLU of the gate/up GEMM epilogue (branch-free, FMA-based division)
   against the IEEE-division form on every binary32 input, and both, with the
   exp behind them, against the oracle on a strided sample plus special values;
-- the reciprocal form of the token-wise INT8 code against the IEEE-division
+- the token-wise INT8 code of the dispatch and row kernels (the quotient
+  from the reciprocal by Markstein's correction) against the IEEE-division
   form on 2^30 random (row absmax, value) pairs, half of them next to a
-  half-integer quotient, and the 16-value group form of the row kernels on
-  2^26 rows."""
+  half-integer quotient, and in groups of 16 on 2^26 rows."""
 import ctypes
 import os
 import subprocess
