@@ -717,15 +717,28 @@ assemble_kernel(int K, const int32_t* __restrict__ row_index, const int8_t* __re
     const long long g = row_index ? row_index[r] : r;
     const uint4* src = reinterpret_cast<const uint4*>(A + g * lda);
     uint4* dst = reinterpret_cast<uint4*>(out + (long long)r * K);
-    for (int c = threadIdx.x; c < K / 16; c += blockDim.x) {
-        const uint4 w = __ldg(src + c);
-        uint4 o0, o1;
-        s8x4_to_f16x4(w.x, o0.x, o0.y);
-        s8x4_to_f16x4(w.y, o0.z, o0.w);
-        s8x4_to_f16x4(w.z, o1.x, o1.y);
-        s8x4_to_f16x4(w.w, o1.z, o1.w);
-        dst[2 * c] = o0;
-        dst[2 * c + 1] = o1;
+    const int nch = K / 16;
+    // four 16-byte loads of the row in flight per thread before converting
+    for (int c0 = threadIdx.x; c0 < nch; c0 += 4 * blockDim.x) {
+        uint4 w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * blockDim.x;
+            if (c < nch) w[u] = __ldg(src + c);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * blockDim.x;
+            if (c < nch) {
+                uint4 o0, o1;
+                s8x4_to_f16x4(w[u].x, o0.x, o0.y);
+                s8x4_to_f16x4(w[u].y, o0.z, o0.w);
+                s8x4_to_f16x4(w[u].z, o1.x, o1.y);
+                s8x4_to_f16x4(w[u].w, o1.z, o1.w);
+                dst[2 * c] = o0;
+                dst[2 * c + 1] = o1;
+            }
+        }
     }
     if (meta && threadIdx.x == 0) s_row[r] = meta[g].scale;
 }
