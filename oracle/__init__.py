@@ -15,7 +15,10 @@ the pins):
   quantize       hand-worked vectors (tests/golden/quant_vectors.txt)
   exp_spec/silu  math.exp within 2 ulp; exact special values
   dispatch       naive re-derivation on tiny inputs + invariants
-  expert_row     int32 accumulators vs numpy int64 matmul; one-hot weights
+  expert_row     int32 accumulators vs numpy int64 matmul; one-hot weights;
+                 the binary32 scale steps g, u, y by a hand-worked row with
+                 distinct power-of-two scales (tests/golden/expert_scale_steps.txt)
+                 and a float64 closed form on random distinct scales
   combine        identity experts reproduce the dequantised input
   buffer formula the page's worked example (225 MiB + 420 MiB)
   eplb           the page's [4, 256] rotation example; replica counts differ
@@ -52,44 +55,54 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def load_library(path: str):
+    """Load a compiled copy of moe_oracle.c and declare its functions (the
+    tests also load copies with planted mistakes through this)."""
+    lib = ctypes.CDLL(path)
+    _declare(lib)
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
-        P = ctypes.c_void_p
-        i32, i64, f32, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double
-        lib.orc_exp_spec.argtypes = [f32]
-        lib.orc_exp_spec.restype = f32
-        lib.orc_silu.argtypes = [f32]
-        lib.orc_silu.restype = f32
-        lib.orc_round_f64_to_bf16.argtypes = [f64]
-        lib.orc_round_f64_to_bf16.restype = ctypes.c_uint16
-        lib.orc_round_f32_to_bf16.argtypes = [f32]
-        lib.orc_round_f32_to_bf16.restype = ctypes.c_uint16
-        lib.orc_quantize_row_f32.argtypes = [i32, P, P, P]
-        lib.orc_quantize_row_f32.restype = None
-        lib.orc_quantize_rows_bf16.argtypes = [i32, i32, P, P, P]
-        lib.orc_quantize_rows_bf16.restype = None
-        lib.orc_route.argtypes = [i32, i32, i32, i32, P, P, P, i32, P, P, P, P]
-        lib.orc_route.restype = i32
-        lib.orc_static_buffer_bytes.argtypes = [i64, i64, i64, i64, i64]
-        lib.orc_static_buffer_bytes.restype = i64
-        lib.orc_dispatch.argtypes = [i32] * 7 + [P] * 11
-        lib.orc_dispatch.restype = i32
-        lib.orc_expert_row.argtypes = [i32, i32, P, f32, P, P, P, P, i32, P, P,
-                                       P, P, P, P, P]
-        lib.orc_expert_row.restype = i32
-        lib.orc_ffn_all.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P,
-                                    i32, P, P]
-        lib.orc_ffn_all.restype = i32
-        lib.orc_combine.argtypes = [i32, i32, i32, i32, P, P, P, P]
-        lib.orc_combine.restype = i32
-        lib.orc_num_threads.argtypes = []
-        lib.orc_num_threads.restype = i32
-        _lib = lib
-        return lib
+        _lib = load_library(build())
+        return _lib
+
+
+def _declare(lib):
+    P = ctypes.c_void_p
+    i32, i64, f32, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double
+    lib.orc_exp_spec.argtypes = [f32]
+    lib.orc_exp_spec.restype = f32
+    lib.orc_silu.argtypes = [f32]
+    lib.orc_silu.restype = f32
+    lib.orc_round_f64_to_bf16.argtypes = [f64]
+    lib.orc_round_f64_to_bf16.restype = ctypes.c_uint16
+    lib.orc_round_f32_to_bf16.argtypes = [f32]
+    lib.orc_round_f32_to_bf16.restype = ctypes.c_uint16
+    lib.orc_quantize_row_f32.argtypes = [i32, P, P, P]
+    lib.orc_quantize_row_f32.restype = None
+    lib.orc_quantize_rows_bf16.argtypes = [i32, i32, P, P, P]
+    lib.orc_quantize_rows_bf16.restype = None
+    lib.orc_route.argtypes = [i32, i32, i32, i32, P, P, P, i32, P, P, P, P]
+    lib.orc_route.restype = i32
+    lib.orc_static_buffer_bytes.argtypes = [i64, i64, i64, i64, i64]
+    lib.orc_static_buffer_bytes.restype = i64
+    lib.orc_dispatch.argtypes = [i32] * 7 + [P] * 11
+    lib.orc_dispatch.restype = i32
+    lib.orc_expert_row.argtypes = [i32, i32, P, f32, P, P, P, P, i32, P, P,
+                                   P, P, P, P, P]
+    lib.orc_expert_row.restype = i32
+    lib.orc_ffn_all.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P,
+                                i32, P, P]
+    lib.orc_ffn_all.restype = i32
+    lib.orc_combine.argtypes = [i32, i32, i32, i32, P, P, P, P]
+    lib.orc_combine.restype = i32
+    lib.orc_num_threads.argtypes = []
+    lib.orc_num_threads.restype = i32
 
 
 def _p(a):
@@ -201,8 +214,9 @@ def dispatch(x_bits: np.ndarray, phys_idx: np.ndarray, E_phys: int, R: int, S: i
 
 # ------------------------------------------------------------- expert FFN
 def expert_row(xq: np.ndarray, xs: float, w_gu: np.ndarray, s_gu: np.ndarray,
-               w_d: np.ndarray, s_d: np.ndarray, cfmt: int = 1, debug: bool = False):
-    """One routed row through one expert.  Returns (message, scale[, debug dict])."""
+               w_d: np.ndarray, s_d: np.ndarray, cfmt: int = 1, debug: bool = False, lib=None):
+    """One routed row through one expert.  Returns (message, scale[, debug dict]).
+    `lib` (optional) is another compiled copy of the oracle (load_library)."""
     H = xq.shape[0]
     I = w_d.shape[1]
     xq = np.ascontiguousarray(xq, dtype=np.int8)
@@ -218,7 +232,7 @@ def expert_row(xq: np.ndarray, xs: float, w_gu: np.ndarray, s_gu: np.ndarray,
                    sh=np.zeros(1, np.float32), acc_d=np.empty(H, np.int32),
                    y=np.empty(H, np.float32))
     g = (lambda n: _p(dbg[n]) if dbg else None)
-    _load().orc_expert_row(H, I, _p(xq), float(xs), _p(w_gu), _p(s_gu), _p(w_d),
+    (lib or _load()).orc_expert_row(H, I, _p(xq), float(xs), _p(w_gu), _p(s_gu), _p(w_d),
                            _p(s_d), cfmt, _p(msg), _p(sc), g("acc_gu"), g("hq"),
                            g("sh"), g("acc_d"), g("y"))
     if debug:
