@@ -35,6 +35,7 @@ from expert_dispatch_combine_gb300 import synth  # noqa: E402
 DEFAULT_WORKLOAD = "c2_decode_zipf"
 METRIC = "routed tokens/s per MoE layer on 1 GB300; dispatch/combine us and % HBM roofline"
 UNIT = "tokens/s"
+L2_BYTES = 129 * 1024 * 1024
 
 
 def _peaks():
@@ -158,53 +159,29 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle
-def oracle_sample(w: synth.Workload, target_s: float, min_tokens: int = 16):
-    """Time the CPU oracle on the first n tokens of the workload, n chosen so
-    that one pass takes about target_s.  Returns (tokens/s, n, seconds, cores)."""
-    _, n, dt, _ = oracle_sample_fixed(w, min_tokens)
-    n2 = int(max(min_tokens, min(w.T, target_s * n / max(dt, 1e-9))))
-    if n2 > n:
-        _ORC_CACHE.clear()
-        _, n, dt, _ = oracle_sample_fixed(w, n2)
-    import oracle
-    return n / dt, n, dt, oracle.num_threads()
-
-
-def run_reference(args, rank: int, world: int):
-    if rank != 0:
-        return
-    w = synth.WORKLOADS[args.workload]
-    # calibrate one sample size, then time warmup + steps samples
-    tps, n, dt, cores = oracle_sample(w, target_s=args.ref_sample_s)
-    times = []
-    for i in range(args.warmup + args.steps):
-        v, n_i, dt_i, _ = oracle_sample_fixed(w, n)
-        if i >= args.warmup:
-            times.append(dt_i)
-    total = sum(times)
-    value = args.steps * n / total
-    line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8/f32",
-        "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "H": w.H, "E_log": w.E_log, "E_phys": w.E_phys,
-                   "k": w.k, "I": w.I, "ranks": w.R},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"first {n} of {w.T} tokens per step through the whole oracle layer"},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line))
+def config_of(w: synth.Workload, world: int, weight_bytes: int | None = None) -> dict:
+    """The `config` object of both arms' JSON lines (same keys, same values)."""
+    wb = weight_bytes if weight_bytes is not None else 3 * w.E_log * w.H * w.I
+    inputs = (f"{wb / 1e9:.3f} GB of int8 weights of the touched experts streamed every step and "
+              f"{2 * w.T * w.H / 1e6:.1f} MB of bf16 hidden rows")
+    l2 = ("inputs larger than L2 (129 MB): " if wb + 2 * w.T * w.H > L2_BYTES else
+          "inputs fit in L2 (129 MB), not flushed between steps: ") + inputs
+    return {"workload": w.name, "T": w.T, "H": w.H, "E_log": w.E_log, "E_phys": w.E_phys, "k": w.k,
+            "I": w.I, "ranks": w.R, "src_ranks": w.S, "messages": "int8 dispatch, int8 combine",
+            "l2": l2, "parallelism": f"replicas x{world}"}
 
 
 _ORC_CACHE = {}
 
 
-def oracle_sample_fixed(w, n):
+def _oracle_inputs(w: synth.Workload, n: int):
+    """The first n tokens of the workload (n a multiple of n_src_ranks) and the
+    expert weights they route to."""
     import oracle
 
     key = (w.name, n)
     if key not in _ORC_CACHE:
+        _ORC_CACHE.clear()
         lg = np.ascontiguousarray(synth.logits(w)[:n])
         x = np.random.default_rng([w.seed, 3]).standard_normal((w.T, w.H), dtype=np.float32)[:n]
         xb = synth.f32_to_bf16_bits(np.ascontiguousarray(x))
@@ -217,11 +194,105 @@ def oracle_sample_fixed(w, n):
         need = set(int(p2l[p]) if p2l is not None else int(p) for p in np.unique(pidx))
         weights = {e: synth.expert_weights_np(w, e) for e in need}
         _ORC_CACHE[key] = (lg, xb, weights, rep, nc, p2l)
-    lg, xb, weights, rep, nc, p2l = _ORC_CACHE[key]
+    return _ORC_CACHE[key]
+
+
+def oracle_run(w: synth.Workload, n: int) -> dict:
+    """One pass of the oracle's four stages over the first n tokens, with the
+    workload's source ranks (n_src_ranks = S): tokens/s and ms per stage."""
+    import oracle
+
+    lg, xb, weights, rep, nc, p2l = _oracle_inputs(w, n)
+    ms = {}
     t0 = time.perf_counter()
-    oracle.layer(lg, xb, weights, w.E_phys, w.R, 1, w.k, w.I, 1, rep, nc, p2l)
-    dt = time.perf_counter() - t0
-    return n / dt, n, dt, oracle.num_threads()
+    _, wt, pidx, _ = oracle.route(lg, w.k, w.E_phys, rep, nc)
+    t1 = time.perf_counter()
+    xq, xs = oracle.quantize_bf16(xb)
+    oracle.dispatch(xb, pidx, w.E_phys, w.R, w.S, fmt=1)
+    t2 = time.perf_counter()
+    cb, cs = oracle.ffn_all(xq, xs, pidx, weights, w.I, 1, p2l)
+    t3 = time.perf_counter()
+    oracle.combine(cb, cs, wt, 1)
+    t4 = time.perf_counter()
+    ms = {"route": 1e3 * (t1 - t0), "quantise_dispatch": 1e3 * (t2 - t1), "ffn": 1e3 * (t3 - t2),
+          "combine": 1e3 * (t4 - t3)}
+    return {"value": n / (t4 - t0), "tokens": n, "seconds": t4 - t0, "threads": oracle.num_threads(),
+            "stages_ms": ms}
+
+
+def oracle_tokens(w: synth.Workload, target_s: float) -> int:
+    """Tokens (a multiple of n_src_ranks) for one oracle pass of about target_s."""
+    n = w.S * max(1, 16 // w.S)
+    r = oracle_run(w, n)
+    n2 = int(target_s * n / max(r["seconds"], 1e-9)) // w.S * w.S
+    return int(min(w.T, max(n, n2)))
+
+
+def cpu_baseline(w: synth.Workload, target_s: float) -> dict:
+    """The oracle on the host: the workload sampled on all OpenMP threads,
+    plus one thread on the tiny layer and on a slice of the decode batch."""
+    import oracle
+
+    threads = oracle.num_threads()
+    n = oracle_tokens(w, target_s)
+    r = oracle_run(w, n)
+    single = {}
+    oracle.set_num_threads(1)
+    try:
+        for name, tokens in (("c0_tiny", None), ("c1_decode", 32)):
+            ws = synth.WORKLOADS[name]
+            nt = ws.T if tokens is None else tokens
+            o = oracle_run(ws, nt)
+            single[name] = {"value": o["value"], "unit": UNIT, "tokens": nt, "of": ws.T,
+                            "stages_ms": o["stages_ms"]}
+    finally:
+        oracle.set_num_threads(threads)
+    return {"value": r["value"], "unit": UNIT, "cores": r["threads"], "threads": r["threads"],
+            "host_cores": os.cpu_count(), "kind": "oracle",
+            "sample": (f"first {n} of {w.T} tokens ({w.S} source ranks) through the oracle's route, "
+                       f"quantise + dispatch, expert FFN and combine ({r['seconds']:.1f} s)"),
+            "stages_ms": r["stages_ms"], "single_thread": single}
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    import oracle
+
+    w = synth.WORKLOADS[args.workload]
+    # the experts the whole batch touches (the GPU arm's `config` counts the same)
+    rep = nc = p2l = None
+    if w.eplb:
+        _, _, _, cnt0 = oracle.route(synth.logits(w), w.k)
+        from oracle import eplb
+        rep, nc, p2l = eplb.plan(cnt0[None, :].astype(np.float64), w.E_phys, w.placement_ranks)
+    _, _, _, cnt = oracle.route(synth.logits(w), w.k, w.E_phys, rep, nc)
+    touched = np.nonzero(cnt)[0]
+    if p2l is not None:
+        touched = np.unique(p2l[touched])
+    n = oracle_tokens(w, args.ref_sample_s)
+    times, stages = [], {}
+    for i in range(args.warmup + args.steps):
+        r = oracle_run(w, n)
+        if i >= args.warmup:
+            times.append(r["seconds"])
+            for k_, v in r["stages_ms"].items():
+                stages[k_] = stages.get(k_, 0.0) + v / args.steps
+    total = sum(times)
+    value = args.steps * n / total
+    sample = f"first {n} of {w.T} tokens per step ({w.S} source ranks) through the whole oracle layer"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 (exact int64 accumulation), f32 epilogue", "data": "synthetic",
+        "config": config_of(w, world, len(touched) * 3 * w.H * w.I),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "threads": oracle.num_threads(), "host_cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample, "stages_ms": stages},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
 
 
 # ------------------------------------------------------------------- ours
@@ -298,6 +369,9 @@ def run_ours(args, rank: int, world: int):
     kern = {"gemm_gate_up": 0.0, "gemm_down": 0.0}
     reps = max(1, min(args.steps, 5))
     B.moe_profile_enable(True)
+    stage_sampler = ClockSampler(local)
+    time.sleep(0.3)
+    swall0 = time.time()
     for _ in range(reps):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         # keep the GPU busy for about 2 ms so that the host has enqueued all
@@ -322,6 +396,7 @@ def run_ours(args, rank: int, world: int):
         gu_ms, dn_ms = B.moe_profile_read()
         kern["gemm_gate_up"] += gu_ms / reps
         kern["gemm_down"] += dn_ms / reps
+    stage_clocks = stage_sampler.stop(swall0, time.time())
     B.moe_profile_enable(False)
     tramp_us = None
     if w.S < w.R:
@@ -369,7 +444,21 @@ def run_ours(args, rank: int, world: int):
     stages["dispatch_combine_hbm_frac"] = dc_bytes / dc_s / 1e9 / hbm
     ffn_tflops = alg["ffn_ops"] / (acc["ffn"] / 1000) / 1e12
     stages["ffn_tflops"] = ffn_tflops
-    peak_tc = peaks["bf16_tflops_sustained"]
+    # the tensor peak that applies: the burst figure while the SM clock held its
+    # maximum with no power cap during the stage timing (the kernels are timed in
+    # short runs), else the sustained figure under the power cap; both fractions
+    # are reported
+    burst, sustained = peaks["bf16_tflops"], peaks["bf16_tflops_sustained"]
+    at_max = (stage_clocks.get("sm_mhz") is not None and stage_clocks.get("sm_max_mhz")
+              and stage_clocks["sm_mhz"] >= 0.97 * stage_clocks["sm_max_mhz"])
+    capped = "sw_power_cap" in stage_clocks.get("reasons", [])
+    use_burst = bool(at_max) and not capped
+    peak_tc = burst if use_burst else sustained
+    peak_tc_name = ("burst (SM clock at its maximum, no power cap during the stage timing)" if use_burst
+                    else "sustained (SM clock below its maximum or power-capped during the stage timing)")
+    stages["ffn_frac_burst"] = ffn_tflops / burst
+    stages["ffn_frac_sustained"] = ffn_tflops / sustained
+    stages["clocks"] = stage_clocks
     gu_name = ("gemv_kernel<gate|up> (int8 dp4a weight streaming)" if ffn_path == B.MOE_FFN_GEMV
                else "gemm_tc_kernel<gate|up> (exact int8 on tcgen05 kind::f16)")
     if kern["gemm_gate_up"] > 0:
@@ -387,7 +476,9 @@ def run_ours(args, rank: int, world: int):
                         "kernel": gu_name,
                         "algorithmic_ops_per_launch": alg["gate_up_ops"],
                         "algorithmic_bytes_per_launch": alg["gate_up_bytes"],
-                        "peak_source": f"{peak_kind} bf16 sustained (exact int8 runs on the fp16 tensor path)"}
+                        "frac_burst": gu_tflops / burst, "frac_sustained": gu_tflops / sustained,
+                        "peak_source": (f"{peak_kind} bf16 {peak_tc_name}; exact int8 runs on the "
+                                        "fp16 tensor path")}
         else:  # decode-sized batches stream the weights: HBM-bound
             gu_gbs = alg["gate_up_bytes"] / (kern["gemm_gate_up"] / 1000) / 1e9
             roofline = {"bound": "hbm", "achieved": gu_gbs, "peak": hbm, "unit": "GB/s",
@@ -400,58 +491,45 @@ def run_ours(args, rank: int, world: int):
         roofline = {"bound": "alu", "achieved": ffn_tflops, "peak": None, "unit": "TFLOP/s",
                     "frac": None, "traffic": None, "kernel": "moe_expert_ffn (dp4a path)"}
 
-    # ---- end to end through the public API with host buffers.  A serving loop
-    # double-buffers: while step i runs on the compute stream, the copy stream
-    # moves step i+1's inputs in and step i-1's output out, so each step has
-    # its own layer buffers (two MoELayer objects over the same weights).
-    lg_pin = torch.from_numpy(lg_h).pin_memory()
-    x_pin = torch.from_numpy(x_h.view(np.int16)).pin_memory()
-    out_pin = torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()
+    # ---- end to end through the C ABI with host buffers (moe_layer_host): every
+    # step copies its inputs in from page-locked host memory, runs the layer and
+    # copies the output back, all enqueued by the library.  A serving loop
+    # alternates two streams and two buffer sets, so one step's copies overlap
+    # the other step's kernels.
+    h_lg = torch.from_numpy(lg_h).pin_memory()
+    h_x = torch.from_numpy(x_h.view(np.int16)).pin_memory()
+    h_out = [torch.empty((w.T, w.H), dtype=torch.int16).pin_memory() for _ in range(2)]
     layers = [layer, MoELayer(shape, w_gu, s_gu, w_d, s_d, rep_table=rep, n_copies=nc,
                               phys_to_weight=p2l, device=dev)]
-    lg_d = [torch.empty_like(logits) for _ in range(2)]
-    x_d = [torch.empty((w.T, w.H), dtype=torch.int16, device=dev) for _ in range(2)]
-    cstream = torch.cuda.Stream(device=dev)
-    e_steps = max(2, min(args.steps, 6))
-    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of the set copied in
-    ev_done = [torch.cuda.Event() for _ in range(2)]  # layer of the set finished
-    ev_out = [torch.cuda.Event() for _ in range(2)]   # output of the set copied out
+    streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    for i in range(2):  # warm-up of both sets
+        layers[i].forward_host(h_lg, h_x, h_out[i], stream=streams[i])
     torch.cuda.synchronize()
     barrier()
+    e_steps = max(2, args.steps)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    cstream.wait_event(e0)
-    with torch.cuda.stream(cstream):
-        lg_d[0].copy_(lg_pin, non_blocking=True)
-        x_d[0].copy_(x_pin, non_blocking=True)
-        ev_in[0].record(cstream)
+    for st_ in streams:
+        st_.wait_event(e0)
     for i in range(e_steps):
-        s_, n_ = i % 2, (i + 1) % 2
-        stream.wait_event(ev_in[s_])
-        if i >= 2:
-            stream.wait_event(ev_out[s_])  # this set's previous output has been read back
-        out = layers[s_].forward(lg_d[s_], x_d[s_].view(torch.bfloat16), stream=stream)
-        ev_done[s_].record(stream)
-        with torch.cuda.stream(cstream):
-            if i + 1 < e_steps:
-                if i >= 1:
-                    cstream.wait_event(ev_done[n_])  # step i-1 has consumed that set's inputs
-                lg_d[n_].copy_(lg_pin, non_blocking=True)
-                x_d[n_].copy_(x_pin, non_blocking=True)
-                ev_in[n_].record(cstream)
-            cstream.wait_event(ev_done[s_])
-            out_pin.copy_(out.view(torch.int16), non_blocking=True)
-            ev_out[s_].record(cstream)
-    stream.wait_stream(cstream)
+        layers[i % 2].forward_host(h_lg, h_x, h_out[i % 2], stream=streams[i % 2])
+    for st_ in streams:
+        done = torch.cuda.Event()
+        done.record(st_)
+        stream.wait_event(done)
     e1.record(stream)
     torch.cuda.synchronize()
+    # the host copies hold the layer's output (same inputs every step)
+    ref_bits = layer.buf.out.view(torch.int16).cpu()
+    e2e_checked = bool(torch.equal(h_out[0], ref_bits) and torch.equal(h_out[1], ref_bits))
     del layers[1]
     e_ms, e_value = replica_aggregate(e0.elapsed_time(e1) / e_steps, w.T, world, dev)
     e2e = {"value": e_value, "unit": UNIT,
            "h2d_bytes_per_step": lg_h.nbytes + x_h.nbytes, "d2h_bytes_per_step": w.T * w.H * 2,
-           "steps": e_steps,
-           "pipelining": "two buffer sets: step i+1's inputs copied in and step i's output "
-                         "copied out on a second stream while the next layer runs"}
+           "steps": e_steps, "api": "moe_layer_host (C ABI, host buffers)",
+           "output_checked": e2e_checked,
+           "pipelining": "two streams and two buffer sets: one step's copies overlap the "
+                         "other step's kernels"}
     formats = None
     if w.msg_formats:
         # FusedDispatch and FusedCombine alone, with bf16 (unquantised) and with
@@ -492,9 +570,7 @@ def run_ours(args, rank: int, world: int):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tps, n, dt, cores = oracle_sample(w, target_s=args.ref_sample_s)
-        cpu = {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"first {n} of {w.T} tokens through the whole oracle layer ({dt:.1f} s)"}
+        cpu = cpu_baseline(w, target_s=args.ref_sample_s)
 
     if rank == 0:
         line = {
@@ -502,13 +578,7 @@ def run_ours(args, rank: int, world: int):
             "warmup": args.warmup, "ms_per_step": ms_all, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8 (exact int32 accumulation), f32 epilogue",
             "data": "synthetic",
-            "config": {"workload": w.name, "T": w.T, "H": w.H, "E_log": w.E_log, "E_phys": w.E_phys,
-                       "k": w.k, "I": w.I, "ranks": w.R, "src_ranks": w.S,
-                       "messages": "int8 dispatch, int8 combine",
-                       "l2": (f"inputs larger than L2: {3 * w.E_log * w.H * w.I / 1e9:.2f} GB of int8 "
-                              f"expert weights (the touched experts' streamed every step) and "
-                              f"{2 * w.T * w.H / 1e6:.1f} MB of bf16 hidden per step"),
-                       "parallelism": f"replicas x{world}"},
+            "config": config_of(w, world, len(touched) * 3 * w.H * w.I),
             "stages": stages,
             "roofline": roofline,
             "cpu_baseline": cpu,

@@ -19,7 +19,9 @@ LIB_PATH = os.path.join(_PKG, "_build", "libmoe_gb300.so")
 MOE_MSG_BF16, MOE_MSG_INT8 = 0, 1
 STATUS = {0: "ok", 1: "invalid argument", 2: "buffer or workspace too small",
           3: "static buffer capacity exceeded", 4: "CUDA launch error",
-          5: "device wait timed out", 6: "unsupported configuration"}
+          5: "device wait timed out", 6: "unsupported configuration",
+          7: "device-side index check failed"}
+MOE_OK, MOE_ERR_CAPACITY, MOE_ERR_TIMEOUT, MOE_ERR_INDEX = 0, 3, 5, 7
 
 
 class MoeError(RuntimeError):
@@ -58,7 +60,8 @@ EXPORTED = ("moe_status_string", "moe_static_buffer_bytes", "moe_query_layout", 
             "moe_device_status", "moe_last_cuda_error", "moe_profile_enable", "moe_profile_read",
             "moe_dispatch_noalloc", "moe_dispatch_noalloc_max_scratch", "moe_layer_graph_create",
             "moe_graph_launch", "moe_graph_destroy", "moe_eplb_collect", "moe_expert_ffn_combine",
-            "moe_trampoline_bytes", "moe_dispatch_trampoline", "moe_expert_ffn_path")
+            "moe_trampoline_bytes", "moe_dispatch_trampoline", "moe_expert_ffn_path",
+            "moe_layer_host")
 
 _lib = None
 
@@ -87,6 +90,8 @@ def load(path: str = LIB_PATH):
         "moe_combine": ([PS, P, i64, P, P, P], ctypes.c_int),
         "moe_layer": ([PS, P, P, P, P, i32, ctypes.POINTER(moe_expert_weights),
                        ctypes.POINTER(moe_routing), P, i64, P, i64, P, i64, P, P], ctypes.c_int),
+        "moe_layer_host": ([PS, P, P, P, P, P, P, P, i32, ctypes.POINTER(moe_expert_weights),
+                            ctypes.POINTER(moe_routing), P, i64, P, i64, P, i64, P, P], ctypes.c_int),
         "moe_gemm_workspace_bytes": ([i32, i64, i32], i64),
         "moe_device_status": ([P, ctypes.POINTER(i32), P], ctypes.c_int),
         "moe_launch_count": ([], i64),
@@ -307,6 +312,23 @@ def moe_layer(shape: Shape, logits, x, w_gate_up, s_gate_up, w_down, s_down, rou
         ctypes.byref(w), ctypes.byref(r), _ptr(dispatch_buf), dispatch_buf.numel(),
         _ptr(combine_buf), combine_buf.numel(), _ptr(workspace), workspace.numel(), _ptr(out),
         _stream(stream)))
+
+
+def moe_layer_host(shape: Shape, h_logits, h_x, h_out, d_logits, d_x, w_gate_up, s_gate_up, w_down,
+                   s_down, routing: dict, dispatch_buf, combine_buf, workspace, d_out, rep_table=None,
+                   n_copies=None, phys_to_weight=None, stream=None):
+    """The whole layer from host tensors (page-locked CPU tensors: h_logits f32,
+    h_x and h_out 16-bit) to host: the copies in, moe_layer and the copy out,
+    all enqueued on `stream` by the library."""
+    cs = shape.c()
+    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight)
+    r = moe_routing(*[_ptr(routing[n]) for n, _ in moe_routing._fields_])
+    mc = int(rep_table.shape[1]) if rep_table is not None else 0
+    _check("moe_layer_host", load().moe_layer_host(
+        ctypes.byref(cs), _ptr(h_logits), _ptr(h_x), _ptr(h_out), _ptr(d_logits), _ptr(d_x),
+        _ptr(rep_table), _ptr(n_copies), mc, ctypes.byref(w), ctypes.byref(r), _ptr(dispatch_buf),
+        dispatch_buf.numel(), _ptr(combine_buf), combine_buf.numel(), _ptr(workspace),
+        workspace.numel(), _ptr(d_out), _stream(stream)))
 
 
 def moe_layer_graph_create(shape: Shape, logits, x, w_gate_up, s_gate_up, w_down, s_down,

@@ -1,5 +1,6 @@
 // api.cu -- the extern "C" entry points declared in include/moe.h: host-side
 // validation, buffer layout, and the launch sequence of each step.
+#include <limits.h>
 #include <string.h>
 
 #include <atomic>
@@ -15,6 +16,11 @@ void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed);
 static bool g_prof_on = false;
 static cudaEvent_t g_prof_ev[kProfSlots][2] = {};
 cudaEvent_t prof_event(int slot, int end) { return g_prof_on ? g_prof_ev[slot][end] : nullptr; }
+
+cudaError_t clear_status(void* ws, cudaStream_t st) {
+    count_launches(1);
+    return cudaMemsetAsync(ws, 0, 256, st);
+}
 }  // namespace moe
 
 namespace {
@@ -77,6 +83,7 @@ const char* moe_status_string(moe_status s) {
         case MOE_ERR_CUDA: return "CUDA launch error";
         case MOE_ERR_TIMEOUT: return "device wait timed out";
         case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MOE_ERR_INDEX: return "device-side index check failed";
     }
     return "unknown status";
 }
@@ -252,12 +259,17 @@ moe_status moe_combine(const moe_shape* shape, const void* combine_buf, int64_t 
                                       (cudaStream_t)stream));
 }
 
-moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t* x,
-                     const int32_t* rep_table, const int32_t* n_copies, int32_t max_copies,
-                     const moe_expert_weights* weights, const moe_routing* routing,
-                     void* dispatch_buf, int64_t dispatch_bytes, void* combine_buf,
-                     int64_t combine_bytes, void* workspace, int64_t workspace_bytes,
-                     uint16_t* out, moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Host-side checks of moe_layer's arguments (nothing is enqueued).
+moe_status check_layer_args(const moe_shape* shape, const float* logits, const uint16_t* x,
+                            const int32_t* rep_table, const int32_t* n_copies, int32_t max_copies,
+                            const moe_expert_weights* weights, const moe_routing* routing,
+                            const void* dispatch_buf, int64_t dispatch_bytes, const void* combine_buf,
+                            int64_t combine_bytes, const void* workspace, int64_t workspace_bytes,
+                            const uint16_t* out, moe_layout* L) {
     moe_status st = check_shape(shape);
     if (st != MOE_OK) return st;
     if (shape->dispatch_fmt != MOE_MSG_INT8) return MOE_ERR_UNSUPPORTED;
@@ -277,25 +289,79 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t
     }
     Dims d = make_dims(*shape);
     if ((st = check_weights(d, weights)) != MOE_OK) return st;
-    moe_layout L;
-    fill_layout(d, &L);
-    if (dispatch_bytes < L.dispatch_bytes || combine_bytes < L.combine_bytes ||
-        workspace_bytes < L.workspace_bytes)
+    fill_layout(d, L);
+    if (dispatch_bytes < L->dispatch_bytes || combine_bytes < L->combine_bytes ||
+        workspace_bytes < L->workspace_bytes)
         return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t* x,
+                     const int32_t* rep_table, const int32_t* n_copies, int32_t max_copies,
+                     const moe_expert_weights* weights, const moe_routing* routing,
+                     void* dispatch_buf, int64_t dispatch_bytes, void* combine_buf,
+                     int64_t combine_bytes, void* workspace, int64_t workspace_bytes,
+                     uint16_t* out, moe_stream_t stream) {
+    moe_layout L;
+    moe_status st = check_layer_args(shape, logits, x, rep_table, n_copies, max_copies, weights,
+                                     routing, dispatch_buf, dispatch_bytes, combine_buf,
+                                     combine_bytes, workspace, workspace_bytes, out, &L);
+    if (st != MOE_OK) return st;
+    const moe_routing& r = *routing;
+    const Dims d = make_dims(*shape);
     const WsLayout wl = make_ws(d);
     cudaStream_t s = (cudaStream_t)stream;
     if ((st = cuda_status(launch_route(d, logits, rep_table, n_copies, max_copies, r.topk_idx,
                                        r.topk_w, r.phys_idx, r.expert_counts, s))) != MOE_OK)
         return st;
+    // the status word is cleared once, by the dispatch, and covers the whole layer
     if ((st = cuda_status(launch_dispatch(d, x, r.phys_idx, dispatch_buf, L.dispatch_meta_offset,
                                           r.rank_counts, r.expert_offsets, r.expert_rows,
-                                          workspace, wl, s))) != MOE_OK)
+                                          workspace, wl, s, /*clear=*/true))) != MOE_OK)
         return st;
     if ((st = cuda_status(launch_ffn(d, dispatch_buf, L.dispatch_meta_offset, r.expert_offsets,
                                      r.expert_rows, *weights, combine_buf, L.combine_scale_offset,
-                                     workspace, wl, s))) != MOE_OK)
+                                     workspace, wl, s, FusedCombine{nullptr, nullptr},
+                                     /*clear=*/false))) != MOE_OK)
         return st;
     return cuda_status(launch_combine(d, combine_buf, L.combine_scale_offset, r.topk_w, out, s));
+}
+
+moe_status moe_layer_host(const moe_shape* shape, const float* h_logits, const uint16_t* h_x,
+                          uint16_t* h_out, float* d_logits, uint16_t* d_x, const int32_t* rep_table,
+                          const int32_t* n_copies, int32_t max_copies,
+                          const moe_expert_weights* weights, const moe_routing* routing,
+                          void* dispatch_buf, int64_t dispatch_bytes, void* combine_buf,
+                          int64_t combine_bytes, void* workspace, int64_t workspace_bytes,
+                          uint16_t* d_out, moe_stream_t stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (!h_logits || !h_x || !h_out || !d_logits || !d_x || !d_out) return MOE_ERR_INVALID_ARG;
+    if (!aligned(h_logits, 16) || !aligned(h_x, 16) || !aligned(h_out, 16) || !aligned(d_logits, 16))
+        return MOE_ERR_INVALID_ARG;
+    moe_layout L;
+    if ((st = check_layer_args(shape, d_logits, d_x, rep_table, n_copies, max_copies, weights,
+                               routing, dispatch_buf, dispatch_bytes, combine_buf, combine_bytes,
+                               workspace, workspace_bytes, d_out, &L)) != MOE_OK)
+        return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t lg_bytes = sizeof(float) * (size_t)shape->T * shape->E_log;
+    const size_t x_bytes = 2 * (size_t)shape->T * shape->H;
+    if ((st = cuda_status(cudaMemcpyAsync(d_logits, h_logits, lg_bytes, cudaMemcpyHostToDevice, s))) !=
+            MOE_OK ||
+        (st = cuda_status(cudaMemcpyAsync(d_x, h_x, x_bytes, cudaMemcpyHostToDevice, s))) != MOE_OK)
+        return st;
+    count_launches(2);
+    if ((st = moe_layer(shape, d_logits, d_x, rep_table, n_copies, max_copies, weights, routing,
+                        dispatch_buf, dispatch_bytes, combine_buf, combine_bytes, workspace,
+                        workspace_bytes, d_out, stream)) != MOE_OK)
+        return st;
+    count_launches(1);
+    return cuda_status(cudaMemcpyAsync(h_out, d_out, x_bytes, cudaMemcpyDeviceToHost, s));
 }
 
 moe_status moe_profile_enable(int32_t on) {
@@ -356,12 +422,13 @@ moe_status moe_grouped_gemm_s8(int32_t n_groups, const int32_t* offsets, int64_t
     if (K % 64 == 0)
         return cuda_status(launch_grouped_gemm_tc(n_groups, offsets, max_rows, row_index, A, lda, B,
                                                   N, K, C, workspace, (cudaStream_t)stream));
-    if (cudaMemsetAsync(workspace, 0, 256, (cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
-    count_launches(1);
-    return cuda_status(launch_grouped_gemm_s8(n_groups, offsets, max_rows, row_index, A, lda, B,
-                                              (long long)N * K, nullptr, N, K, C,
+    moe_status st = cuda_status(clear_status(workspace, (cudaStream_t)stream));
+    if (st != MOE_OK) return st;
+    // the rows of A are the caller's: no bound on the row list's entries here
+    return cuda_status(launch_grouped_gemm_s8(n_groups, offsets, max_rows, row_index, LLONG_MAX, A,
+                                              lda, B, (long long)N * K, nullptr, n_groups, N, K, C,
                                               ws_ptr<int32_t>(workspace, 256),
-                                              (cudaStream_t)stream));
+                                              ws_ptr<int>(workspace, 0), (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -16,6 +16,11 @@
 //                  expert (warp match_any + popc, an exclusive scan across
 //                  warps) -> slot within (dst, src), rank within (src, expert),
 //                  rank_counts[dst][src], hist[src][expert].  No atomics.
+//                  A physical id outside [0, E_phys) drops its message
+//                  (MOE_ERR_INDEX); a message whose slot would reach
+//                  max_tokens (only a replica table mapping two routes of one
+//                  token onto one expert can cause it) is marked -1 and
+//                  dropped (MOE_ERR_CAPACITY).
 //   layout_expert  one block: per-expert prefix over sources and over experts
 //                  -> src_base, expert_offsets.
 //   scatter        one block per token: bf16 row -> shared memory, absmax,
@@ -35,10 +40,10 @@ namespace {
 constexpr int kLayoutMaxWarps = 16;
 
 __global__ void __launch_bounds__(kLayoutMaxWarps * 32)
-layout_src_kernel(int lb, int k, int epr, int R, int E_phys, int S,
+layout_src_kernel(int lb, int k, int epr, int R, int E_phys, int S, int mt,
                   const int32_t* __restrict__ phys_idx, int32_t* __restrict__ slot_local,
                   int32_t* __restrict__ erank, int32_t* __restrict__ rank_counts,
-                  int32_t* __restrict__ hist) {
+                  int32_t* __restrict__ hist, int* __restrict__ err) {
     extern __shared__ int smem[];
     const int W = blockDim.x >> 5;
     int* cntD = smem;                // [W][R]
@@ -59,13 +64,16 @@ layout_src_kernel(int lb, int k, int epr, int R, int E_phys, int S,
 
     for (int r = r0; r < r1; ++r) {
         int i = r * 32 + lane;
-        bool valid = i < N;
+        const bool valid = i < N;
         int p = valid ? phys_idx[base + i] : -1;
-        int dst = valid ? p / epr : -1;
+        const bool ok = valid && p >= 0 && p < E_phys;  // caller data: keep the id in range
+        if (valid && !ok) post_status(err, MOE_ERR_INDEX);
+        p = ok ? p : -1;
+        int dst = ok ? p / epr : -1;
         unsigned pd = __match_any_sync(0xffffffffu, dst);
         unsigned pe = __match_any_sync(0xffffffffu, p);
-        if (valid && (pd & lt) == 0) cntD[w * R + dst] += __popc(pd);
-        if (valid && (pe & lt) == 0) cntE[w * E_phys + p] += __popc(pe);
+        if (ok && (pd & lt) == 0) cntD[w * R + dst] += __popc(pd);
+        if (ok && (pe & lt) == 0) cntE[w * E_phys + p] += __popc(pe);
         __syncwarp();
     }
     __syncthreads();
@@ -90,26 +98,33 @@ layout_src_kernel(int lb, int k, int epr, int R, int E_phys, int S,
     __syncthreads();
     for (int r = r0; r < r1; ++r) {
         int i = r * 32 + lane;
-        bool valid = i < N;
+        const bool valid = i < N;
         int p = valid ? phys_idx[base + i] : -1;
-        int dst = valid ? p / epr : -1;
+        const bool ok = valid && p >= 0 && p < E_phys;
+        p = ok ? p : -1;
+        int dst = ok ? p / epr : -1;
         unsigned pd = __match_any_sync(0xffffffffu, dst);
         unsigned pe = __match_any_sync(0xffffffffu, p);
-        int sl = 0, er = 0;
-        if (valid) {
+        int sl = -1, er = 0;
+        if (ok) {
             sl = cntD[w * R + dst] + __popc(pd & lt);
             er = cntE[w * E_phys + p] + __popc(pe & lt);
+            if (sl >= mt) {  // the pair's static area is full: drop the message
+                post_status(err, MOE_ERR_CAPACITY);
+                sl = -1;
+            }
         }
         __syncwarp();
-        if (valid && (pd & lt) == 0) cntD[w * R + dst] += __popc(pd);
-        if (valid && (pe & lt) == 0) cntE[w * E_phys + p] += __popc(pe);
+        if (ok && (pd & lt) == 0) cntD[w * R + dst] += __popc(pd);
+        if (ok && (pe & lt) == 0) cntE[w * E_phys + p] += __popc(pe);
         __syncwarp();
         if (valid) {
             slot_local[base + i] = sl;
             erank[base + i] = er;
         }
     }
-    for (int b = threadIdx.x; b < R; b += blockDim.x) rank_counts[(long long)b * S + src] = totD[b];
+    // messages actually placed in each pair's area (at most max_tokens)
+    for (int b = threadIdx.x; b < R; b += blockDim.x) rank_counts[(long long)b * S + src] = min(totD[b], mt);
     for (int b = threadIdx.x; b < E_phys; b += blockDim.x) hist[(long long)src * E_phys + b] = totE[b];
 }
 
@@ -201,6 +216,26 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
     const int src = t / lb, bs = t - src * lb;
     const int nch = H / 8;  // 16-byte chunks of 8 bf16
     const long long tk = (long long)t * k;
+    // kDirect, kHop2: the route threads look up their message slots and expert
+    // row positions first, so that these dependent loads overlap the row's
+    // loads.  my_slot < 0: no message is written (a physical id outside
+    // [0, E_phys), or a full static area); for a full area the expert's row
+    // list still gets an entry, pointed at the pair's last slot (written by
+    // another message), so that every entry names a written slot.
+    long long my_slot = -1, my_fill = -1;
+    int my_erow = -1;
+    if (MODE != kHop1 && threadIdx.x >= 32 && threadIdx.x < 32 + k) {
+        const int j = threadIdx.x - 32;
+        const int p = MODE == kHop2 ? troutes[tk + j] : phys_idx[tk + j];
+        if (p >= 0 && p < E_phys) {
+            const int sl = slot_local[tk + j];
+            const long long pair = ((long long)(p / epr) * S + src) * mt;
+            my_erow = expert_offsets[p] + src_base[(long long)src * E_phys + p] + erank[tk + j];
+            my_slot = sl >= 0 ? pair + sl : -1;
+            my_fill = pair + mt - 1;
+        }
+        s_slot[j] = my_slot;
+    }
     if constexpr (MODE == kHop2) {
         // the token as the trampoline holds it: the message row, its scale and routes
         const uint4* tr = reinterpret_cast<const uint4*>(trows + (long long)t * drow);
@@ -210,42 +245,25 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
         __syncthreads();
         const float scale = tmeta[t].scale;
         if (threadIdx.x == 0) {
-            for (int j = 0; j < k; ++j) {
-                int p = troutes[tk + j];
-                int dst = p / epr;
-                long long g = ((long long)dst * S + src) * mt + slot_local[tk + j];
-                bulk_store_s2g(dbuf + g * drow, sm, (unsigned)drow);
-            }
+            for (int j = 0; j < k; ++j)
+                if (s_slot[j] >= 0) bulk_store_s2g(dbuf + s_slot[j] * drow, sm, (unsigned)drow);
             asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
         }
         if (threadIdx.x >= 32 && threadIdx.x < 32 + k) {
-            int j = threadIdx.x - 32;
-            int p = troutes[tk + j];
-            int dst = p / epr;
-            long long g = ((long long)dst * S + src) * mt + slot_local[tk + j];
-            moe_dispatch_meta m;
-            m.scale = scale;
-            m.src_rank = src;
-            m.batch_slot = bs;
-            m.route_slot = j;
-            meta[g] = m;
-            expert_rows[expert_offsets[p] + src_base[(long long)src * E_phys + p] + erank[tk + j]] =
-                (int32_t)g;
+            if (my_slot >= 0) {
+                moe_dispatch_meta m;
+                m.scale = scale;
+                m.src_rank = src;
+                m.batch_slot = bs;
+                m.route_slot = threadIdx.x - 32;
+                meta[my_slot] = m;
+                expert_rows[my_erow] = (int32_t)my_slot;
+            } else if (my_erow >= 0) {
+                expert_rows[my_erow] = (int32_t)my_fill;
+            }
         }
         if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
         return;
-    }
-    // kDirect: the route threads look up their message slots and expert row
-    // positions now, so that these dependent loads overlap the row's loads
-    // instead of following the quantisation
-    long long my_slot = 0;
-    int my_erow = 0;
-    if (MODE == kDirect && threadIdx.x >= 32 && threadIdx.x < 32 + k) {
-        const int j = threadIdx.x - 32;
-        const int p = phys_idx[tk + j];
-        my_slot = ((long long)(p / epr) * S + src) * mt + slot_local[tk + j];
-        my_erow = expert_offsets[p] + src_base[(long long)src * E_phys + p] + erank[tk + j];
-        s_slot[j] = my_slot;
     }
     const uint4* xr = reinterpret_cast<const uint4*>(x + (long long)t * H);
     float amax = 0.f;
@@ -327,17 +345,22 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
         return;
     }
     if (threadIdx.x == 0) {
-        for (int j = 0; j < k; ++j) bulk_store_s2g(dbuf + s_slot[j] * drow, src_row, (unsigned)drow);
+        for (int j = 0; j < k; ++j)
+            if (s_slot[j] >= 0) bulk_store_s2g(dbuf + s_slot[j] * drow, src_row, (unsigned)drow);
         asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
     }
     if (threadIdx.x >= 32 && threadIdx.x < 32 + k) {
-        moe_dispatch_meta m;
-        m.scale = scale;
-        m.src_rank = src;
-        m.batch_slot = bs;
-        m.route_slot = threadIdx.x - 32;
-        meta[my_slot] = m;
-        expert_rows[my_erow] = (int32_t)my_slot;
+        if (my_slot >= 0) {
+            moe_dispatch_meta m;
+            m.scale = scale;
+            m.src_rank = src;
+            m.batch_slot = bs;
+            m.route_slot = threadIdx.x - 32;
+            meta[my_slot] = m;
+            expert_rows[my_erow] = (int32_t)my_slot;
+        } else if (my_erow >= 0) {
+            expert_rows[my_erow] = (int32_t)my_fill;
+        }
     }
     if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
 }
@@ -367,8 +390,9 @@ cudaError_t launch_layout(const Dims& d, const int32_t* phys_idx, int32_t* rank_
                                              (int)smem1);
         if (e != cudaSuccess) return e;
     }
-    layout_src_kernel<<<d.S, W * 32, smem1, st>>>(d.lb, d.k, d.epr, d.R, d.E_phys, d.S, phys_idx,
-                                                  slot_local, erank, rank_counts, hist);
+    layout_src_kernel<<<d.S, W * 32, smem1, st>>>(d.lb, d.k, d.epr, d.R, d.E_phys, d.S, d.mt,
+                                                  phys_idx, slot_local, erank, rank_counts, hist,
+                                                  ws_ptr<int>(ws, 0));
     layout_expert_kernel<<<1, 1024, 0, st>>>(d.S, d.E_phys, hist, src_base, expert_offsets);
     count_launches(2);
     return cudaGetLastError();
@@ -401,8 +425,10 @@ cudaError_t launch_scatter(const Dims& d, const uint16_t* x, const int32_t* phys
 cudaError_t launch_dispatch(const Dims& d, const uint16_t* x, const int32_t* phys_idx,
                             void* dbuf, long long meta_off, int32_t* rank_counts,
                             int32_t* expert_offsets, int32_t* expert_rows, void* ws,
-                            const WsLayout& wl, cudaStream_t st) {
-    cudaError_t e = launch_layout(d, phys_idx, rank_counts, expert_offsets, ws, wl, st);
+                            const WsLayout& wl, cudaStream_t st, bool clear) {
+    cudaError_t e = clear ? clear_status(ws, st) : cudaSuccess;
+    if (e != cudaSuccess) return e;
+    e = launch_layout(d, phys_idx, rank_counts, expert_offsets, ws, wl, st);
     if (e != cudaSuccess) return e;
     return launch_scatter<kDirect>(d, x, phys_idx, dbuf, meta_off, expert_offsets, expert_rows, ws,
                                    wl, nullptr, nullptr, nullptr, st);
@@ -423,6 +449,8 @@ cudaError_t launch_dispatch_trampoline(const Dims& d, const uint16_t* x, const i
                                        int32_t* expert_rows, void* ws, const WsLayout& wl,
                                        cudaStream_t st) {
     const TrampolineLayout tl = trampoline_layout(d);
+    cudaError_t e0 = clear_status(ws, st);
+    if (e0 != cudaSuccess) return e0;
     char* tb = static_cast<char*>(tbuf);
     char* trows = tb + tl.rows;
     moe_dispatch_meta* tmeta = reinterpret_cast<moe_dispatch_meta*>(tb + tl.meta);

@@ -19,9 +19,10 @@
 // exits.  Shapes whose scratch does not fit are rejected with
 // MOE_ERR_WORKSPACE before anything is enqueued.  Every call shares the
 // array; its contents are those of the last call (the dispatch kernels write
-// every scratch word they later read, so nothing needs clearing), and calls
-// that overlap on the GPU -- on different streams, or from several host
-// threads -- race on it.
+// every scratch word they later read; the status word at its start, where
+// the device-side index checks post their codes, is cleared by each call
+// and not exposed), and calls that overlap on the GPU -- on different
+// streams, or from several host threads -- race on it.
 #include <mutex>
 
 #include "internal.cuh"
@@ -78,9 +79,10 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_shape* shape, const uint16_
     // the dispatch kernels use the workspace only below the tile-prefix region
     if (wl.tiles > kNoallocScratchBytes) return MOE_ERR_WORKSPACE;
     void* scratch = nullptr;
-    if (scratch_for_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
-    const cudaError_t e = moe::launch_dispatch(d, x, phys_idx, dispatch_buf, L.dispatch_meta_offset,
-                                               rank_counts, expert_offsets, expert_rows, scratch,
-                                               wl, (cudaStream_t)stream);
-    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    const cudaError_t es = scratch_for_current_device(&scratch);
+    if (es != cudaSuccess) return moe::record_cuda_status(es);
+    return moe::record_cuda_status(moe::launch_dispatch(d, x, phys_idx, dispatch_buf,
+                                                        L.dispatch_meta_offset, rank_counts,
+                                                        expert_offsets, expert_rows, scratch, wl,
+                                                        (cudaStream_t)stream));
 }

@@ -11,13 +11,16 @@
 
 namespace {
 
-__global__ void eplb_collect_kernel(int E_phys, const int32_t* __restrict__ expert_counts,
+// A phys_to_logical entry outside [0, E_log) is caller data that names no
+// logical expert: its count is skipped.
+__global__ void eplb_collect_kernel(int E_log, int E_phys, const int32_t* __restrict__ expert_counts,
                                     const int32_t* __restrict__ phys_to_logical,
                                     long long* __restrict__ load) {
     for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < E_phys; p += gridDim.x * blockDim.x) {
         const int e = phys_to_logical ? phys_to_logical[p] : p;
         const int c = expert_counts[p];
-        if (c) atomicAdd(reinterpret_cast<unsigned long long*>(load + e), (unsigned long long)c);
+        if (c && e >= 0 && e < E_log)
+            atomicAdd(reinterpret_cast<unsigned long long*>(load + e), (unsigned long long)c);
     }
 }
 
@@ -31,7 +34,7 @@ extern "C" moe_status moe_eplb_collect(int32_t E_log, int32_t E_phys, const int3
     const int threads = 256;
     const int blocks = (E_phys + threads - 1) / threads;
     eplb_collect_kernel<<<blocks, threads, 0, (cudaStream_t)stream>>>(
-        E_phys, expert_counts, phys_to_logical, reinterpret_cast<long long*>(load));
+        E_log, E_phys, expert_counts, phys_to_logical, reinterpret_cast<long long*>(load));
     moe::count_launches(1);
     return moe::record_cuda_status(cudaGetLastError());
 }

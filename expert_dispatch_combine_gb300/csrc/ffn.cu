@@ -26,12 +26,28 @@ namespace {
 
 // --------------------------------------------------------- tile prefix
 // tile_prefix[g] = sum_{g' < g} ceil(M_g' / BM), g = 0..G (one block).
+// The offsets and weight sets are caller data.  Unless offsets[0] = 0, the
+// offsets never decrease, offsets[G] <= max_rows and every weight set lies in
+// [0, n_sets), the kernel posts MOE_ERR_INDEX and describes no tile at all,
+// so no GEMM that reads this prefix addresses memory outside its buffers.
 __global__ void __launch_bounds__(1024)
-tile_prefix_kernel(int G, int BM, const int32_t* __restrict__ offsets,
-                   int32_t* __restrict__ tile_prefix, int4* __restrict__ table,
-                   const int32_t* __restrict__ g2s) {
+tile_prefix_kernel(int G, int BM, const int32_t* __restrict__ offsets, long long max_rows,
+                   int n_sets, int32_t* __restrict__ tile_prefix, int4* __restrict__ table,
+                   const int32_t* __restrict__ g2s, int* __restrict__ err) {
     __shared__ int s_warp[32];
     __shared__ int s_carry;
+    int bad = 0;
+    for (int g = threadIdx.x; g < G; g += 1024) {
+        if (offsets[g + 1] < offsets[g]) bad = 1;
+        const int set = g2s ? g2s[g] : g;
+        if (set < 0 || set >= n_sets) bad = 1;
+    }
+    if (threadIdx.x == 0 && (offsets[0] != 0 || (long long)offsets[G] > max_rows)) bad = 1;
+    if (__syncthreads_or(bad)) {
+        if (threadIdx.x == 0 && err) post_status(err, MOE_ERR_INDEX);
+        for (int g = threadIdx.x; g <= G; g += 1024) tile_prefix[g] = 0;
+        return;
+    }
     if (threadIdx.x == 0) s_carry = 0;
     __syncthreads();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -85,9 +101,9 @@ constexpr int kBM = 64, kBN = 64, kBKW = 16;  // BK = 64 bytes = 16 words
 __global__ void __launch_bounds__(256)
 gemm_s8_simt_kernel(int G, const int32_t* __restrict__ offsets,
                     const int32_t* __restrict__ tile_prefix, const int32_t* __restrict__ row_index,
-                    const int8_t* __restrict__ A, long long lda, const int8_t* __restrict__ B,
-                    long long bstride, const int32_t* __restrict__ g2s, int N, int K,
-                    int32_t* __restrict__ C) {
+                    long long a_rows, const int8_t* __restrict__ A, long long lda,
+                    const int8_t* __restrict__ B, long long bstride, const int32_t* __restrict__ g2s,
+                    int N, int K, int32_t* __restrict__ C, int* __restrict__ err) {
     __shared__ int As[kBM][kBKW + 1];
     __shared__ int Bs[kBN][kBKW + 1];
     const int tile = blockIdx.x;
@@ -101,9 +117,14 @@ gemm_s8_simt_kernel(int G, const int32_t* __restrict__ offsets,
 
     const int tid = threadIdx.x;
     const int lr = tid >> 2, lq = tid & 3;  // load row, 16-byte quarter
-    const bool a_ok = m0 + lr < mend;
+    bool a_ok = m0 + lr < mend;
     long long arow = 0;
     if (a_ok) arow = row_index ? row_index[m0 + lr] : (m0 + lr);
+    if (a_ok && (arow < 0 || arow >= a_rows)) {  // row list entry outside A: read zeros
+        post_status(err, MOE_ERR_INDEX);
+        a_ok = false;
+        arow = 0;
+    }
     const int8_t* ap = A + arow * lda + lq * 16;
     const bool b_ok = n0 + lr < N;
     const int8_t* bp = Bg + (long long)(n0 + lr) * K + lq * 16;
@@ -169,18 +190,24 @@ constexpr int kRowThreads = 256;
 
 // SwiGLU + token-wise requantisation of one routed row.
 __global__ void __launch_bounds__(kRowThreads)
-swiglu_requant_kernel(int I, int E_phys, const int32_t* __restrict__ expert_offsets,
+swiglu_requant_kernel(int I, int E_phys, int n_sets, long long nslots,
+                      const int32_t* __restrict__ expert_offsets,
                       const int32_t* __restrict__ expert_rows,
                       const moe_dispatch_meta* __restrict__ meta,
                       const int32_t* __restrict__ p2w, const float* __restrict__ s_gu,
                       const int32_t* __restrict__ acc_gu, int8_t* __restrict__ hq,
-                      float* __restrict__ sh) {
+                      float* __restrict__ sh, int* __restrict__ err) {
     extern __shared__ float s_h[];
     __shared__ float s_red[kRowThreads / 32];
     const int r = blockIdx.x;
     const int p = find_group(expert_offsets, E_phys, r);
     const int set = p2w ? p2w[p] : p;
-    const float s = meta[expert_rows[r]].scale;
+    const long long g = expert_rows[r];
+    if (set < 0 || set >= n_sets || g < 0 || g >= nslots) {  // caller data out of range
+        if (threadIdx.x == 0) post_status(err, MOE_ERR_INDEX);
+        return;
+    }
+    const float s = meta[g].scale;
     const int32_t* acc = acc_gu + (long long)r * 2 * I;
     const float* sg = s_gu + (long long)set * 2 * I;
     float amax = 0.f;
@@ -201,18 +228,28 @@ swiglu_requant_kernel(int I, int E_phys, const int32_t* __restrict__ expert_offs
 
 // Down-projection epilogue: y, then the return message into the combine row.
 __global__ void __launch_bounds__(kRowThreads)
-return_kernel(int H, int k, int lb, int E_phys, int int8_msgs, long long crow,
-              const int32_t* __restrict__ expert_offsets, const int32_t* __restrict__ expert_rows,
+return_kernel(int H, int k, int lb, int S, int E_phys, int n_sets, long long nslots, int int8_msgs,
+              long long crow, const int32_t* __restrict__ expert_offsets,
+              const int32_t* __restrict__ expert_rows,
               const moe_dispatch_meta* __restrict__ meta, const int32_t* __restrict__ p2w,
               const float* __restrict__ s_d, const int32_t* __restrict__ acc_d,
               const float* __restrict__ sh, unsigned char* __restrict__ cbuf,
-              float* __restrict__ cscale) {
+              float* __restrict__ cscale, int* __restrict__ err) {
     extern __shared__ float s_y[];
     __shared__ float s_red[kRowThreads / 32];
     const int r = blockIdx.x;
     const int p = find_group(expert_offsets, E_phys, r);
     const int set = p2w ? p2w[p] : p;
-    const moe_dispatch_meta m = meta[expert_rows[r]];
+    const long long g = expert_rows[r];
+    if (set < 0 || set >= n_sets || g < 0 || g >= nslots) {
+        if (threadIdx.x == 0) post_status(err, MOE_ERR_INDEX);
+        return;
+    }
+    const moe_dispatch_meta m = meta[g];
+    if (!meta_in_range(m, S, lb, k)) {  // the slot holds no message of this shape
+        if (threadIdx.x == 0) post_status(err, MOE_ERR_INDEX);
+        return;
+    }
     const long long tj = ((long long)m.src_rank * lb + m.batch_slot) * k + m.route_slot;
     const int32_t* acc = acc_d + (long long)r * H;
     const float* sd = s_d + (long long)set * H;
@@ -243,25 +280,28 @@ cudaError_t set_smem(const void* fn, size_t bytes) {
 
 }  // namespace
 
-cudaError_t launch_tile_prefix(int G, int BM, const int32_t* offsets, int32_t* tile_prefix,
-                               cudaStream_t st, int4* table, const int32_t* g2s) {
-    tile_prefix_kernel<<<1, 1024, 0, st>>>(G, BM, offsets, tile_prefix, table, g2s);
+cudaError_t launch_tile_prefix(int G, int BM, const int32_t* offsets, long long max_rows, int n_sets,
+                               int32_t* tile_prefix, int* err, cudaStream_t st, int4* table,
+                               const int32_t* g2s) {
+    tile_prefix_kernel<<<1, 1024, 0, st>>>(G, BM, offsets, max_rows, n_sets, tile_prefix, table, g2s,
+                                           err);
     count_launches(1);
     return cudaGetLastError();
 }
 
 cudaError_t launch_grouped_gemm_s8(int n_groups, const int32_t* offsets, long long max_rows,
-                                   const int32_t* row_index, const int8_t* A, long long lda,
-                                   const int8_t* B, long long b_group_stride,
-                                   const int32_t* group_to_set, int N, int K, int32_t* C,
-                                   int32_t* tile_prefix, cudaStream_t st) {
-    cudaError_t e0 = launch_tile_prefix(n_groups, kBM, offsets, tile_prefix, st);
+                                   const int32_t* row_index, long long a_rows, const int8_t* A,
+                                   long long lda, const int8_t* B, long long b_group_stride,
+                                   const int32_t* group_to_set, int n_sets, int N, int K, int32_t* C,
+                                   int32_t* tile_prefix, int* err, cudaStream_t st) {
+    cudaError_t e0 = launch_tile_prefix(n_groups, kBM, offsets, max_rows, n_sets, tile_prefix, err, st,
+                                        nullptr, group_to_set);
     if (e0 != cudaSuccess) return e0;
     long long max_tiles = (max_rows + kBM - 1) / kBM + n_groups;
     if (max_tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
     dim3 grid((unsigned)max_tiles, (unsigned)((N + kBN - 1) / kBN));
-    gemm_s8_simt_kernel<<<grid, 256, 0, st>>>(n_groups, offsets, tile_prefix, row_index, A, lda,
-                                              B, b_group_stride, group_to_set, N, K, C);
+    gemm_s8_simt_kernel<<<grid, 256, 0, st>>>(n_groups, offsets, tile_prefix, row_index, a_rows, A,
+                                              lda, B, b_group_stride, group_to_set, N, K, C, err);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -269,7 +309,7 @@ cudaError_t launch_grouped_gemm_s8(int n_groups, const int32_t* offsets, long lo
 cudaError_t launch_ffn_simt(const Dims& d, const void* dbuf, long long meta_off,
                             const int32_t* expert_offsets, const int32_t* expert_rows,
                             const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                            const WsLayout& wl, cudaStream_t st) {
+                            const WsLayout& wl, cudaStream_t st, bool clear) {
     const long long M = (long long)d.T * d.k;
     const moe_dispatch_meta* meta =
         reinterpret_cast<const moe_dispatch_meta*>(static_cast<const char*>(dbuf) + meta_off);
@@ -281,27 +321,29 @@ cudaError_t launch_ffn_simt(const Dims& d, const void* dbuf, long long meta_off,
     unsigned char* cb = static_cast<unsigned char*>(cbuf);
     cudaError_t e;
 
-    if ((e = cudaMemsetAsync(ws_ptr<int>(ws, 0), 0, 256, st)) != cudaSuccess) return e;
-    count_launches(1);
-    e = launch_grouped_gemm_s8(d.E_phys, expert_offsets, M, expert_rows,
+    int* err = ws_ptr<int>(ws, 0);
+    if (clear && (e = clear_status(ws, st)) != cudaSuccess) return e;
+    e = launch_grouped_gemm_s8(d.E_phys, expert_offsets, M, expert_rows, d.nslots,
                                static_cast<const int8_t*>(dbuf), d.drow, w.w_gate_up,
-                               2LL * d.I * d.H, w.phys_to_weight, 2 * d.I, d.H, acc_gu, tiles, st);
+                               2LL * d.I * d.H, w.phys_to_weight, w.n_sets, 2 * d.I, d.H, acc_gu,
+                               tiles, err, st);
     if (e != cudaSuccess) return e;
     size_t sm1 = sizeof(float) * (size_t)d.I;
     if ((e = set_smem((const void*)swiglu_requant_kernel, sm1)) != cudaSuccess) return e;
     swiglu_requant_kernel<<<(unsigned)M, kRowThreads, sm1, st>>>(
-        d.I, d.E_phys, expert_offsets, expert_rows, meta, w.phys_to_weight, w.s_gate_up, acc_gu,
-        hq, sh);
-    e = launch_grouped_gemm_s8(d.E_phys, expert_offsets, M, nullptr, hq, d.I, w.w_down,
-                               (long long)d.H * d.I, w.phys_to_weight, d.H, d.I, acc_d, tiles, st);
+        d.I, d.E_phys, w.n_sets, d.nslots, expert_offsets, expert_rows, meta, w.phys_to_weight,
+        w.s_gate_up, acc_gu, hq, sh, err);
+    e = launch_grouped_gemm_s8(d.E_phys, expert_offsets, M, nullptr, M, hq, d.I, w.w_down,
+                               (long long)d.H * d.I, w.phys_to_weight, w.n_sets, d.H, d.I, acc_d,
+                               tiles, err, st);
     if (e != cudaSuccess) return e;
     const int int8_msgs = d.cfmt == MOE_MSG_INT8 ? 1 : 0;
     size_t sm2 = int8_msgs ? sizeof(float) * (size_t)d.H : 0;
     if ((e = set_smem((const void*)return_kernel, sm2)) != cudaSuccess) return e;
     return_kernel<<<(unsigned)M, kRowThreads, sm2, st>>>(
-        d.H, d.k, d.lb, d.E_phys, int8_msgs, d.crow, expert_offsets, expert_rows, meta,
-        w.phys_to_weight, w.s_down, acc_d, sh, cb,
-        reinterpret_cast<float*>(cb + scale_off));
+        d.H, d.k, d.lb, d.S, d.E_phys, w.n_sets, d.nslots, int8_msgs, d.crow, expert_offsets,
+        expert_rows, meta, w.phys_to_weight, w.s_down, acc_d, sh, cb,
+        reinterpret_cast<float*>(cb + scale_off), err);
     count_launches(2);
     return cudaGetLastError();
 }

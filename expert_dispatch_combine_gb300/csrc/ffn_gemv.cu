@@ -63,6 +63,10 @@ struct Params {
     const float* s_h;             // down: per-row scale of h
     float* out;                   // h [M][I] or y [M][H]
     unsigned* rowmax;             // [M] |out| maximum (float bits)
+    long long M;                  // routed rows (rows of out)
+    long long nslots;             // dispatch slots (rows of dbuf)
+    int n_sets;                   // weight sets
+    int* err;                     // workspace status word
 };
 
 // 16 bytes of a weight row that is read once: no L1 allocation.
@@ -99,6 +103,12 @@ __global__ void __launch_bounds__(THREADS, 2) gemv_kernel(const Params P) {
     const int r_begin = P.offsets[e], r_end = P.offsets[e + 1];
     if (r_begin == r_end) return;
     const int set = P.p2w ? P.p2w[e] : e;
+    // offsets and weight sets are caller data: an expert whose rows or
+    // weight set fall outside the buffers is skipped
+    if (r_begin < 0 || r_end < r_begin || r_end > P.M || set < 0 || set >= P.n_sets) {
+        if (threadIdx.x == 0) post_status(P.err, MOE_ERR_INDEX);
+        return;
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int K = P.K;
     // this warp's weight rows
@@ -123,13 +133,21 @@ __global__ void __launch_bounds__(THREADS, 2) gemv_kernel(const Params P) {
         // stage the pass's token rows as int8
         if constexpr (KIND == GATE_UP) {
             const int nvec = K / 16;
+            // a row-list entry outside the dispatch buffer reads as a zero row
             for (int i = threadIdx.x; i < n * nvec; i += THREADS) {
                 const int t = i / nvec, c = i - t * nvec;
                 const long long slot = P.expert_rows[t0 + t];
-                reinterpret_cast<int4*>(xs + t * K)[c] =
-                    __ldg(reinterpret_cast<const int4*>(P.dbuf + slot * P.drow) + c);
+                int4 v = make_int4(0, 0, 0, 0);
+                if (slot >= 0 && slot < P.nslots)
+                    v = __ldg(reinterpret_cast<const int4*>(P.dbuf + slot * P.drow) + c);
+                reinterpret_cast<int4*>(xs + t * K)[c] = v;
             }
-            if (threadIdx.x < n) s_tok[threadIdx.x] = P.meta[P.expert_rows[t0 + threadIdx.x]].scale;
+            if (threadIdx.x < n) {
+                const long long slot = P.expert_rows[t0 + threadIdx.x];
+                const bool ok = slot >= 0 && slot < P.nslots;
+                if (!ok) post_status(P.err, MOE_ERR_INDEX);
+                s_tok[threadIdx.x] = ok ? P.meta[slot].scale : 0.f;
+            }
         } else {
             const int nvec = K / 8;  // 8 fp16 codes -> 8 int8
             for (int i = threadIdx.x; i < n * nvec; i += THREADS) {
@@ -256,7 +274,7 @@ bool ffn_gemv_fits(const Dims& d) {
 cudaError_t launch_ffn_gemv(const Dims& d, const void* dbuf, long long meta_off,
                             const int32_t* expert_offsets, const int32_t* expert_rows,
                             const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                            const WsLayout& wl, cudaStream_t st) {
+                            const WsLayout& wl, cudaStream_t st, bool clear) {
     const long long M = (long long)d.T * d.k;
     const moe_dispatch_meta* meta =
         reinterpret_cast<const moe_dispatch_meta*>(static_cast<const char*>(dbuf) + meta_off);
@@ -268,15 +286,16 @@ cudaError_t launch_ffn_gemv(const Dims& d, const void* dbuf, long long meta_off,
     __half* hq16 = ws_ptr<__half>(ws, wl.hq16);
     float* ybuf = ws_ptr<float>(ws, wl.ybuf);
     cudaError_t e;
-    if ((e = cudaMemsetAsync(err, 0, 256, st)) != cudaSuccess) return e;
+    if (clear && (e = clear_status(ws, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(hmax, 0, sizeof(unsigned) * 2 * M, st)) != cudaSuccess) return e;
-    count_launches(2);
+    count_launches(1);
 
     gv::Params P1 = {};
     P1.offsets = expert_offsets; P1.p2w = w.phys_to_weight; P1.w = w.w_gate_up; P1.s_ch = w.s_gate_up;
     P1.K = d.H; P1.nout = d.I;
     P1.expert_rows = expert_rows; P1.dbuf = static_cast<const int8_t*>(dbuf); P1.drow = d.drow; P1.meta = meta;
     P1.out = hbuf; P1.rowmax = hmax;
+    P1.M = M; P1.nslots = d.nslots; P1.n_sets = w.n_sets; P1.err = err;
     if (cudaEvent_t ev = prof_event(0, 0)) cudaEventRecord(ev, st);
     if ((e = gv::launch<gv::GATE_UP>(P1, d.E_phys, d.I / 32, st)) != cudaSuccess) return e;
     if (cudaEvent_t ev = prof_event(0, 1)) cudaEventRecord(ev, st);
@@ -288,12 +307,14 @@ cudaError_t launch_ffn_gemv(const Dims& d, const void* dbuf, long long meta_off,
     P2.K = d.I; P2.nout = d.H;
     P2.hq16 = hq16; P2.s_h = sh;
     P2.out = ybuf; P2.rowmax = ymax;
+    P2.M = M; P2.nslots = d.nslots; P2.n_sets = w.n_sets; P2.err = err;
     if (cudaEvent_t ev = prof_event(1, 0)) cudaEventRecord(ev, st);
     if ((e = gv::launch<gv::DOWN>(P2, d.E_phys, d.H / (64 * gv::DOWN_GROUPS), st)) != cudaSuccess) return e;
     if (cudaEvent_t ev = prof_event(1, 1)) cudaEventRecord(ev, st);
 
     return launch_retquant_rows(d, M, ybuf, ymax, expert_rows, meta, static_cast<unsigned char*>(cbuf),
-                                reinterpret_cast<float*>(static_cast<unsigned char*>(cbuf) + scale_off), st);
+                                reinterpret_cast<float*>(static_cast<unsigned char*>(cbuf) + scale_off), err,
+                                st);
 }
 
 }  // namespace moe

@@ -43,6 +43,7 @@
 // MOE_ERR_TIMEOUT in the workspace status word, waits briefly for its own
 // copies in flight, frees TMEM and returns.
 #include <algorithm>
+#include <climits>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -122,7 +123,8 @@ struct Params {
     const moe_dispatch_meta* meta;
     unsigned char* cbuf;
     long long crow;
-    int k, lb;
+    int k, lb, S;
+    long long nslots;            // EPI_BF16MSG: dispatch slots (range of expert_rows entries)
     int tma_out;                 // epilogue may use tensor stores for full groups
     int* err;
 };
@@ -226,17 +228,23 @@ __device__ __forceinline__ void epilogue_direct(const Params& P, const TileInfo&
         const bool chok = ch < P.nout;
         const float sd = chok ? P.s_ch[(long long)ti.set * P.rows_per_set + ch] : 0.f;
         const float sr_l = lane_ok ? P.s_row[ti.r0 + j0 + lane] : 0.f;
-        int tj_l = 0;
+        int tj_l = -1;  // -1: no valid message for this token (slot or metadata out of range)
         if (lane_ok) {
-            const moe_dispatch_meta m = P.meta[P.expert_rows[ti.r0 + j0 + lane]];
-            tj_l = (m.src_rank * P.lb + m.batch_slot) * P.k + m.route_slot;
+            const long long g = P.expert_rows[ti.r0 + j0 + lane];
+            bool ok = g >= 0 && g < P.nslots;
+            if (ok) {
+                const moe_dispatch_meta m = P.meta[g];
+                ok = meta_in_range(m, P.S, P.lb, P.k);
+                if (ok) tj_l = (m.src_rank * P.lb + m.batch_slot) * P.k + m.route_slot;
+            }
+            if (!ok) post_status(P.err, MOE_ERR_INDEX);
         }
 #pragma unroll
         for (int j = 0; j < GT; ++j) {
             const float sr = __shfl_sync(0xffffffffu, sr_l, j);
             const int tj = __shfl_sync(0xffffffffu, tj_l, j);
             const float y = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sd);
-            if (chok && j0 + j < ti.nvalid)
+            if (chok && j0 + j < ti.nvalid && tj >= 0)
                 reinterpret_cast<__nv_bfloat16*>(P.cbuf + (long long)tj * P.crow)[ch] =
                     __float2bfloat16_rn(y);
         }
@@ -709,15 +717,25 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
 // ------------------------------------------------------------ helpers
 // Gather rows (optionally through row_index) of an int8 matrix and convert
 // them to fp16 (exact); optionally copy the dispatch scale of each row.
+// A row-list entry outside [0, a_rows) gives a zero row (and scale) and
+// posts MOE_ERR_INDEX.
 __global__ void __launch_bounds__(128)
-assemble_kernel(int K, const int32_t* __restrict__ row_index, const int8_t* __restrict__ A,
-                long long lda, const moe_dispatch_meta* __restrict__ meta, __half* __restrict__ out,
-                float* __restrict__ s_row) {
+assemble_kernel(int K, const int32_t* __restrict__ row_index, long long a_rows,
+                const int8_t* __restrict__ A, long long lda, const moe_dispatch_meta* __restrict__ meta,
+                __half* __restrict__ out, float* __restrict__ s_row, int* __restrict__ err) {
     const int r = blockIdx.x;
     const long long g = row_index ? row_index[r] : r;
-    const uint4* src = reinterpret_cast<const uint4*>(A + g * lda);
     uint4* dst = reinterpret_cast<uint4*>(out + (long long)r * K);
     const int nch = K / 16;
+    if (g < 0 || g >= a_rows) {
+        for (int c = threadIdx.x; c < 2 * nch; c += blockDim.x) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        if (threadIdx.x == 0) {
+            post_status(err, MOE_ERR_INDEX);
+            if (meta) s_row[r] = 0.f;
+        }
+        return;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(A + g * lda);
     // four 16-byte loads of the row in flight per thread before converting
     for (int c0 = threadIdx.x; c0 < nch; c0 += 4 * blockDim.x) {
         uint4 w[4];
@@ -829,13 +847,21 @@ requant_kernel(int I, const float* __restrict__ h, const unsigned* __restrict__ 
 // the work.
 template <bool kFuse>
 __global__ void __launch_bounds__(kRowThreads)
-retquant_kernel(int H, int k, int lb, long long crow, const float* __restrict__ y,
-                const unsigned* __restrict__ rowmax, const int32_t* __restrict__ expert_rows,
-                const moe_dispatch_meta* __restrict__ meta, unsigned char* __restrict__ cbuf,
-                float* __restrict__ cscale, const float* __restrict__ topk_w, int* __restrict__ ready,
-                uint16_t* __restrict__ out) {
+retquant_kernel(int H, int k, int lb, int S, long long nslots, long long crow,
+                const float* __restrict__ y, const unsigned* __restrict__ rowmax,
+                const int32_t* __restrict__ expert_rows, const moe_dispatch_meta* __restrict__ meta,
+                unsigned char* __restrict__ cbuf, float* __restrict__ cscale,
+                const float* __restrict__ topk_w, int* __restrict__ ready, uint16_t* __restrict__ out,
+                int* __restrict__ err) {
     const int r = blockIdx.x;
     const int nch = H / 16;
+    {  // the row's dispatch slot and metadata are caller data: skip a row that is out of range
+        const long long g = expert_rows[r];
+        if (g < 0 || g >= nslots || !meta_in_range(meta[g], S, lb, k)) {
+            if (threadIdx.x == 0) post_status(err, MOE_ERR_INDEX);
+            return;
+        }
+    }
     const float4* src = reinterpret_cast<const float4*>(y + (long long)r * H);
     const int nt = blockDim.x;
     for (int c0 = threadIdx.x; c0 < nch; c0 += 2 * nt) {
@@ -1017,11 +1043,14 @@ cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long lo
     int32_t* tp = ws_ptr<int32_t>(ws, gw.tiles);
     int4* ttab = ws_ptr<int4>(ws, gw.ttab);
     __half* a16 = ws_ptr<__half>(ws, gw.a16);
-    cudaError_t e = cudaMemsetAsync(err, 0, 256, st);
+    cudaError_t e = clear_status(ws, st);
     if (e != cudaSuccess) return e;
-    count_launches(1);
-    if ((e = launch_tile_prefix(n_groups, BN_LARGE, offsets, tp, st, ttab)) != cudaSuccess) return e;
-    assemble_kernel<<<(unsigned)max_rows, 128, 0, st>>>(K, row_index, A, lda, nullptr, a16, nullptr);
+    if ((e = launch_tile_prefix(n_groups, BN_LARGE, offsets, max_rows, n_groups, tp, err, st, ttab)) !=
+        cudaSuccess)
+        return e;
+    // the rows of A are the caller's: no bound on the row list's entries here
+    assemble_kernel<<<(unsigned)max_rows, 128, 0, st>>>(K, row_index, LLONG_MAX, A, lda, nullptr, a16,
+                                                        nullptr, err);
     count_launches(1);
     CUtensorMap mw, mx[2], mo;
     const bool tma_out = N % 128 == 0;
@@ -1042,7 +1071,7 @@ template <int BNV>
 cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                    const int32_t* expert_offsets, const int32_t* expert_rows,
                    const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                   const WsLayout& wl, cudaStream_t st, const FusedCombine& fc) {
+                   const WsLayout& wl, cudaStream_t st, const FusedCombine& fc, bool clear) {
     const long long M = (long long)d.T * d.k;
     const moe_dispatch_meta* meta =
         reinterpret_cast<const moe_dispatch_meta*>(static_cast<const char*>(dbuf) + meta_off);
@@ -1062,20 +1091,21 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     const int E_w = w.n_sets;
     cudaError_t e;
 
-    if ((e = cudaMemsetAsync(err, 0, 256, st)) != cudaSuccess) return e;
+    if (clear && (e = clear_status(ws, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(hmax, 0, sizeof(unsigned) * 2 * M, st)) != cudaSuccess) return e;
-    count_launches(2);
+    count_launches(1);
     const bool fuse = fc.out != nullptr && int8_ret;
     int* ready = ws_ptr<int>(ws, wl.ready);
     if (fuse) {
         if ((e = cudaMemsetAsync(ready, 0, sizeof(int) * d.T, st)) != cudaSuccess) return e;
         count_launches(1);
     }
-    if ((e = launch_tile_prefix(d.E_phys, BNV, expert_offsets, tp, st, ttab, w.phys_to_weight)) !=
-        cudaSuccess)
+    if ((e = launch_tile_prefix(d.E_phys, BNV, expert_offsets, M, E_w, tp, err, st, ttab,
+                                w.phys_to_weight)) != cudaSuccess)
         return e;
-    assemble_kernel<<<(unsigned)M, 128, 0, st>>>(d.H, expert_rows, static_cast<const int8_t*>(dbuf),
-                                                 d.drow, meta, a16, s_row);
+    assemble_kernel<<<(unsigned)M, 128, 0, st>>>(d.H, expert_rows, d.nslots,
+                                                 static_cast<const int8_t*>(dbuf), d.drow, meta, a16,
+                                                 s_row, err);
     count_launches(1);
 
     CUtensorMap mwgu, mx1[2], mo1, mwd, mx2[2], mo2;
@@ -1113,15 +1143,16 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
         if ((e = launch_gemm<EPI_F32, BNV>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
         if (fuse)
             retquant_kernel<true><<<(unsigned)M, kRowThreads, 0, st>>>(
-                d.H, d.k, d.lb, d.crow, ybuf, ymax, expert_rows, meta, cb,
-                reinterpret_cast<float*>(cb + scale_off), fc.topk_w, ready, fc.out);
+                d.H, d.k, d.lb, d.S, d.nslots, d.crow, ybuf, ymax, expert_rows, meta, cb,
+                reinterpret_cast<float*>(cb + scale_off), fc.topk_w, ready, fc.out, err);
         else
             retquant_kernel<false><<<(unsigned)M, kRowThreads, 0, st>>>(
-                d.H, d.k, d.lb, d.crow, ybuf, ymax, expert_rows, meta, cb,
-                reinterpret_cast<float*>(cb + scale_off), nullptr, nullptr, nullptr);
+                d.H, d.k, d.lb, d.S, d.nslots, d.crow, ybuf, ymax, expert_rows, meta, cb,
+                reinterpret_cast<float*>(cb + scale_off), nullptr, nullptr, nullptr, err);
         count_launches(1);
     } else {
         P2.expert_rows = expert_rows; P2.meta = meta; P2.cbuf = cb; P2.crow = d.crow; P2.k = d.k; P2.lb = d.lb;
+        P2.S = d.S; P2.nslots = d.nslots;
         if ((e = launch_gemm<EPI_BF16MSG, BNV>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
     }
     return cudaGetLastError();
@@ -1138,9 +1169,10 @@ cudaError_t launch_requant_rows(int I, long long M, const float* h, const unsign
 
 cudaError_t launch_retquant_rows(const Dims& d, long long M, const float* y, const unsigned* rowmax,
                                  const int32_t* expert_rows, const moe_dispatch_meta* meta,
-                                 unsigned char* cbuf, float* cscale, cudaStream_t st) {
+                                 unsigned char* cbuf, float* cscale, int* err, cudaStream_t st) {
     tc::retquant_kernel<false><<<(unsigned)M, tc::kRowThreads, 0, st>>>(
-        d.H, d.k, d.lb, d.crow, y, rowmax, expert_rows, meta, cbuf, cscale, nullptr, nullptr, nullptr);
+        d.H, d.k, d.lb, d.S, d.nslots, d.crow, y, rowmax, expert_rows, meta, cbuf, cscale, nullptr,
+        nullptr, nullptr, err);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -1151,13 +1183,13 @@ cudaError_t launch_retquant_rows(const Dims& d, long long M, const float* y, con
 cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                           const int32_t* expert_offsets, const int32_t* expert_rows,
                           const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                          const WsLayout& wl, cudaStream_t st, const FusedCombine& fc) {
+                          const WsLayout& wl, cudaStream_t st, const FusedCombine& fc, bool clear) {
     const long long M = (long long)d.T * d.k;
     if (M <= 32LL * d.E_phys)
         return tc::ffn_tc<tc::BN_DECODE>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
-                                         scale_off, ws, wl, st, fc);
+                                         scale_off, ws, wl, st, fc, clear);
     return tc::ffn_tc<tc::BN_LARGE>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
-                                    scale_off, ws, wl, st, fc);
+                                    scale_off, ws, wl, st, fc, clear);
 }
 
 }  // namespace moe

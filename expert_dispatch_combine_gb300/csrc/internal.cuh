@@ -52,7 +52,7 @@ inline long long tile_table_entries(int n_groups, long long max_rows, int bm) {
 }
 
 // Workspace carve-up.  Every region is 256-byte aligned; offset 0 holds the
-// int32 device status word (MOE_OK or MOE_ERR_TIMEOUT).
+// int32 device status word (MOE_OK or the first error a kernel posted).
 struct WsLayout {
     long long slot_local;  // int32 [T*k]   slot of (t, j) within its (dst, src) pair
     long long erank;       // int32 [T*k]   rank of token t among its source's tokens for expert p
@@ -127,6 +127,22 @@ inline T* ws_ptr(void* ws, long long off) { return reinterpret_cast<T*>(static_c
 
 // Number of kernels (and memsets) this library has enqueued in this process.
 void count_launches(int n);
+
+#ifdef __CUDACC__
+// Posts `code` to the workspace status word unless an earlier code is there
+// (the first one posted stays).
+__device__ __forceinline__ void post_status(int* err, int code) { atomicCAS(err, 0, code); }
+
+// Whether a dispatch slot's metadata names a message of this shape (the
+// slot may hold stale or foreign contents if a row list is corrupt).
+__device__ __forceinline__ bool meta_in_range(const moe_dispatch_meta& m, int S, int lb, int k) {
+    return (unsigned)m.src_rank < (unsigned)S && (unsigned)m.batch_slot < (unsigned)lb &&
+           (unsigned)m.route_slot < (unsigned)k;
+}
+#endif
+
+// Clears the workspace status word (one 256-byte memset) on `st`.
+cudaError_t clear_status(void* ws, cudaStream_t st);
 // Trampoline area of the two-hop dispatch: [T][drow] message rows, [T]
 // moe_dispatch_meta (route_slot = k: the routes follow), [T][k] int32
 // physical expert ids.  Trampoline s holds the rows of source rank s's tokens.
@@ -154,30 +170,38 @@ cudaError_t launch_route(const Dims& d, const float* logits, const int32_t* rep_
                          const int32_t* n_copies, int max_copies, int32_t* topk_idx,
                          float* topk_w, int32_t* phys_idx, int32_t* expert_counts,
                          cudaStream_t st);
+// FusedDispatch; with `clear` the workspace status word is cleared first.
 cudaError_t launch_dispatch(const Dims& d, const uint16_t* x, const int32_t* phys_idx,
                             void* dbuf, long long meta_off, int32_t* rank_counts,
                             int32_t* expert_offsets, int32_t* expert_rows, void* ws,
-                            const WsLayout& wl, cudaStream_t st);
+                            const WsLayout& wl, cudaStream_t st, bool clear = true);
 cudaError_t launch_combine(const Dims& d, const void* cbuf, long long scale_off,
                            const float* topk_w, uint16_t* out, cudaStream_t st);
+// CUDA-core grouped GEMM; row_index entries must lie in [0, a_rows), weight
+// sets in [0, n_sets) (else MOE_ERR_INDEX is posted to *err).
 cudaError_t launch_grouped_gemm_s8(int n_groups, const int32_t* offsets, long long max_rows,
-                                   const int32_t* row_index, const int8_t* A, long long lda,
-                                   const int8_t* B, long long b_group_stride,
-                                   const int32_t* group_to_set, int N, int K, int32_t* C,
-                                   int32_t* tile_prefix, cudaStream_t st);
+                                   const int32_t* row_index, long long a_rows, const int8_t* A,
+                                   long long lda, const int8_t* B, long long b_group_stride,
+                                   const int32_t* group_to_set, int n_sets, int N, int K, int32_t* C,
+                                   int32_t* tile_prefix, int* err, cudaStream_t st);
 // Exclusive prefix of the token tiles (at most BM rows) of each of G groups,
 // tile_prefix[G] = their total; with a non-null `table`, also one entry per
-// token tile: (weight set = g2s[g] or g, first row, rows, group g).
-cudaError_t launch_tile_prefix(int G, int BM, const int32_t* offsets, int32_t* tile_prefix,
-                               cudaStream_t st, int4* table = nullptr, const int32_t* g2s = nullptr);
+// token tile: (weight set = g2s[g] or g, first row, rows, group g).  Offsets
+// that are not a nondecreasing prefix from 0 to at most max_rows, or a weight
+// set outside [0, n_sets), give no tiles and post MOE_ERR_INDEX to *err.
+cudaError_t launch_tile_prefix(int G, int BM, const int32_t* offsets, long long max_rows, int n_sets,
+                               int32_t* tile_prefix, int* err, cudaStream_t st,
+                               int4* table = nullptr, const int32_t* g2s = nullptr);
 cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long long max_rows,
                                    const int32_t* row_index, const int8_t* A, long long lda,
                                    const int8_t* B, int N, int K, int32_t* C, void* ws,
                                    cudaStream_t st);
+// The expert FFN launchers clear the workspace status word first when
+// `clear` is set (moe_layer clears it once, before the dispatch).
 cudaError_t launch_ffn_simt(const Dims& d, const void* dbuf, long long meta_off,
                             const int32_t* expert_offsets, const int32_t* expert_rows,
                             const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                            const WsLayout& wl, cudaStream_t st);
+                            const WsLayout& wl, cudaStream_t st, bool clear);
 // FusedCombine folded into the expert FFN (moe_layer, INT8 return messages,
 // tensor-core path): gate weights and the output.  Null members: no fusion.
 struct FusedCombine {
@@ -187,15 +211,17 @@ struct FusedCombine {
 cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                           const int32_t* expert_offsets, const int32_t* expert_rows,
                           const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                          const WsLayout& wl, cudaStream_t st, const FusedCombine& fc);
+                          const WsLayout& wl, cudaStream_t st, const FusedCombine& fc, bool clear);
 // The token-wise requantisation of h (row kernel of the tensor-core path):
 // hq as exact fp16 integers and the scales s_h, from h and its row maxima.
 cudaError_t launch_requant_rows(int I, long long M, const float* h, const unsigned* rowmax, void* hq16,
                                 float* sh, cudaStream_t st);
-// INT8 return messages from y and its row maxima into the combine rows.
+// INT8 return messages from y and its row maxima into the combine rows
+// (rows whose dispatch slot or metadata is out of range are skipped and
+// MOE_ERR_INDEX is posted to *err).
 cudaError_t launch_retquant_rows(const Dims& d, long long M, const float* y, const unsigned* rowmax,
                                  const int32_t* expert_rows, const moe_dispatch_meta* meta,
-                                 unsigned char* cbuf, float* cscale, cudaStream_t st);
+                                 unsigned char* cbuf, float* cscale, int* err, cudaStream_t st);
 // Decode batches (at most kGemvRowsPerExpert routed rows per expert on
 // average, INT8 return messages, H and I multiples of 512): the expert FFN
 // by streamed CUDA-core matrix-vector products, same outputs as launch_ffn_tc.
@@ -203,7 +229,7 @@ bool ffn_gemv_fits(const Dims& d);
 cudaError_t launch_ffn_gemv(const Dims& d, const void* dbuf, long long meta_off,
                             const int32_t* expert_offsets, const int32_t* expert_rows,
                             const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                            const WsLayout& wl, cudaStream_t st);
+                            const WsLayout& wl, cudaStream_t st, bool clear);
 // Whether launch_ffn performs the combine itself for this shape.
 inline bool ffn_fuses_combine(const Dims& d, const WsLayout& wl) {
     return wl.tc && d.cfmt == MOE_MSG_INT8;
@@ -212,15 +238,16 @@ inline cudaError_t launch_ffn(const Dims& d, const void* dbuf, long long meta_of
                               const int32_t* expert_offsets, const int32_t* expert_rows,
                               const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
                               const WsLayout& wl, cudaStream_t st,
-                              const FusedCombine& fc = FusedCombine{nullptr, nullptr}) {
+                              const FusedCombine& fc = FusedCombine{nullptr, nullptr},
+                              bool clear = true) {
     if (!wl.tc)
         return launch_ffn_simt(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf, scale_off, ws,
-                               wl, st);
+                               wl, st, clear);
     if (fc.out == nullptr && ffn_gemv_fits(d))
         return launch_ffn_gemv(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf, scale_off, ws,
-                               wl, st);
+                               wl, st, clear);
     return launch_ffn_tc(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf, scale_off, ws, wl,
-                         st, fc);
+                         st, fc, clear);
 }
 
 }  // namespace moe

@@ -20,19 +20,23 @@ class LayerBuffers:
         self.layout = L = B.moe_query_layout(shape)
         T, k = shape.T, shape.k
         dev = torch.device(device)
-        self.dispatch = torch.empty(L["dispatch_bytes"], dtype=torch.uint8, device=dev)
-        self.combine = torch.empty(L["combine_bytes"], dtype=torch.uint8, device=dev)
-        self.workspace = torch.empty(max(256, L["workspace_bytes"]), dtype=torch.uint8, device=dev)
+        a = self._alloc
+        self.dispatch = a((L["dispatch_bytes"],), torch.uint8, dev)
+        self.combine = a((L["combine_bytes"],), torch.uint8, dev)
+        self.workspace = a((max(256, L["workspace_bytes"]),), torch.uint8, dev)
         self.routing = dict(
-            topk_idx=torch.empty((T, k), dtype=torch.int32, device=dev),
-            topk_w=torch.empty((T, k), dtype=torch.float32, device=dev),
-            phys_idx=torch.empty((T, k), dtype=torch.int32, device=dev),
-            expert_counts=torch.empty(shape.E_phys, dtype=torch.int32, device=dev),
-            rank_counts=torch.empty((shape.n_ranks, shape.n_src_ranks), dtype=torch.int32, device=dev),
-            expert_offsets=torch.empty(shape.E_phys + 1, dtype=torch.int32, device=dev),
-            expert_rows=torch.empty(T * k, dtype=torch.int32, device=dev),
+            topk_idx=a((T, k), torch.int32, dev),
+            topk_w=a((T, k), torch.float32, dev),
+            phys_idx=a((T, k), torch.int32, dev),
+            expert_counts=a((shape.E_phys,), torch.int32, dev),
+            rank_counts=a((shape.n_ranks, shape.n_src_ranks), torch.int32, dev),
+            expert_offsets=a((shape.E_phys + 1,), torch.int32, dev),
+            expert_rows=a((T * k,), torch.int32, dev),
         )
-        self.out = torch.empty((T, shape.H), dtype=torch.bfloat16, device=dev)
+        self.out = a((T, shape.H), torch.bfloat16, dev)
+
+    def _alloc(self, shape, dtype, device) -> torch.Tensor:
+        return torch.empty(shape, dtype=dtype, device=device)
 
     # views into the static buffers
     def dispatch_rows(self) -> torch.Tensor:
@@ -66,11 +70,11 @@ class MoELayer:
     layer's output buffer)."""
 
     def __init__(self, shape: Shape, w_gate_up, s_gate_up, w_down, s_down, rep_table=None,
-                 n_copies=None, phys_to_weight=None, device="cuda"):
+                 n_copies=None, phys_to_weight=None, device="cuda", buffers: LayerBuffers | None = None):
         self.shape = shape
         self.w = (w_gate_up, s_gate_up, w_down, s_down)
         self.rep_table, self.n_copies, self.phys_to_weight = rep_table, n_copies, phys_to_weight
-        self.buf = LayerBuffers(shape, device)
+        self.buf = buffers if buffers is not None else LayerBuffers(shape, device)
 
     def forward(self, logits: torch.Tensor, x: torch.Tensor, stream=None) -> torch.Tensor:
         b = self.buf
@@ -78,6 +82,22 @@ class MoELayer:
                     b.out, rep_table=self.rep_table, n_copies=self.n_copies,
                     phys_to_weight=self.phys_to_weight, stream=stream)
         return b.out
+
+    def forward_host(self, h_logits: torch.Tensor, h_x: torch.Tensor, h_out: torch.Tensor,
+                     stream=None) -> None:
+        """Host to host through moe_layer_host: h_logits f32 [T, E_log], h_x and
+        h_out 16-bit [T, H] CPU tensors (page-locked for asynchronous copies).
+        h_out holds the output once `stream` has passed this call."""
+        b = self.buf
+        if not hasattr(self, "_stage"):
+            s = self.shape
+            dev = b.out.device
+            self._stage = (torch.empty((s.T, s.E_log), dtype=torch.float32, device=dev),
+                           torch.empty((s.T, s.H), dtype=torch.int16, device=dev))
+        d_lg, d_x = self._stage
+        B.moe_layer_host(self.shape, h_logits, h_x, h_out, d_lg, d_x, *self.w, b.routing, b.dispatch,
+                         b.combine, b.workspace, b.out, rep_table=self.rep_table,
+                         n_copies=self.n_copies, phys_to_weight=self.phys_to_weight, stream=stream)
 
 
 class GraphedLayer:

@@ -33,8 +33,27 @@
  *     misaligned buffer) or MOE_ERR_WORKSPACE (a buffer smaller than
  *     moe_query_layout reports) and enqueues nothing.
  *   - MOE_ERR_CUDA means a launch failed; the stream may hold part of the
- *     work.  MOE_ERR_CAPACITY is reserved: the static buffers are sized for
- *     the worst case, so no valid input can overflow them.
+ *     work.
+ *   - Device-side checks.  Every index the kernels take from a caller's
+ *     device array (physical expert ids, replica-table entries, row lists,
+ *     offsets, message metadata, weight-set ids) is checked against its
+ *     range before it addresses memory.  A bad index never leads to an
+ *     access outside the caller's buffers: the access is skipped (or made
+ *     on an in-range element whose result is meaningless) and a code is
+ *     posted to the device status word at the start of the workspace,
+ *     read with moe_device_status:
+ *       MOE_ERR_INDEX     an index outside its range (the outputs of that
+ *                         call are unspecified);
+ *       MOE_ERR_CAPACITY  a (destination, source) pair received more than
+ *                         max_tokens messages, which only a replica table
+ *                         that maps two routes of one token onto one
+ *                         physical expert can cause (the extra messages are
+ *                         dropped);
+ *       MOE_ERR_TIMEOUT   a bounded device wait gave up.
+ *     The first code posted stays.  Each entry point that takes a
+ *     workspace clears the word when its work starts on the stream
+ *     (moe_layer once, for the whole layer), so the word describes the most
+ *     recent such call.
  *   - Device buffers passed as `void*` must be 256-byte aligned.
  *   - All integer outputs (indices, counts, offsets, slots, INT8 codes, int32
  *     accumulators) are deterministic and bit-exact with respect to the
@@ -60,7 +79,8 @@ typedef enum {
     MOE_ERR_CAPACITY = 3,
     MOE_ERR_CUDA = 4,
     MOE_ERR_TIMEOUT = 5,
-    MOE_ERR_UNSUPPORTED = 6
+    MOE_ERR_UNSUPPORTED = 6,
+    MOE_ERR_INDEX = 7
 } moe_status;
 
 /* Message formats ([X] P041/P089: INT8 halves message bytes; bf16 is the
@@ -180,7 +200,8 @@ moe_status moe_eplb_collect(int32_t E_log, int32_t E_phys, const int32_t* expert
 /* Gate top-k ([X] P038) with renormalised softmax weights and the EPLB map
  * ([X] P078-P079), plus per-physical-expert counts (the Collect kernel of
  * [X] P068).
- *   logits (device) f32 [T][E_log], finite.
+ *   logits (device) f32 [T][E_log], finite.  A NaN logit is read as -inf, so
+ *   that the indices stay valid (the weights of such a row are unspecified).
  *   Selection: logit descending, ties to the lower expert id; topk_idx[t][j]
  *   (device, int32 [T][k]) is the j-th selected logical expert (route_slot j).
  *   topk_w[t][j] (device, f32 [T][k]) = e^(l_j - l_0) / sum_i e^(l_i - l_0)
@@ -188,8 +209,14 @@ moe_status moe_eplb_collect(int32_t E_log, int32_t E_phys, const int32_t* expert
  *   rep_table (device, nullable) int32 [E_log][max_copies], n_copies (device)
  *   int32 [E_log]: phys_idx[t][j] = rep_table[e][t mod n_copies[e]] for
  *   e = topk_idx[t][j]; with rep_table NULL, phys_idx = topk_idx and
- *   E_phys must equal E_log.
- *   expert_counts (device) int32 [E_phys]: messages per physical expert.
+ *   E_phys must equal E_log.  The table must list, for each logical expert
+ *   e, n_copies[e] in [1, max_copies] distinct physical slots that hold e;
+ *   an entry outside [0, E_phys) or a copy count outside [1, max_copies]
+ *   gives phys_idx = -1 for that route (not counted), which moe_dispatch
+ *   then reports as MOE_ERR_INDEX.
+ *   expert_counts (device) int32 [E_phys]: messages per physical expert,
+ *   counted without atomics (per-warp histograms summed across one thread
+ *   block cluster).
  * No workspace is used. */
 moe_status moe_route(const moe_shape* shape, const float* logits, const int32_t* rep_table,
                      const int32_t* n_copies, int32_t max_copies, int32_t* topk_idx,
@@ -209,7 +236,9 @@ moe_status moe_route(const moe_shape* shape, const float* logits, const int32_t*
  *   per physical expert; expert_rows (device) int32 [T*k]: for each expert,
  *   the slot ids g of its messages in ascending token order (the expert's
  *   gathered input rows, [C] assemble_expert_inputs).
- *   Slots not written keep their previous contents.  Uses the workspace. */
+ *   Slots not written keep their previous contents.  Uses the workspace.
+ *   A phys_idx entry outside [0, E_phys) drops that message (MOE_ERR_INDEX
+ *   in the status word). */
 moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, const int32_t* phys_idx,
                         void* dispatch_buf, int64_t dispatch_bytes, int32_t* rank_counts,
                         int32_t* expert_offsets, int32_t* expert_rows, void* workspace,
@@ -237,8 +266,11 @@ typedef struct {
  * codes q, scale s):
  *   acc_g[i] = sum_h q[h] Wg[i][h], acc_u[i] = sum_h q[h] Wu[i][h]  (exact int32)
  *   g = (acc_g * s) * sg[i], u = (acc_u * s) * su[i]   (binary32, two roundings)
- *   h = g / (1 + e(-g)) * u, e the binary32 exp specification (Cody-Waite
- *       reduction, degree-7 Taylor polynomial, see the design notes)
+ *   h = g / (1 + e(-g)) * u, e the binary32 exp specification: n =
+ *       rint(x * RN(1/ln2)), r = (x - n*LN2_HI) - n*LN2_LO with ln 2 split
+ *       into a 14-bit head and a tail, e^r by the degree-7 Taylor polynomial
+ *       in Horner form, times 2^n; one rounding per operation, no fused
+ *       multiply-add; +inf above x = 88, 0 below x = -87
  *   hq, s_h = token-wise INT8 quantisation of h (as in moe_dispatch)
  *   acc_d[c] = sum_i hq[i] Wd[c][i] (exact int32), y = (acc_d * s_h) * sd[c]
  *   return message at combine row (t, j), t = src_rank*lb + batch_slot,
@@ -302,6 +334,27 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t
                      void* dispatch_buf, int64_t dispatch_bytes, void* combine_buf,
                      int64_t combine_bytes, void* workspace, int64_t workspace_bytes,
                      uint16_t* out, moe_stream_t stream);
+
+/* The whole layer from host memory to host memory: on `stream`, copies
+ * h_logits (host, f32 [T][E_log]) into d_logits (device, same shape) and h_x
+ * (host, bf16 [T][H]) into d_x (device), runs moe_layer on them with the
+ * other arguments as moe_layer takes them, and copies the output d_out
+ * (device, bf16 [T][H]) back into h_out (host).  One cudaMemcpyAsync per
+ * copy; nothing is allocated and the stream is not synchronised: h_out holds
+ * the result once `stream` has reached that point.  Host buffers should be
+ * page-locked (cudaHostAlloc or cudaHostRegister), or the copies may block
+ * the calling thread.  A serving loop overlaps one step's copies with
+ * another step's kernels by alternating two streams and two sets of device
+ * buffers (the host input may be shared; each set needs its own h_out).
+ * Argument errors are those of moe_layer plus null or misaligned (16-byte)
+ * d_logits / d_x / host pointers. */
+moe_status moe_layer_host(const moe_shape* shape, const float* h_logits, const uint16_t* h_x,
+                          uint16_t* h_out, float* d_logits, uint16_t* d_x, const int32_t* rep_table,
+                          const int32_t* n_copies, int32_t max_copies,
+                          const moe_expert_weights* weights, const moe_routing* routing,
+                          void* dispatch_buf, int64_t dispatch_bytes, void* combine_buf,
+                          int64_t combine_bytes, void* workspace, int64_t workspace_bytes,
+                          uint16_t* d_out, moe_stream_t stream);
 
 /* The decode layer as a CUDA graph ([C] "EP320：token 去找专家": the static
  * dispatch/combine buffers are allocated once, reused by every decode step
@@ -406,9 +459,10 @@ moe_status moe_dispatch_noalloc(const moe_shape* shape, const uint16_t* x, const
 int64_t moe_dispatch_noalloc_max_scratch(void);
 
 /* Reads the device status word that the library's kernels keep at the start
- * of `workspace` (device): MOE_OK, or MOE_ERR_TIMEOUT if a bounded device
- * wait gave up during the last moe_expert_ffn / moe_layer /
- * moe_grouped_gemm_s8 call that used this workspace.  Synchronises `stream`. */
+ * of `workspace` (device): MOE_OK, or the first code a device-side check
+ * posted (MOE_ERR_INDEX, MOE_ERR_CAPACITY, MOE_ERR_TIMEOUT; see the
+ * conventions at the top) during the most recent call that used this
+ * workspace.  Synchronises `stream`. */
 moe_status moe_device_status(const void* workspace, int32_t* status, moe_stream_t stream);
 
 /* Text of the CUDA error behind the last MOE_ERR_CUDA returned on the

@@ -103,6 +103,8 @@ def _declare(lib):
     lib.orc_combine.restype = i32
     lib.orc_num_threads.argtypes = []
     lib.orc_num_threads.restype = i32
+    lib.orc_set_num_threads.argtypes = [i32]
+    lib.orc_set_num_threads.restype = None
 
 
 def _p(a):
@@ -114,6 +116,11 @@ def _p(a):
 
 def num_threads() -> int:
     return _load().orc_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops (results do not depend on it)."""
+    _load().orc_set_num_threads(int(n))
 
 
 # ------------------------------------------------------------------ scalars

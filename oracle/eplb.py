@@ -12,7 +12,7 @@ Follows "xDeepServe on CloudMatrix384", section "专家负载均衡":
              free redundant slot, adding the replica's share to that rank;
   P078-P079  forward-time map physical(i, e) = R_e[i mod |R_e|].
 
-Readings where the page is silent (also listed in the design notes):
+Readings where the page is silent:
   - ties: lower expert id / lower rank id win;
   - a replica's share is total_load[e] / (number of instances of e), and a
     rank's starting load is the sum of the shares of its primary experts;

@@ -445,3 +445,15 @@ int orc_num_threads(void)
     return 1;
 #endif
 }
+
+/* Threads the parallel loops above use from now on (n >= 1); the timed
+ * single-thread baseline sets 1.  No effect on any result: every parallel
+ * loop writes disjoint rows. */
+void orc_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

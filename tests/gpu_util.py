@@ -55,9 +55,45 @@ def compare_bf16(got_bits: np.ndarray, ref_bits: np.ndarray):
     return max_abs, rel
 
 
-def make_layer(w: synth.Workload, cfmt=B.MOE_MSG_INT8, device="cuda"):
+CANARY_BYTES = 4096
+CANARY = 0xA5
+
+
+def _guarded(nbytes: int, dtype, shape, device, tails: list):
+    """A caller buffer of `nbytes` followed by CANARY_BYTES of the canary byte
+    (a separate allocation per buffer, so its start keeps torch's alignment);
+    the tail view goes to `tails`."""
+    raw = torch.empty(nbytes + CANARY_BYTES, dtype=torch.uint8, device=device)
+    raw[nbytes:].fill_(CANARY)
+    tails.append(raw[nbytes:])
+    return raw[:nbytes].view(dtype).view(shape)
+
+
+class CanaryBuffers(LayerBuffers):
+    """LayerBuffers in which every buffer the library writes (dispatch,
+    combine, workspace, output, routing arrays) is followed by canary bytes;
+    check() asserts that no kernel wrote past the end of any of them."""
+
+    def __init__(self, shape, device="cuda"):
+        dev = torch.device(device)
+        self.tails = []
+        self._dev = dev
+        super().__init__(shape, device)
+
+    def _alloc(self, shape, dtype, device):
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        return _guarded(n, dtype, shape, self._dev, self.tails)
+
+    def check(self):
+        torch.cuda.synchronize()
+        for t in self.tails:
+            assert bool((t == CANARY).all()), "a kernel wrote past the end of a caller buffer"
+
+
+def make_layer(w: synth.Workload, cfmt=B.MOE_MSG_INT8, device="cuda", canary=True):
     """MoELayer with the workload's weights resident on the device (plus the
-    EPLB map for replicated workloads)."""
+    EPLB map for replicated workloads); with `canary` its buffers carry
+    canary tails (CanaryBuffers)."""
     shape = shape_of(w, B.MOE_MSG_INT8, cfmt)
     w_gu, s_gu, w_d, s_d = synth.all_weights_torch(w, device)
     rep = nc = p2l = None
@@ -65,8 +101,8 @@ def make_layer(w: synth.Workload, cfmt=B.MOE_MSG_INT8, device="cuda"):
         r, n, p = eplb_map(w)
         rep, nc, p2l = (torch.from_numpy(a).to(device) for a in (r, n, p))
     return MoELayer(shape, w_gu, s_gu, w_d, s_d, rep_table=rep, n_copies=nc, phys_to_weight=p2l,
-                    device=device)
+                    device=device, buffers=CanaryBuffers(shape, device) if canary else None)
 
 
 __all__ = ["lib", "shape_of", "bits_to_bf16_tensor", "bf16_tensor_to_bits", "compare_bf16",
-           "make_layer", "eplb_map", "LayerBuffers", "MAX_ABS", "REL_L2"]
+           "make_layer", "eplb_map", "LayerBuffers", "CanaryBuffers", "MAX_ABS", "REL_L2"]

@@ -43,6 +43,9 @@ def test_header_symbols_exported(lib):
 def test_status_strings(lib):
     assert B.moe_status_string(0) == "ok"
     assert "invalid" in B.moe_status_string(1)
+    assert "index" in B.moe_status_string(B.MOE_ERR_INDEX)
+    for code, text in B.STATUS.items():
+        assert B.moe_status_string(code) != "unknown status", code
     assert B.moe_status_string(99) == "unknown status"
 
 

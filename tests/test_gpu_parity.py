@@ -114,6 +114,7 @@ def _full_layer_check(w, cfmt, xb=None):
     max_abs, rel = compare_bf16(bf16_tensor_to_bits(out), ref["out"])
     assert max_abs <= MAX_ABS and rel <= REL_L2, (max_abs, rel)
     assert B.moe_device_status(b.workspace) == 0
+    b.check()  # no kernel wrote past any caller buffer
 
 
 @pytest.mark.parametrize("cfmt", [B.MOE_MSG_INT8, B.MOE_MSG_BF16])
