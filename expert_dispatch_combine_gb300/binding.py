@@ -61,7 +61,7 @@ EXPORTED = ("moe_status_string", "moe_static_buffer_bytes", "moe_query_layout", 
             "moe_dispatch_noalloc", "moe_dispatch_noalloc_max_scratch", "moe_layer_graph_create",
             "moe_graph_launch", "moe_graph_destroy", "moe_eplb_collect", "moe_expert_ffn_combine",
             "moe_trampoline_bytes", "moe_dispatch_trampoline", "moe_expert_ffn_path",
-            "moe_layer_host")
+            "moe_layer_host", "moe_expert_ffn_combine_ex")
 
 _lib = None
 
@@ -111,6 +111,8 @@ def load(path: str = LIB_PATH):
         "moe_dispatch_trampoline": ([PS, P, P, P, i64, P, i64, P, P, P, P, i64, P], ctypes.c_int),
         "moe_expert_ffn_combine": ([PS, P, i64, P, P, ctypes.POINTER(moe_expert_weights), P, P, i64,
                                     P, P, i64, P], ctypes.c_int),
+        "moe_expert_ffn_combine_ex": ([PS, P, i64, P, P, ctypes.POINTER(moe_expert_weights), P, P, i64,
+                                       P, P, i64, i32, i64, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -291,6 +293,18 @@ def moe_expert_ffn_combine(shape: Shape, dispatch_buf, expert_offsets, expert_ro
         ctypes.byref(cs), _ptr(dispatch_buf), dispatch_buf.numel(), _ptr(expert_offsets),
         _ptr(expert_rows), ctypes.byref(w), _ptr(topk_w), _ptr(combine_buf), combine_buf.numel(),
         _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def moe_expert_ffn_combine_ex(shape: Shape, dispatch_buf, expert_offsets, expert_rows, w_gate_up,
+                              s_gate_up, w_down, s_down, topk_w, combine_buf, out, workspace,
+                              expected: int, wait_ns: int, phys_to_weight=None, stream=None):
+    """moe_expert_ffn_combine with the combine's wait target and bound given."""
+    cs = shape.c()
+    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight)
+    _check("moe_expert_ffn_combine_ex", load().moe_expert_ffn_combine_ex(
+        ctypes.byref(cs), _ptr(dispatch_buf), dispatch_buf.numel(), _ptr(expert_offsets),
+        _ptr(expert_rows), ctypes.byref(w), _ptr(topk_w), _ptr(combine_buf), combine_buf.numel(),
+        _ptr(out), _ptr(workspace), workspace.numel(), int(expected), int(wait_ns), _stream(stream)))
 
 
 def moe_combine(shape: Shape, combine_buf, topk_w, out, stream=None):

@@ -27,6 +27,9 @@ namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Bound of each token's wait in moe_expert_ffn_combine (2 s).
+constexpr int64_t kCombineWaitNs = 2000000000LL;
+
 moe_status check_shape(const moe_shape* s) {
     if (!s) return MOE_ERR_INVALID_ARG;
     if (s->T < 1 || s->H < 16 || s->H > 16384 || s->H % 16) return MOE_ERR_INVALID_ARG;
@@ -216,12 +219,12 @@ moe_status moe_expert_ffn(const moe_shape* shape, const void* dispatch_buf,
                                   workspace, make_ws(d), (cudaStream_t)stream));
 }
 
-moe_status moe_expert_ffn_combine(const moe_shape* shape, const void* dispatch_buf,
-                                  int64_t dispatch_bytes, const int32_t* expert_offsets,
-                                  const int32_t* expert_rows, const moe_expert_weights* weights,
-                                  const float* topk_w, void* combine_buf, int64_t combine_bytes,
-                                  uint16_t* out, void* workspace, int64_t workspace_bytes,
-                                  moe_stream_t stream) {
+moe_status moe_expert_ffn_combine_ex(const moe_shape* shape, const void* dispatch_buf,
+                                     int64_t dispatch_bytes, const int32_t* expert_offsets,
+                                     const int32_t* expert_rows, const moe_expert_weights* weights,
+                                     const float* topk_w, void* combine_buf, int64_t combine_bytes,
+                                     uint16_t* out, void* workspace, int64_t workspace_bytes,
+                                     int32_t expected, int64_t wait_ns, moe_stream_t stream) {
     moe_status st = check_shape(shape);
     if (st != MOE_OK) return st;
     if (shape->dispatch_fmt != MOE_MSG_INT8) return MOE_ERR_UNSUPPORTED;
@@ -231,6 +234,7 @@ moe_status moe_expert_ffn_combine(const moe_shape* shape, const void* dispatch_b
     if (!aligned(dispatch_buf, 256) || !aligned(combine_buf, 256) || !aligned(workspace, 256) ||
         !aligned(out, 16))
         return MOE_ERR_INVALID_ARG;
+    if (expected < 1 || wait_ns < 1) return MOE_ERR_INVALID_ARG;
     Dims d = make_dims(*shape);
     const WsLayout wl = make_ws(d);
     if (!ffn_fuses_combine(d, wl)) return MOE_ERR_UNSUPPORTED;
@@ -240,9 +244,22 @@ moe_status moe_expert_ffn_combine(const moe_shape* shape, const void* dispatch_b
     if (dispatch_bytes < L.dispatch_bytes || combine_bytes < L.combine_bytes ||
         workspace_bytes < L.workspace_bytes)
         return MOE_ERR_WORKSPACE;
+    FusedCombine fc{topk_w, out, expected, (unsigned long long)wait_ns};
     return cuda_status(launch_ffn(d, dispatch_buf, L.dispatch_meta_offset, expert_offsets,
                                   expert_rows, *weights, combine_buf, L.combine_scale_offset,
-                                  workspace, wl, (cudaStream_t)stream, FusedCombine{topk_w, out}));
+                                  workspace, wl, (cudaStream_t)stream, fc));
+}
+
+moe_status moe_expert_ffn_combine(const moe_shape* shape, const void* dispatch_buf,
+                                  int64_t dispatch_bytes, const int32_t* expert_offsets,
+                                  const int32_t* expert_rows, const moe_expert_weights* weights,
+                                  const float* topk_w, void* combine_buf, int64_t combine_bytes,
+                                  uint16_t* out, void* workspace, int64_t workspace_bytes,
+                                  moe_stream_t stream) {
+    if (!shape) return MOE_ERR_INVALID_ARG;
+    return moe_expert_ffn_combine_ex(shape, dispatch_buf, dispatch_bytes, expert_offsets, expert_rows,
+                                     weights, topk_w, combine_buf, combine_bytes, out, workspace,
+                                     workspace_bytes, shape->k, kCombineWaitNs, stream);
 }
 
 moe_status moe_combine(const moe_shape* shape, const void* combine_buf, int64_t combine_bytes,

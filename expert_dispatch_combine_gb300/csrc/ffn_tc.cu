@@ -9,10 +9,17 @@
 // (assemble_expert_inputs, run_local_experts, remote_write_combine).
 //
 // sm_103a has no integer tcgen05.mma, so the int8 contraction runs on
-// kind::f16: every int8 value is exact in fp16, every product (|p| <= 16129)
-// is exact in fp32, and the fp32 accumulator is drained to int32 every 1024
-// K (1024 * 16129 < 2^24, so every partial sum is an exact integer).  The
-// int32 results equal the integer matrix product bit for bit.
+// kind::f16: every int8 value is exact in fp16, every product is exact in
+// fp32, and the fp32 accumulator is drained to int32 at the end of each
+// chunk of K, added in int32.  A chunk is exact when every partial sum is an
+// integer below 2^24 in magnitude: always for chunks of 1024 K (1024 * 128 *
+// 128 = 2^24), and for longer chunks whenever every row's codes satisfy
+// sum_{k in chunk} |a_k| * 128 < 2^24 (|w| <= 128 for int8 weights).  The
+// kernel that writes the activation rows (assemble for the gate/up GEMM,
+// requant for the down GEMM) posts, per launch, the longest chunk plan that
+// holds for all of its rows (chunk_level); the GEMM drains at that plan's
+// boundaries.  The int32 results equal the integer matrix product bit for
+// bit for every plan.
 //
 // GEMM structure (one CTA per SM, persistent over tiles):
 //   D^T[channel][token] = W[channel][:] . X[token][:]
@@ -58,7 +65,9 @@ namespace tc {
 
 constexpr int BK = 64;                           // K per stage
 constexpr int CK = 16;                           // stages per exact chunk (1024 K)
-constexpr int CKP = CK / 2;                      // stage pairs per exact chunk
+constexpr int CKP = CK / 2;                      // stage pairs per chunk exact for any data
+constexpr int kChunkLevels = 3;                  // plans 0..2: K in 1, 2, 4 chunks; 3: CKP-pair chunks
+constexpr int kL1Bound = 131071;                 // floor((2^24 - 1) / 128)
 constexpr int BOX_ROWS = 32;                     // token rows per activation TMA box
 constexpr int BOX_BYTES = BOX_ROWS * BK * 2;     // 4 KB
 constexpr int A_BYTES = 128 * BK;                // 8 KB int8 weights per stage
@@ -126,8 +135,16 @@ struct Params {
     int k, lb, S;
     long long nslots;            // EPI_BF16MSG: dispatch slots (range of expert_rows entries)
     int tma_out;                 // epilogue may use tensor stores for full groups
+    const unsigned* chunk_level; // chunk plan of the activation rows (null: 1024-K chunks)
     int* err;
 };
+
+// Stage pairs per exact chunk under plan `level` for a reduction of ksp pairs:
+// plan l < kChunkLevels splits K into 2^l chunks, the last plan uses chunks of
+// CKP pairs (1024 K), which are exact for any int8 data.
+__host__ __device__ __forceinline__ int chunk_pairs(int level, int ksp) {
+    return level >= kChunkLevels ? CKP : (ksp + (1 << level) - 1) >> level;
+}
 
 struct TileInfo {
     int set, r0, nvalid, nmma, mb;
@@ -471,7 +488,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     // K stages in pairs; an odd count gets one more stage entirely beyond K,
     // which TMA fills with zeros (it adds nothing to the sums)
     const int KSP = (P.K / BK + 1) / 2;
-    const int nchunks = (2 * KSP + CK - 1) / CK;
+    // chunk plan of this launch (written by the kernel that produced the rows)
+    const int level = P.chunk_level ? min(kChunkLevels, (int)*reinterpret_cast<const volatile unsigned*>(P.chunk_level))
+                                    : kChunkLevels;
+    const int ckp = chunk_pairs(level, KSP);
+    const int nchunks = (KSP + ckp - 1) / ckp;
     const int wgi = warp >> 2;
 
     if (wgi == 0) {
@@ -534,8 +555,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 e_next = tile_entry(P, tile + gridDim.x, total_tiles);
                 const uint32_t idesc = ptx::idesc_f16_f32(128, ti.nmma);
                 for (int kp = 0; kp < KSP; ++kp, ++pr) {
-                    const bool first = (kp % CKP) == 0;
-                    const bool last = (kp % CKP) == CKP - 1 || kp == KSP - 1;
+                    const bool first = (kp % ckp) == 0;
+                    const bool last = (kp % ckp) == ckp - 1 || kp == KSP - 1;
                     const uint32_t b = q & 1;
                     if (first) {
                         // the drains must have taken this buffer's previous chunk
@@ -715,14 +736,52 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
 }
 
 // ------------------------------------------------------------ helpers
+constexpr int kMaxPlanPairs = 128;  // stage pairs a row's chunk plan is computed for (K <= 16384)
+
+// sum |q| over 16 int8 codes (four words), exact (|q| <= 128).
+__device__ __forceinline__ unsigned abs_sum16(const uint4& w) {
+    unsigned s = __dp4a(__vabsdiffs4(w.x, 0u), 0x01010101u, 0u);
+    s = __dp4a(__vabsdiffs4(w.y, 0u), 0x01010101u, s);
+    s = __dp4a(__vabsdiffs4(w.z, 0u), 0x01010101u, s);
+    return __dp4a(__vabsdiffs4(w.w, 0u), 0x01010101u, s);
+}
+
+// The lowest chunk plan under which every chunk of this row satisfies
+// sum |a_k| <= kL1Bound (s_pair[p]: sum |a_k| over stage pair p), posted to
+// *level by atomic max, so the launch takes the plan that holds for all of
+// its rows.  Plans whose chunks are at most CKP pairs long need no check.
+__device__ __forceinline__ void post_chunk_level(const int* s_pair, int ksp, unsigned* level) {
+    int lvl = kChunkLevels;
+    for (int l = 0; l < kChunkLevels; ++l) {
+        const int ckp = chunk_pairs(l, ksp);
+        bool ok = ckp <= CKP;
+        if (!ok) {
+            ok = true;
+            for (int c0 = 0; ok && c0 < ksp; c0 += ckp) {
+                int sum = 0;
+                for (int p = c0; p < min(ksp, c0 + ckp); ++p) sum += s_pair[p];
+                ok = sum <= kL1Bound;
+            }
+        }
+        if (ok) {
+            lvl = l;
+            break;
+        }
+    }
+    if (lvl > 0) atomicMax(level, (unsigned)lvl);
+}
+
 // Gather rows (optionally through row_index) of an int8 matrix and convert
-// them to fp16 (exact); optionally copy the dispatch scale of each row.
+// them to fp16 (exact); optionally copy the dispatch scale of each row; with
+// a non-null `level` (K <= 16384), post the row's chunk plan.
 // A row-list entry outside [0, a_rows) gives a zero row (and scale) and
 // posts MOE_ERR_INDEX.
 __global__ void __launch_bounds__(128)
 assemble_kernel(int K, const int32_t* __restrict__ row_index, long long a_rows,
                 const int8_t* __restrict__ A, long long lda, const moe_dispatch_meta* __restrict__ meta,
-                __half* __restrict__ out, float* __restrict__ s_row, int* __restrict__ err) {
+                __half* __restrict__ out, float* __restrict__ s_row, unsigned* __restrict__ level,
+                int* __restrict__ err) {
+    __shared__ int s_pair[kMaxPlanPairs];
     const int r = blockIdx.x;
     const long long g = row_index ? row_index[r] : r;
     uint4* dst = reinterpret_cast<uint4*>(out + (long long)r * K);
@@ -736,6 +795,12 @@ assemble_kernel(int K, const int32_t* __restrict__ row_index, long long a_rows,
         return;
     }
     const uint4* src = reinterpret_cast<const uint4*>(A + g * lda);
+    const int ksp = (K / BK + 1) / 2;
+    const bool plan = level != nullptr && ksp <= kMaxPlanPairs;
+    if (plan) {
+        for (int p = threadIdx.x; p < ksp; p += blockDim.x) s_pair[p] = 0;
+        __syncthreads();
+    }
     // four 16-byte loads of the row in flight per thread before converting
     for (int c0 = threadIdx.x; c0 < nch; c0 += 4 * blockDim.x) {
         uint4 w[4];
@@ -755,10 +820,15 @@ assemble_kernel(int K, const int32_t* __restrict__ row_index, long long a_rows,
                 s8x4_to_f16x4(w[u].w, o1.z, o1.w);
                 dst[2 * c] = o0;
                 dst[2 * c + 1] = o1;
+                if (plan) atomicAdd(&s_pair[c >> 3], (int)abs_sum16(w[u]));  // 8 chunks of 16 per pair
             }
         }
     }
     if (meta && threadIdx.x == 0) s_row[r] = meta[g].scale;
+    if (plan) {
+        __syncthreads();
+        if (threadIdx.x == 0) post_chunk_level(s_pair, ksp, level);
+    }
 }
 
 template <int NT>
@@ -799,8 +869,15 @@ __device__ __forceinline__ void load_chunk16(const float4* __restrict__ src, int
 // reduced by the gate/up GEMM's epilogue): hq as exact fp16 integers, s_h.
 __global__ void __launch_bounds__(kRowMaxThreads)
 requant_kernel(int I, const float* __restrict__ h, const unsigned* __restrict__ rowmax,
-               __half* __restrict__ hq, float* __restrict__ sh) {
+               __half* __restrict__ hq, float* __restrict__ sh, unsigned* __restrict__ level) {
+    __shared__ int s_pair[kMaxPlanPairs];
     const int r = blockIdx.x;
+    const int ksp = (I / BK + 1) / 2;
+    const bool plan = level != nullptr && ksp <= kMaxPlanPairs;
+    if (plan) {
+        for (int p = threadIdx.x; p < ksp; p += blockDim.x) s_pair[p] = 0;
+        __syncthreads();
+    }
     const int nch = I / 16;
     const float4* src = reinterpret_cast<const float4*>(h + (long long)r * I);
     uint4* dst = reinterpret_cast<uint4*>(hq + (long long)r * I);
@@ -830,46 +907,46 @@ requant_kernel(int I, const float* __restrict__ h, const unsigned* __restrict__ 
             for (int i = 0; i < 8; ++i) o[i] = codes_to_f16x2(q[2 * i], q[2 * i + 1]);
             dst[2 * c] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+            if (plan) {
+                int l1 = 0;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) l1 += abs(q[e]);
+                atomicAdd(&s_pair[c >> 3], l1);  // 8 chunks of 16 per pair
+            }
         }
     }
     if (threadIdx.x == 0) sh[r] = row_scale(__uint_as_float(rowmax[r]));
+    if (plan) {
+        __syncthreads();
+        if (threadIdx.x == 0) post_chunk_level(s_pair, ksp, level);
+    }
 }
 
-// INT8 return message: token-wise codes of y (row absmax reduced by the down
-// GEMM's epilogue) into the combine row (t, j).
-// With kFuse (moe_layer) it also performs FusedCombine as the pages' fused
-// path does: once all k contributions of token t are in ("CloudMatrix384 LLM
-// Serving", "EP320" fused_moe listing; "xDeepServe", COMBINE procedure).  Each
-// block publishes its message (stores, fence, then an atomic increment of the
-// token's readiness counter); the block that brings the counter to k reads
-// the token's k messages back through L2 and writes out[t], with the
-// arithmetic of the combine kernel.  Nothing waits: the last contributor does
-// the work.
-template <bool kFuse>
-__global__ void __launch_bounds__(kRowThreads)
-retquant_kernel(int H, int k, int lb, int S, long long nslots, long long crow,
-                const float* __restrict__ y, const unsigned* __restrict__ rowmax,
-                const int32_t* __restrict__ expert_rows, const moe_dispatch_meta* __restrict__ meta,
-                unsigned char* __restrict__ cbuf, float* __restrict__ cscale,
-                const float* __restrict__ topk_w, int* __restrict__ ready, uint16_t* __restrict__ out,
-                int* __restrict__ err) {
-    const int r = blockIdx.x;
-    const int nch = H / 16;
-    {  // the row's dispatch slot and metadata are caller data: skip a row that is out of range
-        const long long g = expert_rows[r];
-        if (g < 0 || g >= nslots || !meta_in_range(meta[g], S, lb, k)) {
-            if (threadIdx.x == 0) post_status(err, MOE_ERR_INDEX);
-            return;
-        }
+// INT8 return message of expert row r: token-wise codes of y (its row absmax
+// was reduced by the down GEMM's epilogue) into the combine row (t, j), and
+// its scale.  Returns t * k + j, or -1 (and MOE_ERR_INDEX) if the row's
+// dispatch slot or metadata is out of range.  Called by all threads of a
+// block of kRowThreads with the same r.
+__device__ __forceinline__ long long quantise_return_row(
+    int r, int H, int k, int lb, int S, long long nslots, long long crow, const float* __restrict__ y,
+    const unsigned* __restrict__ rowmax, const int32_t* __restrict__ expert_rows,
+    const moe_dispatch_meta* __restrict__ meta, unsigned char* __restrict__ cbuf,
+    float* __restrict__ cscale, int* __restrict__ err) {
+    const long long g = expert_rows[r];
+    if (g < 0 || g >= nslots || !meta_in_range(meta[g], S, lb, k)) {  // caller data out of range
+        if (threadIdx.x == 0) post_status(err, MOE_ERR_INDEX);
+        return -1;
     }
+    const int nch = H / 16;
     const float4* src = reinterpret_cast<const float4*>(y + (long long)r * H);
     const int nt = blockDim.x;
+    long long tj = 0;
     for (int c0 = threadIdx.x; c0 < nch; c0 += 2 * nt) {
         float4 v[2][4];
         load_chunk16(src, c0, nch, v[0]);
         load_chunk16(src, c0 + nt, nch, v[1]);
-        const moe_dispatch_meta m = meta[expert_rows[r]];
-        const long long tj = ((long long)m.src_rank * lb + m.batch_slot) * k + m.route_slot;
+        const moe_dispatch_meta m = meta[g];
+        tj = ((long long)m.src_rank * lb + m.batch_slot) * k + m.route_slot;
         uint4* dst = reinterpret_cast<uint4*>(cbuf + tj * crow);
         const float s = row_scale(__uint_as_float(rowmax[r]));
         const float rs = quant_rcp(s);
@@ -895,36 +972,120 @@ retquant_kernel(int H, int k, int lb, int S, long long nslots, long long crow,
             dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
-    if (threadIdx.x == 0) {
-        const moe_dispatch_meta m = meta[expert_rows[r]];
-        cscale[((long long)m.src_rank * lb + m.batch_slot) * k + m.route_slot] =
-            row_scale(__uint_as_float(rowmax[r]));
+    const moe_dispatch_meta m = meta[g];
+    tj = ((long long)m.src_rank * lb + m.batch_slot) * k + m.route_slot;
+    if (threadIdx.x == 0) cscale[tj] = row_scale(__uint_as_float(rowmax[r]));
+    return tj;
+}
+
+// INT8 return messages, one block per expert row.
+__global__ void __launch_bounds__(kRowThreads)
+retquant_kernel(int H, int k, int lb, int S, long long nslots, long long crow,
+                const float* __restrict__ y, const unsigned* __restrict__ rowmax,
+                const int32_t* __restrict__ expert_rows, const moe_dispatch_meta* __restrict__ meta,
+                unsigned char* __restrict__ cbuf, float* __restrict__ cscale, int* __restrict__ err) {
+    quantise_return_row(blockIdx.x, H, k, lb, S, nslots, crow, y, rowmax, expert_rows, meta, cbuf,
+                        cscale, err);
+}
+
+// Acquire load of a readiness counter (device scope).
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded wait until *ctr >= target: gives up (false) after limit_ns of
+// %globaltimer time, posting MOE_ERR_TIMEOUT, or at once when another thread
+// has posted any error.  Never traps.
+__device__ __forceinline__ bool wait_count(const int* ctr, int target, int* err, uint64_t limit_ns) {
+    if (ld_acquire(ctr) >= target) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(64);
+        if (ld_acquire(ctr) >= target) return true;
+        if ((it & 7) == 0) {
+            if (*reinterpret_cast<volatile int*>(err) != 0) return false;
+            if (ptx::globaltimer() - t0 > limit_ns) {
+                atomicCAS(err, 0, MOE_ERR_TIMEOUT);
+                return false;
+            }
+        }
     }
-    if constexpr (kFuse) {
-        constexpr int kMaxK = 32;
-        __shared__ int s_last;
-        __shared__ float s_w[kMaxK], s_s[kMaxK];
-        const moe_dispatch_meta m = meta[expert_rows[r]];
-        const long long t = (long long)m.src_rank * lb + m.batch_slot;
-        __threadfence();  // this thread's message stores, device-wide, before the count
+}
+
+// FusedCombine folded into the return messages, as the pages' fused path runs
+// it ("CloudMatrix384 LLM Serving", "EP320" fused_moe listing: the combine of a
+// token waits until all k contributions are in; "xDeepServe", COMBINE
+// procedure).  One persistent kernel (cooperative launch, every block
+// resident) takes work items from an atomic ticket: items 0 .. M-1 are the
+// expert rows, M .. M+T-1 the tokens.
+//   row r:    write its INT8 return message (quantise_return_row), fence,
+//             then count it in ready[t];
+//   token t:  one thread waits until ready[t] reaches `expected` (wait_count,
+//             bounded), then the block sums the k messages as the combine
+//             kernel does and writes out[t].
+// Every row item is taken before any token item, by a running block that
+// waits for nothing, so each wait ends once the rows are written; the bound
+// only catches a count that can never be reached (a lost message, or an
+// `expected` other than k), which posts MOE_ERR_TIMEOUT and skips the token.
+struct RetCombine {
+    int H, k, lb, S, expected;
+    long long M, T, nslots, crow;
+    uint64_t wait_ns;
+    const float* y;
+    const unsigned* rowmax;
+    const int32_t* expert_rows;
+    const moe_dispatch_meta* meta;
+    unsigned char* cbuf;
+    float* cscale;
+    const float* topk_w;
+    int* ready;  // [T] readiness counters, then the work ticket
+    uint16_t* out;
+    int* err;
+};
+
+__global__ void __launch_bounds__(kRowThreads) retcombine_kernel(const RetCombine P) {
+    constexpr int kMaxK = 32;
+    constexpr int kUnroll = 8;
+    __shared__ long long s_item;
+    __shared__ int s_ok;
+    __shared__ float s_w[kMaxK], s_s[kMaxK];
+    int* ticket = P.ready + P.T;
+    for (;;) {
+        if (threadIdx.x == 0) s_item = atomicAdd(ticket, 1);
         __syncthreads();
-        if (threadIdx.x == 0) s_last = atomicAdd(ready + t, 1) == k - 1;
+        const long long item = s_item;
         __syncthreads();
-        if (!s_last) return;
-        __threadfence();  // the other contributors' messages are visible from here on
-        if (threadIdx.x < k) {
-            s_w[threadIdx.x] = topk_w[t * k + threadIdx.x];
-            s_s[threadIdx.x] = __ldcg(cscale + t * k + threadIdx.x);
+        if (item >= P.M + P.T) return;
+        if (item < P.M) {
+            const long long tj = quantise_return_row((int)item, P.H, P.k, P.lb, P.S, P.nslots, P.crow,
+                                                     P.y, P.rowmax, P.expert_rows, P.meta, P.cbuf,
+                                                     P.cscale, P.err);
+            if (tj < 0) continue;
+            __threadfence();  // this thread's message stores, device-wide, before the count
+            __syncthreads();
+            if (threadIdx.x == 0) atomicAdd(P.ready + tj / P.k, 1);
+            continue;
+        }
+        const long long t = item - P.M;
+        if (threadIdx.x == 0) s_ok = wait_count(P.ready + t, P.expected, P.err, P.wait_ns);
+        __syncthreads();
+        if (!s_ok) continue;
+        __threadfence();  // the k messages are visible from here on
+        if (threadIdx.x < P.k) {
+            s_w[threadIdx.x] = P.topk_w[t * P.k + threadIdx.x];
+            s_s[threadIdx.x] = __ldcg(P.cscale + t * P.k + threadIdx.x);
         }
         __syncthreads();
-        constexpr int kUnroll = 8;
-        const unsigned char* rows = cbuf + t * k * crow;
-        uint4* orow = reinterpret_cast<uint4*>(out + t * H);
-        for (int c = threadIdx.x; c < nch; c += kRowThreads) {
+        const int k = P.k;
+        const unsigned char* rows = P.cbuf + t * k * P.crow;
+        uint4* orow = reinterpret_cast<uint4*>(P.out + t * P.H);
+        for (int c = threadIdx.x; c < P.H / 16; c += kRowThreads) {
             uint4 q[kUnroll][2];
 #pragma unroll
             for (int j = 0; j < kUnroll; ++j)
-                if (j < k) load16<true, true>(rows + j * crow, c, q[j]);
+                if (j < k) load16<true, true>(rows + j * P.crow, c, q[j]);
             float acc[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) acc[i] = 0.f;
@@ -933,7 +1094,7 @@ retquant_kernel(int H, int k, int lb, int S, long long nslots, long long crow,
                 if (j < k) accumulate16<true>(q[j], s_w[j], s_s[j], acc);
             for (int j = kUnroll; j < k; ++j) {
                 uint4 q2[2];
-                load16<true, true>(rows + j * crow, c, q2);
+                load16<true, true>(rows + j * P.crow, c, q2);
                 accumulate16<true>(q2, s_w[j], s_s[j], acc);
             }
 #pragma unroll
@@ -946,6 +1107,7 @@ retquant_kernel(int H, int k, int lb, int S, long long nslots, long long crow,
                 orow[2 * c + h] = o;
             }
         }
+        __syncthreads();  // s_w / s_s are free for the next token
     }
 }
 
@@ -1048,9 +1210,11 @@ cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long lo
     if ((e = launch_tile_prefix(n_groups, BN_LARGE, offsets, max_rows, n_groups, tp, err, st, ttab)) !=
         cudaSuccess)
         return e;
-    // the rows of A are the caller's: no bound on the row list's entries here
+    // the rows of A are the caller's: no bound on the row list's entries here;
+    // their chunk plan goes to a word of the (just cleared) status region
+    unsigned* level = ws_ptr<unsigned>(ws, 128);
     assemble_kernel<<<(unsigned)max_rows, 128, 0, st>>>(K, row_index, LLONG_MAX, A, lda, nullptr, a16,
-                                                        nullptr, err);
+                                                        nullptr, level, err);
     count_launches(1);
     CUtensorMap mw, mx[2], mo;
     const bool tma_out = N % 128 == 0;
@@ -1061,7 +1225,7 @@ cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long lo
     Params P = {};
     P.G = n_groups; P.offsets = offsets; P.tile_prefix = tp; P.ttab = ttab; P.g2s = nullptr;
     P.K = K; P.rows_per_set = N; P.nout = N; P.mb_count = (N + 127) / 128; P.box1_off = 64;
-    P.c_i32 = C; P.err = err; P.tma_out = tma_out;
+    P.c_i32 = C; P.err = err; P.tma_out = tma_out; P.chunk_level = level;
     return launch_gemm<EPI_I32, BN_LARGE>(P, mw, mx, mo, st);
 }
 
@@ -1084,6 +1248,7 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     float* hbuf = ws_ptr<float>(ws, wl.hbuf);
     unsigned* hmax = ws_ptr<unsigned>(ws, wl.rowmax);
     unsigned* ymax = hmax + M;
+    unsigned* level = hmax + 2 * M;  // chunk plans of the gate/up and down GEMMs
     __half* hq16 = ws_ptr<__half>(ws, wl.hq16);
     float* ybuf = ws_ptr<float>(ws, wl.ybuf);
     unsigned char* cb = static_cast<unsigned char*>(cbuf);
@@ -1092,12 +1257,12 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     cudaError_t e;
 
     if (clear && (e = clear_status(ws, st)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(hmax, 0, sizeof(unsigned) * 2 * M, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(hmax, 0, sizeof(unsigned) * (2 * M + 2), st)) != cudaSuccess) return e;
     count_launches(1);
     const bool fuse = fc.out != nullptr && int8_ret;
     int* ready = ws_ptr<int>(ws, wl.ready);
-    if (fuse) {
-        if ((e = cudaMemsetAsync(ready, 0, sizeof(int) * d.T, st)) != cudaSuccess) return e;
+    if (fuse) {  // readiness counters and the work ticket start at zero
+        if ((e = cudaMemsetAsync(ready, 0, sizeof(int) * (d.T + 1), st)) != cudaSuccess) return e;
         count_launches(1);
     }
     if ((e = launch_tile_prefix(d.E_phys, BNV, expert_offsets, M, E_w, tp, err, st, ttab,
@@ -1105,7 +1270,7 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
         return e;
     assemble_kernel<<<(unsigned)M, 128, 0, st>>>(d.H, expert_rows, d.nslots,
                                                  static_cast<const int8_t*>(dbuf), d.drow, meta, a16,
-                                                 s_row, err);
+                                                 s_row, level, err);
     count_launches(1);
 
     CUtensorMap mwgu, mx1[2], mo1, mwd, mx2[2], mo2;
@@ -1127,28 +1292,45 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     P1.g2s = w.phys_to_weight;
     P1.K = d.H; P1.rows_per_set = 2 * d.I; P1.nout = d.I; P1.mb_count = d.I / 64; P1.box1_off = d.I;
     P1.s_row = s_row; P1.s_ch = w.s_gate_up; P1.out_f32 = hbuf; P1.rowmax = hmax; P1.err = err;
-    P1.tma_out = 1;
+    P1.tma_out = 1; P1.chunk_level = level;
     if ((e = launch_gemm<EPI_GU, BNV>(P1, mwgu, mx1, mo1, st)) != cudaSuccess) return e;
 
-    requant_kernel<<<(unsigned)M, row_threads(d.I), 0, st>>>(d.I, hbuf, hmax, hq16, sh);
+    requant_kernel<<<(unsigned)M, row_threads(d.I), 0, st>>>(d.I, hbuf, hmax, hq16, sh, level + 1);
     count_launches(1);
 
     Params P2 = {};
     P2.G = d.E_phys; P2.offsets = expert_offsets; P2.tile_prefix = tp; P2.ttab = ttab;
     P2.g2s = w.phys_to_weight;
     P2.K = d.I; P2.rows_per_set = d.H; P2.nout = d.H; P2.mb_count = (d.H + 127) / 128; P2.box1_off = 64;
-    P2.s_row = sh; P2.s_ch = w.s_down; P2.err = err; P2.tma_out = y_tma;
+    P2.s_row = sh; P2.s_ch = w.s_down; P2.err = err; P2.tma_out = y_tma; P2.chunk_level = level + 1;
     if (int8_ret) {
         P2.out_f32 = ybuf; P2.rowmax = ymax;
         if ((e = launch_gemm<EPI_F32, BNV>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
-        if (fuse)
-            retquant_kernel<true><<<(unsigned)M, kRowThreads, 0, st>>>(
+        if (fuse) {
+            RetCombine R;
+            R.H = d.H; R.k = d.k; R.lb = d.lb; R.S = d.S; R.expected = fc.expected;
+            R.M = M; R.T = d.T; R.nslots = d.nslots; R.crow = d.crow; R.wait_ns = fc.wait_ns;
+            R.y = ybuf; R.rowmax = ymax; R.expert_rows = expert_rows; R.meta = meta; R.cbuf = cb;
+            R.cscale = reinterpret_cast<float*>(cb + scale_off); R.topk_w = fc.topk_w; R.ready = ready;
+            R.out = fc.out; R.err = err;
+            // every block resident (cooperative launch): blocks wait on counters
+            // that other blocks of this launch advance
+            int per_sm = 0;
+            if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, retcombine_kernel, kRowThreads,
+                                                                   0)) != cudaSuccess)
+                return e;
+            const long long items = M + d.T;
+            const unsigned grid = (unsigned)std::max<long long>(
+                1, std::min<long long>(items, (long long)std::max(per_sm, 1) * sm_count()));
+            void* args[] = {&R};
+            if ((e = cudaLaunchCooperativeKernel((const void*)retcombine_kernel, dim3(grid),
+                                                 dim3(kRowThreads), args, 0, st)) != cudaSuccess)
+                return e;
+        } else {
+            retquant_kernel<<<(unsigned)M, kRowThreads, 0, st>>>(
                 d.H, d.k, d.lb, d.S, d.nslots, d.crow, ybuf, ymax, expert_rows, meta, cb,
-                reinterpret_cast<float*>(cb + scale_off), fc.topk_w, ready, fc.out, err);
-        else
-            retquant_kernel<false><<<(unsigned)M, kRowThreads, 0, st>>>(
-                d.H, d.k, d.lb, d.S, d.nslots, d.crow, ybuf, ymax, expert_rows, meta, cb,
-                reinterpret_cast<float*>(cb + scale_off), nullptr, nullptr, nullptr, err);
+                reinterpret_cast<float*>(cb + scale_off), err);
+        }
         count_launches(1);
     } else {
         P2.expert_rows = expert_rows; P2.meta = meta; P2.cbuf = cb; P2.crow = d.crow; P2.k = d.k; P2.lb = d.lb;
@@ -1162,7 +1344,8 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
 
 cudaError_t launch_requant_rows(int I, long long M, const float* h, const unsigned* rowmax, void* hq16,
                                 float* sh, cudaStream_t st) {
-    tc::requant_kernel<<<(unsigned)M, tc::row_threads(I), 0, st>>>(I, h, rowmax, static_cast<__half*>(hq16), sh);
+    tc::requant_kernel<<<(unsigned)M, tc::row_threads(I), 0, st>>>(I, h, rowmax, static_cast<__half*>(hq16), sh,
+                                                                   nullptr);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -1170,9 +1353,8 @@ cudaError_t launch_requant_rows(int I, long long M, const float* h, const unsign
 cudaError_t launch_retquant_rows(const Dims& d, long long M, const float* y, const unsigned* rowmax,
                                  const int32_t* expert_rows, const moe_dispatch_meta* meta,
                                  unsigned char* cbuf, float* cscale, int* err, cudaStream_t st) {
-    tc::retquant_kernel<false><<<(unsigned)M, tc::kRowThreads, 0, st>>>(
-        d.H, d.k, d.lb, d.S, d.nslots, d.crow, y, rowmax, expert_rows, meta, cbuf, cscale, nullptr,
-        nullptr, nullptr, err);
+    tc::retquant_kernel<<<(unsigned)M, tc::kRowThreads, 0, st>>>(
+        d.H, d.k, d.lb, d.S, d.nslots, d.crow, y, rowmax, expert_rows, meta, cbuf, cscale, err);
     count_launches(1);
     return cudaGetLastError();
 }

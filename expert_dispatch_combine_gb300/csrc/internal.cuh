@@ -61,13 +61,13 @@ struct WsLayout {
     long long tiles;       // int32 [E_phys + 1]  grouped-GEMM tile prefix
     long long ttab;        // int4  [tile_table_entries]  (set, first row, rows, group) per token tile
     long long sh;          // f32   [T*k]   requantisation scale of h
-    long long ready;       // int32 [T]     return messages in per token (fused combine)
+    long long ready;       // int32 [T+1]   return messages in per token, then a work ticket (fused combine)
     // SIMT expert FFN
     long long acc_gu;      // int32 [T*k][2I]
     long long hq;          // int8  [T*k][I]
     long long acc_d;       // int32 [T*k][H]
     // tensor-core expert FFN
-    long long rowmax;      // u32   [2][T*k]  absmax of h and of y (float bits)
+    long long rowmax;      // u32   [2][T*k]  absmax of h and of y (float bits), then 2 chunk-plan words
     long long s_row;       // f32   [T*k]     dispatch scale of each expert row
     long long a16;         // fp16  [T*k][H]  expert input rows
     long long hbuf;        // f32   [T*k][I]  SwiGLU output h
@@ -88,10 +88,10 @@ inline WsLayout make_ws(const Dims& d) {
     w.tiles = o;      o = align_up(o + 4LL * (d.E_phys + 1), 256);
     w.ttab = o;       o = align_up(o + 16LL * tile_table_entries(d.E_phys, tk, kTcMinTileRows), 256);
     w.sh = o;         o = align_up(o + 4 * tk, 256);
-    w.ready = o;      o = align_up(o + 4LL * d.T, 256);
+    w.ready = o;      o = align_up(o + 4LL * (d.T + 1), 256);
     w.tc = ffn_uses_tc(d);
     if (w.tc) {
-        w.rowmax = o; o = align_up(o + 8 * tk, 256);
+        w.rowmax = o; o = align_up(o + 8 * tk + 8, 256);
         w.s_row = o;  o = align_up(o + 4 * tk, 256);
         w.a16 = o;    o = align_up(o + 2 * tk * d.H, 256);
         w.hbuf = o;   o = align_up(o + 4 * tk * d.I, 256);
@@ -202,11 +202,14 @@ cudaError_t launch_ffn_simt(const Dims& d, const void* dbuf, long long meta_off,
                             const int32_t* expert_offsets, const int32_t* expert_rows,
                             const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
                             const WsLayout& wl, cudaStream_t st, bool clear);
-// FusedCombine folded into the expert FFN (moe_layer, INT8 return messages,
-// tensor-core path): gate weights and the output.  Null members: no fusion.
+// FusedCombine folded into the expert FFN (INT8 return messages, tensor-core
+// path): gate weights, the output, the contributions each token's combine
+// waits for (k) and the bound of that wait.  Null members: no fusion.
 struct FusedCombine {
     const float* topk_w;  // [T][k]
     uint16_t* out;        // bf16 [T][H]
+    int expected = 0;
+    unsigned long long wait_ns = 0;
 };
 cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                           const int32_t* expert_offsets, const int32_t* expert_rows,

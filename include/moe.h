@@ -293,26 +293,43 @@ moe_status moe_combine(const moe_shape* shape, const void* combine_buf, int64_t 
                        const float* topk_w, uint16_t* out, moe_stream_t stream);
 
 /* moe_expert_ffn and moe_combine in one pass, with the combine of each token
- * done as soon as its k return messages are in ([C] "EP320" fused_moe
- * listing; [X] COMBINE procedure): every message writer publishes its message
- * (stores, device-scope fence, atomic increment of the token's readiness
- * counter in the workspace) and the writer that completes the count reads
- * the token's k messages back and writes out[t].  Nothing waits on a flag:
- * the last contributor does the work.  Same outputs as moe_expert_ffn
- * followed by moe_combine, bit for bit (combine_buf holds the messages too).
+ * started once its k return messages are in ([C] "EP320" fused_moe listing:
+ * combine waits until all contributions have arrived; [X] COMBINE
+ * procedure).  After the two expert GEMMs, one persistent kernel (cooperative
+ * launch, every block resident) takes work items from an atomic ticket in
+ * the workspace: first the T*k expert rows, then the T tokens.  A row's
+ * block writes its INT8 return message, fences and increments the token's
+ * readiness counter; a token's block waits, with a bounded spin on
+ * %globaltimer, until the counter reaches k, then sums the k messages and
+ * writes out[t].  Every row is taken before any token by a block that waits
+ * for nothing, so each wait ends once the rows are written.  Same outputs as
+ * moe_expert_ffn followed by moe_combine, bit for bit (combine_buf holds the
+ * messages too).
  *   Arguments: those of moe_expert_ffn plus topk_w and out of moe_combine.
  *   UNSUPPORTED unless combine_fmt is MOE_MSG_INT8 and the tensor-core path
  *   applies (H and I multiples of 64).
- * On the GB300 measurements (c2_decode_zipf, c4_prefill) the two separate
- * calls are faster: the k messages of a token come from rows spread over the
- * whole launch, so the completing writers arrive late and unevenly.  moe_layer
- * therefore uses the separate calls. */
+ * A wait that reaches its bound (2 s; only a lost message can cause it)
+ * posts MOE_ERR_TIMEOUT to the status word and skips that token; once any
+ * error is posted the remaining waits give up at once, so the kernel always
+ * ends.  moe_layer keeps the separate calls (faster on the measured
+ * workloads: the last return messages of a token come late in the launch). */
 moe_status moe_expert_ffn_combine(const moe_shape* shape, const void* dispatch_buf,
                                   int64_t dispatch_bytes, const int32_t* expert_offsets,
                                   const int32_t* expert_rows, const moe_expert_weights* weights,
                                   const float* topk_w, void* combine_buf, int64_t combine_bytes,
                                   uint16_t* out, void* workspace, int64_t workspace_bytes,
                                   moe_stream_t stream);
+/* moe_expert_ffn_combine with the wait's target and bound given: each token's
+ * combine waits until `expected` (>= 1; k for the layer) messages are in, at
+ * most wait_ns (>= 1) nanoseconds.  A target no token can reach (more than k)
+ * makes the first wait run out, post MOE_ERR_TIMEOUT and return; this is the
+ * path a lost message would take, and the call still completes. */
+moe_status moe_expert_ffn_combine_ex(const moe_shape* shape, const void* dispatch_buf,
+                                     int64_t dispatch_bytes, const int32_t* expert_offsets,
+                                     const int32_t* expert_rows, const moe_expert_weights* weights,
+                                     const float* topk_w, void* combine_buf, int64_t combine_bytes,
+                                     uint16_t* out, void* workspace, int64_t workspace_bytes,
+                                     int32_t expected, int64_t wait_ns, moe_stream_t stream);
 
 /* Routing arrays produced inside moe_layer (all device, caller-owned). */
 typedef struct {

@@ -254,6 +254,39 @@ def test_grouped_gemm_exact_worst_case(K, N):
     assert B.moe_device_status(ws) == 0
 
 
+@pytest.mark.parametrize("c", [18, 19, 36, 37, 73, 74, 127])
+def test_grouped_gemm_chunk_plans(c):
+    """Rows of codes with magnitude c, except c - 1 at every 16th element, and
+    weights 127 * sign(code) on the even channels: every product is positive,
+    the partial sums grow to 127 * sum |a| and every 16-element block adds an
+    odd amount, so a sum past 2^24 cannot be held exactly.  At K = 7168 the
+    mean |a| = c - 1/16 puts the rows just inside or just outside the bound of
+    each chunk plan (whole K: c <= 18; two chunks: c <= 36; four: c <= 73;
+    else 1024-K chunks); a plan chosen too long would round."""
+    K, N = 7168, 64
+    rng = np.random.default_rng(c)
+    G = 2
+    sizes = np.array([130, 77])
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    M = int(offs[-1])
+    mag = np.where(np.arange(K) % 16 == 0, c - 1, c)
+    sign = np.where(rng.random((M, K)) < 0.5, 1, -1)
+    A = (sign * mag).astype(np.int8)
+    Bw = np.where(rng.random((G, N, K)) < 0.5, 127, -127).astype(np.int8)
+    Bw[:, ::2] = (127 * sign[0]).astype(np.int8)   # even channels follow row 0's signs
+    ref = np.empty((M, N), np.int64)
+    for g in range(G):
+        ref[offs[g]:offs[g + 1]] = A[offs[g]:offs[g + 1]].astype(np.int64) @ Bw[g].astype(np.int64).T
+    assert np.abs(ref).max() == 127 * int(mag.sum())  # row 0 reaches the full sum
+    ws = torch.empty(B.moe_gemm_workspace_bytes(G, M, K), dtype=torch.uint8, device="cuda")
+    C = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    B.moe_grouped_gemm_s8(torch.from_numpy(offs).cuda(), M, torch.from_numpy(A).cuda(), K,
+                          torch.from_numpy(Bw).cuda(), C, ws)
+    torch.cuda.synchronize()
+    assert (_np(C).astype(np.int64) == ref).all()
+    assert B.moe_device_status(ws) == 0
+
+
 @pytest.mark.parametrize("K", [64, 192, 320])
 def test_grouped_gemm_odd_stage_counts_many_tiles(K):
     """1, 3 or 5 K stages of 64 per tile, and several tiles per CTA, so that
