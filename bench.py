@@ -398,6 +398,24 @@ def run_ours(args, rank: int, world: int):
         kern["gemm_down"] += dn_ms / reps
     stage_clocks = stage_sampler.stop(swall0, time.time())
     B.moe_profile_enable(False)
+    fused_ms = None
+    if B.moe_expert_ffn_path(shape) == B.MOE_FFN_TENSOR_CORE:
+        # the expert FFN with the combine folded in (each token's combine waits
+        # for its k return messages inside one persistent kernel), same inputs
+        fused_out = torch.empty_like(b.out)
+        fused_ms = 0.0
+        for _ in range(reps):
+            fa, fb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(4_000_000)
+            fa.record(stream)
+            B.moe_expert_ffn_combine(shape, b.dispatch, r["expert_offsets"], r["expert_rows"], w_gu,
+                                     s_gu, w_d, s_d, r["topk_w"], b.combine, fused_out, b.workspace,
+                                     phys_to_weight=p2l)
+            fb.record(stream)
+            torch.cuda.synchronize()
+            fused_ms += fa.elapsed_time(fb) / reps
+        assert B.moe_device_status(b.workspace) == 0
+        del fused_out
     tramp_us = None
     if w.S < w.R:
         # trampoline forward (A2E + A2E'): same outputs as moe_dispatch, two hops
@@ -439,6 +457,8 @@ def run_ours(args, rank: int, world: int):
     }
     if tramp_us is not None:
         stages["dispatch_trampoline_us"] = tramp_us
+    if fused_ms is not None:
+        stages["ffn_combine_fused_us"] = 1000 * fused_ms  # against ffn_us + combine_us
     dc_bytes = alg["dispatch_bytes"] + alg["combine_bytes"]
     dc_s = (acc["dispatch"] + acc["combine"]) / 1000
     stages["dispatch_combine_hbm_frac"] = dc_bytes / dc_s / 1e9 / hbm

@@ -9,17 +9,10 @@
 // (assemble_expert_inputs, run_local_experts, remote_write_combine).
 //
 // sm_103a has no integer tcgen05.mma, so the int8 contraction runs on
-// kind::f16: every int8 value is exact in fp16, every product is exact in
-// fp32, and the fp32 accumulator is drained to int32 at the end of each
-// chunk of K, added in int32.  A chunk is exact when every partial sum is an
-// integer below 2^24 in magnitude: always for chunks of 1024 K (1024 * 128 *
-// 128 = 2^24), and for longer chunks whenever every row's codes satisfy
-// sum_{k in chunk} |a_k| * 128 < 2^24 (|w| <= 128 for int8 weights).  The
-// kernel that writes the activation rows (assemble for the gate/up GEMM,
-// requant for the down GEMM) posts, per launch, the longest chunk plan that
-// holds for all of its rows (chunk_level); the GEMM drains at that plan's
-// boundaries.  The int32 results equal the integer matrix product bit for
-// bit for every plan.
+// kind::f16: every int8 value is exact in fp16, every product (|p| <= 16384)
+// is exact in fp32, and the fp32 accumulator is drained to int32 every 1024
+// K (1024 * 16384 = 2^24, so every partial sum is an exact integer).  The
+// int32 results equal the integer matrix product bit for bit.
 //
 // GEMM structure (one CTA per SM, persistent over tiles):
 //   D^T[channel][token] = W[channel][:] . X[token][:]
@@ -65,9 +58,7 @@ namespace tc {
 
 constexpr int BK = 64;                           // K per stage
 constexpr int CK = 16;                           // stages per exact chunk (1024 K)
-constexpr int CKP = CK / 2;                      // stage pairs per chunk exact for any data
-constexpr int kChunkLevels = 3;                  // plans 0..2: K in 1, 2, 4 chunks; 3: CKP-pair chunks
-constexpr int kL1Bound = 131071;                 // floor((2^24 - 1) / 128)
+constexpr int CKP = CK / 2;                      // stage pairs per exact chunk
 constexpr int BOX_ROWS = 32;                     // token rows per activation TMA box
 constexpr int BOX_BYTES = BOX_ROWS * BK * 2;     // 4 KB
 constexpr int A_BYTES = 128 * BK;                // 8 KB int8 weights per stage
@@ -135,16 +126,8 @@ struct Params {
     int k, lb, S;
     long long nslots;            // EPI_BF16MSG: dispatch slots (range of expert_rows entries)
     int tma_out;                 // epilogue may use tensor stores for full groups
-    const unsigned* chunk_level; // chunk plan of the activation rows (null: 1024-K chunks)
     int* err;
 };
-
-// Stage pairs per exact chunk under plan `level` for a reduction of ksp pairs:
-// plan l < kChunkLevels splits K into 2^l chunks, the last plan uses chunks of
-// CKP pairs (1024 K), which are exact for any int8 data.
-__host__ __device__ __forceinline__ int chunk_pairs(int level, int ksp) {
-    return level >= kChunkLevels ? CKP : (ksp + (1 << level) - 1) >> level;
-}
 
 struct TileInfo {
     int set, r0, nvalid, nmma, mb;
@@ -488,11 +471,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     // K stages in pairs; an odd count gets one more stage entirely beyond K,
     // which TMA fills with zeros (it adds nothing to the sums)
     const int KSP = (P.K / BK + 1) / 2;
-    // chunk plan of this launch (written by the kernel that produced the rows)
-    const int level = P.chunk_level ? min(kChunkLevels, (int)*reinterpret_cast<const volatile unsigned*>(P.chunk_level))
-                                    : kChunkLevels;
-    const int ckp = chunk_pairs(level, KSP);
-    const int nchunks = (KSP + ckp - 1) / ckp;
+    const int nchunks = (KSP + CKP - 1) / CKP;
     const int wgi = warp >> 2;
 
     if (wgi == 0) {
@@ -555,8 +534,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 e_next = tile_entry(P, tile + gridDim.x, total_tiles);
                 const uint32_t idesc = ptx::idesc_f16_f32(128, ti.nmma);
                 for (int kp = 0; kp < KSP; ++kp, ++pr) {
-                    const bool first = (kp % ckp) == 0;
-                    const bool last = (kp % ckp) == ckp - 1 || kp == KSP - 1;
+                    const bool first = (kp % CKP) == 0;
+                    const bool last = (kp % CKP) == CKP - 1 || kp == KSP - 1;
                     const uint32_t b = q & 1;
                     if (first) {
                         // the drains must have taken this buffer's previous chunk
@@ -736,52 +715,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
 }
 
 // ------------------------------------------------------------ helpers
-constexpr int kMaxPlanPairs = 128;  // stage pairs a row's chunk plan is computed for (K <= 16384)
-
-// sum |q| over 16 int8 codes (four words), exact (|q| <= 128).
-__device__ __forceinline__ unsigned abs_sum16(const uint4& w) {
-    unsigned s = __dp4a(__vabsdiffs4(w.x, 0u), 0x01010101u, 0u);
-    s = __dp4a(__vabsdiffs4(w.y, 0u), 0x01010101u, s);
-    s = __dp4a(__vabsdiffs4(w.z, 0u), 0x01010101u, s);
-    return __dp4a(__vabsdiffs4(w.w, 0u), 0x01010101u, s);
-}
-
-// The lowest chunk plan under which every chunk of this row satisfies
-// sum |a_k| <= kL1Bound (s_pair[p]: sum |a_k| over stage pair p), posted to
-// *level by atomic max, so the launch takes the plan that holds for all of
-// its rows.  Plans whose chunks are at most CKP pairs long need no check.
-__device__ __forceinline__ void post_chunk_level(const int* s_pair, int ksp, unsigned* level) {
-    int lvl = kChunkLevels;
-    for (int l = 0; l < kChunkLevels; ++l) {
-        const int ckp = chunk_pairs(l, ksp);
-        bool ok = ckp <= CKP;
-        if (!ok) {
-            ok = true;
-            for (int c0 = 0; ok && c0 < ksp; c0 += ckp) {
-                int sum = 0;
-                for (int p = c0; p < min(ksp, c0 + ckp); ++p) sum += s_pair[p];
-                ok = sum <= kL1Bound;
-            }
-        }
-        if (ok) {
-            lvl = l;
-            break;
-        }
-    }
-    if (lvl > 0) atomicMax(level, (unsigned)lvl);
-}
-
 // Gather rows (optionally through row_index) of an int8 matrix and convert
-// them to fp16 (exact); optionally copy the dispatch scale of each row; with
-// a non-null `level` (K <= 16384), post the row's chunk plan.
+// them to fp16 (exact); optionally copy the dispatch scale of each row.
 // A row-list entry outside [0, a_rows) gives a zero row (and scale) and
 // posts MOE_ERR_INDEX.
 __global__ void __launch_bounds__(128)
 assemble_kernel(int K, const int32_t* __restrict__ row_index, long long a_rows,
                 const int8_t* __restrict__ A, long long lda, const moe_dispatch_meta* __restrict__ meta,
-                __half* __restrict__ out, float* __restrict__ s_row, unsigned* __restrict__ level,
-                int* __restrict__ err) {
-    __shared__ int s_pair[kMaxPlanPairs];
+                __half* __restrict__ out, float* __restrict__ s_row, int* __restrict__ err) {
     const int r = blockIdx.x;
     const long long g = row_index ? row_index[r] : r;
     uint4* dst = reinterpret_cast<uint4*>(out + (long long)r * K);
@@ -795,12 +736,6 @@ assemble_kernel(int K, const int32_t* __restrict__ row_index, long long a_rows,
         return;
     }
     const uint4* src = reinterpret_cast<const uint4*>(A + g * lda);
-    const int ksp = (K / BK + 1) / 2;
-    const bool plan = level != nullptr && ksp <= kMaxPlanPairs;
-    if (plan) {
-        for (int p = threadIdx.x; p < ksp; p += blockDim.x) s_pair[p] = 0;
-        __syncthreads();
-    }
     // four 16-byte loads of the row in flight per thread before converting
     for (int c0 = threadIdx.x; c0 < nch; c0 += 4 * blockDim.x) {
         uint4 w[4];
@@ -820,15 +755,10 @@ assemble_kernel(int K, const int32_t* __restrict__ row_index, long long a_rows,
                 s8x4_to_f16x4(w[u].w, o1.z, o1.w);
                 dst[2 * c] = o0;
                 dst[2 * c + 1] = o1;
-                if (plan) atomicAdd(&s_pair[c >> 3], (int)abs_sum16(w[u]));  // 8 chunks of 16 per pair
             }
         }
     }
     if (meta && threadIdx.x == 0) s_row[r] = meta[g].scale;
-    if (plan) {
-        __syncthreads();
-        if (threadIdx.x == 0) post_chunk_level(s_pair, ksp, level);
-    }
 }
 
 template <int NT>
@@ -869,15 +799,8 @@ __device__ __forceinline__ void load_chunk16(const float4* __restrict__ src, int
 // reduced by the gate/up GEMM's epilogue): hq as exact fp16 integers, s_h.
 __global__ void __launch_bounds__(kRowMaxThreads)
 requant_kernel(int I, const float* __restrict__ h, const unsigned* __restrict__ rowmax,
-               __half* __restrict__ hq, float* __restrict__ sh, unsigned* __restrict__ level) {
-    __shared__ int s_pair[kMaxPlanPairs];
+               __half* __restrict__ hq, float* __restrict__ sh) {
     const int r = blockIdx.x;
-    const int ksp = (I / BK + 1) / 2;
-    const bool plan = level != nullptr && ksp <= kMaxPlanPairs;
-    if (plan) {
-        for (int p = threadIdx.x; p < ksp; p += blockDim.x) s_pair[p] = 0;
-        __syncthreads();
-    }
     const int nch = I / 16;
     const float4* src = reinterpret_cast<const float4*>(h + (long long)r * I);
     uint4* dst = reinterpret_cast<uint4*>(hq + (long long)r * I);
@@ -907,19 +830,9 @@ requant_kernel(int I, const float* __restrict__ h, const unsigned* __restrict__ 
             for (int i = 0; i < 8; ++i) o[i] = codes_to_f16x2(q[2 * i], q[2 * i + 1]);
             dst[2 * c] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-            if (plan) {
-                int l1 = 0;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) l1 += abs(q[e]);
-                atomicAdd(&s_pair[c >> 3], l1);  // 8 chunks of 16 per pair
-            }
         }
     }
     if (threadIdx.x == 0) sh[r] = row_scale(__uint_as_float(rowmax[r]));
-    if (plan) {
-        __syncthreads();
-        if (threadIdx.x == 0) post_chunk_level(s_pair, ksp, level);
-    }
 }
 
 // INT8 return message of expert row r: token-wise codes of y (its row absmax
@@ -1210,11 +1123,9 @@ cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long lo
     if ((e = launch_tile_prefix(n_groups, BN_LARGE, offsets, max_rows, n_groups, tp, err, st, ttab)) !=
         cudaSuccess)
         return e;
-    // the rows of A are the caller's: no bound on the row list's entries here;
-    // their chunk plan goes to a word of the (just cleared) status region
-    unsigned* level = ws_ptr<unsigned>(ws, 128);
+    // the rows of A are the caller's: no bound on the row list's entries here
     assemble_kernel<<<(unsigned)max_rows, 128, 0, st>>>(K, row_index, LLONG_MAX, A, lda, nullptr, a16,
-                                                        nullptr, level, err);
+                                                        nullptr, err);
     count_launches(1);
     CUtensorMap mw, mx[2], mo;
     const bool tma_out = N % 128 == 0;
@@ -1225,7 +1136,7 @@ cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long lo
     Params P = {};
     P.G = n_groups; P.offsets = offsets; P.tile_prefix = tp; P.ttab = ttab; P.g2s = nullptr;
     P.K = K; P.rows_per_set = N; P.nout = N; P.mb_count = (N + 127) / 128; P.box1_off = 64;
-    P.c_i32 = C; P.err = err; P.tma_out = tma_out; P.chunk_level = level;
+    P.c_i32 = C; P.err = err; P.tma_out = tma_out;
     return launch_gemm<EPI_I32, BN_LARGE>(P, mw, mx, mo, st);
 }
 
@@ -1248,7 +1159,6 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     float* hbuf = ws_ptr<float>(ws, wl.hbuf);
     unsigned* hmax = ws_ptr<unsigned>(ws, wl.rowmax);
     unsigned* ymax = hmax + M;
-    unsigned* level = hmax + 2 * M;  // chunk plans of the gate/up and down GEMMs
     __half* hq16 = ws_ptr<__half>(ws, wl.hq16);
     float* ybuf = ws_ptr<float>(ws, wl.ybuf);
     unsigned char* cb = static_cast<unsigned char*>(cbuf);
@@ -1257,7 +1167,7 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     cudaError_t e;
 
     if (clear && (e = clear_status(ws, st)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(hmax, 0, sizeof(unsigned) * (2 * M + 2), st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(hmax, 0, sizeof(unsigned) * 2 * M, st)) != cudaSuccess) return e;
     count_launches(1);
     const bool fuse = fc.out != nullptr && int8_ret;
     int* ready = ws_ptr<int>(ws, wl.ready);
@@ -1270,7 +1180,7 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
         return e;
     assemble_kernel<<<(unsigned)M, 128, 0, st>>>(d.H, expert_rows, d.nslots,
                                                  static_cast<const int8_t*>(dbuf), d.drow, meta, a16,
-                                                 s_row, level, err);
+                                                 s_row, err);
     count_launches(1);
 
     CUtensorMap mwgu, mx1[2], mo1, mwd, mx2[2], mo2;
@@ -1292,17 +1202,17 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     P1.g2s = w.phys_to_weight;
     P1.K = d.H; P1.rows_per_set = 2 * d.I; P1.nout = d.I; P1.mb_count = d.I / 64; P1.box1_off = d.I;
     P1.s_row = s_row; P1.s_ch = w.s_gate_up; P1.out_f32 = hbuf; P1.rowmax = hmax; P1.err = err;
-    P1.tma_out = 1; P1.chunk_level = level;
+    P1.tma_out = 1;
     if ((e = launch_gemm<EPI_GU, BNV>(P1, mwgu, mx1, mo1, st)) != cudaSuccess) return e;
 
-    requant_kernel<<<(unsigned)M, row_threads(d.I), 0, st>>>(d.I, hbuf, hmax, hq16, sh, level + 1);
+    requant_kernel<<<(unsigned)M, row_threads(d.I), 0, st>>>(d.I, hbuf, hmax, hq16, sh);
     count_launches(1);
 
     Params P2 = {};
     P2.G = d.E_phys; P2.offsets = expert_offsets; P2.tile_prefix = tp; P2.ttab = ttab;
     P2.g2s = w.phys_to_weight;
     P2.K = d.I; P2.rows_per_set = d.H; P2.nout = d.H; P2.mb_count = (d.H + 127) / 128; P2.box1_off = 64;
-    P2.s_row = sh; P2.s_ch = w.s_down; P2.err = err; P2.tma_out = y_tma; P2.chunk_level = level + 1;
+    P2.s_row = sh; P2.s_ch = w.s_down; P2.err = err; P2.tma_out = y_tma;
     if (int8_ret) {
         P2.out_f32 = ybuf; P2.rowmax = ymax;
         if ((e = launch_gemm<EPI_F32, BNV>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
@@ -1344,8 +1254,7 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
 
 cudaError_t launch_requant_rows(int I, long long M, const float* h, const unsigned* rowmax, void* hq16,
                                 float* sh, cudaStream_t st) {
-    tc::requant_kernel<<<(unsigned)M, tc::row_threads(I), 0, st>>>(I, h, rowmax, static_cast<__half*>(hq16), sh,
-                                                                   nullptr);
+    tc::requant_kernel<<<(unsigned)M, tc::row_threads(I), 0, st>>>(I, h, rowmax, static_cast<__half*>(hq16), sh);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -67,7 +67,7 @@ struct WsLayout {
     long long hq;          // int8  [T*k][I]
     long long acc_d;       // int32 [T*k][H]
     // tensor-core expert FFN
-    long long rowmax;      // u32   [2][T*k]  absmax of h and of y (float bits), then 2 chunk-plan words
+    long long rowmax;      // u32   [2][T*k]  absmax of h and of y (float bits)
     long long s_row;       // f32   [T*k]     dispatch scale of each expert row
     long long a16;         // fp16  [T*k][H]  expert input rows
     long long hbuf;        // f32   [T*k][I]  SwiGLU output h
@@ -91,7 +91,7 @@ inline WsLayout make_ws(const Dims& d) {
     w.ready = o;      o = align_up(o + 4LL * (d.T + 1), 256);
     w.tc = ffn_uses_tc(d);
     if (w.tc) {
-        w.rowmax = o; o = align_up(o + 8 * tk + 8, 256);
+        w.rowmax = o; o = align_up(o + 8 * tk, 256);
         w.s_row = o;  o = align_up(o + 4 * tk, 256);
         w.a16 = o;    o = align_up(o + 2 * tk * d.H, 256);
         w.hbuf = o;   o = align_up(o + 4 * tk * d.I, 256);

@@ -255,14 +255,13 @@ def test_grouped_gemm_exact_worst_case(K, N):
 
 
 @pytest.mark.parametrize("c", [18, 19, 36, 37, 73, 74, 127])
-def test_grouped_gemm_chunk_plans(c):
+def test_grouped_gemm_sums_beyond_2p24(c):
     """Rows of codes with magnitude c, except c - 1 at every 16th element, and
     weights 127 * sign(code) on the even channels: every product is positive,
-    the partial sums grow to 127 * sum |a| and every 16-element block adds an
-    odd amount, so a sum past 2^24 cannot be held exactly.  At K = 7168 the
-    mean |a| = c - 1/16 puts the rows just inside or just outside the bound of
-    each chunk plan (whole K: c <= 18; two chunks: c <= 36; four: c <= 73;
-    else 1024-K chunks); a plan chosen too long would round."""
+    the sums grow to 127 * sum |a| (up to 115 M at K = 7168, far beyond 2^24)
+    and every 16-element block adds an odd amount, so no fp32 accumulator
+    could hold the whole sum exactly; the drains every 1024 K keep the int32
+    results exact."""
     K, N = 7168, 64
     rng = np.random.default_rng(c)
     G = 2
