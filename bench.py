@@ -366,7 +366,7 @@ def run_ours(args, rank: int, world: int):
     r = b.routing
     names = ["route", "dispatch", "ffn", "combine"]
     acc = {n: 0.0 for n in names}
-    kern = {"gemm_gate_up": 0.0, "gemm_down": 0.0}
+    kern = {"gemm_gate_up": 0.0, "gemm_down": 0.0, "narrow_gate_up": 0.0, "narrow_down": 0.0}
     reps = max(1, min(args.steps, 5))
     B.moe_profile_enable(True)
     stage_sampler = ClockSampler(local)
@@ -393,9 +393,11 @@ def run_ours(args, rank: int, world: int):
         torch.cuda.synchronize()
         for i, n in enumerate(names):
             acc[n] += evs[i].elapsed_time(evs[i + 1]) / reps
-        gu_ms, dn_ms = B.moe_profile_read()
+        gu_ms, dn_ms, ngu_ms, ndn_ms = B.moe_profile_read(4)
         kern["gemm_gate_up"] += gu_ms / reps
         kern["gemm_down"] += dn_ms / reps
+        kern["narrow_gate_up"] += max(ngu_ms, 0.0) / reps
+        kern["narrow_down"] += max(ndn_ms, 0.0) / reps
     stage_clocks = stage_sampler.stop(swall0, time.time())
     B.moe_profile_enable(False)
     fused_ms = None
@@ -433,18 +435,28 @@ def run_ours(args, rank: int, world: int):
         tramp_us = 1000 * t_ms
         del tbuf
     alg = algorithmic(w)
-    # gate|up kernel bytes: int8 gate/up rows of the weight sets this step touches, the
-    # fp16 expert rows it reads and the f32 h it writes
     cnt_h = layer.buf.routing["expert_counts"].cpu().numpy()
-    touched = np.nonzero(cnt_h)[0]
-    if p2l is not None:
-        touched = np.unique(p2l.cpu().numpy()[touched])
+    p2l_h = p2l.cpu().numpy() if p2l is not None else None
+
+    def weight_sets(mask):
+        idx = np.nonzero(mask)[0]
+        return np.unique(p2l_h[idx]) if p2l_h is not None else idx
+
+    touched = weight_sets(cnt_h > 0)
     ffn_path = B.moe_expert_ffn_path(shape)
-    # the tensor-core GEMM reads the expert rows as fp16 codes, the decode
-    # matrix-vector kernel reads the int8 dispatch rows
+    narrow = B.moe_expert_ffn_narrow_rows(shape)
+    # the kernel measured as the dominant one: the tensor-core gate|up GEMM over
+    # the experts with more than `narrow` rows (the narrow ones run on the
+    # matrix-vector kernels), or the matrix-vector kernel of the decode path;
+    # its bytes: int8 gate/up rows of the weight sets it touches, the expert
+    # rows it reads (fp16 codes for the tensor cores, int8 dispatch rows for
+    # the matrix-vector kernel) and the f32 h it writes
+    wide = cnt_h > narrow if ffn_path != B.MOE_FFN_GEMV else cnt_h > 0
+    rows_k = int(cnt_h[wide].sum())
     act_bytes = 1 if ffn_path == B.MOE_FFN_GEMV else 2
-    alg["gate_up_bytes"] = (len(touched) * 2 * w.I * w.H + w.T * w.k * w.H * act_bytes
-                            + w.T * w.k * w.I * 4)
+    alg["gate_up_ops"] = rows_k * 4 * w.H * w.I
+    alg["gate_up_bytes"] = (len(weight_sets(wide)) * 2 * w.I * w.H + rows_k * w.H * act_bytes
+                            + rows_k * w.I * 4)
     peaks, peak_kind = _peaks()
     hbm = peaks["hbm_gbs"]
     stages = {
@@ -459,6 +471,17 @@ def run_ours(args, rank: int, world: int):
         stages["dispatch_trampoline_us"] = tramp_us
     if fused_ms is not None:
         stages["ffn_combine_fused_us"] = 1000 * fused_ms  # against ffn_us + combine_us
+    if narrow > 0 and ffn_path == B.MOE_FFN_TENSOR_CORE:
+        nmask = (cnt_h > 0) & (cnt_h <= narrow)
+        nsets = len(weight_sets(nmask))
+        nrows = int(cnt_h[nmask].sum())
+        n_us = 1000 * (kern["narrow_gate_up"] + kern["narrow_down"])
+        n_bytes = nsets * 3 * w.H * w.I + nrows * (w.H + 4 * w.I + 2 * w.I + 4 * w.H)
+        stages["narrow_experts"] = {
+            "max_rows": narrow, "experts": int(nmask.sum()), "rows": nrows,
+            "gate_up_us": 1000 * kern["narrow_gate_up"], "down_us": 1000 * kern["narrow_down"],
+            "gbs": n_bytes / (n_us / 1e6) / 1e9 if n_us > 0 else None,
+            "kernels": "gemv_kernel<gate|up>, gemv_kernel<down> (int8 dp4a weight streaming)"}
     dc_bytes = alg["dispatch_bytes"] + alg["combine_bytes"]
     dc_s = (acc["dispatch"] + acc["combine"]) / 1000
     stages["dispatch_combine_hbm_frac"] = dc_bytes / dc_s / 1e9 / hbm
@@ -480,13 +503,15 @@ def run_ours(args, rank: int, world: int):
     stages["ffn_frac_sustained"] = ffn_tflops / sustained
     stages["clocks"] = stage_clocks
     gu_name = ("gemv_kernel<gate|up> (int8 dp4a weight streaming)" if ffn_path == B.MOE_FFN_GEMV
-               else "gemm_tc_kernel<gate|up> (exact int8 on tcgen05 kind::f16)")
+               else "gemm_tc_kernel<gate|up> (exact int8 on tcgen05 kind::f16; experts with more "
+                    f"than {narrow} routed rows)")
     if kern["gemm_gate_up"] > 0:
         # dominant kernel: the gate|up expert GEMM, timed by CUDA events on its stream
         gu_tflops = alg["gate_up_ops"] / (kern["gemm_gate_up"] / 1000) / 1e12
         stages["gemm_gate_up_us"] = 1000 * kern["gemm_gate_up"]
         stages["gemm_down_us"] = 1000 * kern["gemm_down"]
-        stages["gemm_down_tflops"] = alg["down_ops"] / (kern["gemm_down"] / 1000) / 1e12
+        rows_dn = int(cnt_h[wide].sum())
+        stages["gemm_down_tflops"] = rows_dn * 2 * w.H * w.I / (kern["gemm_down"] / 1000) / 1e12
         # bound by the kernel's arithmetic intensity against the measured ridge point
         intensity = alg["gate_up_ops"] / alg["gate_up_bytes"]
         ridge = peak_tc * 1e12 / (hbm * 1e9)

@@ -61,7 +61,7 @@ EXPORTED = ("moe_status_string", "moe_static_buffer_bytes", "moe_query_layout", 
             "moe_dispatch_noalloc", "moe_dispatch_noalloc_max_scratch", "moe_layer_graph_create",
             "moe_graph_launch", "moe_graph_destroy", "moe_eplb_collect", "moe_expert_ffn_combine",
             "moe_trampoline_bytes", "moe_dispatch_trampoline", "moe_expert_ffn_path",
-            "moe_layer_host", "moe_expert_ffn_combine_ex")
+            "moe_layer_host", "moe_expert_ffn_combine_ex", "moe_expert_ffn_narrow_rows")
 
 _lib = None
 
@@ -82,6 +82,7 @@ def load(path: str = LIB_PATH):
         "moe_static_buffer_bytes": ([i64, i64, i64, i64, i64, ctypes.POINTER(i64)], ctypes.c_int),
         "moe_query_layout": ([PS, ctypes.POINTER(moe_layout)], ctypes.c_int),
         "moe_expert_ffn_path": ([PS, ctypes.POINTER(i32)], ctypes.c_int),
+        "moe_expert_ffn_narrow_rows": ([PS, ctypes.POINTER(i32)], ctypes.c_int),
         "moe_eplb_plan": ([i32, i32, i32, i32, P, i32, P, P, P], ctypes.c_int),
         "moe_route": ([PS, P, P, P, i32, P, P, P, P, P], ctypes.c_int),
         "moe_dispatch": ([PS, P, P, P, i64, P, P, P, P, i64, P], ctypes.c_int),
@@ -192,6 +193,15 @@ def moe_expert_ffn_path(shape: Shape) -> int:
     out = ctypes.c_int32(0)
     cs = shape.c()
     _check("moe_expert_ffn_path", load().moe_expert_ffn_path(ctypes.byref(cs), ctypes.byref(out)))
+    return out.value
+
+
+def moe_expert_ffn_narrow_rows(shape: Shape) -> int:
+    """Experts with 1..n routed rows run on the matrix-vector kernels beside
+    the tensor-core GEMMs (0: none)."""
+    out = ctypes.c_int32(0)
+    cs = shape.c()
+    _check("moe_expert_ffn_narrow_rows", load().moe_expert_ffn_narrow_rows(ctypes.byref(cs), ctypes.byref(out)))
     return out.value
 
 
@@ -376,11 +386,12 @@ def moe_profile_enable(on: bool) -> None:
     _check("moe_profile_enable", load().moe_profile_enable(1 if on else 0))
 
 
-def moe_profile_read() -> tuple[float, float]:
-    """(gate/up GEMM ms, down GEMM ms) of the most recent expert FFN."""
-    ms = (ctypes.c_float * 2)()
-    _check("moe_profile_read", load().moe_profile_read(ctypes.cast(ms, ctypes.c_void_p), 2))
-    return float(ms[0]), float(ms[1])
+def moe_profile_read(n: int = 2) -> tuple:
+    """(gate/up GEMM ms, down GEMM ms[, narrow-expert gate/up ms, narrow-expert
+    down ms]) of the most recent expert FFN; -1 for a kernel that did not run."""
+    ms = (ctypes.c_float * n)()
+    _check("moe_profile_read", load().moe_profile_read(ctypes.cast(ms, ctypes.c_void_p), n))
+    return tuple(float(v) for v in ms)
 
 
 def moe_launch_count() -> int:

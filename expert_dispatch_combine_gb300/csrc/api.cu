@@ -15,7 +15,12 @@ void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed);
 
 static bool g_prof_on = false;
 static cudaEvent_t g_prof_ev[kProfSlots][2] = {};
-cudaEvent_t prof_event(int slot, int end) { return g_prof_on ? g_prof_ev[slot][end] : nullptr; }
+static bool g_prof_recorded[kProfSlots] = {};
+cudaEvent_t prof_event(int slot, int end) {
+    if (!g_prof_on) return nullptr;
+    if (end) g_prof_recorded[slot] = true;
+    return g_prof_ev[slot][end];
+}
 
 cudaError_t clear_status(void* ws, cudaStream_t st) {
     count_launches(1);
@@ -110,6 +115,16 @@ moe_status moe_query_layout(const moe_shape* shape, moe_layout* layout) {
     if (st != MOE_OK) return st;
     if (!layout) return MOE_ERR_INVALID_ARG;
     fill_layout(make_dims(*shape), layout);
+    return MOE_OK;
+}
+
+moe_status moe_expert_ffn_narrow_rows(const moe_shape* shape, int32_t* rows) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    if (!rows) return MOE_ERR_INVALID_ARG;
+    const Dims d = make_dims(*shape);
+    const WsLayout wl = make_ws(d);
+    *rows = (wl.tc && !ffn_gemv_fits(d)) ? narrow_expert_rows(d) : 0;
     return MOE_OK;
 }
 
@@ -388,15 +403,17 @@ moe_status moe_profile_enable(int32_t on) {
                 if (!g_prof_ev[s][e] && cudaEventCreate(&g_prof_ev[s][e]) != cudaSuccess)
                     return cuda_status(cudaGetLastError());
     }
+    if (on && !g_prof_on)
+        for (int s = 0; s < kProfSlots; ++s) g_prof_recorded[s] = false;
     g_prof_on = on != 0;
     return MOE_OK;
 }
 
 moe_status moe_profile_read(float* ms, int32_t n) {
     if (!ms || n < 1) return MOE_ERR_INVALID_ARG;
+    for (int s = 0; s < n; ++s) ms[s] = -1.f;
     for (int s = 0; s < kProfSlots && s < n; ++s) {
-        ms[s] = -1.f;
-        if (!g_prof_ev[s][0] || !g_prof_ev[s][1]) continue;
+        if (!g_prof_recorded[s] || !g_prof_ev[s][0] || !g_prof_ev[s][1]) continue;
         if (cudaEventSynchronize(g_prof_ev[s][1]) != cudaSuccess) return cuda_status(cudaGetLastError());
         float t = 0.f;
         if (cudaEventElapsedTime(&t, g_prof_ev[s][0], g_prof_ev[s][1]) == cudaSuccess) ms[s] = t;

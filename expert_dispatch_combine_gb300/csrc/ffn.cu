@@ -30,12 +30,16 @@ namespace {
 // offsets never decrease, offsets[G] <= max_rows and every weight set lies in
 // [0, n_sets), the kernel posts MOE_ERR_INDEX and describes no tile at all,
 // so no GEMM that reads this prefix addresses memory outside its buffers.
+// Groups with 1..skip_rows rows get no tile; with a non-null `narrow`, their
+// ids are listed in ascending order in narrow[1..] and their number in
+// narrow[0] (for the kernels that take them).
 __global__ void __launch_bounds__(1024)
 tile_prefix_kernel(int G, int BM, const int32_t* __restrict__ offsets, long long max_rows,
                    int n_sets, int32_t* __restrict__ tile_prefix, int4* __restrict__ table,
-                   const int32_t* __restrict__ g2s, int* __restrict__ err) {
-    __shared__ int s_warp[32];
-    __shared__ int s_carry;
+                   const int32_t* __restrict__ g2s, int* __restrict__ err, int skip_rows,
+                   int32_t* __restrict__ narrow) {
+    __shared__ int s_warp[32], s_nwarp[32];
+    __shared__ int s_carry, s_ncarry;
     int bad = 0;
     for (int g = threadIdx.x; g < G; g += 1024) {
         if (offsets[g + 1] < offsets[g]) bad = 1;
@@ -46,37 +50,56 @@ tile_prefix_kernel(int G, int BM, const int32_t* __restrict__ offsets, long long
     if (__syncthreads_or(bad)) {
         if (threadIdx.x == 0 && err) post_status(err, MOE_ERR_INDEX);
         for (int g = threadIdx.x; g <= G; g += 1024) tile_prefix[g] = 0;
+        if (threadIdx.x == 0 && narrow) narrow[0] = 0;
         return;
     }
-    if (threadIdx.x == 0) s_carry = 0;
+    if (threadIdx.x == 0) {
+        s_carry = 0;
+        s_ncarry = 0;
+    }
     __syncthreads();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     for (int b0 = 0; b0 < G; b0 += 1024) {
         int g = b0 + threadIdx.x;
-        int n = 0;
+        int n = 0, nf = 0;
         if (g < G) {
             int m = offsets[g + 1] - offsets[g];
-            n = (m + BM - 1) / BM;
+            n = m > skip_rows ? (m + BM - 1) / BM : 0;  // narrow groups: no tile here
+            nf = m >= 1 && m <= skip_rows;
         }
-        int v = n;
+        int v = n, vn = nf;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             int o = __shfl_up_sync(0xffffffffu, v, off);
-            if (lane >= off) v += o;
+            int on = __shfl_up_sync(0xffffffffu, vn, off);
+            if (lane >= off) {
+                v += o;
+                vn += on;
+            }
         }
-        if (lane == 31) s_warp[w] = v;
+        if (lane == 31) {
+            s_warp[w] = v;
+            s_nwarp[w] = vn;
+        }
         __syncthreads();
         if (w == 0) {
-            int x = s_warp[lane];
+            int x = s_warp[lane], xn = s_nwarp[lane];
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 int o = __shfl_up_sync(0xffffffffu, x, off);
-                if (lane >= off) x += o;
+                int on = __shfl_up_sync(0xffffffffu, xn, off);
+                if (lane >= off) {
+                    x += o;
+                    xn += on;
+                }
             }
             s_warp[lane] = x;
+            s_nwarp[lane] = xn;
         }
         __syncthreads();
         int incl = v + (w > 0 ? s_warp[w - 1] : 0) + s_carry;
+        const int nincl = vn + (w > 0 ? s_nwarp[w - 1] : 0) + s_ncarry;
+        if (narrow && nf) narrow[1 + nincl - 1] = g;
         if (g < G) {
             tile_prefix[g] = incl - n;
             if (table) {
@@ -87,10 +110,16 @@ tile_prefix_kernel(int G, int BM, const int32_t* __restrict__ offsets, long long
             }
         }
         __syncthreads();
-        if (threadIdx.x == 1023) s_carry = incl;
+        if (threadIdx.x == 1023) {
+            s_carry = incl;
+            s_ncarry = nincl;
+        }
         __syncthreads();
     }
-    if (threadIdx.x == 0) tile_prefix[G] = s_carry;
+    if (threadIdx.x == 0) {
+        tile_prefix[G] = s_carry;
+        if (narrow) narrow[0] = s_ncarry;
+    }
 }
 
 // ------------------------------------------------------- SIMT int8 GEMM
@@ -282,9 +311,9 @@ cudaError_t set_smem(const void* fn, size_t bytes) {
 
 cudaError_t launch_tile_prefix(int G, int BM, const int32_t* offsets, long long max_rows, int n_sets,
                                int32_t* tile_prefix, int* err, cudaStream_t st, int4* table,
-                               const int32_t* g2s) {
+                               const int32_t* g2s, int skip_rows, int32_t* narrow) {
     tile_prefix_kernel<<<1, 1024, 0, st>>>(G, BM, offsets, max_rows, n_sets, tile_prefix, table, g2s,
-                                           err);
+                                           err, skip_rows, narrow);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -29,6 +29,8 @@
 // After the K loop the warp's 64 partial sums (8 rows x 8 tokens) are reduced
 // over the lanes by a reduce-scatter of shuffles (62 exchanges), which leaves
 // lane L with the finished sums of row L / 4 and tokens 2(L % 4), 2(L % 4)+1.
+#include <algorithm>
+#include <climits>
 #include <cuda_fp16.h>
 
 #include "device_math.cuh"
@@ -66,6 +68,7 @@ struct Params {
     long long M;                  // routed rows (rows of out)
     long long nslots;             // dispatch slots (rows of dbuf)
     int n_sets;                   // weight sets
+    const int32_t* list;          // null: block row y takes expert y; else the experts list[1..list[0]]
     int* err;                     // workspace status word
 };
 
@@ -95,11 +98,10 @@ __device__ __forceinline__ void reduce_scatter64(int (&a)[ROWS * NT], int lane) 
     }
 }
 
+// One expert's share of the block: output channels blockIdx.x of expert e.
+// xs [NT][K] holds a pass's token rows, s_tok their scales.
 template <int KIND>
-__global__ void __launch_bounds__(THREADS, 2) gemv_kernel(const Params P) {
-    extern __shared__ __align__(16) int8_t xs[];  // [NT][K] token rows of this expert
-    __shared__ float s_tok[NT];                   // their scales
-    const int e = blockIdx.y;
+__device__ __forceinline__ void gemv_expert(const Params& P, int e, int8_t* xs, float* s_tok) {
     const int r_begin = P.offsets[e], r_end = P.offsets[e + 1];
     if (r_begin == r_end) return;
     const int set = P.p2w ? P.p2w[e] : e;
@@ -252,8 +254,26 @@ __global__ void __launch_bounds__(THREADS, 2) gemv_kernel(const Params P) {
     }
 }
 
+// Every pass of gemv_expert starts with a block barrier before it stages
+// token rows, so consecutive experts of one block never overlap in xs.
+template <int KIND>
+__global__ void __launch_bounds__(THREADS, 2) gemv_kernel(const Params P) {
+    extern __shared__ __align__(16) int8_t xs[];  // [NT][K] token rows of the current expert
+    __shared__ float s_tok[NT];                   // their scales
+    if (P.list == nullptr) {
+        gemv_expert<KIND>(P, blockIdx.y, xs, s_tok);
+        return;
+    }
+    const int n = P.list[0];
+    for (int i = blockIdx.y; i < n; i += gridDim.y) gemv_expert<KIND>(P, P.list[1 + i], xs, s_tok);
+}
+
+// Grid: nblocks_x channel blocks times E experts (no list), or times enough
+// block rows to cover the GPU a few times over (list: the rows stride over
+// the listed experts).
 template <int KIND>
 cudaError_t launch(const Params& P, int E, int nblocks_x, cudaStream_t st) {
+    if (P.list != nullptr) E = std::max(1, std::min(E, (1024 + nblocks_x - 1) / nblocks_x));
     const size_t smem = (size_t)NT * P.K;
     cudaError_t e = cudaFuncSetAttribute(gemv_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
@@ -265,10 +285,45 @@ cudaError_t launch(const Params& P, int E, int nblocks_x, cudaStream_t st) {
 
 }  // namespace gv
 
+bool gemv_kernels_fit(const Dims& d) {
+    return d.cfmt == MOE_MSG_INT8 && d.H % gv::KSTEP == 0 && d.I % gv::KSTEP == 0 &&
+           (size_t)gv::NT * d.H <= 200 * 1024;
+}
+
 bool ffn_gemv_fits(const Dims& d) {
     const long long M = (long long)d.T * d.k;
-    return d.cfmt == MOE_MSG_INT8 && d.H % gv::KSTEP == 0 && d.I % gv::KSTEP == 0 &&
-           (size_t)gv::NT * d.H <= 200 * 1024 && M <= (long long)kGemvRowsPerExpert * d.E_phys;
+    return gemv_kernels_fit(d) && M <= (long long)kGemvRowsPerExpert * d.E_phys;
+}
+
+cudaError_t launch_gemv_gate_up(const Dims& d, const void* dbuf, const moe_dispatch_meta* meta,
+                                const int32_t* expert_offsets, const int32_t* expert_rows,
+                                const moe_expert_weights& w, float* hbuf, unsigned* hmax, int* err,
+                                const int32_t* list, int prof_slot, cudaStream_t st) {
+    gv::Params P = {};
+    P.offsets = expert_offsets; P.p2w = w.phys_to_weight; P.w = w.w_gate_up; P.s_ch = w.s_gate_up;
+    P.K = d.H; P.nout = d.I;
+    P.expert_rows = expert_rows; P.dbuf = static_cast<const int8_t*>(dbuf); P.drow = d.drow; P.meta = meta;
+    P.out = hbuf; P.rowmax = hmax;
+    P.M = (long long)d.T * d.k; P.nslots = d.nslots; P.n_sets = w.n_sets; P.list = list; P.err = err;
+    if (cudaEvent_t ev = prof_event(prof_slot, 0)) cudaEventRecord(ev, st);
+    cudaError_t e = gv::launch<gv::GATE_UP>(P, d.E_phys, d.I / 32, st);
+    if (cudaEvent_t ev = prof_event(prof_slot, 1)) cudaEventRecord(ev, st);
+    return e;
+}
+
+cudaError_t launch_gemv_down(const Dims& d, const int32_t* expert_offsets, const moe_expert_weights& w,
+                             const void* hq16, const float* sh, float* ybuf, unsigned* ymax, int* err,
+                             const int32_t* list, int prof_slot, cudaStream_t st) {
+    gv::Params P = {};
+    P.offsets = expert_offsets; P.p2w = w.phys_to_weight; P.w = w.w_down; P.s_ch = w.s_down;
+    P.K = d.I; P.nout = d.H;
+    P.hq16 = static_cast<const __half*>(hq16); P.s_h = sh;
+    P.out = ybuf; P.rowmax = ymax;
+    P.M = (long long)d.T * d.k; P.nslots = d.nslots; P.n_sets = w.n_sets; P.list = list; P.err = err;
+    if (cudaEvent_t ev = prof_event(prof_slot, 0)) cudaEventRecord(ev, st);
+    cudaError_t e = gv::launch<gv::DOWN>(P, d.E_phys, d.H / (64 * gv::DOWN_GROUPS), st);
+    if (cudaEvent_t ev = prof_event(prof_slot, 1)) cudaEventRecord(ev, st);
+    return e;
 }
 
 cudaError_t launch_ffn_gemv(const Dims& d, const void* dbuf, long long meta_off,
@@ -283,35 +338,18 @@ cudaError_t launch_ffn_gemv(const Dims& d, const void* dbuf, long long meta_off,
     float* hbuf = ws_ptr<float>(ws, wl.hbuf);
     unsigned* hmax = ws_ptr<unsigned>(ws, wl.rowmax);
     unsigned* ymax = hmax + M;
-    __half* hq16 = ws_ptr<__half>(ws, wl.hq16);
+    void* hq16 = ws_ptr<void>(ws, wl.hq16);
     float* ybuf = ws_ptr<float>(ws, wl.ybuf);
     cudaError_t e;
     if (clear && (e = clear_status(ws, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(hmax, 0, sizeof(unsigned) * 2 * M, st)) != cudaSuccess) return e;
     count_launches(1);
-
-    gv::Params P1 = {};
-    P1.offsets = expert_offsets; P1.p2w = w.phys_to_weight; P1.w = w.w_gate_up; P1.s_ch = w.s_gate_up;
-    P1.K = d.H; P1.nout = d.I;
-    P1.expert_rows = expert_rows; P1.dbuf = static_cast<const int8_t*>(dbuf); P1.drow = d.drow; P1.meta = meta;
-    P1.out = hbuf; P1.rowmax = hmax;
-    P1.M = M; P1.nslots = d.nslots; P1.n_sets = w.n_sets; P1.err = err;
-    if (cudaEvent_t ev = prof_event(0, 0)) cudaEventRecord(ev, st);
-    if ((e = gv::launch<gv::GATE_UP>(P1, d.E_phys, d.I / 32, st)) != cudaSuccess) return e;
-    if (cudaEvent_t ev = prof_event(0, 1)) cudaEventRecord(ev, st);
-
+    if ((e = launch_gemv_gate_up(d, dbuf, meta, expert_offsets, expert_rows, w, hbuf, hmax, err, nullptr, 0,
+                                 st)) != cudaSuccess)
+        return e;
     if ((e = launch_requant_rows(d.I, M, hbuf, hmax, hq16, sh, st)) != cudaSuccess) return e;
-
-    gv::Params P2 = {};
-    P2.offsets = expert_offsets; P2.p2w = w.phys_to_weight; P2.w = w.w_down; P2.s_ch = w.s_down;
-    P2.K = d.I; P2.nout = d.H;
-    P2.hq16 = hq16; P2.s_h = sh;
-    P2.out = ybuf; P2.rowmax = ymax;
-    P2.M = M; P2.nslots = d.nslots; P2.n_sets = w.n_sets; P2.err = err;
-    if (cudaEvent_t ev = prof_event(1, 0)) cudaEventRecord(ev, st);
-    if ((e = gv::launch<gv::DOWN>(P2, d.E_phys, d.H / (64 * gv::DOWN_GROUPS), st)) != cudaSuccess) return e;
-    if (cudaEvent_t ev = prof_event(1, 1)) cudaEventRecord(ev, st);
-
+    if ((e = launch_gemv_down(d, expert_offsets, w, hq16, sh, ybuf, ymax, err, nullptr, 1, st)) != cudaSuccess)
+        return e;
     return launch_retquant_rows(d, M, ybuf, ymax, expert_rows, meta, static_cast<unsigned char*>(cbuf),
                                 reinterpret_cast<float*>(static_cast<unsigned char*>(cbuf) + scale_off), err,
                                 st);

@@ -1175,8 +1175,12 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
         if ((e = cudaMemsetAsync(ready, 0, sizeof(int) * (d.T + 1), st)) != cudaSuccess) return e;
         count_launches(1);
     }
+    // experts with few rows go to the matrix-vector kernels (same outputs),
+    // listed by the tile-prefix kernel
+    const int narrow = narrow_expert_rows(d);
+    int32_t* nlist = narrow > 0 ? ws_ptr<int32_t>(ws, wl.narrow) : nullptr;
     if ((e = launch_tile_prefix(d.E_phys, BNV, expert_offsets, M, E_w, tp, err, st, ttab,
-                                w.phys_to_weight)) != cudaSuccess)
+                                w.phys_to_weight, narrow, nlist)) != cudaSuccess)
         return e;
     assemble_kernel<<<(unsigned)M, 128, 0, st>>>(d.H, expert_rows, d.nslots,
                                                  static_cast<const int8_t*>(dbuf), d.drow, meta, a16,
@@ -1204,6 +1208,10 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     P1.s_row = s_row; P1.s_ch = w.s_gate_up; P1.out_f32 = hbuf; P1.rowmax = hmax; P1.err = err;
     P1.tma_out = 1;
     if ((e = launch_gemm<EPI_GU, BNV>(P1, mwgu, mx1, mo1, st)) != cudaSuccess) return e;
+    if (narrow > 0 &&
+        (e = launch_gemv_gate_up(d, dbuf, meta, expert_offsets, expert_rows, w, hbuf, hmax, err, nlist, 2,
+                                 st)) != cudaSuccess)
+        return e;
 
     requant_kernel<<<(unsigned)M, row_threads(d.I), 0, st>>>(d.I, hbuf, hmax, hq16, sh);
     count_launches(1);
@@ -1216,6 +1224,10 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     if (int8_ret) {
         P2.out_f32 = ybuf; P2.rowmax = ymax;
         if ((e = launch_gemm<EPI_F32, BNV>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
+        if (narrow > 0 &&
+            (e = launch_gemv_down(d, expert_offsets, w, hq16, sh, ybuf, ymax, err, nlist, 3, st)) !=
+                cudaSuccess)
+            return e;
         if (fuse) {
             RetCombine R;
             R.H = d.H; R.k = d.k; R.lb = d.lb; R.S = d.S; R.expected = fc.expected;

@@ -44,6 +44,11 @@ constexpr int kTcMinTileRows = 64;
 // Routed rows per expert (on average) up to which the expert FFN streams the
 // weights through CUDA-core matrix-vector products instead of the tensor cores.
 constexpr int kGemvRowsPerExpert = 4;
+// Alongside the tensor-core GEMMs, experts with at most this many routed rows
+// (two passes of the matrix-vector kernels' 8 token rows) are computed by the
+// matrix-vector kernels: for them the tensor-core pipeline is bound by
+// converting the whole expert's weights for a handful of tokens.
+constexpr int kNarrowExpertRows = 16;
 
 // Token tiles of a grouped GEMM over n_groups groups and max_rows rows, at
 // most bm rows per tile (each group adds at most one partial tile).
@@ -62,6 +67,7 @@ struct WsLayout {
     long long ttab;        // int4  [tile_table_entries]  (set, first row, rows, group) per token tile
     long long sh;          // f32   [T*k]   requantisation scale of h
     long long ready;       // int32 [T+1]   return messages in per token, then a work ticket (fused combine)
+    long long narrow;      // int32 [E_phys+1]  number of narrow experts, then their ids
     // SIMT expert FFN
     long long acc_gu;      // int32 [T*k][2I]
     long long hq;          // int8  [T*k][I]
@@ -89,6 +95,7 @@ inline WsLayout make_ws(const Dims& d) {
     w.ttab = o;       o = align_up(o + 16LL * tile_table_entries(d.E_phys, tk, kTcMinTileRows), 256);
     w.sh = o;         o = align_up(o + 4 * tk, 256);
     w.ready = o;      o = align_up(o + 4LL * (d.T + 1), 256);
+    w.narrow = o;     o = align_up(o + 4LL * (d.E_phys + 1), 256);
     w.tc = ffn_uses_tc(d);
     if (w.tc) {
         w.rowmax = o; o = align_up(o + 8 * tk, 256);
@@ -161,8 +168,10 @@ cudaError_t launch_dispatch_trampoline(const Dims& d, const uint16_t* x, const i
 moe_status record_cuda_status(cudaError_t e);
 
 // Optional kernel timing: when enabled, the expert GEMM launches are
-// bracketed by CUDA events (slot 0: gate/up GEMM, slot 1: down GEMM).
-constexpr int kProfSlots = 2;
+// bracketed by CUDA events (slot 0: gate/up GEMM, slot 1: down GEMM; slots 2
+// and 3: the matrix-vector kernels of the narrow experts beside the
+// tensor-core GEMMs).
+constexpr int kProfSlots = 4;
 cudaEvent_t prof_event(int slot, int end);  // nullptr when profiling is off
 
 // Kernel launchers (each returns cudaGetLastError() after its launches).
@@ -189,9 +198,13 @@ cudaError_t launch_grouped_gemm_s8(int n_groups, const int32_t* offsets, long lo
 // token tile: (weight set = g2s[g] or g, first row, rows, group g).  Offsets
 // that are not a nondecreasing prefix from 0 to at most max_rows, or a weight
 // set outside [0, n_sets), give no tiles and post MOE_ERR_INDEX to *err.
+// Groups with 1..skip_rows rows get no tile (another kernel takes them); with
+// a non-null `narrow`, their ids go to narrow[1..] and their number to
+// narrow[0].
 cudaError_t launch_tile_prefix(int G, int BM, const int32_t* offsets, long long max_rows, int n_sets,
                                int32_t* tile_prefix, int* err, cudaStream_t st,
-                               int4* table = nullptr, const int32_t* g2s = nullptr);
+                               int4* table = nullptr, const int32_t* g2s = nullptr, int skip_rows = 0,
+                               int32_t* narrow = nullptr);
 cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long long max_rows,
                                    const int32_t* row_index, const int8_t* A, long long lda,
                                    const int8_t* B, int N, int K, int32_t* C, void* ws,
@@ -229,6 +242,22 @@ cudaError_t launch_retquant_rows(const Dims& d, long long M, const float* y, con
 // average, INT8 return messages, H and I multiples of 512): the expert FFN
 // by streamed CUDA-core matrix-vector products, same outputs as launch_ffn_tc.
 bool ffn_gemv_fits(const Dims& d);
+// Whether the matrix-vector kernels apply to the shape at all (INT8 return
+// messages, H and I multiples of 512, token rows within shared memory).
+bool gemv_kernels_fit(const Dims& d);
+// Rows up to which an expert runs on the matrix-vector kernels beside the
+// tensor-core GEMMs (0: none).
+inline int narrow_expert_rows(const Dims& d) { return gemv_kernels_fit(d) ? kNarrowExpertRows : 0; }
+// The matrix-vector kernels on their own, writing h / y and their row maxima
+// exactly as the tensor-core epilogues do: every expert (list == nullptr), or
+// the experts listed in list[1..list[0]]; prof_slot selects the timing events.
+cudaError_t launch_gemv_gate_up(const Dims& d, const void* dbuf, const moe_dispatch_meta* meta,
+                                const int32_t* expert_offsets, const int32_t* expert_rows,
+                                const moe_expert_weights& w, float* hbuf, unsigned* hmax, int* err,
+                                const int32_t* list, int prof_slot, cudaStream_t st);
+cudaError_t launch_gemv_down(const Dims& d, const int32_t* expert_offsets, const moe_expert_weights& w,
+                             const void* hq16, const float* sh, float* ybuf, unsigned* ymax, int* err,
+                             const int32_t* list, int prof_slot, cudaStream_t st);
 cudaError_t launch_ffn_gemv(const Dims& d, const void* dbuf, long long meta_off,
                             const int32_t* expert_offsets, const int32_t* expert_rows,
                             const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,

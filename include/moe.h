@@ -153,6 +153,16 @@ typedef struct {
 enum { MOE_FFN_CUDA_CORE = 0, MOE_FFN_TENSOR_CORE = 1, MOE_FFN_GEMV = 2 };
 moe_status moe_expert_ffn_path(const moe_shape* shape, int32_t* path);
 
+/* On the tensor-core path, physical experts with 1 to *rows routed rows are
+ * computed by the weight-streaming matrix-vector kernels instead, in the
+ * same launch sequence and with the same outputs bit for bit: for an expert
+ * with a handful of tokens the tensor-core pipeline spends its time
+ * converting the expert's whole weight matrix, while the matrix-vector
+ * kernels stream it at the memory roofline.  *rows is 16 where those kernels
+ * apply (INT8 return messages, H and I multiples of 512), else 0 (and 0 when
+ * the whole FFN already runs on them, MOE_FFN_GEMV).  Host only. */
+moe_status moe_expert_ffn_narrow_rows(const moe_shape* shape, int32_t* rows);
+
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(moe_status s);
 
@@ -490,7 +500,11 @@ const char* moe_last_cuda_error(void);
  * tensor-core expert GEMM launch (or matrix-vector kernel of the decode
  * path, see moe_expert_ffn_path) is bracketed by CUDA events on its stream;
  * moe_profile_read synchronises on them and returns the durations (ms) of
- * the most recent gate/up kernel (ms[0]) and down kernel (ms[1]), -1 if none. */
+ * the most recent gate/up kernel (ms[0]) and down kernel (ms[1]), and of the
+ * matrix-vector kernels that took the narrow experts beside the tensor-core
+ * GEMMs (ms[2] gate/up, ms[3] down; see moe_expert_ffn_narrow_rows); -1 for
+ * a kernel not run since profiling was enabled.  n (>= 1) values are
+ * written. */
 moe_status moe_profile_enable(int32_t on);
 moe_status moe_profile_read(float* ms, int32_t n);
 

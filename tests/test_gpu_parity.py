@@ -72,11 +72,13 @@ def test_route_ties_and_k_equals_e():
 
 
 # -------------------------------------------------------------- whole layer
-def _full_layer_check(w, cfmt, xb=None):
+def _full_layer_check(w, cfmt, xb=None, lg=None):
     """Every intermediate and the output of moe_layer against the oracle
-    (hidden rows from the workload's generator unless xb, bf16 bits, is given)."""
+    (hidden rows and logits from the workload's generator unless xb, bf16
+    bits, or lg, f32 logits, is given)."""
     layer = make_layer(w, cfmt)
-    lg = synth.logits(w)
+    if lg is None:
+        lg = synth.logits(w)
     if xb is None:
         xb = synth.hidden_bits(w)
     out = layer.forward(torch.from_numpy(lg).cuda(), bits_to_bf16_tensor(xb))
@@ -176,6 +178,41 @@ def _special_rows(w):
 def test_layer_special_rows(dims):
     w = synth.custom("special_rows", seed=7, **dims)
     _full_layer_check(w, B.MOE_MSG_INT8, xb=_special_rows(w))
+
+
+def _logits_for_counts(T, E, k, counts, seed):
+    """Logits whose top-k routing gives each expert e exactly counts[e] rows
+    (sum = T * k, each count at most T): the list in which expert e appears
+    counts[e] times, expert by expert, fills slot j of token t at position
+    j * T + t, so an expert's copies (fewer than T apart) never meet in one
+    token; the chosen experts get large distinct logits."""
+    rng = np.random.default_rng(seed)
+    deck = np.repeat(np.arange(E), counts)
+    assert len(deck) == T * k and max(counts) <= T
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    choice = deck.reshape(k, T).T
+    for t in range(T):
+        for j, e in enumerate(choice[t]):
+            lg[t, e] = 20.0 - j
+    return lg
+
+
+@pytest.mark.parametrize("counts", [
+    [16, 17, 1, 2, 60, 8, 120, 32],     # both sides of the 16-row threshold, one expert at 16
+    [0, 3, 128, 15, 16, 0, 17, 77],     # empty experts, one in every token
+])
+def test_layer_hybrid_narrow_experts(counts):
+    """Tensor-core path with the narrow experts (1..16 rows) on the
+    matrix-vector kernels: H and I multiples of 512, INT8 return messages."""
+    T, E, k = 128, 8, 2
+    w = synth.custom("hybrid", seed=13, T=T, H=512, E_log=E, k=k, I=512, R=4, S=4)
+    assert B.moe_expert_ffn_path(shape_of(w)) == B.MOE_FFN_TENSOR_CORE
+    assert B.moe_expert_ffn_narrow_rows(shape_of(w)) == 16
+    counts = np.array(counts)
+    lg = _logits_for_counts(T, E, k, counts, seed=len(counts))
+    _, _, _, cnt = oracle.route(lg, k)
+    assert (cnt == counts).all()
+    _full_layer_check(w, B.MOE_MSG_INT8, lg=lg)
 
 
 def test_layer_eplb_tiny():
