@@ -50,24 +50,30 @@ FFN_TC_SRC = os.path.join(ROOT, "expert_dispatch_combine_gb300", "csrc", "ffn_tc
 FFN_GEMV_SRC = os.path.join(ROOT, "expert_dispatch_combine_gb300", "csrc", "ffn_gemv.cu")
 
 
-def measured_traffic(workload: str, gemv: bool = False):
+def measured_traffic(alg_bytes: int, gemv: bool = False):
     """DRAM bytes per launch of the gate/up kernel (tensor-core GEMM, or the
-    decode matrix-vector kernel) from the committed ncu summary, if it was
-    taken on this workload with the current kernel source (else None)."""
-    prefix, src_file = ("gemv_gate_up_", FFN_GEMV_SRC) if gemv else ("gemm_tc_gate_up_", FFN_TC_SRC)
-    path = os.path.join(ROOT, "profiles", prefix + workload + ".md")
+    matrix-vector kernel of the decode path) for a launch of `alg_bytes`
+    algorithmic bytes: the traffic / algorithmic ratio the committed ncu
+    summary measured on its small workload (prof_e32, prof_decode_e32), times
+    alg_bytes; None unless that summary was taken with the current kernel
+    source.  The kernel's traffic grows with the units it serves (weights per
+    touched expert, rows, h), so the ratio carries over."""
+    name, src_file = (("gemv_gate_up_prof_decode_e32.md", FFN_GEMV_SRC) if gemv
+                      else ("gemm_tc_gate_up_prof_e32.md", FFN_TC_SRC))
     try:
-        txt = open(path).read()
+        txt = open(os.path.join(ROOT, "profiles", name)).read()
         src = hashlib.sha1(open(src_file, "rb").read()).hexdigest()
     except OSError:
         return None
-    kv = dict(l.split(":", 1) for l in txt.splitlines() if l.startswith(("source_sha1:", "traffic_bytes_per_launch:")))
+    keys = ("source_sha1:", "traffic_bytes_per_launch:", "algorithmic_bytes_per_launch:")
+    kv = dict(l.split(":", 1) for l in txt.splitlines() if l.startswith(keys))
     if kv.get("source_sha1", "").strip() != src:
         return None
     try:
-        return int(kv["traffic_bytes_per_launch"].strip())
-    except (KeyError, ValueError):
+        ratio = int(kv["traffic_bytes_per_launch"]) / int(kv["algorithmic_bytes_per_launch"])
+    except (KeyError, ValueError, ZeroDivisionError):
         return None
+    return int(round(ratio * alg_bytes))
 
 
 # ------------------------------------------------------------- bookkeeping
@@ -517,7 +523,9 @@ def run_ours(args, rank: int, world: int):
         ridge = peak_tc * 1e12 / (hbm * 1e9)
         if intensity >= ridge:
             roofline = {"bound": "tensor", "achieved": gu_tflops, "peak": peak_tc, "unit": "TFLOP/s",
-                        "frac": gu_tflops / peak_tc, "traffic": measured_traffic(w.name, ffn_path == B.MOE_FFN_GEMV),
+                        "frac": gu_tflops / peak_tc,
+                        "traffic": measured_traffic(alg["gate_up_bytes"], ffn_path == B.MOE_FFN_GEMV),
+                        "traffic_source": "scaled from the small-workload ncu capture (profiles/)",
                         "kernel": gu_name,
                         "algorithmic_ops_per_launch": alg["gate_up_ops"],
                         "algorithmic_bytes_per_launch": alg["gate_up_bytes"],
@@ -527,7 +535,9 @@ def run_ours(args, rank: int, world: int):
         else:  # decode-sized batches stream the weights: HBM-bound
             gu_gbs = alg["gate_up_bytes"] / (kern["gemm_gate_up"] / 1000) / 1e9
             roofline = {"bound": "hbm", "achieved": gu_gbs, "peak": hbm, "unit": "GB/s",
-                        "frac": gu_gbs / hbm, "traffic": measured_traffic(w.name, ffn_path == B.MOE_FFN_GEMV),
+                        "frac": gu_gbs / hbm,
+                        "traffic": measured_traffic(alg["gate_up_bytes"], ffn_path == B.MOE_FFN_GEMV),
+                        "traffic_source": "scaled from the small-workload ncu capture (profiles/)",
                         "kernel": gu_name,
                         "algorithmic_ops_per_launch": alg["gate_up_ops"],
                         "algorithmic_bytes_per_launch": alg["gate_up_bytes"],
