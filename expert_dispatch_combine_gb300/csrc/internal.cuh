@@ -45,10 +45,13 @@ constexpr int kTcMinTileRows = 64;
 // weights through CUDA-core matrix-vector products instead of the tensor cores.
 constexpr int kGemvRowsPerExpert = 4;
 // Alongside the tensor-core GEMMs, experts with at most this many routed rows
-// (two passes of the matrix-vector kernels' 8 token rows) are computed by the
-// matrix-vector kernels: for them the tensor-core pipeline is bound by
-// converting the whole expert's weights for a handful of tokens.
-constexpr int kNarrowExpertRows = 16;
+// (one pass of the matrix-vector kernels' 8 token rows, so their weights
+// stream once) are computed by the matrix-vector kernels: for them the
+// tensor-core pipeline is bound by converting the whole expert's weights for
+// a handful of tokens.  Measured at c2_decode_zipf: 8 rows 8.77 ms per layer,
+// 12 rows 8.83, 16 rows 8.84, 24 rows 9.16, 48 rows 9.60 (each extra pass
+// streams the weights again).
+constexpr int kNarrowExpertRows = 8;
 
 // Token tiles of a grouped GEMM over n_groups groups and max_rows rows, at
 // most bm rows per tile (each group adds at most one partial tile).

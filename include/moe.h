@@ -158,7 +158,7 @@ moe_status moe_expert_ffn_path(const moe_shape* shape, int32_t* path);
  * same launch sequence and with the same outputs bit for bit: for an expert
  * with a handful of tokens the tensor-core pipeline spends its time
  * converting the expert's whole weight matrix, while the matrix-vector
- * kernels stream it at the memory roofline.  *rows is 16 where those kernels
+ * kernels stream it at the memory roofline.  *rows is 8 where those kernels
  * apply (INT8 return messages, H and I multiples of 512), else 0 (and 0 when
  * the whole FFN already runs on them, MOE_FFN_GEMV).  Host only. */
 moe_status moe_expert_ffn_narrow_rows(const moe_shape* shape, int32_t* rows);

@@ -198,16 +198,16 @@ def _logits_for_counts(T, E, k, counts, seed):
 
 
 @pytest.mark.parametrize("counts", [
-    [16, 17, 1, 2, 60, 8, 120, 32],     # both sides of the 16-row threshold, one expert at 16
+    [8, 9, 1, 2, 60, 16, 120, 40],      # both sides of the 8-row threshold, one expert at 8
     [0, 3, 128, 15, 16, 0, 17, 77],     # empty experts, one in every token
 ])
 def test_layer_hybrid_narrow_experts(counts):
-    """Tensor-core path with the narrow experts (1..16 rows) on the
+    """Tensor-core path with the narrow experts (1..8 rows) on the
     matrix-vector kernels: H and I multiples of 512, INT8 return messages."""
     T, E, k = 128, 8, 2
     w = synth.custom("hybrid", seed=13, T=T, H=512, E_log=E, k=k, I=512, R=4, S=4)
     assert B.moe_expert_ffn_path(shape_of(w)) == B.MOE_FFN_TENSOR_CORE
-    assert B.moe_expert_ffn_narrow_rows(shape_of(w)) == 16
+    assert B.moe_expert_ffn_narrow_rows(shape_of(w)) == 8
     counts = np.array(counts)
     lg = _logits_for_counts(T, E, k, counts, seed=len(counts))
     _, _, _, cnt = oracle.route(lg, k)
