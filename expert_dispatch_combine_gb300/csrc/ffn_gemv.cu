@@ -15,9 +15,9 @@
 // each warp streams 8 weight rows with coalesced 16-byte loads and forms the
 // dot products with the (at most 8) token rows of its expert, held in shared
 // memory, by dp4a: four int8 products summed into int32, exact.  The outputs
-// are those of the tensor-core path, bit for bit: h = SiLU(g) u in f32 with
-// its per-row |h| maximum (gate/up), y in f32 with its per-row |y| maximum
-// (down); requant_rows and retquant_rows take it from there.
+// are those of the tensor-core path, bit for bit: g and u in f32 (gate/up;
+// SwiGLU follows in the requantisation kernel), y in f32 with its per-row
+// |y| maximum (down); requant_rows and retquant_rows take it from there.
 //
 // Block (256 threads, 8 warps) = one expert and 32 gate/up channel pairs
 // (gate/up), or one expert and 4 groups of 64 output channels (down: its
@@ -63,8 +63,8 @@ struct Params {
     const moe_dispatch_meta* meta;
     const __half* hq16;
     const float* s_h;             // down: per-row scale of h
-    float* out;                   // h [M][I] or y [M][H]
-    unsigned* rowmax;             // [M] |out| maximum (float bits)
+    float* out;                   // g and u [M][2I] (gate/up) or y [M][H] (down)
+    unsigned* rowmax;             // down: [M] |y| maximum (float bits)
     long long M;                  // routed rows (rows of out)
     long long nslots;             // dispatch slots (rows of dbuf)
     int n_sets;                   // weight sets
@@ -199,34 +199,16 @@ __device__ __forceinline__ void gemv_expert(const Params& P, int e, int8_t* xs, 
             const int row = lane >> 2, tl = 2 * (lane & 3);
             if constexpr (KIND == GATE_UP) {
                 // lanes 0..15 hold gate rows, lanes 16..31 the up rows of the same
-                // channels and tokens
-                const int c = ch0 + (row & 3);
-                const int up0 = __shfl_xor_sync(0xffffffffu, acc[0], 16);
-                const int up1 = __shfl_xor_sync(0xffffffffu, acc[1], 16);
-                float mx[2] = {0.f, 0.f};
-                if (lane < 16) {
-                    const float sg = P.s_ch[(long long)set * 2 * P.nout + c];
-                    const float su = P.s_ch[(long long)set * 2 * P.nout + P.nout + c];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int t = tl + u;
-                        if (t < n) {
-                            const float st = s_tok[t];
-                            const float g = __fmul_rn(__fmul_rn(__int2float_rn(acc[u]), st), sg);
-                            const float uv = __fmul_rn(__fmul_rn(__int2float_rn(u ? up1 : up0), st), su);
-                            const float h = __fmul_rn(silu_fast(g), uv);
-                            P.out[(long long)(t0 + t) * P.nout + c] = h;
-                            mx[u] = fabsf(h);
-                        }
-                    }
-                }
-                // per-token maximum over the warp's 4 channels (lane bits 2 and 3)
+                // channels and tokens: each writes its scaled projection, g to
+                // column c and u to column I + c of the token's [2I] row
+                const int col = (lane < 16 ? 0 : P.nout) + ch0 + (row & 3);
+                const float sc = P.s_ch[(long long)set * 2 * P.nout + col];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    float m = mx[u];
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                    if (lane < 4 && tl + u < n) atomicMax(&P.rowmax[t0 + tl + u], __float_as_uint(m));
+                    const int t = tl + u;
+                    if (t < n)
+                        P.out[(long long)(t0 + t) * 2 * P.nout + col] =
+                            __fmul_rn(__fmul_rn(__int2float_rn(acc[u]), s_tok[t]), sc);
                 }
             } else {
                 const int c = ch0 + g * 64 + row;
@@ -297,13 +279,13 @@ bool ffn_gemv_fits(const Dims& d) {
 
 cudaError_t launch_gemv_gate_up(const Dims& d, const void* dbuf, const moe_dispatch_meta* meta,
                                 const int32_t* expert_offsets, const int32_t* expert_rows,
-                                const moe_expert_weights& w, float* hbuf, unsigned* hmax, int* err,
+                                const moe_expert_weights& w, float* gubuf, int* err,
                                 const int32_t* list, int prof_slot, cudaStream_t st) {
     gv::Params P = {};
     P.offsets = expert_offsets; P.p2w = w.phys_to_weight; P.w = w.w_gate_up; P.s_ch = w.s_gate_up;
     P.K = d.H; P.nout = d.I;
     P.expert_rows = expert_rows; P.dbuf = static_cast<const int8_t*>(dbuf); P.drow = d.drow; P.meta = meta;
-    P.out = hbuf; P.rowmax = hmax;
+    P.out = gubuf;
     P.M = (long long)d.T * d.k; P.nslots = d.nslots; P.n_sets = w.n_sets; P.list = list; P.err = err;
     if (cudaEvent_t ev = prof_event(prof_slot, 0)) cudaEventRecord(ev, st);
     cudaError_t e = gv::launch<gv::GATE_UP>(P, d.E_phys, d.I / 32, st);
@@ -335,19 +317,18 @@ cudaError_t launch_ffn_gemv(const Dims& d, const void* dbuf, long long meta_off,
         reinterpret_cast<const moe_dispatch_meta*>(static_cast<const char*>(dbuf) + meta_off);
     int* err = ws_ptr<int>(ws, 0);
     float* sh = ws_ptr<float>(ws, wl.sh);
-    float* hbuf = ws_ptr<float>(ws, wl.hbuf);
-    unsigned* hmax = ws_ptr<unsigned>(ws, wl.rowmax);
-    unsigned* ymax = hmax + M;
+    float* gubuf = ws_ptr<float>(ws, wl.gubuf);
+    unsigned* ymax = ws_ptr<unsigned>(ws, wl.rowmax);
     void* hq16 = ws_ptr<void>(ws, wl.hq16);
     float* ybuf = ws_ptr<float>(ws, wl.ybuf);
     cudaError_t e;
     if (clear && (e = clear_status(ws, st)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(hmax, 0, sizeof(unsigned) * 2 * M, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(ymax, 0, sizeof(unsigned) * M, st)) != cudaSuccess) return e;
     count_launches(1);
-    if ((e = launch_gemv_gate_up(d, dbuf, meta, expert_offsets, expert_rows, w, hbuf, hmax, err, nullptr, 0,
+    if ((e = launch_gemv_gate_up(d, dbuf, meta, expert_offsets, expert_rows, w, gubuf, err, nullptr, 0,
                                  st)) != cudaSuccess)
         return e;
-    if ((e = launch_requant_rows(d.I, M, hbuf, hmax, hq16, sh, st)) != cudaSuccess) return e;
+    if ((e = launch_requant_rows(d.I, M, gubuf, hq16, sh, st)) != cudaSuccess) return e;
     if ((e = launch_gemv_down(d, expert_offsets, w, hq16, sh, ybuf, ymax, err, nullptr, 1, st)) != cudaSuccess)
         return e;
     return launch_retquant_rows(d, M, ybuf, ymax, expert_rows, meta, static_cast<unsigned char*>(cbuf),

@@ -34,6 +34,11 @@
 //     one pair while the MMAs of the others run.
 //   Epilogue: each 16-token group is scaled, staged in shared memory and
 //     written with one TMA tensor store (partial groups use plain stores).
+// The gate/up GEMM computes the gate and up projections g, u of all 2I
+// channels in one launch (P088) and writes them as f32; SwiGLU h = SiLU(g) u,
+// its row maximum and the token-wise requantisation run in one row kernel
+// (requant_kernel), so the SiLU's instructions stay off the GEMM's critical
+// path.  The down GEMM's epilogue writes y and reduces its row maximum.
 // Warp roles (16 warps): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
 // warps 4-7 converter, warps 8-15 two drain/epilogue warpgroups.  Register
 // budgets are moved between warpgroups with setmaxnreg (the totals stay
@@ -111,14 +116,14 @@ struct Params {
     const int32_t* g2s;          // nullable: weight set of each group
     int K;                       // reduction length, multiple of 64
     int rows_per_set;            // weight rows per set
-    int nout;                    // output channels per set (EPI_GU: I)
+    int nout;                    // output channels per set (EPI_GU: 2I, gate then up)
     int mb_count;                // channel blocks per token tile
     int box1_off;                // row offset of the second 64-row weight box
     const float* s_row;          // per token-row scale
     const float* s_ch;           // per-channel weight scales [set][rows_per_set]
     int32_t* c_i32;              // EPI_I32: [M][nout]
-    float* out_f32;              // EPI_GU: h [M][I]; EPI_F32: y [M][nout]
-    unsigned* rowmax;            // EPI_GU / EPI_F32: per-row absmax of the output (float bits)
+    float* out_f32;              // EPI_GU: g and u [M][2I]; EPI_F32: y [M][nout]
+    unsigned* rowmax;            // EPI_F32: per-row absmax of y (float bits)
     const int32_t* expert_rows;  // EPI_BF16MSG: row -> dispatch slot
     const moe_dispatch_meta* meta;
     unsigned char* cbuf;
@@ -204,16 +209,8 @@ __device__ __forceinline__ void epilogue_direct(const Params& P, const TileInfo&
                 if (j0 + j < ti.nvalid) P.c_i32[(long long)(ti.r0 + j0 + j) * P.nout + ch] = iv[j];
         }
     } else if constexpr (EPI == EPI_GU || EPI == EPI_F32) {
-        int col, ld;
-        if constexpr (EPI == EPI_GU) {
-            // gate channel c in lane 2c, up channel c in lane 2c + 1 (converter)
-            col = (row & 1) ? P.nout + ti.mb * 64 + (row >> 1) : ti.mb * 64 + (row >> 1);
-            ld = 2 * P.nout;
-        } else {
-            col = ti.mb * 128 + row;
-            ld = P.nout;
-        }
-        const bool chok = (EPI == EPI_GU) || col < P.nout;
+        const int col = ti.mb * 128 + row, ld = P.nout;
+        const bool chok = col < P.nout;
         const float sc = chok ? P.s_ch[(long long)ti.set * P.rows_per_set + col] : 0.f;
         const float sr_l = lane_ok ? P.s_row[ti.r0 + j0 + lane] : 0.f;
         float* out = P.out_f32 + (long long)ti.r0 * ld + col;
@@ -252,61 +249,32 @@ __device__ __forceinline__ void epilogue_direct(const Params& P, const TileInfo&
 }
 
 // Epilogue for a full 16-token group through shared memory and one TMA
-// tensor store (two for EPI_GU: the gate half and the up half).  All four
-// warps of the drain warpgroup take part; `leader` issues the store.
+// tensor store (int32 results).  All four warps of the drain warpgroup take
+// part; `leader` issues the store.
 template <int EPI>
 __device__ __forceinline__ bool epilogue_tma(const Params& P, const TileInfo& ti, int row,
                                              int lane, int j0, const int (&iv)[GT], uint8_t* stg,
                                              const CUtensorMap* tmO, WgBarrier& wg, bool leader) {
-    if constexpr (EPI == EPI_I32) {
-        int32_t* o = reinterpret_cast<int32_t*>(stg) + row;
+    int32_t* o = reinterpret_cast<int32_t*>(stg) + row;
 #pragma unroll
-        for (int j = 0; j < GT; ++j) o[j * 128] = iv[j];
-    } else {
-        const float sr_l = lane < GT ? P.s_row[ti.r0 + j0 + lane] : 0.f;
-        int col;
-        float* o;
-        if constexpr (EPI == EPI_GU) {
-            col = (row & 1) ? P.nout + ti.mb * 64 + (row >> 1) : ti.mb * 64 + (row >> 1);
-            o = reinterpret_cast<float*>(stg) + ((row & 1) ? GT * 64 : 0) + (row >> 1);
-        } else {
-            col = ti.mb * 128 + row;
-            o = reinterpret_cast<float*>(stg) + row;
-        }
-        const bool chok = (EPI == EPI_GU) || col < P.nout;
-        const float sc = chok ? P.s_ch[(long long)ti.set * P.rows_per_set + col] : 0.f;
-#pragma unroll
-        for (int j = 0; j < GT; ++j) {
-            const float sr = __shfl_sync(0xffffffffu, sr_l, j);
-            o[j * (EPI == EPI_GU ? 64 : 128)] = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sc);
-        }
-    }
+    for (int j = 0; j < GT; ++j) o[j * 128] = iv[j];
     ptx::fence_proxy_async_smem();
     if (!wg.sync(lane, P.err)) return false;
     if (leader) {
-        const uint32_t src = ptx::smem_addr(stg);
-        if constexpr (EPI == EPI_GU) {
-            ptx::tma_store_2d(tmO, ti.mb * 64, ti.r0 + j0, src);
-            ptx::tma_store_2d(tmO, P.nout + ti.mb * 64, ti.r0 + j0, src + GT * 64 * 4);
-        } else {
-            ptx::tma_store_2d(tmO, ti.mb * 128, ti.r0 + j0, src);
-        }
+        ptx::tma_store_2d(tmO, ti.mb * 128, ti.r0 + j0, ptx::smem_addr(stg));
         ptx::bulk_commit();
         ptx::bulk_wait_read0();
     }
     return wg.sync(lane, P.err);  // staging buffer free again
 }
 
-// Epilogue of the expert FFN for one 16-token group, staged in shared memory.
-//   EPI_GU: lane 2c holds the gate projection g of the tile's channel c and
-//     lane 2c + 1 the up projection u of the same channel; the two lanes
-//     swap halves through a shuffle and each forms h = SiLU(g) * u for 8 of
-//     the group's tokens, which it stores into the staging buffer.
-//   EPI_F32: y of the tile's 128 output channels.
-// The per-row absolute maximum of this tile's outputs goes to `rowmax` with
-// an atomic max (the token-wise requantisation needs the whole row); the
-// values go out with one TMA tensor store for a full group, plain stores for
-// a partial one.  All four warps of the drain warpgroup take part.
+// Epilogue of the expert FFN for one 16-token group, staged in shared memory:
+// v = (acc * s_row) * s_ch for the tile's 128 channels (EPI_GU: the gate and
+// up projections g and u, channels of [2I]; EPI_F32: y).  For EPI_F32 the
+// per-row absolute maximum of this tile's outputs also goes to `rowmax` with
+// an atomic max (the INT8 return message needs the whole row).  The values go
+// out with one TMA tensor store for a full group, plain stores for a partial
+// one.  All four warps of the drain warpgroup take part.
 // Groups alternate between two staging buffers, with one warpgroup barrier
 // per group: every thread's reads of a buffer precede its arrival at the next
 // group's barrier, and before that barrier the leader waits for the previous
@@ -318,94 +286,39 @@ __device__ __forceinline__ bool epilogue_staged(const Params& P, const TileInfo&
                                                 const CUtensorMap* tmO, WgBarrier& wg, bool leader) {
     const int nv = min(GT, ti.nvalid - j0);  // valid tokens in this group (>= 1)
     const float sr_l = lane < nv ? P.s_row[ti.r0 + j0 + lane] : 0.f;
-    if constexpr (EPI == EPI_GU) {
-        // lane 2c holds the gate projection g of channel c, lane 2c + 1 the up
-        // projection u (see the converter); the even lane forms h for tokens
-        // 0..7 of the group, the odd lane for tokens 8..15, after swapping
-        // the other half through a shuffle
-        const int c = row >> 1;
-        const bool up = row & 1;
-        const int colw = up ? P.nout + ti.mb * 64 + c : ti.mb * 64 + c;
-        const float sc = P.s_ch[(long long)ti.set * P.rows_per_set + colw];
-        float v[GT];
+    const int col = ti.mb * 128 + row;
+    const bool chok = col < P.nout;
+    const float sd = chok ? P.s_ch[(long long)ti.set * P.rows_per_set + col] : 0.f;
 #pragma unroll
-        for (int j = 0; j < GT; ++j) {
-            const float sr = __shfl_sync(0xffffffffu, sr_l, j);
-            v[j] = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sc);
-        }
-        const int tb = up ? 8 : 0;  // this thread's tokens tb .. tb+7
-        float hv[8];
+    for (int j = 0; j < GT; ++j) {
+        const float sr = __shfl_sync(0xffffffffu, sr_l, j);
+        stg[j * 128 + row] = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sd);  // 0 off the edge
+    }
+    ptx::fence_proxy_async_smem();
+    if (leader) ptx::bulk_wait_read0();  // previous group's store has read the other buffer
+    if (!wg.sync(lane, P.err)) return false;
+    if constexpr (EPI == EPI_F32) {  // token row >> 3 of the group; this thread's 16 channels
+        const int j = row >> 3, p = row & 7;
+        float m = 0.f;
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-            // even lane sends g of tokens 8..15, odd lane u of tokens 0..7
-            const float o = __shfl_xor_sync(0xffffffffu, up ? v[jj] : v[8 + jj], 1);
-            const float g = up ? o : v[jj];
-            const float u = up ? v[8 + jj] : o;
-            hv[jj] = __fmul_rn(silu_fast(g), u);
+        for (int q = 0; q < 4; ++q) {
+            const float4 a = *reinterpret_cast<const float4*>(stg + j * 128 + 32 * q + 4 * p);
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
         }
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        if (p == 0 && j < nv) atomicMax(&P.rowmax[ti.r0 + j0 + j], __float_as_uint(m));
+    }
+    if (nv == GT && P.tma_out) {
+        if (leader) {
+            ptx::tma_store_2d(tmO, ti.mb * 128, ti.r0 + j0, ptx::smem_addr(stg));
+            ptx::bulk_commit();
+        }
+    } else if (chok) {
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) stg[(tb + jj) * 64 + c] = hv[jj];
-        ptx::fence_proxy_async_smem();
-        if (leader) ptx::bulk_wait_read0();  // previous group's store has read the other buffer
-        if (!wg.sync(lane, P.err)) return false;
-        {  // token row / 8 = row >> 3 of the group; this thread's 8 channels
-            const int j = row >> 3, p = row & 7;
-            const float4 a = *reinterpret_cast<const float4*>(stg + j * 64 + 4 * p);
-            const float4 b = *reinterpret_cast<const float4*>(stg + j * 64 + 32 + 4 * p);
-            float m = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
-                            fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            if (p == 0 && j < nv) atomicMax(&P.rowmax[ti.r0 + j0 + j], __float_as_uint(m));
-        }
-        if (nv == GT && P.tma_out) {
-            if (leader) {
-                ptx::tma_store_2d(tmO, ti.mb * 64, ti.r0 + j0, ptx::smem_addr(stg));
-                ptx::bulk_commit();
-            }
-        } else {
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                const int j = tb + jj;
-                if (j < nv) P.out_f32[(long long)(ti.r0 + j0 + j) * P.nout + ti.mb * 64 + c] = hv[jj];
-            }
-        }
-    } else {  // EPI_F32
-        const int col = ti.mb * 128 + row;
-        const bool chok = col < P.nout;
-        const float sd = chok ? P.s_ch[(long long)ti.set * P.rows_per_set + col] : 0.f;
-#pragma unroll
-        for (int j = 0; j < GT; ++j) {
-            const float sr = __shfl_sync(0xffffffffu, sr_l, j);
-            stg[j * 128 + row] = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sd);  // 0 off the edge
-        }
-        ptx::fence_proxy_async_smem();
-        if (leader) ptx::bulk_wait_read0();  // previous group's store has read the other buffer
-        if (!wg.sync(lane, P.err)) return false;
-        {  // token row >> 3 of the group; this thread's 16 channels
-            const int j = row >> 3, p = row & 7;
-            float m = 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 a = *reinterpret_cast<const float4*>(stg + j * 128 + 32 * q + 4 * p);
-                m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
-            }
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            if (p == 0 && j < nv) atomicMax(&P.rowmax[ti.r0 + j0 + j], __float_as_uint(m));
-        }
-        if (nv == GT && P.tma_out) {
-            if (leader) {
-                ptx::tma_store_2d(tmO, ti.mb * 128, ti.r0 + j0, ptx::smem_addr(stg));
-                ptx::bulk_commit();
-            }
-        } else if (chok) {
-#pragma unroll
-            for (int j = 0; j < GT; ++j)
-                if (j < nv) P.out_f32[(long long)(ti.r0 + j0 + j) * P.nout + col] = stg[j * 128 + row];
-        }
+        for (int j = 0; j < GT; ++j)
+            if (j < nv) P.out_f32[(long long)(ti.r0 + j0 + j) * P.nout + col] = stg[j * 128 + row];
     }
     return true;
 }
@@ -486,7 +399,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
                 const TileInfo ti = decode(P, tile, e_next);
                 e_next = tile_entry(P, tile + gridDim.x, total_tiles);
-                const int yw0 = ti.set * P.rows_per_set + (EPI == EPI_GU ? ti.mb * 64 : ti.mb * 128);
+                const int yw0 = ti.set * P.rows_per_set + ti.mb * 128;
                 const int yw1 = yw0 + P.box1_off;
                 // nearly full tiles take their activations in one BN-row box
                 // (same shared-memory image as the 32-row boxes), ragged ones
@@ -575,16 +488,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         const int wq = warp & 3;
         const int row = wq * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-        // EPI_GU: TMEM lane 2c takes gate channel c (shared-memory row c), lane
-        // 2c + 1 the matching up channel (row 64 + c), so that the epilogue
-        // finds g and u of one channel in neighbouring lanes
-        const int srow = EPI == EPI_GU ? ((row & 1) << 6) | (row >> 1) : row;
-        const uint8_t* arow_base = stages + B_BYTES + (srow >> 6) * 4096 + (srow & 63) * 64;
-        const int sw = (srow >> 1) & 3;
-        // EPI_GU: a gate lane and its up lane read the same bank positions of
-        // their two boxes; the up lane takes its chunks in the order c ^ 2,
-        // which keeps every 8-lane phase of the loads free of bank conflicts
-        const int rot = EPI == EPI_GU ? (row & 1) << 1 : 0;
+        // TMEM lane `row` takes weight row `row` of the tile (two 64-row boxes)
+        const uint8_t* arow_base = stages + B_BYTES + (row >> 6) * 4096 + (row & 63) * 64;
+        const int sw = (row >> 1) & 3;
         uint32_t pr = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
@@ -608,11 +514,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     const uint8_t* arow = arow_base + (2 * sp + j) * STAGE_BYTES;
                     uint4 w[4];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ rot ^ sw) << 4));
-                    if (EPI == EPI_GU && rot) {  // back to chunk order
-                        const uint4 t0 = w[0], t1 = w[1];
-                        w[0] = w[2]; w[1] = w[3]; w[2] = t0; w[3] = t1;
-                    }
+                    for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ sw) << 4));
                     uint32_t v[32];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -774,11 +676,11 @@ __device__ __forceinline__ float block_max(float v, float* s_red) {
     return r;
 }
 
-// The row kernels below take 16 consecutive values per thread and chunk and
-// issue the loads of two chunks (eight 16-byte loads) before quantising.
+// The row kernels below take 16 consecutive values per thread and chunk.
 // requant runs with row_threads(I) threads, enough that a row is loaded in
 // one pass of two chunks per thread (I = 2048: 64 threads), so a block waits
-// for memory once; retquant keeps kRowThreads (at H = 7168, 224-thread
+// for memory once; retquant issues the loads of two chunks (eight 16-byte
+// loads) before quantising and keeps kRowThreads (at H = 7168, 224-thread
 // blocks that load a row in one pass measured slower: 643 -> 722 us).
 constexpr int kRowThreads = 128;
 constexpr int kRowMaxThreads = 256;
@@ -795,32 +697,62 @@ __device__ __forceinline__ void load_chunk16(const float4* __restrict__ src, int
     }
 }
 
-// Token-wise requantisation of the SwiGLU output h (its row absmax was
-// reduced by the gate/up GEMM's epilogue): hq as exact fp16 integers, s_h.
+// SwiGLU and the token-wise requantisation of its output, one expert row per
+// block: h = SiLU(g) * u from the gate/up GEMM's g and u (h rounded once,
+// SiLU by silu_fast: the exp specification and a correctly rounded
+// quotient), the row's |h| maximum, s_h = max / 127 and the codes of h as
+// exact fp16 integers.  Each thread holds up to CH chunks of 16 values in
+// registers (row_threads(I) threads: CH = 2 covers I <= 8192, 4 covers the
+// largest I), so g and u are read once.
+template <int CH>
 __global__ void __launch_bounds__(kRowMaxThreads)
-requant_kernel(int I, const float* __restrict__ h, const unsigned* __restrict__ rowmax,
-               __half* __restrict__ hq, float* __restrict__ sh) {
+requant_kernel(int I, const float* __restrict__ gu, __half* __restrict__ hq, float* __restrict__ sh) {
+    __shared__ float s_red[kRowMaxThreads / 32];
     const int r = blockIdx.x;
     const int nch = I / 16;
-    const float4* src = reinterpret_cast<const float4*>(h + (long long)r * I);
-    uint4* dst = reinterpret_cast<uint4*>(hq + (long long)r * I);
     const int nt = blockDim.x;
-    for (int c0 = threadIdx.x; c0 < nch; c0 += 2 * nt) {
-        float4 v[2][4];
-        load_chunk16(src, c0, nch, v[0]);
-        load_chunk16(src, c0 + nt, nch, v[1]);
-        const float s = row_scale(__uint_as_float(rowmax[r]));
-        const float rs = quant_rcp(s);
+    const float4* gsrc = reinterpret_cast<const float4*>(gu + (long long)r * 2 * I);
+    const float4* usrc = gsrc + I / 4;
+    float hv[CH][16];
+    float amax = 0.f;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int c = c0 + u * nt;
-            if (c >= nch) break;
-            const float x[16] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y,
-                                 v[u][1].z, v[u][1].w, v[u][2].x, v[u][2].y, v[u][2].z, v[u][2].w,
-                                 v[u][3].x, v[u][3].y, v[u][3].z, v[u][3].w};
+    for (int u = 0; u < CH; ++u) {
+        const int c = threadIdx.x + u * nt;
+        if (c < nch) {
+            float4 g4[4], u4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                g4[i] = __ldg(gsrc + 4 * c + i);
+                u4[i] = __ldg(usrc + 4 * c + i);
+            }
+            const float gg[16] = {g4[0].x, g4[0].y, g4[0].z, g4[0].w, g4[1].x, g4[1].y, g4[1].z, g4[1].w,
+                                  g4[2].x, g4[2].y, g4[2].z, g4[2].w, g4[3].x, g4[3].y, g4[3].z, g4[3].w};
+            const float uu[16] = {u4[0].x, u4[0].y, u4[0].z, u4[0].w, u4[1].x, u4[1].y, u4[1].z, u4[1].w,
+                                  u4[2].x, u4[2].y, u4[2].z, u4[2].w, u4[3].x, u4[3].y, u4[3].z, u4[3].w};
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                hv[u][e] = __fmul_rn(silu_fast(gg[e]), uu[e]);
+                amax = fmaxf(amax, fabsf(hv[u][e]));
+            }
+        }
+    }
+    // row maximum over the block
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    float m = s_red[0];
+    for (int i = 1; i < nt / 32; ++i) m = fmaxf(m, s_red[i]);
+    const float s = row_scale(m);
+    const float rs = quant_rcp(s);
+    uint4* dst = reinterpret_cast<uint4*>(hq + (long long)r * I);
+#pragma unroll
+    for (int u = 0; u < CH; ++u) {
+        const int c = threadIdx.x + u * nt;
+        if (c < nch) {
             int q[16];
             if (s != 0.f) {
-                quant_row_n<16>(x, s, rs, q);
+                quant_row_n<16>(hv[u], s, rs, q);
             } else {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) q[e] = 0;
@@ -832,7 +764,7 @@ requant_kernel(int I, const float* __restrict__ h, const unsigned* __restrict__ 
             dst[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
     }
-    if (threadIdx.x == 0) sh[r] = row_scale(__uint_as_float(rowmax[r]));
+    if (threadIdx.x == 0) sh[r] = s;
 }
 
 // INT8 return message of expert row r: token-wise codes of y (its row absmax
@@ -1156,9 +1088,8 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     float* s_row = ws_ptr<float>(ws, wl.s_row);
     float* sh = ws_ptr<float>(ws, wl.sh);
     __half* a16 = ws_ptr<__half>(ws, wl.a16);
-    float* hbuf = ws_ptr<float>(ws, wl.hbuf);
-    unsigned* hmax = ws_ptr<unsigned>(ws, wl.rowmax);
-    unsigned* ymax = hmax + M;
+    float* gubuf = ws_ptr<float>(ws, wl.gubuf);
+    unsigned* ymax = ws_ptr<unsigned>(ws, wl.rowmax);
     __half* hq16 = ws_ptr<__half>(ws, wl.hq16);
     float* ybuf = ws_ptr<float>(ws, wl.ybuf);
     unsigned char* cb = static_cast<unsigned char*>(cbuf);
@@ -1167,7 +1098,7 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     cudaError_t e;
 
     if (clear && (e = clear_status(ws, st)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(hmax, 0, sizeof(unsigned) * 2 * M, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(ymax, 0, sizeof(unsigned) * M, st)) != cudaSuccess) return e;
     count_launches(1);
     const bool fuse = fc.out != nullptr && int8_ret;
     int* ready = ws_ptr<int>(ws, wl.ready);
@@ -1190,7 +1121,7 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     CUtensorMap mwgu, mx1[2], mo1, mwd, mx2[2], mo2;
     if (!weight_map(&mwgu, w.w_gate_up, d.H, (uint64_t)E_w * 2 * d.I) ||
         !act_map(mx1, a16, d.H, (uint64_t)M, BNV) ||
-        !out_map(&mo1, hbuf, false, (uint64_t)d.I, (uint64_t)M, 64) ||
+        !out_map(&mo1, gubuf, false, (uint64_t)2 * d.I, (uint64_t)M, 128) ||
         !weight_map(&mwd, w.w_down, d.I, (uint64_t)E_w * d.H) ||
         !act_map(mx2, hq16, d.I, (uint64_t)M, BNV))
         return cudaErrorInvalidValue;
@@ -1204,17 +1135,16 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     Params P1 = {};
     P1.G = d.E_phys; P1.offsets = expert_offsets; P1.tile_prefix = tp; P1.ttab = ttab;
     P1.g2s = w.phys_to_weight;
-    P1.K = d.H; P1.rows_per_set = 2 * d.I; P1.nout = d.I; P1.mb_count = d.I / 64; P1.box1_off = d.I;
-    P1.s_row = s_row; P1.s_ch = w.s_gate_up; P1.out_f32 = hbuf; P1.rowmax = hmax; P1.err = err;
+    P1.K = d.H; P1.rows_per_set = 2 * d.I; P1.nout = 2 * d.I; P1.mb_count = 2 * d.I / 128; P1.box1_off = 64;
+    P1.s_row = s_row; P1.s_ch = w.s_gate_up; P1.out_f32 = gubuf; P1.err = err;
     P1.tma_out = 1;
     if ((e = launch_gemm<EPI_GU, BNV>(P1, mwgu, mx1, mo1, st)) != cudaSuccess) return e;
     if (narrow > 0 &&
-        (e = launch_gemv_gate_up(d, dbuf, meta, expert_offsets, expert_rows, w, hbuf, hmax, err, nlist, 2,
+        (e = launch_gemv_gate_up(d, dbuf, meta, expert_offsets, expert_rows, w, gubuf, err, nlist, 2,
                                  st)) != cudaSuccess)
         return e;
 
-    requant_kernel<<<(unsigned)M, row_threads(d.I), 0, st>>>(d.I, hbuf, hmax, hq16, sh);
-    count_launches(1);
+    if ((e = launch_requant_rows(d.I, M, gubuf, hq16, sh, st)) != cudaSuccess) return e;
 
     Params P2 = {};
     P2.G = d.E_phys; P2.offsets = expert_offsets; P2.tile_prefix = tp; P2.ttab = ttab;
@@ -1264,9 +1194,12 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
 
 }  // namespace tc
 
-cudaError_t launch_requant_rows(int I, long long M, const float* h, const unsigned* rowmax, void* hq16,
-                                float* sh, cudaStream_t st) {
-    tc::requant_kernel<<<(unsigned)M, tc::row_threads(I), 0, st>>>(I, h, rowmax, static_cast<__half*>(hq16), sh);
+cudaError_t launch_requant_rows(int I, long long M, const float* gu, void* hq16, float* sh, cudaStream_t st) {
+    const int nt = tc::row_threads(I);
+    if (I / 16 <= 2 * nt)
+        tc::requant_kernel<2><<<(unsigned)M, nt, 0, st>>>(I, gu, static_cast<__half*>(hq16), sh);
+    else
+        tc::requant_kernel<4><<<(unsigned)M, nt, 0, st>>>(I, gu, static_cast<__half*>(hq16), sh);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -76,10 +76,10 @@ struct WsLayout {
     long long hq;          // int8  [T*k][I]
     long long acc_d;       // int32 [T*k][H]
     // tensor-core expert FFN
-    long long rowmax;      // u32   [2][T*k]  absmax of h and of y (float bits)
+    long long rowmax;      // u32   [T*k]     absmax of y (float bits)
     long long s_row;       // f32   [T*k]     dispatch scale of each expert row
     long long a16;         // fp16  [T*k][H]  expert input rows
-    long long hbuf;        // f32   [T*k][I]  SwiGLU output h
+    long long gubuf;       // f32   [T*k][2I] gate and up projections g, u
     long long hq16;        // fp16  [T*k][I]  requantised SwiGLU output
     long long ybuf;        // f32   [T*k][H]  expert output (INT8 return messages only)
     long long total;
@@ -101,10 +101,10 @@ inline WsLayout make_ws(const Dims& d) {
     w.narrow = o;     o = align_up(o + 4LL * (d.E_phys + 1), 256);
     w.tc = ffn_uses_tc(d);
     if (w.tc) {
-        w.rowmax = o; o = align_up(o + 8 * tk, 256);
+        w.rowmax = o; o = align_up(o + 4 * tk, 256);
         w.s_row = o;  o = align_up(o + 4 * tk, 256);
         w.a16 = o;    o = align_up(o + 2 * tk * d.H, 256);
-        w.hbuf = o;   o = align_up(o + 4 * tk * d.I, 256);
+        w.gubuf = o;  o = align_up(o + 8 * tk * d.I, 256);
         w.hq16 = o;   o = align_up(o + 2 * tk * d.I, 256);
         if (d.cfmt == MOE_MSG_INT8) { w.ybuf = o; o = align_up(o + 4 * tk * d.H, 256); }
     } else {
@@ -231,10 +231,10 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                           const int32_t* expert_offsets, const int32_t* expert_rows,
                           const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
                           const WsLayout& wl, cudaStream_t st, const FusedCombine& fc, bool clear);
-// The token-wise requantisation of h (row kernel of the tensor-core path):
-// hq as exact fp16 integers and the scales s_h, from h and its row maxima.
-cudaError_t launch_requant_rows(int I, long long M, const float* h, const unsigned* rowmax, void* hq16,
-                                float* sh, cudaStream_t st);
+// SwiGLU and the token-wise requantisation of its output (row kernel of the
+// tensor-core and matrix-vector paths): h = SiLU(g) * u from g, u [M][2I],
+// hq as exact fp16 integers and the scales s_h.
+cudaError_t launch_requant_rows(int I, long long M, const float* gu, void* hq16, float* sh, cudaStream_t st);
 // INT8 return messages from y and its row maxima into the combine rows
 // (rows whose dispatch slot or metadata is out of range are skipped and
 // MOE_ERR_INDEX is posted to *err).
@@ -251,12 +251,13 @@ bool gemv_kernels_fit(const Dims& d);
 // Rows up to which an expert runs on the matrix-vector kernels beside the
 // tensor-core GEMMs (0: none).
 inline int narrow_expert_rows(const Dims& d) { return gemv_kernels_fit(d) ? kNarrowExpertRows : 0; }
-// The matrix-vector kernels on their own, writing h / y and their row maxima
-// exactly as the tensor-core epilogues do: every expert (list == nullptr), or
-// the experts listed in list[1..list[0]]; prof_slot selects the timing events.
+// The matrix-vector kernels on their own, writing g and u / y and the row
+// maxima of y exactly as the tensor-core epilogues do: every expert (list ==
+// nullptr), or the experts listed in list[1..list[0]]; prof_slot selects the
+// timing events.
 cudaError_t launch_gemv_gate_up(const Dims& d, const void* dbuf, const moe_dispatch_meta* meta,
                                 const int32_t* expert_offsets, const int32_t* expert_rows,
-                                const moe_expert_weights& w, float* hbuf, unsigned* hmax, int* err,
+                                const moe_expert_weights& w, float* gubuf, int* err,
                                 const int32_t* list, int prof_slot, cudaStream_t st);
 cudaError_t launch_gemv_down(const Dims& d, const int32_t* expert_offsets, const moe_expert_weights& w,
                              const void* hq16, const float* sh, float* ybuf, unsigned* ymax, int* err,
