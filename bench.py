@@ -50,16 +50,23 @@ FFN_TC_SRC = os.path.join(ROOT, "expert_dispatch_combine_gb300", "csrc", "ffn_tc
 FFN_GEMV_SRC = os.path.join(ROOT, "expert_dispatch_combine_gb300", "csrc", "ffn_gemv.cu")
 
 
-def measured_traffic(alg_bytes: int, gemv: bool = False):
-    """DRAM bytes per launch of the gate/up kernel (tensor-core GEMM, or the
-    matrix-vector kernel of the decode path) for a launch of `alg_bytes`
-    algorithmic bytes: the traffic / algorithmic ratio the committed ncu
-    summary measured on its small workload (prof_e32, prof_decode_e32), times
-    alg_bytes; None unless that summary was taken with the current kernel
-    source.  The kernel's traffic grows with the units it serves (weights per
-    touched expert, rows, h), so the ratio carries over."""
-    name, src_file = (("gemv_gate_up_prof_decode_e32.md", FFN_GEMV_SRC) if gemv
-                      else ("gemm_tc_gate_up_prof_e32.md", FFN_TC_SRC))
+TRAFFIC_PROFILES = {  # kernel -> (committed ncu summary, source file it was taken on)
+    "tc": ("gemm_tc_gate_up_prof_e32.md", FFN_TC_SRC),
+    "tc_f16": ("gemm_tc_gate_up_f16_prof_e32.md", FFN_TC_SRC),
+    "gemv": ("gemv_gate_up_prof_decode_e32.md", FFN_GEMV_SRC),
+}
+
+
+def measured_traffic(alg_bytes: int, kind: str = "tc"):
+    """DRAM bytes per launch of the gate/up kernel (tensor-core GEMM on the int8
+    weights or on their fp16 copies, or the matrix-vector kernel of the decode
+    path) for a launch of `alg_bytes` algorithmic bytes: the traffic /
+    algorithmic ratio the committed ncu summary measured on its small workload
+    (prof_e32, prof_decode_e32), times alg_bytes; None unless that summary was
+    taken with the current kernel source.  The kernel's traffic grows with the
+    units it serves (weights per touched expert, rows, h), so the ratio
+    carries over."""
+    name, src_file = TRAFFIC_PROFILES[kind]
     try:
         txt = open(os.path.join(ROOT, "profiles", name)).read()
         src = hashlib.sha1(open(src_file, "rb").read()).hexdigest()
@@ -165,7 +172,14 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle
-def config_of(w: synth.Workload, world: int, weight_bytes: int | None = None) -> dict:
+WEIGHT_FORMS = {
+    "f16copy": "int8 W8A8, plus exact fp16 copies read by the tensor-core GEMMs of large batches",
+    "int8": "int8 W8A8 only (tensor-core GEMMs convert int8 tiles on the SM)",
+}
+
+
+def config_of(w: synth.Workload, world: int, weight_bytes: int | None = None,
+              weights: str = "f16copy") -> dict:
     """The `config` object of both arms' JSON lines (same keys, same values)."""
     wb = weight_bytes if weight_bytes is not None else 3 * w.E_log * w.H * w.I
     inputs = (f"{wb / 1e9:.3f} GB of int8 weights of the touched experts streamed every step and "
@@ -174,7 +188,7 @@ def config_of(w: synth.Workload, world: int, weight_bytes: int | None = None) ->
           "inputs fit in L2 (129 MB), not flushed between steps: ") + inputs
     return {"workload": w.name, "T": w.T, "H": w.H, "E_log": w.E_log, "E_phys": w.E_phys, "k": w.k,
             "I": w.I, "ranks": w.R, "src_ranks": w.S, "messages": "int8 dispatch, int8 combine",
-            "l2": l2, "parallelism": f"replicas x{world}"}
+            "weights": WEIGHT_FORMS[weights], "l2": l2, "parallelism": f"replicas x{world}"}
 
 
 _ORC_CACHE = {}
@@ -292,7 +306,7 @@ def run_reference(args, rank: int, world: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8 (exact int64 accumulation), f32 epilogue", "data": "synthetic",
-        "config": config_of(w, world, len(touched) * 3 * w.H * w.I),
+        "config": config_of(w, world, len(touched) * 3 * w.H * w.I, args.weights),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
                          "threads": oracle.num_threads(), "host_cores": os.cpu_count(),
                          "kind": "oracle", "sample": sample, "stages_ms": stages},
@@ -332,7 +346,7 @@ def run_ours(args, rank: int, world: int):
         r_, n_, p_ = B.moe_eplb_plan(cnt.cpu().numpy().astype(np.float64), w.E_phys, w.placement_ranks)
         rep, nc, p2l = (torch.from_numpy(a).to(dev) for a in (r_, n_, p_))
     layer = MoELayer(shape, w_gu, s_gu, w_d, s_d, rep_table=rep, n_copies=nc, phys_to_weight=p2l,
-                     device=dev)
+                     device=dev, f16_weights=args.weights == "f16copy")
     lg_h = synth.logits(w)
     x_h = synth.hidden_bits(w)
     logits = torch.from_numpy(lg_h).to(dev)
@@ -392,7 +406,7 @@ def run_ours(args, rank: int, world: int):
                        r["expert_rows"], b.workspace)
         evs[2].record(stream)
         B.moe_expert_ffn(shape, b.dispatch, r["expert_offsets"], r["expert_rows"], w_gu, s_gu, w_d,
-                         s_d, b.combine, b.workspace, phys_to_weight=p2l)
+                         s_d, b.combine, b.workspace, phys_to_weight=p2l, w_f16=layer.w_f16)
         evs[3].record(stream)
         B.moe_combine(shape, b.combine, r["topk_w"], b.out)
         evs[4].record(stream)
@@ -418,7 +432,7 @@ def run_ours(args, rank: int, world: int):
             fa.record(stream)
             B.moe_expert_ffn_combine(shape, b.dispatch, r["expert_offsets"], r["expert_rows"], w_gu,
                                      s_gu, w_d, s_d, r["topk_w"], b.combine, fused_out, b.workspace,
-                                     phys_to_weight=p2l)
+                                     phys_to_weight=p2l, w_f16=layer.w_f16)
             fb.record(stream)
             torch.cuda.synchronize()
             fused_ms += fa.elapsed_time(fb) / reps
@@ -460,9 +474,16 @@ def run_ours(args, rank: int, world: int):
     wide = cnt_h > narrow if ffn_path != B.MOE_FFN_GEMV else cnt_h > 0
     rows_k = int(cnt_h[wide].sum())
     act_bytes = 1 if ffn_path == B.MOE_FFN_GEMV else 2
+    # the fp16 weight copies serve batches above the decode size (more than 32
+    # routed rows per physical expert on average)
+    f16_used = (layer.w_f16 is not None and ffn_path == B.MOE_FFN_TENSOR_CORE
+                and w.T * w.k > 32 * w.E_phys)
+    w_bytes = 2 if f16_used else 1
+    tkind = "gemv" if ffn_path == B.MOE_FFN_GEMV else "tc_f16" if f16_used else "tc"
     alg["gate_up_ops"] = rows_k * 4 * w.H * w.I
-    alg["gate_up_bytes"] = (len(weight_sets(wide)) * 2 * w.I * w.H + rows_k * w.H * act_bytes
-                            + rows_k * w.I * 4)
+    # weights, expert rows (fp16 codes) in, g and u (f32, 2I per row) out
+    alg["gate_up_bytes"] = (len(weight_sets(wide)) * 2 * w.I * w.H * w_bytes + rows_k * w.H * act_bytes
+                            + rows_k * 2 * w.I * 4)
     peaks, peak_kind = _peaks()
     hbm = peaks["hbm_gbs"]
     stages = {
@@ -509,8 +530,10 @@ def run_ours(args, rank: int, world: int):
     stages["ffn_frac_sustained"] = ffn_tflops / sustained
     stages["clocks"] = stage_clocks
     gu_name = ("gemv_kernel<gate|up> (int8 dp4a weight streaming)" if ffn_path == B.MOE_FFN_GEMV
-               else "gemm_tc_kernel<gate|up> (exact int8 on tcgen05 kind::f16; experts with more "
-                    f"than {narrow} routed rows)")
+               else "gemm_tc_kernel<gate|up> (exact int8 on tcgen05 kind::f16, "
+                    + ("both operands from shared memory, fp16 weight copies" if f16_used
+                       else "int8 weights converted into tensor memory")
+                    + f"; experts with more than {narrow} routed rows)")
     if kern["gemm_gate_up"] > 0:
         # dominant kernel: the gate|up expert GEMM, timed by CUDA events on its stream
         gu_tflops = alg["gate_up_ops"] / (kern["gemm_gate_up"] / 1000) / 1e12
@@ -524,7 +547,7 @@ def run_ours(args, rank: int, world: int):
         if intensity >= ridge:
             roofline = {"bound": "tensor", "achieved": gu_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                         "frac": gu_tflops / peak_tc,
-                        "traffic": measured_traffic(alg["gate_up_bytes"], ffn_path == B.MOE_FFN_GEMV),
+                        "traffic": measured_traffic(alg["gate_up_bytes"], tkind),
                         "traffic_source": "scaled from the small-workload ncu capture (profiles/)",
                         "kernel": gu_name,
                         "algorithmic_ops_per_launch": alg["gate_up_ops"],
@@ -536,7 +559,7 @@ def run_ours(args, rank: int, world: int):
             gu_gbs = alg["gate_up_bytes"] / (kern["gemm_gate_up"] / 1000) / 1e9
             roofline = {"bound": "hbm", "achieved": gu_gbs, "peak": hbm, "unit": "GB/s",
                         "frac": gu_gbs / hbm,
-                        "traffic": measured_traffic(alg["gate_up_bytes"], ffn_path == B.MOE_FFN_GEMV),
+                        "traffic": measured_traffic(alg["gate_up_bytes"], tkind),
                         "traffic_source": "scaled from the small-workload ncu capture (profiles/)",
                         "kernel": gu_name,
                         "algorithmic_ops_per_launch": alg["gate_up_ops"],
@@ -556,6 +579,7 @@ def run_ours(args, rank: int, world: int):
     h_out = [torch.empty((w.T, w.H), dtype=torch.int16).pin_memory() for _ in range(2)]
     layers = [layer, MoELayer(shape, w_gu, s_gu, w_d, s_d, rep_table=rep, n_copies=nc,
                               phys_to_weight=p2l, device=dev)]
+    layers[1].w_f16 = layer.w_f16  # one set of fp16 copies serves both buffer sets
     streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
     for i in range(2):  # warm-up of both sets
         layers[i].forward_host(h_lg, h_x, h_out[i], stream=streams[i])
@@ -633,7 +657,7 @@ def run_ours(args, rank: int, world: int):
             "warmup": args.warmup, "ms_per_step": ms_all, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8 (exact int32 accumulation), f32 epilogue",
             "data": "synthetic",
-            "config": config_of(w, world, len(touched) * 3 * w.H * w.I),
+            "config": config_of(w, world, len(touched) * 3 * w.H * w.I, args.weights),
             "stages": stages,
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -654,6 +678,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.WORKLOADS))
     ap.add_argument("--ref-sample-s", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--weights", default="f16copy", choices=list(WEIGHT_FORMS),
+                    help="f16copy: also keep exact fp16 copies of the int8 weights for the "
+                         "tensor-core GEMMs of large batches; int8: the int8 weights alone")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

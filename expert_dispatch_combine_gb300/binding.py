@@ -45,7 +45,8 @@ class moe_layout(ctypes.Structure):
 class moe_expert_weights(ctypes.Structure):
     _fields_ = [("w_gate_up", ctypes.c_void_p), ("s_gate_up", ctypes.c_void_p),
                 ("w_down", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
-                ("n_sets", ctypes.c_int32), ("phys_to_weight", ctypes.c_void_p)]
+                ("n_sets", ctypes.c_int32), ("phys_to_weight", ctypes.c_void_p),
+                ("w_gate_up_f16", ctypes.c_void_p), ("w_down_f16", ctypes.c_void_p)]
 
 
 class moe_routing(ctypes.Structure):
@@ -61,7 +62,8 @@ EXPORTED = ("moe_status_string", "moe_static_buffer_bytes", "moe_query_layout", 
             "moe_dispatch_noalloc", "moe_dispatch_noalloc_max_scratch", "moe_layer_graph_create",
             "moe_graph_launch", "moe_graph_destroy", "moe_eplb_collect", "moe_expert_ffn_combine",
             "moe_trampoline_bytes", "moe_dispatch_trampoline", "moe_expert_ffn_path",
-            "moe_layer_host", "moe_expert_ffn_combine_ex", "moe_expert_ffn_narrow_rows")
+            "moe_layer_host", "moe_expert_ffn_combine_ex", "moe_expert_ffn_narrow_rows",
+            "moe_weights_to_f16")
 
 _lib = None
 
@@ -114,6 +116,7 @@ def load(path: str = LIB_PATH):
                                     P, P, i64, P], ctypes.c_int),
         "moe_expert_ffn_combine_ex": ([PS, P, i64, P, P, ctypes.POINTER(moe_expert_weights), P, P, i64,
                                        P, P, i64, i32, i64, P], ctypes.c_int),
+        "moe_weights_to_f16": ([P, i64, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -264,15 +267,30 @@ def moe_dispatch_noalloc_max_scratch() -> int:
     return int(load().moe_dispatch_noalloc_max_scratch())
 
 
-def _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight=None) -> moe_expert_weights:
+def _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight=None,
+             w_f16=None) -> moe_expert_weights:
+    """w_f16: None or the pair (w_gate_up_f16, w_down_f16) made by moe_weights_to_f16."""
+    g16, d16 = w_f16 if w_f16 is not None else (None, None)
     return moe_expert_weights(_ptr(w_gate_up), _ptr(s_gate_up), _ptr(w_down), _ptr(s_down),
-                              int(w_gate_up.shape[0]), _ptr(phys_to_weight))
+                              int(w_gate_up.shape[0]), _ptr(phys_to_weight), _ptr(g16), _ptr(d16))
+
+
+def moe_weights_to_f16(src, dst=None, stream=None):
+    """fp16 copy (exact) of an int8 device tensor, same shape; returns dst."""
+    import torch
+    if dst is None:
+        dst = torch.empty(src.shape, dtype=torch.float16, device=src.device)
+    if dst.numel() != src.numel():
+        raise ValueError("moe_weights_to_f16: dst and src differ in size")
+    _check("moe_weights_to_f16", load().moe_weights_to_f16(_ptr(src), src.numel(), _ptr(dst),
+                                                           _stream(stream)))
+    return dst
 
 
 def moe_expert_ffn(shape: Shape, dispatch_buf, expert_offsets, expert_rows, w_gate_up, s_gate_up,
-                   w_down, s_down, combine_buf, workspace, phys_to_weight=None, stream=None):
+                   w_down, s_down, combine_buf, workspace, phys_to_weight=None, stream=None, w_f16=None):
     cs = shape.c()
-    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight)
+    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight, w_f16)
     _check("moe_expert_ffn", load().moe_expert_ffn(
         ctypes.byref(cs), _ptr(dispatch_buf), dispatch_buf.numel(), _ptr(expert_offsets),
         _ptr(expert_rows), ctypes.byref(w), _ptr(combine_buf), combine_buf.numel(),
@@ -296,9 +314,9 @@ def moe_dispatch_trampoline(shape: Shape, x, phys_idx, trampoline_buf, dispatch_
 
 def moe_expert_ffn_combine(shape: Shape, dispatch_buf, expert_offsets, expert_rows, w_gate_up,
                            s_gate_up, w_down, s_down, topk_w, combine_buf, out, workspace,
-                           phys_to_weight=None, stream=None):
+                           phys_to_weight=None, stream=None, w_f16=None):
     cs = shape.c()
-    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight)
+    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight, w_f16)
     _check("moe_expert_ffn_combine", load().moe_expert_ffn_combine(
         ctypes.byref(cs), _ptr(dispatch_buf), dispatch_buf.numel(), _ptr(expert_offsets),
         _ptr(expert_rows), ctypes.byref(w), _ptr(topk_w), _ptr(combine_buf), combine_buf.numel(),
@@ -307,10 +325,10 @@ def moe_expert_ffn_combine(shape: Shape, dispatch_buf, expert_offsets, expert_ro
 
 def moe_expert_ffn_combine_ex(shape: Shape, dispatch_buf, expert_offsets, expert_rows, w_gate_up,
                               s_gate_up, w_down, s_down, topk_w, combine_buf, out, workspace,
-                              expected: int, wait_ns: int, phys_to_weight=None, stream=None):
+                              expected: int, wait_ns: int, phys_to_weight=None, stream=None, w_f16=None):
     """moe_expert_ffn_combine with the combine's wait target and bound given."""
     cs = shape.c()
-    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight)
+    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight, w_f16)
     _check("moe_expert_ffn_combine_ex", load().moe_expert_ffn_combine_ex(
         ctypes.byref(cs), _ptr(dispatch_buf), dispatch_buf.numel(), _ptr(expert_offsets),
         _ptr(expert_rows), ctypes.byref(w), _ptr(topk_w), _ptr(combine_buf), combine_buf.numel(),
@@ -326,9 +344,9 @@ def moe_combine(shape: Shape, combine_buf, topk_w, out, stream=None):
 
 def moe_layer(shape: Shape, logits, x, w_gate_up, s_gate_up, w_down, s_down, routing: dict,
               dispatch_buf, combine_buf, workspace, out, rep_table=None, n_copies=None,
-              phys_to_weight=None, stream=None):
+              phys_to_weight=None, stream=None, w_f16=None):
     cs = shape.c()
-    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight)
+    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight, w_f16)
     r = moe_routing(*[_ptr(routing[n]) for n, _ in moe_routing._fields_])
     mc = int(rep_table.shape[1]) if rep_table is not None else 0
     _check("moe_layer", load().moe_layer(
@@ -340,12 +358,12 @@ def moe_layer(shape: Shape, logits, x, w_gate_up, s_gate_up, w_down, s_down, rou
 
 def moe_layer_host(shape: Shape, h_logits, h_x, h_out, d_logits, d_x, w_gate_up, s_gate_up, w_down,
                    s_down, routing: dict, dispatch_buf, combine_buf, workspace, d_out, rep_table=None,
-                   n_copies=None, phys_to_weight=None, stream=None):
+                   n_copies=None, phys_to_weight=None, stream=None, w_f16=None):
     """The whole layer from host tensors (page-locked CPU tensors: h_logits f32,
     h_x and h_out 16-bit) to host: the copies in, moe_layer and the copy out,
     all enqueued on `stream` by the library."""
     cs = shape.c()
-    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight)
+    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight, w_f16)
     r = moe_routing(*[_ptr(routing[n]) for n, _ in moe_routing._fields_])
     mc = int(rep_table.shape[1]) if rep_table is not None else 0
     _check("moe_layer_host", load().moe_layer_host(
@@ -357,12 +375,13 @@ def moe_layer_host(shape: Shape, h_logits, h_x, h_out, d_logits, d_x, w_gate_up,
 
 def moe_layer_graph_create(shape: Shape, logits, x, w_gate_up, s_gate_up, w_down, s_down,
                            routing: dict, dispatch_buf, combine_buf, workspace, out,
-                           capture_stream, rep_table=None, n_copies=None, phys_to_weight=None) -> int:
+                           capture_stream, rep_table=None, n_copies=None, phys_to_weight=None,
+                           w_f16=None) -> int:
     """Captures moe_layer with these arguments on capture_stream (a
     torch.cuda.Stream other than the legacy default stream); returns the
     graph handle for moe_graph_launch / moe_graph_destroy."""
     cs = shape.c()
-    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight)
+    w = _weights(w_gate_up, s_gate_up, w_down, s_down, phys_to_weight, w_f16)
     r = moe_routing(*[_ptr(routing[n]) for n, _ in moe_routing._fields_])
     mc = int(rep_table.shape[1]) if rep_table is not None else 0
     h = ctypes.c_void_p(None)

@@ -75,6 +75,8 @@ moe_status check_weights(const Dims& d, const moe_expert_weights* w) {
     if (w->n_sets < 1) return MOE_ERR_INVALID_ARG;
     if (!w->phys_to_weight && w->n_sets < d.E_phys) return MOE_ERR_INVALID_ARG;
     if (!aligned(w->w_gate_up, 16) || !aligned(w->w_down, 16)) return MOE_ERR_INVALID_ARG;
+    if (!w->w_gate_up_f16 != !w->w_down_f16) return MOE_ERR_INVALID_ARG;  // both or neither
+    if (!aligned(w->w_gate_up_f16, 16) || !aligned(w->w_down_f16, 16)) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
@@ -126,6 +128,13 @@ moe_status moe_expert_ffn_narrow_rows(const moe_shape* shape, int32_t* rows) {
     const WsLayout wl = make_ws(d);
     *rows = (wl.tc && !ffn_gemv_fits(d)) ? narrow_expert_rows(d) : 0;
     return MOE_OK;
+}
+
+moe_status moe_weights_to_f16(const int8_t* src, int64_t n, uint16_t* dst, moe_stream_t stream) {
+    if (n < 0) return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;  // nothing to copy; the pointers are not used
+    if (!src || !dst || !aligned(src, 16) || !aligned(dst, 16)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_weights_to_f16(src, n, dst, stream));
 }
 
 moe_status moe_expert_ffn_path(const moe_shape* shape, int32_t* path) {

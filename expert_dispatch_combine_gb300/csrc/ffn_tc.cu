@@ -16,10 +16,13 @@
 //
 // GEMM structure (one CTA per SM, persistent over tiles):
 //   D^T[channel][token] = W[channel][:] . X[token][:]
-//   A operand = weights, 128 channel rows per tile: TMA loads int8 tiles into
-//     shared memory; a converter warpgroup turns them into fp16 and stores
-//     them in tensor memory (the A-from-TMEM form of tcgen05.mma), so the
-//     converted weights cost no shared-memory bandwidth;
+//   A operand = weights, 128 channel rows per tile, in one of two forms:
+//     int8 (the layer's weights): TMA loads int8 tiles into shared memory; a
+//     converter warpgroup turns them into fp16 and stores them in tensor
+//     memory (the A-from-TMEM form of tcgen05.mma);
+//     fp16 copies (made once by moe_weights_to_f16, twice the bytes): TMA
+//     loads them straight into shared memory and the MMA reads both operands
+//     from there (the SS form); no conversion on the SM, 256-token tiles;
 //   B operand = activations, up to BN tokens per tile (fp16, K-major, 128B
 //     swizzle), TMA-loaded in 32-row boxes so that small experts only load
 //     the rows they have; the MMA N is the tile's token count rounded up to 16.
@@ -40,7 +43,9 @@
 // (requant_kernel), so the SiLU's instructions stay off the GEMM's critical
 // path.  The down GEMM's epilogue writes y and reduces its row maximum.
 // Warp roles (16 warps): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
-// warps 4-7 converter, warps 8-15 two drain/epilogue warpgroups.  Register
+// warps 4-7 converter (idle with fp16 weights), warps 8-15 two drain/epilogue
+// warpgroups.  Tiles run in raster bands (tile_entry) so that the CTAs that
+// share a weight block start together.  Register
 // budgets are moved between warpgroups with setmaxnreg (the totals stay
 // within the launch allocation).  Each warpgroup covers the four TMEM lane
 // quarters.
@@ -63,48 +68,69 @@ namespace tc {
 
 constexpr int BK = 64;                           // K per stage
 constexpr int CK = 16;                           // stages per exact chunk (1024 K)
-constexpr int CKP = CK / 2;                      // stage pairs per exact chunk
 constexpr int BOX_ROWS = 32;                     // token rows per activation TMA box
 constexpr int BOX_BYTES = BOX_ROWS * BK * 2;     // 4 KB
-constexpr int A_BYTES = 128 * BK;                // 8 KB int8 weights per stage
 constexpr int GT = 16;                           // tokens per epilogue group
 constexpr int STG_BYTES = GT * 128 * 4;          // 8 KB staging buffer; two per drain warpgroup
 constexpr uint32_t TM_ACC = 0, TM_COLS = 512;
 constexpr int THREADS = 512;
 
-// Shapes that depend on the tile's token count BN: 192 or 160 for batches
-// with many rows per expert, 64 for decode-sized batches, where the smaller
-// activation region buys twice the stages (weight bytes in flight).
-// The TMEM columns after the two accumulators hold NAP pairs of A slots
-// (64 columns per stage pair): the converter can fill pair p while the MMAs
-// of pairs p - NAP + 1 .. p - 1 run.  More A pairs than shared-memory pairs
+// Shapes that depend on the tile's token count BN and on the weight operand.
+// int8 weights (AF16 false), converted on the SM: BN 192 for batches with
+// many rows per expert, 64 for decode-sized batches, where the smaller
+// activation region buys twice the stages (weight bytes in flight).  The
+// TMEM columns after the two accumulators hold NAP pairs of A slots (64
+// columns per stage pair): the converter can fill pair p while the MMAs of
+// pairs p - NAP + 1 .. p - 1 run.  More A pairs than shared-memory pairs
 // would never be used.
-template <int BNV>
+// fp16 copies of the int8 weights (AF16 true): both operands are read from
+// shared memory by the MMA, no A slots.  The stage ring is latency-bound
+// (about 192 KB in flight per SM against L2/DRAM latency), so the widest tile
+// wins: BN 256 with four 48 KB stages (measured 0.84 of the bf16 peak on 1024
+// rows per expert, against 0.76 / 0.67 / 0.58 / 0.49 at BN 224 / 192 / 160 /
+// 128).
+template <int BNV, bool AF16 = false>
 struct Tile {
     static constexpr int BN = BNV;                            // tokens per tile
+    static constexpr int A_BYTES = AF16 ? 128 * BK * 2 : 128 * BK;  // weights per stage (16 / 8 KB)
     static constexpr int B_BYTES = BN * BK * 2;               // fp16 activations per stage
-    static constexpr int STAGE_BYTES = B_BYTES + A_BYTES;     // 32, 28 or 16 KB
-    static constexpr int NS = BN == 64 ? 12 : 6;              // shared-memory stages
-    static constexpr int NP = NS / 2;                         // stage pairs
+    static constexpr int STAGE_BYTES = B_BYTES + A_BYTES;
+    // shared-memory stages: for fp16 weights as many as fit beside the
+    // epilogue staging buffers and the barriers
+    static constexpr int NS_F16 = (227 * 1024 - 4 * STG_BYTES - 2048) / STAGE_BYTES;
+    static constexpr int NS = AF16 ? NS_F16 : (BN == 64 ? 12 : 6);
+    // stages per pipeline step (one full/empty barrier pair and one wait of
+    // the MMA thread per step): pairs for int8 weights, single stages for
+    // fp16 weights, whose 48 KB stages would leave only two pair slots
+    static constexpr int SPS = AF16 ? 1 : 2;
+    static constexpr int NP = NS / SPS;                       // step slots
     static constexpr uint32_t TM_A = 2 * BN;                  // after the two accumulators
     static constexpr int NAP_FIT = (TM_COLS - TM_A) / 64;     // A-slot pairs that fit in TMEM
-    static constexpr int NAP = NAP_FIT < NP ? NAP_FIT : NP;   // A-slot pairs used
+    static constexpr int NAP = AF16 ? 0 : (NAP_FIT < NP ? NAP_FIT : NP);  // A-slot pairs used
     static constexpr int HALF = BN / 2;                       // token columns per drain warpgroup
     static constexpr int NGRP = HALF / GT;                    // epilogue groups per drain warpgroup
-    static constexpr int NBARS = 2 * NP + NAP + 4 + 1 + 2;
+    static constexpr int NAB = NAP > 0 ? NAP : 1;             // A-slot barriers (one unused with fp16 weights)
+    static constexpr int NBARS = 2 * NP + NAB + 4 + 1 + 2;
     static constexpr int SMEM_BYTES = NS * STAGE_BYTES + 4 * STG_BYTES + NBARS * 8 + 16 + 1024;
-    static_assert(BN % 32 == 0 && HALF % GT == 0 && NS % 2 == 0, "tile shape");
-    static_assert(STAGE_BYTES % 1024 == 0, "stages start on 128B-swizzle atoms");
+    static_assert(BN % 32 == 0 && BN <= 256 && HALF % GT == 0 && NS % SPS == 0 && CK % SPS == 0, "tile shape");
+    static_assert(B_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "operands start on 128B-swizzle atoms");
     static_assert(SMEM_BYTES <= 227 * 1024, "dynamic shared memory per CTA");
-    static_assert(NAP >= 2 && TM_A + NAP * 64 <= TM_COLS, "two accumulators and two or more A-slot pairs in TMEM");
+    static_assert(AF16 ? TM_A <= TM_COLS : (NAP >= 2 && TM_A + NAP * 64 <= TM_COLS),
+                  "two accumulators (and, for int8 weights, two or more A-slot pairs) in TMEM");
 };
-constexpr int BN_LARGE = kTcTileRows, BN_DECODE = kTcMinTileRows;
+// token tiles per raster band (tile order, below)
+constexpr int kRasterTokenTiles = 8;
+constexpr int BN_LARGE = kTcTileRows, BN_DECODE = kTcMinTileRows, BN_F16 = kTcTileRowsF16;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 20000000ull;
 // per-thread register budgets after setmaxnreg: 128 threads each at
-// 48 (producer/MMA) + 96 (converter) + 2 x 184 (drains) = 65,536 <= 512 x 128
+// 48 (producer/MMA) + 96 (converter) + 2 x 184 (drains) = 65,536 <= 512 x 128;
+// with fp16 weights the converter warpgroup idles at the minimum, 24, and the
+// drains (128 token columns each at BN 256) take 216: 64,512
 constexpr uint32_t REG_CTRL = 48, REG_CONV = 96, REG_DRAIN = 184;
+constexpr uint32_t REG_IDLE = 24, REG_DRAIN_F16 = 216;
 static_assert(128 * (REG_CTRL + REG_CONV + 2 * REG_DRAIN) <= THREADS * 128, "register split");
+static_assert(128 * (REG_CTRL + REG_IDLE + 2 * REG_DRAIN_F16) <= THREADS * 128, "register split (fp16 weights)");
 
 enum { EPI_I32 = 0, EPI_GU = 1, EPI_F32 = 2, EPI_BF16MSG = 3 };
 
@@ -138,15 +164,34 @@ struct TileInfo {
     int set, r0, nvalid, nmma, mb;
 };
 
-// Tile t covers token tile t / mb_count and channel block t % mb_count.  Each
-// role loads the table entry of its next tile one tile ahead, so the load's
-// latency hides behind the current tile.
-__device__ __forceinline__ int4 tile_entry(const Params& P, int tile, int total_tiles) {
-    return tile < total_tiles ? __ldg(P.ttab + tile / P.mb_count) : make_int4(0, 0, 0, 0);
+// Tile order: group by group (group g owns tiles [tp[g], tp[g+1]) * mb_count,
+// tp the tile prefix); inside a group, its token tiles in bands of up to
+// kRasterTokenTiles, and inside a band channel block by channel block with
+// the band's token tiles side by side.  CTAs that start together then share
+// each weight block (one DRAM read for the band, taken in step), while a
+// band's activations stay few enough to live in L2 across its channel
+// blocks.  Each role loads the table entry of its next tile one tile ahead,
+// so the three dependent loads hide behind the current tile.
+struct TileRef {
+    int4 e;  // token-tile table entry
+    int mb;  // channel block
+};
+__device__ __forceinline__ TileRef tile_entry(const Params& P, int tile, int total_tiles) {
+    if (tile >= total_tiles) return TileRef{make_int4(0, 0, 0, 0), 0};
+    // tile / mb_count is a token tile of the same group (not of this tile)
+    const int g = __ldg(P.ttab + tile / P.mb_count).w;
+    const int t0 = __ldg(P.tile_prefix + g), nt = __ldg(P.tile_prefix + g + 1) - t0;
+    const int local = tile - t0 * P.mb_count;  // in [0, nt * mb_count)
+    const int band = local / (kRasterTokenTiles * P.mb_count);
+    const int r = local - band * kRasterTokenTiles * P.mb_count;
+    const int bs = min(kRasterTokenTiles, nt - band * kRasterTokenTiles);  // token tiles in the band
+    const int mb = r / bs;
+    return TileRef{__ldg(P.ttab + t0 + band * kRasterTokenTiles + (r - mb * bs)), mb};
 }
-__device__ __forceinline__ TileInfo decode(const Params& P, int tile, const int4& e) {
+__device__ __forceinline__ TileInfo decode(const Params& P, int tile, const TileRef& r) {
+    const int4& e = r.e;
     TileInfo t;
-    t.mb = tile % P.mb_count;
+    t.mb = r.mb;
     t.set = e.x;
     t.r0 = e.y;
     t.nvalid = e.z;
@@ -323,14 +368,16 @@ __device__ __forceinline__ bool epilogue_staged(const Params& P, const TileInfo&
     return true;
 }
 
-template <int EPI, int BNV>
+template <int EPI, int BNV, bool AF16>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                const __grid_constant__ CUtensorMap tmXb,
                const __grid_constant__ CUtensorMap tmO, const Params P) {
-    using TL = Tile<BNV>;
-    constexpr int BN = TL::BN, NS = TL::NS, NP = TL::NP, NAP = TL::NAP, HALF = TL::HALF, NGRP = TL::NGRP;
-    constexpr int B_BYTES = TL::B_BYTES, STAGE_BYTES = TL::STAGE_BYTES, NBARS = TL::NBARS;
+    using TL = Tile<BNV, AF16>;
+    constexpr int BN = TL::BN, NS = TL::NS, NP = TL::NP, NAP = TL::NAB, HALF = TL::HALF, NGRP = TL::NGRP;
+    constexpr int SPS = TL::SPS, CKP = CK / SPS;  // stages per step; steps per exact chunk
+    constexpr int A_BYTES = TL::A_BYTES, B_BYTES = TL::B_BYTES, STAGE_BYTES = TL::STAGE_BYTES;
+    constexpr int NBARS = TL::NBARS;
     constexpr uint32_t TM_A = TL::TM_A;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -342,8 +389,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
-    auto fullp = [&](int sp) { return bar(sp); };        // both stages of pair slot sp loaded
-    auto emptyp = [&](int sp) { return bar(NP + sp); };  // pair slot sp consumed by the MMAs
+    auto fullp = [&](int sp) { return bar(sp); };        // the stages of step slot sp loaded
+    auto emptyp = [&](int sp) { return bar(NP + sp); };  // step slot sp consumed by the MMAs
     auto afull = [&](int p) { return bar(2 * NP + p); };  // A-slot pair p converted
     auto accfull = [&](int b) { return bar(2 * NP + NAP + b); };
     auto accempty = [&](int b) { return bar(2 * NP + NAP + 2 + b); };
@@ -381,9 +428,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     const uint32_t tmem = *tmem_slot;
 
     const int total_tiles = P.tile_prefix[P.G] * P.mb_count;
-    // K stages in pairs; an odd count gets one more stage entirely beyond K,
-    // which TMA fills with zeros (it adds nothing to the sums)
-    const int KSP = (P.K / BK + 1) / 2;
+    // K stages in steps of SPS; with pairs, an odd count gets one more stage
+    // entirely beyond K, which TMA fills with zeros (it adds nothing to the sums)
+    const int KSP = (P.K / BK + SPS - 1) / SPS;
     const int nchunks = (KSP + CKP - 1) / CKP;
     const int wgi = warp >> 2;
 
@@ -395,7 +442,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             // expect_tx for both stages' bytes, then the loads of both.
             uint32_t pr = 0;  // stage pairs issued
             bool ok = true;
-            int4 e_next = tile_entry(P, blockIdx.x, total_tiles);
+            TileRef e_next = tile_entry(P, blockIdx.x, total_tiles);
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
                 const TileInfo ti = decode(P, tile, e_next);
                 e_next = tile_entry(P, tile + gridDim.x, total_tiles);
@@ -406,7 +453,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 // only the 32-row boxes they need
                 const int nb = (ti.nmma + BOX_ROWS - 1) / BOX_ROWS;
                 const bool one_box = nb == BN / BOX_ROWS;
-                const uint32_t bytes = 2 * (A_BYTES + nb * BOX_BYTES);
+                const uint32_t bytes = SPS * (A_BYTES + nb * BOX_BYTES);
                 for (int kp = 0; kp < KSP; ++kp, ++pr) {
                     const int sp = pr % NP;
                     if (!ptx::mbar_wait(emptyp(sp), ((pr / NP) & 1) ^ 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
@@ -415,11 +462,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     }
                     ptx::mbar_expect_tx(fullp(sp), bytes);
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const uint32_t st = ptx::smem_addr(stages + (2 * sp + j) * STAGE_BYTES);
-                        const int x = (2 * kp + j) * BK;  // beyond K (padding stage): zero fill
-                        ptx::tma_load_2d(st + B_BYTES, &tmW, x, yw0, fullp(sp));
-                        ptx::tma_load_2d(st + B_BYTES + 4096, &tmW, x, yw1, fullp(sp));
+                    for (int j = 0; j < SPS; ++j) {
+                        const uint32_t st = ptx::smem_addr(stages + (SPS * sp + j) * STAGE_BYTES);
+                        const int x = (SPS * kp + j) * BK;  // beyond K (padding stage): zero fill
+                        if constexpr (AF16) {  // one 128-row fp16 box, 128B swizzle
+                            ptx::tma_load_2d(st + B_BYTES, &tmW, x, yw0, fullp(sp));
+                        } else {               // two 64-row int8 boxes, 64B swizzle
+                            ptx::tma_load_2d(st + B_BYTES, &tmW, x, yw0, fullp(sp));
+                            ptx::tma_load_2d(st + B_BYTES + 4096, &tmW, x, yw1, fullp(sp));
+                        }
                         if (one_box) {
                             ptx::tma_load_2d(st, &tmXb, x, ti.r0, fullp(sp));
                         } else {
@@ -435,13 +486,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             }
         } else if (warp == 1 && lane == 0) {
             // --------------------------------------------- MMA issuer
-            // Per stage pair: one wait (converted weights, which the converter
-            // signals only after it has seen the pair's loads land), 8 MMAs at
-            // constant descriptor offsets, one commit that releases the pair.
+            // Per step: one wait (int8 weights: for the converted weights of
+            // the stage pair, which the converter signals only after it has
+            // seen the pair's loads land; fp16 weights: for the stage's loads),
+            // 8 or 4 MMAs at constant descriptor offsets, one commit that
+            // releases the step's slot.
             uint32_t pr = 0, q = 0;
             bool ok = true;
             const uint64_t bdesc0 = ptx::sdesc_k_sw128(ptx::smem_addr(stages));
-            int4 e_next = tile_entry(P, blockIdx.x, total_tiles);
+            const uint64_t adesc0 = ptx::sdesc_k_sw128(ptx::smem_addr(stages + B_BYTES));
+            TileRef e_next = tile_entry(P, blockIdx.x, total_tiles);
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
                 const TileInfo ti = decode(P, tile, e_next);
                 e_next = tile_entry(P, tile + gridDim.x, total_tiles);
@@ -457,20 +511,35 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                             break;
                         }
                     }
-                    if (!ptx::mbar_wait(afull(pr % NAP), (pr / NAP) & 1, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
+                    const int sp = pr % NP;
+                    const uint32_t ready = AF16 ? fullp(sp) : afull(pr % NAP);
+                    const uint32_t ready_par = AF16 ? (pr / NP) & 1 : (pr / NAP) & 1;
+                    if (!ptx::mbar_wait(ready, ready_par, P.err, WAIT_NS, MOE_ERR_TIMEOUT)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const int sp = pr % NP;
-                    const uint64_t bd = bdesc0 + static_cast<uint64_t>((2 * sp * STAGE_BYTES) >> 4);
-                    const uint32_t abase = tmem + TM_A + (pr % NAP) * 64;
+                    const uint64_t soff = static_cast<uint64_t>((SPS * sp * STAGE_BYTES) >> 4);
+                    const uint64_t bd = bdesc0 + soff;
                     const uint32_t d = tmem + TM_ACC + b * BN;
-                    ptx::mma_f16_ts(d, abase, bd, idesc, first ? 0u : 1u);
+                    if constexpr (AF16) {
+                        // the A and B images have the same layout: one K step
+                        // (16 elements, 32 bytes) is +2 in both descriptors
+                        const uint64_t ad = adesc0 + soff;
+                        ptx::mma_f16_ss(d, ad, bd, idesc, first ? 0u : 1u);
 #pragma unroll
-                    for (int kk = 1; kk < 2 * BK / 16; ++kk)
-                        ptx::mma_f16_ts(d, abase + kk * 8,
-                                        bd + (kk >> 2) * (STAGE_BYTES >> 4) + (kk & 3) * 2, idesc, 1u);
+                        for (int kk = 1; kk < SPS * BK / 16; ++kk) {
+                            const uint64_t o = (kk >> 2) * (STAGE_BYTES >> 4) + (kk & 3) * 2;
+                            ptx::mma_f16_ss(d, ad + o, bd + o, idesc, 1u);
+                        }
+                    } else {
+                        const uint32_t abase = tmem + TM_A + (pr % NAP) * 64;
+                        ptx::mma_f16_ts(d, abase, bd, idesc, first ? 0u : 1u);
+#pragma unroll
+                        for (int kk = 1; kk < SPS * BK / 16; ++kk)
+                            ptx::mma_f16_ts(d, abase + kk * 8,
+                                            bd + (kk >> 2) * (STAGE_BYTES >> 4) + (kk & 3) * 2, idesc, 1u);
+                    }
                     ptx::tc_commit(emptyp(sp));  // both stages and their A slots are consumed
                     if (last) {
                         ptx::tc_commit(accfull(b));
@@ -482,6 +551,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             ptx::tc_commit(done_bar);
             mbar_wait_quiet(done_bar, 0, WAIT_NS);
         }
+    } else if (wgi == 1 && AF16) {
+        reg_dealloc<REG_IDLE>();  // fp16 weights: nothing to convert
     } else if (wgi == 1) {
         // ------------------------------------------------------- converter
         reg_dealloc<REG_CONV>();
@@ -533,7 +604,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         }
     } else {
         // ---------------------------- chunk drain and epilogue (2 groups)
-        reg_alloc<REG_DRAIN>();
+        reg_alloc<AF16 ? REG_DRAIN_F16 : REG_DRAIN>();
         const int h = wgi - 2;                 // token columns [h*HALF, h*HALF + HALF)
         const int wq = warp & 3;
         const int row = wq * 32 + lane;
@@ -545,7 +616,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         uint32_t q = 0;
         bool ok = true;
         WgBarrier wgb{wg_bar(h), 0};
-        int4 e_next = tile_entry(P, blockIdx.x, total_tiles);
+        TileRef e_next = tile_entry(P, blockIdx.x, total_tiles);
         for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
             const TileInfo ti = decode(P, tile, e_next);
             e_next = tile_entry(P, tile + gridDim.x, total_tiles);
@@ -1001,16 +1072,16 @@ int sm_count() {
     return cached[dev];
 }
 
-template <int EPI, int BNV>
+template <int EPI, int BNV, bool AF16 = false>
 cudaError_t launch_gemm(const Params& P, const CUtensorMap& w, const CUtensorMap (&x)[2],
                         const CUtensorMap& o, cudaStream_t st) {
-    constexpr int smem = Tile<BNV>::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, BNV>,
+    constexpr int smem = Tile<BNV, AF16>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, BNV, AF16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int slot = EPI == EPI_GU ? 0 : 1;
     if (cudaEvent_t ev = prof_event(slot, 0)) cudaEventRecord(ev, st);
-    gemm_tc_kernel<EPI, BNV><<<sm_count(), THREADS, smem, st>>>(w, x[0], x[1], o, P);
+    gemm_tc_kernel<EPI, BNV, AF16><<<sm_count(), THREADS, smem, st>>>(w, x[0], x[1], o, P);
     if (cudaEvent_t ev = prof_event(slot, 1)) cudaEventRecord(ev, st);
     count_launches(1);
     return cudaGetLastError();
@@ -1018,6 +1089,12 @@ cudaError_t launch_gemm(const Params& P, const CUtensorMap& w, const CUtensorMap
 
 bool weight_map(CUtensorMap* m, const int8_t* w, int K, uint64_t rows) {
     return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, K, rows, BK, 64, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+// fp16 copy of the weights: boxes of 64 K x 128 rows, the same 128B-swizzled
+// K-major image as the activations.
+bool weight_map(CUtensorMap* m, const uint16_t* w, int K, uint64_t rows) {
+    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w, K, rows, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Activation maps: [0] boxes of BOX_ROWS rows, [1] boxes of bn rows (a tile).
@@ -1074,7 +1151,7 @@ cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long lo
 
 namespace tc {
 
-template <int BNV>
+template <int BNV, bool AF16>
 cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                    const int32_t* expert_offsets, const int32_t* expert_rows,
                    const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
@@ -1119,10 +1196,12 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     count_launches(1);
 
     CUtensorMap mwgu, mx1[2], mo1, mwd, mx2[2], mo2;
-    if (!weight_map(&mwgu, w.w_gate_up, d.H, (uint64_t)E_w * 2 * d.I) ||
-        !act_map(mx1, a16, d.H, (uint64_t)M, BNV) ||
+    const bool wmaps = AF16 ? weight_map(&mwgu, w.w_gate_up_f16, d.H, (uint64_t)E_w * 2 * d.I) &&
+                                  weight_map(&mwd, w.w_down_f16, d.I, (uint64_t)E_w * d.H)
+                            : weight_map(&mwgu, w.w_gate_up, d.H, (uint64_t)E_w * 2 * d.I) &&
+                                  weight_map(&mwd, w.w_down, d.I, (uint64_t)E_w * d.H);
+    if (!wmaps || !act_map(mx1, a16, d.H, (uint64_t)M, BNV) ||
         !out_map(&mo1, gubuf, false, (uint64_t)2 * d.I, (uint64_t)M, 128) ||
-        !weight_map(&mwd, w.w_down, d.I, (uint64_t)E_w * d.H) ||
         !act_map(mx2, hq16, d.I, (uint64_t)M, BNV))
         return cudaErrorInvalidValue;
     const bool y_tma = int8_ret && d.H >= 128;
@@ -1138,7 +1217,7 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     P1.K = d.H; P1.rows_per_set = 2 * d.I; P1.nout = 2 * d.I; P1.mb_count = 2 * d.I / 128; P1.box1_off = 64;
     P1.s_row = s_row; P1.s_ch = w.s_gate_up; P1.out_f32 = gubuf; P1.err = err;
     P1.tma_out = 1;
-    if ((e = launch_gemm<EPI_GU, BNV>(P1, mwgu, mx1, mo1, st)) != cudaSuccess) return e;
+    if ((e = launch_gemm<EPI_GU, BNV, AF16>(P1, mwgu, mx1, mo1, st)) != cudaSuccess) return e;
     if (narrow > 0 &&
         (e = launch_gemv_gate_up(d, dbuf, meta, expert_offsets, expert_rows, w, gubuf, err, nlist, 2,
                                  st)) != cudaSuccess)
@@ -1153,7 +1232,7 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     P2.s_row = sh; P2.s_ch = w.s_down; P2.err = err; P2.tma_out = y_tma;
     if (int8_ret) {
         P2.out_f32 = ybuf; P2.rowmax = ymax;
-        if ((e = launch_gemm<EPI_F32, BNV>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
+        if ((e = launch_gemm<EPI_F32, BNV, AF16>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
         if (narrow > 0 &&
             (e = launch_gemv_down(d, expert_offsets, w, hq16, sh, ybuf, ymax, err, nlist, 3, st)) !=
                 cudaSuccess)
@@ -1184,15 +1263,49 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                 reinterpret_cast<float*>(cb + scale_off), err);
         }
         count_launches(1);
+
     } else {
         P2.expert_rows = expert_rows; P2.meta = meta; P2.cbuf = cb; P2.crow = d.crow; P2.k = d.k; P2.lb = d.lb;
         P2.S = d.S; P2.nslots = d.nslots;
-        if ((e = launch_gemm<EPI_BF16MSG, BNV>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
+        if ((e = launch_gemm<EPI_BF16MSG, BNV, AF16>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
 
 }  // namespace tc
+
+// fp16 copy of an int8 array (exact): 16 values per thread and step, the
+// tail of n % 16 values one per thread.
+__global__ void __launch_bounds__(256) weights_to_f16_kernel(const int8_t* __restrict__ src, long long n,
+                                                             uint16_t* __restrict__ dst) {
+    const long long nv = n / 16;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+        const uint4 w = __ldg(s4 + i);
+        uint4 o0, o1;
+        s8x4_to_f16x4(w.x, o0.x, o0.y);
+        s8x4_to_f16x4(w.y, o0.z, o0.w);
+        s8x4_to_f16x4(w.z, o1.x, o1.y);
+        s8x4_to_f16x4(w.w, o1.z, o1.w);
+        d4[2 * i] = o0;
+        d4[2 * i + 1] = o1;
+    }
+    if (blockIdx.x == 0)
+        for (long long i = nv * 16 + threadIdx.x; i < n; i += blockDim.x)
+            dst[i] = __half_as_ushort(__int2half_rn(src[i]));
+}
+
+cudaError_t launch_weights_to_f16(const int8_t* src, long long n, uint16_t* dst, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const long long nv = n / 16;
+    const long long want = std::max<long long>(1, (nv + 255) / 256);
+    const unsigned grid = (unsigned)std::min<long long>(want, 8LL * tc::sm_count());
+    weights_to_f16_kernel<<<grid, 256, 0, st>>>(src, n, dst);
+    count_launches(1);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_requant_rows(int I, long long M, const float* gu, void* hq16, float* sh, cudaStream_t st) {
     const int nt = tc::row_threads(I);
@@ -1214,18 +1327,24 @@ cudaError_t launch_retquant_rows(const Dims& d, long long M, const float* y, con
 }
 
 // Decode-sized batches (at most 32 routed rows per expert on average) take
-// 64-token tiles: their tiles are mostly weight streaming, and the smaller
-// activation region doubles the stages in flight.
+// 64-token tiles on the int8 weights: their tiles are mostly weight
+// streaming, and the smaller activation region doubles the stages in flight.
+// Larger batches take the fp16 weight copies when the caller gives them
+// (256-token tiles, nothing converted on the SM), else 192-token tiles on the
+// int8 weights.
 cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                           const int32_t* expert_offsets, const int32_t* expert_rows,
                           const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
                           const WsLayout& wl, cudaStream_t st, const FusedCombine& fc, bool clear) {
     const long long M = (long long)d.T * d.k;
     if (M <= 32LL * d.E_phys)
-        return tc::ffn_tc<tc::BN_DECODE>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
-                                         scale_off, ws, wl, st, fc, clear);
-    return tc::ffn_tc<tc::BN_LARGE>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
-                                    scale_off, ws, wl, st, fc, clear);
+        return tc::ffn_tc<tc::BN_DECODE, false>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
+                                                scale_off, ws, wl, st, fc, clear);
+    if (w.w_gate_up_f16 && w.w_down_f16)
+        return tc::ffn_tc<tc::BN_F16, true>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
+                                            scale_off, ws, wl, st, fc, clear);
+    return tc::ffn_tc<tc::BN_LARGE, false>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
+                                           scale_off, ws, wl, st, fc, clear);
 }
 
 }  // namespace moe

@@ -39,6 +39,8 @@ inline bool ffn_uses_tc(const Dims& d) { return d.H % 64 == 0 && d.I % 64 == 0; 
 
 // Token rows per tile of the tensor-core grouped GEMM.
 constexpr int kTcTileRows = 192;
+// Token rows per tile when the caller gives fp16 copies of the weights.
+constexpr int kTcTileRowsF16 = 256;
 // Token rows per tile of its decode variant (few rows per expert).
 constexpr int kTcMinTileRows = 64;
 // Routed rows per expert (on average) up to which the expert FFN streams the
@@ -231,6 +233,8 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                           const int32_t* expert_offsets, const int32_t* expert_rows,
                           const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
                           const WsLayout& wl, cudaStream_t st, const FusedCombine& fc, bool clear);
+// fp16 copy of an int8 array (moe_weights_to_f16).
+cudaError_t launch_weights_to_f16(const int8_t* src, long long n, uint16_t* dst, cudaStream_t st);
 // SwiGLU and the token-wise requantisation of its output (row kernel of the
 // tensor-core and matrix-vector paths): h = SiLU(g) * u from g, u [M][2I],
 // hq as exact fp16 integers and the scales s_h.

@@ -67,12 +67,20 @@ class MoELayer:
 
     forward(logits, x) runs route -> FusedDispatch -> experts -> FusedCombine
     through moe_layer and returns the bf16 output tensor (a view of the
-    layer's output buffer)."""
+    layer's output buffer).
+
+    f16_weights=True also keeps exact fp16 copies of the two weight arrays
+    (moe_weights_to_f16, made once here): batches above the decode size then
+    run the tensor-core GEMMs on them, with the same outputs bit for bit, at
+    twice the weight bytes held."""
 
     def __init__(self, shape: Shape, w_gate_up, s_gate_up, w_down, s_down, rep_table=None,
-                 n_copies=None, phys_to_weight=None, device="cuda", buffers: LayerBuffers | None = None):
+                 n_copies=None, phys_to_weight=None, device="cuda", buffers: LayerBuffers | None = None,
+                 f16_weights: bool = False):
         self.shape = shape
         self.w = (w_gate_up, s_gate_up, w_down, s_down)
+        self.w_f16 = (B.moe_weights_to_f16(w_gate_up), B.moe_weights_to_f16(w_down)) \
+            if f16_weights else None
         self.rep_table, self.n_copies, self.phys_to_weight = rep_table, n_copies, phys_to_weight
         self.buf = buffers if buffers is not None else LayerBuffers(shape, device)
 
@@ -80,7 +88,7 @@ class MoELayer:
         b = self.buf
         B.moe_layer(self.shape, logits, x, *self.w, b.routing, b.dispatch, b.combine, b.workspace,
                     b.out, rep_table=self.rep_table, n_copies=self.n_copies,
-                    phys_to_weight=self.phys_to_weight, stream=stream)
+                    phys_to_weight=self.phys_to_weight, stream=stream, w_f16=self.w_f16)
         return b.out
 
     def forward_host(self, h_logits: torch.Tensor, h_x: torch.Tensor, h_out: torch.Tensor,
@@ -97,7 +105,8 @@ class MoELayer:
         d_lg, d_x = self._stage
         B.moe_layer_host(self.shape, h_logits, h_x, h_out, d_lg, d_x, *self.w, b.routing, b.dispatch,
                          b.combine, b.workspace, b.out, rep_table=self.rep_table,
-                         n_copies=self.n_copies, phys_to_weight=self.phys_to_weight, stream=stream)
+                         n_copies=self.n_copies, phys_to_weight=self.phys_to_weight, stream=stream,
+                         w_f16=self.w_f16)
 
 
 class GraphedLayer:
@@ -120,7 +129,8 @@ class GraphedLayer:
             x = torch.zeros((s.T, s.H), dtype=torch.bfloat16, device=dev)
             g = B.moe_layer_graph_create(s, lg, x, *layer.w, buf.routing, buf.dispatch, buf.combine,
                                          buf.workspace, buf.out, cap, rep_table=layer.rep_table,
-                                         n_copies=layer.n_copies, phys_to_weight=layer.phys_to_weight)
+                                         n_copies=layer.n_copies, phys_to_weight=layer.phys_to_weight,
+                                         w_f16=layer.w_f16)
             self.sets.append((buf, lg, x, g))
 
     def step(self, logits: torch.Tensor, x: torch.Tensor, stream=None) -> torch.Tensor:

@@ -260,7 +260,15 @@ moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, const int32_t
  *   w_down (device) int8 [E_w][H][I]; s_down (device) f32 [E_w][H].
  *   phys_to_weight (device, nullable) int32 [E_phys]: weight set of each
  *   physical expert (replicas alias their logical expert); NULL means
- *   physical expert p uses set p (E_w >= E_phys). */
+ *   physical expert p uses set p (E_w >= E_phys).
+ *   w_gate_up_f16, w_down_f16 (device, nullable, both or neither; 16-byte
+ *   aligned): fp16 copies of w_gate_up and w_down in the same layout, made
+ *   once by moe_weights_to_f16 (every int8 value is exact in fp16).  With
+ *   them, batches above the decode size (more than 32 routed rows per
+ *   physical expert on average) run the tensor-core GEMMs on the copies
+ *   instead of converting int8 weight tiles on the SM: the same results bit
+ *   for bit, at twice the weight bytes held and read.  The int8 arrays stay
+ *   required (decode batches and experts with few rows read them). */
 typedef struct {
     const int8_t* w_gate_up;
     const float* s_gate_up;
@@ -268,7 +276,16 @@ typedef struct {
     const float* s_down;
     int32_t n_sets; /* E_w */
     const int32_t* phys_to_weight;
+    const uint16_t* w_gate_up_f16;
+    const uint16_t* w_down_f16;
 } moe_expert_weights;
+
+/* dst[i] = the fp16 encoding of the int8 value src[i], i in [0, n): the
+ * weight copies of moe_expert_weights.  src and dst (device) 16-byte
+ * aligned, n >= 0 (any value; a multiple of 16 takes only vector stores).
+ * Enqueued on `stream`; n = 0 does nothing.  INVALID_ARG for n < 0, or for
+ * null or misaligned pointers with n > 0. */
+moe_status moe_weights_to_f16(const int8_t* src, int64_t n, uint16_t* dst, moe_stream_t stream);
 
 /* Grouped W8A8 SwiGLU expert FFN ([X] P085 equation, P088, P089; [C]
  * run_local_experts and remote_write_combine).  Requires INT8 dispatch

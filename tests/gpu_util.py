@@ -90,10 +90,11 @@ class CanaryBuffers(LayerBuffers):
             assert bool((t == CANARY).all()), "a kernel wrote past the end of a caller buffer"
 
 
-def make_layer(w: synth.Workload, cfmt=B.MOE_MSG_INT8, device="cuda", canary=True):
+def make_layer(w: synth.Workload, cfmt=B.MOE_MSG_INT8, device="cuda", canary=True, f16_weights=False):
     """MoELayer with the workload's weights resident on the device (plus the
     EPLB map for replicated workloads); with `canary` its buffers carry
-    canary tails (CanaryBuffers)."""
+    canary tails (CanaryBuffers); with `f16_weights` it also keeps the fp16
+    weight copies that the tensor-core GEMMs of large batches read."""
     shape = shape_of(w, B.MOE_MSG_INT8, cfmt)
     w_gu, s_gu, w_d, s_d = synth.all_weights_torch(w, device)
     rep = nc = p2l = None
@@ -101,7 +102,8 @@ def make_layer(w: synth.Workload, cfmt=B.MOE_MSG_INT8, device="cuda", canary=Tru
         r, n, p = eplb_map(w)
         rep, nc, p2l = (torch.from_numpy(a).to(device) for a in (r, n, p))
     return MoELayer(shape, w_gu, s_gu, w_d, s_d, rep_table=rep, n_copies=nc, phys_to_weight=p2l,
-                    device=device, buffers=CanaryBuffers(shape, device) if canary else None)
+                    device=device, buffers=CanaryBuffers(shape, device) if canary else None,
+                    f16_weights=f16_weights)
 
 
 __all__ = ["lib", "shape_of", "bits_to_bf16_tensor", "bf16_tensor_to_bits", "compare_bf16",

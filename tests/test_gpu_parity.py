@@ -72,11 +72,12 @@ def test_route_ties_and_k_equals_e():
 
 
 # -------------------------------------------------------------- whole layer
-def _full_layer_check(w, cfmt, xb=None, lg=None):
+def _full_layer_check(w, cfmt, xb=None, lg=None, f16_weights=False):
     """Every intermediate and the output of moe_layer against the oracle
     (hidden rows and logits from the workload's generator unless xb, bf16
-    bits, or lg, f32 logits, is given)."""
-    layer = make_layer(w, cfmt)
+    bits, or lg, f32 logits, is given; with f16_weights the layer also holds
+    the fp16 weight copies)."""
+    layer = make_layer(w, cfmt, f16_weights=f16_weights)
     if lg is None:
         lg = synth.logits(w)
     if xb is None:
