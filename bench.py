@@ -182,8 +182,10 @@ def config_of(w: synth.Workload, world: int, weight_bytes: int | None = None,
               weights: str = "f16copy") -> dict:
     """The `config` object of both arms' JSON lines (same keys, same values)."""
     wb = weight_bytes if weight_bytes is not None else 3 * w.E_log * w.H * w.I
-    inputs = (f"{wb / 1e9:.3f} GB of int8 weights of the touched experts streamed every step and "
-              f"{2 * w.T * w.H / 1e6:.1f} MB of bf16 hidden rows")
+    form = (" (the tensor-core GEMMs read their fp16 copies, twice the bytes, for experts above "
+            "8 rows in batches above the decode size)" if weights == "f16copy" else "")
+    inputs = (f"{wb / 1e9:.3f} GB of int8 weights of the touched experts{form} streamed every step "
+              f"and {2 * w.T * w.H / 1e6:.1f} MB of bf16 hidden rows")
     l2 = ("inputs larger than L2 (129 MB): " if wb + 2 * w.T * w.H > L2_BYTES else
           "inputs fit in L2 (129 MB), not flushed between steps: ") + inputs
     return {"workload": w.name, "T": w.T, "H": w.H, "E_log": w.E_log, "E_phys": w.E_phys, "k": w.k,
