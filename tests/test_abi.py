@@ -169,3 +169,31 @@ def test_eplb_planner_on_workload_counts(lib):
     assert nc.sum() == w.E_phys
     # the hottest expert got the most copies
     assert nc[np.argmax(cnt)] == nc.max() > 1
+
+
+def test_weight_copies_rejected_before_enqueue(lib):
+    """moe_weights_to_f16 and the optional fp16 weight fields: argument errors
+    are returned on the host (fake device pointers, never dereferenced)."""
+    P = ctypes.c_void_p
+    fake = 1 << 40
+    assert lib.moe_weights_to_f16(None, 16, P(fake), None) == 1            # null source
+    assert lib.moe_weights_to_f16(P(fake), 16, None, None) == 1            # null destination
+    assert lib.moe_weights_to_f16(P(fake), -1, P(fake), None) == 1         # negative count
+    assert lib.moe_weights_to_f16(P(fake + 8), 16, P(fake), None) == 1     # misaligned
+    assert lib.moe_weights_to_f16(None, 0, None, None) == 0                # nothing to copy
+    shape = B.Shape(64, 256, 16, 16, 2, 128, 4, 4)
+    s = shape.c()
+    L = B.moe_query_layout(shape)
+
+    def ffn(w):
+        return lib.moe_expert_ffn(ctypes.byref(s), P(fake), L["dispatch_bytes"], P(fake), P(fake),
+                                  ctypes.byref(w), P(fake), L["combine_bytes"], P(fake),
+                                  L["workspace_bytes"], None)
+
+    def weights(g16, d16):
+        return B.moe_expert_weights(fake, fake, fake, fake, 16, None, g16, d16)
+
+    assert ffn(weights(fake, None)) == 1        # gate/up copy without the down copy
+    assert ffn(weights(None, fake)) == 1        # down copy without the gate/up copy
+    assert ffn(weights(fake + 8, fake)) == 1    # misaligned copy
+    assert ffn(weights(fake, fake + 2)) == 1
