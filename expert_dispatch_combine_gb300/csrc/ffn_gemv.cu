@@ -250,12 +250,19 @@ __global__ void __launch_bounds__(THREADS, 2) gemv_kernel(const Params P) {
     for (int i = blockIdx.y; i < n; i += gridDim.y) gemv_expert<KIND>(P, P.list[1 + i], xs, s_tok);
 }
 
+// Blocks of a list-mode launch (the narrow experts beside the tensor-core
+// GEMMs, whose number only the device knows): at c2_decode_zipf (101 narrow
+// experts) 1024 blocks, each looping over about six experts, streamed the
+// weights at 5.66 TB/s; 4096, most blocks taking one expert, at 6.21 TB/s
+// (2048: 6.13, 8192 and 16384: 6.20).
+constexpr int kListBlocks = 4096;
+
 // Grid: nblocks_x channel blocks times E experts (no list), or times enough
-// block rows to cover the GPU a few times over (list: the rows stride over
-// the listed experts).
+// block rows to cover kListBlocks blocks (list: the rows stride over the
+// listed experts; rows beyond the list's length end at once).
 template <int KIND>
 cudaError_t launch(const Params& P, int E, int nblocks_x, cudaStream_t st) {
-    if (P.list != nullptr) E = std::max(1, std::min(E, (1024 + nblocks_x - 1) / nblocks_x));
+    if (P.list != nullptr) E = std::max(1, std::min(E, (kListBlocks + nblocks_x - 1) / nblocks_x));
     const size_t smem = (size_t)NT * P.K;
     cudaError_t e = cudaFuncSetAttribute(gemv_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
