@@ -383,11 +383,15 @@ def run_ours(args, rank: int, world: int):
     ms = ev0.elapsed_time(ev1) / args.steps
     ms_all, value = replica_aggregate(ms, w.T, world, dev)
 
-    # ---- per-stage timing (same stream, CUDA events between the four calls)
+    # ---- per-stage timing: the four steps inside moe_layer (the library's
+    # events around them; on the tensor-core path its dispatch also writes the
+    # FFN's input rows), and the four entry points called one by one (same
+    # stream, CUDA events between the calls)
     b = layer.buf
     r = b.routing
     names = ["route", "dispatch", "ffn", "combine"]
     acc = {n: 0.0 for n in names}
+    sep = {n: 0.0 for n in names}
     kern = {"gemm_gate_up": 0.0, "gemm_down": 0.0, "narrow_gate_up": 0.0, "narrow_down": 0.0}
     reps = max(1, min(args.steps, 5))
     B.moe_profile_enable(True)
@@ -395,10 +399,20 @@ def run_ours(args, rank: int, world: int):
     time.sleep(0.3)
     swall0 = time.time()
     for _ in range(reps):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         # keep the GPU busy for about 2 ms so that the host has enqueued all
-        # four calls before the first event: the stage times then hold device
+        # the calls before the first event: the stage times then hold device
         # time only, not the host's launch latency of a call on an idle GPU
+        torch.cuda._sleep(4_000_000)
+        layer.forward(logits, x)
+        torch.cuda.synchronize()
+        prof = B.moe_profile_read(8)
+        kern["gemm_gate_up"] += prof[0] / reps
+        kern["gemm_down"] += prof[1] / reps
+        kern["narrow_gate_up"] += max(prof[2], 0.0) / reps
+        kern["narrow_down"] += max(prof[3], 0.0) / reps
+        for i, n in enumerate(names):
+            acc[n] += prof[4 + i] / reps
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         torch.cuda._sleep(4_000_000)
         evs[0].record(stream)
         B.moe_route(shape, logits, r["topk_idx"], r["topk_w"], r["phys_idx"], r["expert_counts"],
@@ -414,12 +428,7 @@ def run_ours(args, rank: int, world: int):
         evs[4].record(stream)
         torch.cuda.synchronize()
         for i, n in enumerate(names):
-            acc[n] += evs[i].elapsed_time(evs[i + 1]) / reps
-        gu_ms, dn_ms, ngu_ms, ndn_ms = B.moe_profile_read(4)
-        kern["gemm_gate_up"] += gu_ms / reps
-        kern["gemm_down"] += dn_ms / reps
-        kern["narrow_gate_up"] += max(ngu_ms, 0.0) / reps
-        kern["narrow_down"] += max(ndn_ms, 0.0) / reps
+            sep[n] += evs[i].elapsed_time(evs[i + 1]) / reps
     stage_clocks = stage_sampler.stop(swall0, time.time())
     B.moe_profile_enable(False)
     fused_ms = None
@@ -488,18 +497,31 @@ def run_ours(args, rank: int, world: int):
                             + rows_k * 2 * w.I * 4)
     peaks, peak_kind = _peaks()
     hbm = peaks["hbm_gbs"]
+    # inside moe_layer on the tensor-core path the dispatch also writes each
+    # message's fp16 expert input row and its scale (M * (2H + 4) bytes), which
+    # the FFN then does not assemble
+    staged = ffn_path == B.MOE_FFN_TENSOR_CORE
+    staged_bytes = w.T * w.k * (2 * w.H + 4) if staged else 0
     stages = {
+        "as_run_in": "moe_layer (library events around its four steps)",
         "route_us": 1000 * acc["route"],
         "dispatch_us": 1000 * acc["dispatch"],
         "ffn_us": 1000 * acc["ffn"],
         "combine_us": 1000 * acc["combine"],
-        "dispatch_gbs": alg["dispatch_bytes"] / (acc["dispatch"] / 1000) / 1e9,
+        "dispatch_stages_ffn_rows": staged,
+        "dispatch_gbs": (alg["dispatch_bytes"] + staged_bytes) / (acc["dispatch"] / 1000) / 1e9,
         "combine_gbs": alg["combine_bytes"] / (acc["combine"] / 1000) / 1e9,
+        "separate_calls": {
+            "route_us": 1000 * sep["route"], "dispatch_us": 1000 * sep["dispatch"],
+            "ffn_us": 1000 * sep["ffn"], "combine_us": 1000 * sep["combine"],
+            "dispatch_gbs": alg["dispatch_bytes"] / (sep["dispatch"] / 1000) / 1e9,
+            "note": "moe_route, moe_dispatch, moe_expert_ffn (with its assembly step), moe_combine"},
     }
     if tramp_us is not None:
         stages["dispatch_trampoline_us"] = tramp_us
     if fused_ms is not None:
-        stages["ffn_combine_fused_us"] = 1000 * fused_ms  # against ffn_us + combine_us
+        # against separate_calls' ffn_us + combine_us (both assemble the input rows)
+        stages["ffn_combine_fused_us"] = 1000 * fused_ms
     if narrow > 0 and ffn_path == B.MOE_FFN_TENSOR_CORE:
         nmask = (cnt_h > 0) & (cnt_h <= narrow)
         nsets = len(weight_sets(nmask))
@@ -511,8 +533,10 @@ def run_ours(args, rank: int, world: int):
             "gate_up_us": 1000 * kern["narrow_gate_up"], "down_us": 1000 * kern["narrow_down"],
             "gbs": n_bytes / (n_us / 1e6) / 1e9 if n_us > 0 else None,
             "kernels": "gemv_kernel<gate|up>, gemv_kernel<down> (int8 dp4a weight streaming)"}
+    # FusedDispatch + FusedCombine as message movement (the separate entry
+    # points: the dispatch writes the messages only)
     dc_bytes = alg["dispatch_bytes"] + alg["combine_bytes"]
-    dc_s = (acc["dispatch"] + acc["combine"]) / 1000
+    dc_s = (sep["dispatch"] + sep["combine"]) / 1000
     stages["dispatch_combine_hbm_frac"] = dc_bytes / dc_s / 1e9 / hbm
     ffn_tflops = alg["ffn_ops"] / (acc["ffn"] / 1000) / 1e12
     stages["ffn_tflops"] = ffn_tflops

@@ -406,8 +406,9 @@ def moe_profile_enable(on: bool) -> None:
 
 
 def moe_profile_read(n: int = 2) -> tuple:
-    """(gate/up GEMM ms, down GEMM ms[, narrow-expert gate/up ms, narrow-expert
-    down ms]) of the most recent expert FFN; -1 for a kernel that did not run."""
+    """(gate/up GEMM ms, down GEMM ms, narrow-expert gate/up ms, narrow-expert
+    down ms, then moe_layer's route, dispatch, FFN and combine ms), the first n
+    of them, from the most recent calls; -1 for what did not run."""
     ms = (ctypes.c_float * n)()
     _check("moe_profile_read", load().moe_profile_read(ctypes.cast(ms, ctypes.c_void_p), n))
     return tuple(float(v) for v in ms)

@@ -356,20 +356,36 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t
     const Dims d = make_dims(*shape);
     const WsLayout wl = make_ws(d);
     cudaStream_t s = (cudaStream_t)stream;
+    // profiling events around the four steps (slots 4..7), when enabled
+    auto mark = [&](int slot, int end) {
+        if (cudaEvent_t ev = prof_event(slot, end)) cudaEventRecord(ev, s);
+    };
+    mark(4, 0);
     if ((st = cuda_status(launch_route(d, logits, rep_table, n_copies, max_copies, r.topk_idx,
                                        r.topk_w, r.phys_idx, r.expert_counts, s))) != MOE_OK)
         return st;
-    // the status word is cleared once, by the dispatch, and covers the whole layer
+    mark(4, 1);
+    // the status word is cleared once, by the dispatch, and covers the whole
+    // layer; on the tensor-core FFN path the dispatch also writes the FFN's
+    // fp16 input rows, and the FFN skips its assembly step
+    const bool stage = ffn_takes_tc(d, wl);
+    mark(5, 0);
     if ((st = cuda_status(launch_dispatch(d, x, r.phys_idx, dispatch_buf, L.dispatch_meta_offset,
                                           r.rank_counts, r.expert_offsets, r.expert_rows,
-                                          workspace, wl, s, /*clear=*/true))) != MOE_OK)
+                                          workspace, wl, s, /*clear=*/true, stage))) != MOE_OK)
         return st;
+    mark(5, 1);
+    mark(6, 0);
     if ((st = cuda_status(launch_ffn(d, dispatch_buf, L.dispatch_meta_offset, r.expert_offsets,
                                      r.expert_rows, *weights, combine_buf, L.combine_scale_offset,
                                      workspace, wl, s, FusedCombine{nullptr, nullptr},
-                                     /*clear=*/false))) != MOE_OK)
+                                     /*clear=*/false, /*rows_ready=*/stage))) != MOE_OK)
         return st;
-    return cuda_status(launch_combine(d, combine_buf, L.combine_scale_offset, r.topk_w, out, s));
+    mark(6, 1);
+    mark(7, 0);
+    st = cuda_status(launch_combine(d, combine_buf, L.combine_scale_offset, r.topk_w, out, s));
+    mark(7, 1);
+    return st;
 }
 
 moe_status moe_layer_host(const moe_shape* shape, const float* h_logits, const uint16_t* h_x,

@@ -28,6 +28,7 @@
 //                  (shared -> global) of the code row into the k slots, plus
 //                  the 16-byte metadata and the expert row list entries.
 #include <algorithm>
+#include <cuda_fp16.h>
 
 #include "device_math.cuh"
 #include "internal.cuh"
@@ -204,13 +205,14 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
                const int32_t* __restrict__ expert_offsets, char* __restrict__ dbuf,
                moe_dispatch_meta* __restrict__ meta, int32_t* __restrict__ expert_rows,
                char* __restrict__ trows, moe_dispatch_meta* __restrict__ tmeta,
-               int32_t* __restrict__ troutes) {
+               int32_t* __restrict__ troutes, __half* __restrict__ a16, float* __restrict__ s_row) {
     extern __shared__ __align__(128) unsigned char sm[];
     uint4* srow = reinterpret_cast<uint4*>(sm);                 // bf16 row, 2H bytes
     uint2* scode = reinterpret_cast<uint2*>(sm + 2 * (size_t)H);  // H codes
     __shared__ float s_red[kScatterThreads / 32];
     __shared__ float s_scale;
     __shared__ long long s_slot[kMaxRoutes];  // kDirect: message slot of each route
+    __shared__ int s_erow[kMaxRoutes];        // kDirect with a16: expert row of each route
 
     const int t = blockIdx.x;
     const int src = t / lb, bs = t - src * lb;
@@ -235,6 +237,7 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
             my_fill = pair + mt - 1;
         }
         s_slot[j] = my_slot;
+        s_erow[j] = my_erow;
     }
     if constexpr (MODE == kHop2) {
         // the token as the trampoline holds it: the message row, its scale and routes
@@ -320,7 +323,11 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
                 quant_row_n<8>(x, scale, rscale, c8);
                 q.x = pack4(c8[0], c8[1], c8[2], c8[3]);
                 q.y = pack4(c8[4], c8[5], c8[6], c8[7]);
+                if (MODE == kDirect && a16)  // the chunk's codes as fp16, over its bf16 values
+                    srow[c] = make_uint4(codes_to_f16x2(c8[0], c8[1]), codes_to_f16x2(c8[2], c8[3]),
+                                         codes_to_f16x2(c8[4], c8[5]), codes_to_f16x2(c8[6], c8[7]));
             }
+            if (MODE == kDirect && a16 && scale == 0.f) srow[c] = make_uint4(0u, 0u, 0u, 0u);
             scode[c] = q;
         }
         src_row = reinterpret_cast<const unsigned char*>(scode);
@@ -347,9 +354,15 @@ scatter_kernel(int H, int k, int lb, int epr, int S, int mt, int E_phys, int int
     if (threadIdx.x == 0) {
         for (int j = 0; j < k; ++j)
             if (s_slot[j] >= 0) bulk_store_s2g(dbuf + s_slot[j] * drow, src_row, (unsigned)drow);
+        // moe_layer: the expert FFN's input rows too (the expert-input assembly
+        // of the tensor-core FFN, done here from the codes in shared memory)
+        if (a16 && int8_msgs)
+            for (int j = 0; j < k; ++j)
+                if (s_erow[j] >= 0) bulk_store_s2g(a16 + (long long)s_erow[j] * H, sm, (unsigned)(2 * H));
         asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
     }
     if (threadIdx.x >= 32 && threadIdx.x < 32 + k) {
+        if (a16 && int8_msgs && my_erow >= 0) s_row[my_erow] = scale;
         if (my_slot >= 0) {
             moe_dispatch_meta m;
             m.scale = scale;
@@ -402,7 +415,7 @@ template <int MODE>
 cudaError_t launch_scatter(const Dims& d, const uint16_t* x, const int32_t* phys_idx, void* dbuf,
                            long long meta_off, int32_t* expert_offsets, int32_t* expert_rows,
                            void* ws, const WsLayout& wl, char* trows, moe_dispatch_meta* tmeta,
-                           int32_t* troutes, cudaStream_t st) {
+                           int32_t* troutes, cudaStream_t st, bool stage_rows = false) {
     size_t smem3 = (size_t)d.H * 2 + (d.dfmt == MOE_MSG_INT8 ? (size_t)d.H : 0);
     if (smem3 > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(scatter_kernel<MODE>,
@@ -415,7 +428,8 @@ cudaError_t launch_scatter(const Dims& d, const uint16_t* x, const int32_t* phys
         phys_idx, ws_ptr<int32_t>(ws, wl.slot_local), ws_ptr<int32_t>(ws, wl.erank),
         ws_ptr<int32_t>(ws, wl.src_base), expert_offsets, static_cast<char*>(dbuf),
         reinterpret_cast<moe_dispatch_meta*>(static_cast<char*>(dbuf) + meta_off), expert_rows,
-        trows, tmeta, troutes);
+        trows, tmeta, troutes, stage_rows ? ws_ptr<__half>(ws, wl.a16) : nullptr,
+        stage_rows ? ws_ptr<float>(ws, wl.s_row) : nullptr);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -425,13 +439,14 @@ cudaError_t launch_scatter(const Dims& d, const uint16_t* x, const int32_t* phys
 cudaError_t launch_dispatch(const Dims& d, const uint16_t* x, const int32_t* phys_idx,
                             void* dbuf, long long meta_off, int32_t* rank_counts,
                             int32_t* expert_offsets, int32_t* expert_rows, void* ws,
-                            const WsLayout& wl, cudaStream_t st, bool clear) {
+                            const WsLayout& wl, cudaStream_t st, bool clear, bool stage_rows) {
     cudaError_t e = clear ? clear_status(ws, st) : cudaSuccess;
     if (e != cudaSuccess) return e;
     e = launch_layout(d, phys_idx, rank_counts, expert_offsets, ws, wl, st);
     if (e != cudaSuccess) return e;
     return launch_scatter<kDirect>(d, x, phys_idx, dbuf, meta_off, expert_offsets, expert_rows, ws,
-                                   wl, nullptr, nullptr, nullptr, st);
+                                   wl, nullptr, nullptr, nullptr, st,
+                                   stage_rows && wl.tc && d.dfmt == MOE_MSG_INT8);
 }
 
 TrampolineLayout trampoline_layout(const Dims& d) {

@@ -1155,7 +1155,8 @@ template <int BNV, bool AF16>
 cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                    const int32_t* expert_offsets, const int32_t* expert_rows,
                    const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                   const WsLayout& wl, cudaStream_t st, const FusedCombine& fc, bool clear) {
+                   const WsLayout& wl, cudaStream_t st, const FusedCombine& fc, bool clear,
+                   bool rows_ready) {
     const long long M = (long long)d.T * d.k;
     const moe_dispatch_meta* meta =
         reinterpret_cast<const moe_dispatch_meta*>(static_cast<const char*>(dbuf) + meta_off);
@@ -1190,10 +1191,12 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     if ((e = launch_tile_prefix(d.E_phys, BNV, expert_offsets, M, E_w, tp, err, st, ttab,
                                 w.phys_to_weight, narrow, nlist)) != cudaSuccess)
         return e;
-    assemble_kernel<<<(unsigned)M, 128, 0, st>>>(d.H, expert_rows, d.nslots,
-                                                 static_cast<const int8_t*>(dbuf), d.drow, meta, a16,
-                                                 s_row, err);
-    count_launches(1);
+    if (!rows_ready) {  // else the dispatch of moe_layer wrote them (launch_dispatch, stage_rows)
+        assemble_kernel<<<(unsigned)M, 128, 0, st>>>(d.H, expert_rows, d.nslots,
+                                                     static_cast<const int8_t*>(dbuf), d.drow, meta, a16,
+                                                     s_row, err);
+        count_launches(1);
+    }
 
     CUtensorMap mwgu, mx1[2], mo1, mwd, mx2[2], mo2;
     const bool wmaps = AF16 ? weight_map(&mwgu, w.w_gate_up_f16, d.H, (uint64_t)E_w * 2 * d.I) &&
@@ -1335,16 +1338,17 @@ cudaError_t launch_retquant_rows(const Dims& d, long long M, const float* y, con
 cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                           const int32_t* expert_offsets, const int32_t* expert_rows,
                           const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                          const WsLayout& wl, cudaStream_t st, const FusedCombine& fc, bool clear) {
+                          const WsLayout& wl, cudaStream_t st, const FusedCombine& fc, bool clear,
+                          bool rows_ready) {
     const long long M = (long long)d.T * d.k;
     if (M <= 32LL * d.E_phys)
         return tc::ffn_tc<tc::BN_DECODE, false>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
-                                                scale_off, ws, wl, st, fc, clear);
+                                                scale_off, ws, wl, st, fc, clear, rows_ready);
     if (w.w_gate_up_f16 && w.w_down_f16)
         return tc::ffn_tc<tc::BN_F16, true>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
-                                            scale_off, ws, wl, st, fc, clear);
+                                            scale_off, ws, wl, st, fc, clear, rows_ready);
     return tc::ffn_tc<tc::BN_LARGE, false>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
-                                           scale_off, ws, wl, st, fc, clear);
+                                           scale_off, ws, wl, st, fc, clear, rows_ready);
 }
 
 }  // namespace moe

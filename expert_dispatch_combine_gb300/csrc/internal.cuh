@@ -175,8 +175,9 @@ moe_status record_cuda_status(cudaError_t e);
 // Optional kernel timing: when enabled, the expert GEMM launches are
 // bracketed by CUDA events (slot 0: gate/up GEMM, slot 1: down GEMM; slots 2
 // and 3: the matrix-vector kernels of the narrow experts beside the
-// tensor-core GEMMs).
-constexpr int kProfSlots = 4;
+// tensor-core GEMMs), and so are the four steps inside moe_layer (slots 4..7:
+// route, dispatch, expert FFN, combine).
+constexpr int kProfSlots = 8;
 cudaEvent_t prof_event(int slot, int end);  // nullptr when profiling is off
 
 // Kernel launchers (each returns cudaGetLastError() after its launches).
@@ -185,10 +186,15 @@ cudaError_t launch_route(const Dims& d, const float* logits, const int32_t* rep_
                          float* topk_w, int32_t* phys_idx, int32_t* expert_counts,
                          cudaStream_t st);
 // FusedDispatch; with `clear` the workspace status word is cleared first.
+// With `stage_rows` (moe_layer, tensor-core FFN next, INT8 messages) the
+// scatter also writes the tensor-core FFN's input rows into the workspace:
+// the fp16 codes of each message at its expert-row position and its scale,
+// what the FFN's assembly step would compute from the messages.
 cudaError_t launch_dispatch(const Dims& d, const uint16_t* x, const int32_t* phys_idx,
                             void* dbuf, long long meta_off, int32_t* rank_counts,
                             int32_t* expert_offsets, int32_t* expert_rows, void* ws,
-                            const WsLayout& wl, cudaStream_t st, bool clear = true);
+                            const WsLayout& wl, cudaStream_t st, bool clear = true,
+                            bool stage_rows = false);
 cudaError_t launch_combine(const Dims& d, const void* cbuf, long long scale_off,
                            const float* topk_w, uint16_t* out, cudaStream_t st);
 // CUDA-core grouped GEMM; row_index entries must lie in [0, a_rows), weight
@@ -229,10 +235,13 @@ struct FusedCombine {
     int expected = 0;
     unsigned long long wait_ns = 0;
 };
+// rows_ready: the input rows and their scales are in the workspace already
+// (written by a staging dispatch), so the assembly step is skipped.
 cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                           const int32_t* expert_offsets, const int32_t* expert_rows,
                           const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
-                          const WsLayout& wl, cudaStream_t st, const FusedCombine& fc, bool clear);
+                          const WsLayout& wl, cudaStream_t st, const FusedCombine& fc, bool clear,
+                          bool rows_ready = false);
 // fp16 copy of an int8 array (moe_weights_to_f16).
 cudaError_t launch_weights_to_f16(const int8_t* src, long long n, uint16_t* dst, cudaStream_t st);
 // SwiGLU and the token-wise requantisation of its output (row kernel of the
@@ -279,7 +288,7 @@ inline cudaError_t launch_ffn(const Dims& d, const void* dbuf, long long meta_of
                               const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
                               const WsLayout& wl, cudaStream_t st,
                               const FusedCombine& fc = FusedCombine{nullptr, nullptr},
-                              bool clear = true) {
+                              bool clear = true, bool rows_ready = false) {
     if (!wl.tc)
         return launch_ffn_simt(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf, scale_off, ws,
                                wl, st, clear);
@@ -287,7 +296,10 @@ inline cudaError_t launch_ffn(const Dims& d, const void* dbuf, long long meta_of
         return launch_ffn_gemv(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf, scale_off, ws,
                                wl, st, clear);
     return launch_ffn_tc(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf, scale_off, ws, wl,
-                         st, fc, clear);
+                         st, fc, clear, rows_ready);
 }
+// Whether launch_ffn takes the tensor-core GEMMs (and reads the staged
+// expert input rows) for this shape without a fused combine.
+inline bool ffn_takes_tc(const Dims& d, const WsLayout& wl) { return wl.tc && !ffn_gemv_fits(d); }
 
 }  // namespace moe

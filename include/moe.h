@@ -370,8 +370,16 @@ typedef struct {
 } moe_routing;
 
 /* The whole layer: moe_route -> moe_dispatch -> moe_expert_ffn ->
- * moe_combine on one stream, with the same definitions.  rep_table /
- * n_copies may be NULL (no replicas). */
+ * moe_combine on one stream, with the same definitions and outputs.  When the
+ * expert FFN takes the tensor-core GEMMs (moe_expert_ffn_path), the dispatch
+ * kernel also writes the FFN's input rows (the fp16 codes of each message at
+ * its position in the expert row lists, with its scale) into the workspace,
+ * and the FFN skips the assembly step that would read them back from the
+ * dispatch buffer ([C] assemble_expert_inputs, fused into the dispatch).
+ * Under MOE_ERR_CAPACITY the row of a dropped message then holds that
+ * token's codes rather than a copy of another message (the outputs of such a
+ * call are unspecified either way).  rep_table / n_copies may be NULL (no
+ * replicas). */
 moe_status moe_layer(const moe_shape* shape, const float* logits, const uint16_t* x,
                      const int32_t* rep_table, const int32_t* n_copies, int32_t max_copies,
                      const moe_expert_weights* weights, const moe_routing* routing,
@@ -517,11 +525,14 @@ const char* moe_last_cuda_error(void);
  * tensor-core expert GEMM launch (or matrix-vector kernel of the decode
  * path, see moe_expert_ffn_path) is bracketed by CUDA events on its stream;
  * moe_profile_read synchronises on them and returns the durations (ms) of
- * the most recent gate/up kernel (ms[0]) and down kernel (ms[1]), and of the
+ * the most recent gate/up kernel (ms[0]) and down kernel (ms[1]), of the
  * matrix-vector kernels that took the narrow experts beside the tensor-core
- * GEMMs (ms[2] gate/up, ms[3] down; see moe_expert_ffn_narrow_rows); -1 for
- * a kernel not run since profiling was enabled.  n (>= 1) values are
- * written. */
+ * GEMMs (ms[2] gate/up, ms[3] down; see moe_expert_ffn_narrow_rows), and of
+ * the four steps of the most recent moe_layer call (ms[4] route, ms[5]
+ * dispatch, ms[6] expert FFN, ms[7] combine: inside moe_layer the dispatch
+ * also writes the tensor-core FFN's fp16 input rows, which the FFN then does
+ * not assemble); -1 for anything not run since profiling was enabled.
+ * n (>= 1) values are written, at most 8 of them meaningful. */
 moe_status moe_profile_enable(int32_t on);
 moe_status moe_profile_read(float* ms, int32_t n);
 
