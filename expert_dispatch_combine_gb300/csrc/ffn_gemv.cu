@@ -330,12 +330,10 @@ cudaError_t launch_ffn_gemv(const Dims& d, const void* dbuf, long long meta_off,
     float* ybuf = ws_ptr<float>(ws, wl.ybuf);
     cudaError_t e;
     if (clear && (e = clear_status(ws, st)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(ymax, 0, sizeof(unsigned) * M, st)) != cudaSuccess) return e;
-    count_launches(1);
     if ((e = launch_gemv_gate_up(d, dbuf, meta, expert_offsets, expert_rows, w, gubuf, err, nullptr, 0,
                                  st)) != cudaSuccess)
         return e;
-    if ((e = launch_requant_rows(d.I, M, gubuf, hq16, sh, st)) != cudaSuccess) return e;
+    if ((e = launch_requant_rows(d.I, M, gubuf, hq16, sh, ymax, st)) != cudaSuccess) return e;
     if ((e = launch_gemv_down(d, expert_offsets, w, hq16, sh, ybuf, ymax, err, nullptr, 1, st)) != cudaSuccess)
         return e;
     return launch_retquant_rows(d, M, ybuf, ymax, expert_rows, meta, static_cast<unsigned char*>(cbuf),

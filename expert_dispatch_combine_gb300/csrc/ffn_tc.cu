@@ -777,9 +777,11 @@ __device__ __forceinline__ void load_chunk16(const float4* __restrict__ src, int
 // largest I), so g and u are read once.
 template <int CH>
 __global__ void __launch_bounds__(kRowMaxThreads)
-requant_kernel(int I, const float* __restrict__ gu, __half* __restrict__ hq, float* __restrict__ sh) {
+requant_kernel(int I, const float* __restrict__ gu, __half* __restrict__ hq, float* __restrict__ sh,
+               unsigned* __restrict__ ymax) {
     __shared__ float s_red[kRowMaxThreads / 32];
     const int r = blockIdx.x;
+    if (threadIdx.x == 0) ymax[r] = 0u;  // the down epilogue's row maximum of y starts at 0
     const int nch = I / 16;
     const int nt = blockDim.x;
     const float4* gsrc = reinterpret_cast<const float4*>(gu + (long long)r * 2 * I);
@@ -1176,8 +1178,6 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     cudaError_t e;
 
     if (clear && (e = clear_status(ws, st)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(ymax, 0, sizeof(unsigned) * M, st)) != cudaSuccess) return e;
-    count_launches(1);
     const bool fuse = fc.out != nullptr && int8_ret;
     int* ready = ws_ptr<int>(ws, wl.ready);
     if (fuse) {  // readiness counters and the work ticket start at zero
@@ -1226,7 +1226,7 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                                  st)) != cudaSuccess)
         return e;
 
-    if ((e = launch_requant_rows(d.I, M, gubuf, hq16, sh, st)) != cudaSuccess) return e;
+    if ((e = launch_requant_rows(d.I, M, gubuf, hq16, sh, ymax, st)) != cudaSuccess) return e;
 
     Params P2 = {};
     P2.G = d.E_phys; P2.offsets = expert_offsets; P2.tile_prefix = tp; P2.ttab = ttab;
@@ -1310,12 +1310,13 @@ cudaError_t launch_weights_to_f16(const int8_t* src, long long n, uint16_t* dst,
     return cudaGetLastError();
 }
 
-cudaError_t launch_requant_rows(int I, long long M, const float* gu, void* hq16, float* sh, cudaStream_t st) {
+cudaError_t launch_requant_rows(int I, long long M, const float* gu, void* hq16, float* sh, unsigned* ymax,
+                                cudaStream_t st) {
     const int nt = tc::row_threads(I);
     if (I / 16 <= 2 * nt)
-        tc::requant_kernel<2><<<(unsigned)M, nt, 0, st>>>(I, gu, static_cast<__half*>(hq16), sh);
+        tc::requant_kernel<2><<<(unsigned)M, nt, 0, st>>>(I, gu, static_cast<__half*>(hq16), sh, ymax);
     else
-        tc::requant_kernel<4><<<(unsigned)M, nt, 0, st>>>(I, gu, static_cast<__half*>(hq16), sh);
+        tc::requant_kernel<4><<<(unsigned)M, nt, 0, st>>>(I, gu, static_cast<__half*>(hq16), sh, ymax);
     count_launches(1);
     return cudaGetLastError();
 }

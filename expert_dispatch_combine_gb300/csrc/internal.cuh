@@ -246,8 +246,10 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
 cudaError_t launch_weights_to_f16(const int8_t* src, long long n, uint16_t* dst, cudaStream_t st);
 // SwiGLU and the token-wise requantisation of its output (row kernel of the
 // tensor-core and matrix-vector paths): h = SiLU(g) * u from g, u [M][2I],
-// hq as exact fp16 integers and the scales s_h.
-cudaError_t launch_requant_rows(int I, long long M, const float* gu, void* hq16, float* sh, cudaStream_t st);
+// hq as exact fp16 integers and the scales s_h; it also zeroes each row's
+// word of ymax, which the down projection's epilogue then max-reduces.
+cudaError_t launch_requant_rows(int I, long long M, const float* gu, void* hq16, float* sh, unsigned* ymax,
+                                cudaStream_t st);
 // INT8 return messages from y and its row maxima into the combine rows
 // (rows whose dispatch slot or metadata is out of range are skipped and
 // MOE_ERR_INDEX is posted to *err).
