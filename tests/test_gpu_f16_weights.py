@@ -50,6 +50,9 @@ F16_CASES = {
     "partial_block": dict(T=600, H=1088, E_log=8, k=2, I=192, R=2, S=4),        # 17 stages, 8.5 channel blocks
     "chunks": dict(T=520, H=2112, E_log=8, k=2, I=128, R=4, S=2),               # 33 stages: 3 exact chunks
     "zipf": dict(T=1024, H=512, E_log=16, k=4, I=256, R=8, S=4, zipf=1.3),      # hot experts, several tiles
+    # tiles of at most 64 rows take two 64-K stages per ring slot; odd stage
+    # counts (33 for gate/up, 3 for down) end on a zero-filled half slot
+    "packed_odd": dict(T=200, H=2112, E_log=8, k=2, I=192, R=2, S=2, zipf=1.3),
 }
 
 
