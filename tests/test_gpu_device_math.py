@@ -1,6 +1,6 @@
 """Device arithmetic of the library against its straightforward forms:
 
-- the SiLU of the gate/up GEMM epilogue (branch-free, FMA-based division)
+- the SiLU of the requantisation row kernel (branch-free, FMA-based division)
   against the IEEE-division form on every binary32 input, and both, with the
   exp behind them, against the oracle on a strided sample plus special values;
 - the token-wise INT8 code of the dispatch and row kernels (the quotient
