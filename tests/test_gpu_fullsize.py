@@ -1,5 +1,6 @@
 """Full-size parity: the DeepSeek-V3-shaped workloads through moe_layer (the
-launch configuration bench.py times), compared with the oracle
+launch configuration bench.py times, with and without the fp16 weight
+copies), compared with the oracle
 
   - in full for every index array (routing, counts, dispatch layout, meta);
   - on sampled tokens for the INT8 codes of the dispatch messages, the return
@@ -36,10 +37,14 @@ def _sample(T, n=10, seed=0):
     return sorted(set(base + extra))
 
 
-@pytest.mark.parametrize("name", ["c1_decode", "c2_decode_zipf", "c3_eplb", "c4_prefill"])
-def test_fullsize_layer_sampled(name):
+@pytest.mark.parametrize("name,f16", [
+    ("c1_decode", False), ("c2_decode_zipf", False), ("c3_eplb", False), ("c4_prefill", False),
+    # the tensor-core GEMMs on the fp16 weight copies (bench.py's default form)
+    ("c2_decode_zipf", True), ("c3_eplb", True), ("c4_prefill", True),
+])
+def test_fullsize_layer_sampled(name, f16):
     w = synth.WORKLOADS[name]
-    layer = make_layer(w)
+    layer = make_layer(w, f16_weights=f16)
     lg = synth.logits(w)
     xb = synth.hidden_bits(w)
     out = layer.forward(torch.from_numpy(lg).cuda(), bits_to_bf16_tensor(xb))
@@ -89,9 +94,10 @@ def test_fullsize_layer_sampled(name):
     torch.cuda.empty_cache()
 
 
-def test_fullsize_repeat_is_bitwise_deterministic():
-    w = synth.WORKLOADS["c1_decode"]
-    layer = make_layer(w)
+@pytest.mark.parametrize("name,f16", [("c1_decode", False), ("c2_decode_zipf", True)])
+def test_fullsize_repeat_is_bitwise_deterministic(name, f16):
+    w = synth.WORKLOADS[name]
+    layer = make_layer(w, f16_weights=f16)
     lg = torch.from_numpy(synth.logits(w)).cuda()
     x = bits_to_bf16_tensor(synth.hidden_bits(w))
     a = layer.forward(lg, x).clone()
