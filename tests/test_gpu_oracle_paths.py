@@ -127,13 +127,16 @@ def _oracle_layer(w, lg, xb, cfmt=B.MOE_MSG_INT8):
     return oracle.layer(lg, xb, weights, w.E_phys, w.R, w.S, w.k, w.I, cfmt, rep, nc, p2l)
 
 
-@pytest.mark.parametrize("w", [
-    synth.WORKLOADS["c0_tiny"],
-    synth.custom("eplb_tiny", T=96, H=128, E_log=16, E_phys=24, k=2, I=64, R=8, seed=3,
-                 zipf=1.2, eplb=True),
-], ids=["c0_tiny", "eplb_tiny"])
-def test_graph_replay_vs_oracle(w):
-    layer = make_layer(w)
+@pytest.mark.parametrize("w,f16", [
+    (synth.WORKLOADS["c0_tiny"], False),
+    (synth.custom("eplb_tiny", T=96, H=128, E_log=16, E_phys=24, k=2, I=64, R=8, seed=3,
+                  zipf=1.2, eplb=True), False),
+    # 1024 routed rows over 8 experts: the tensor-core GEMMs on the fp16 weight
+    # copies, and the dispatch writing their input rows, inside the graph
+    (synth.custom("graph_f16", T=512, H=256, E_log=8, k=2, I=128, R=4, seed=5, zipf=1.2), True),
+], ids=["c0_tiny", "eplb_tiny", "f16_copies"])
+def test_graph_replay_vs_oracle(w, f16):
+    layer = make_layer(w, f16_weights=f16)
     gl = GraphedLayer(layer, n_sets=2)
     try:
         for step in range(4):
