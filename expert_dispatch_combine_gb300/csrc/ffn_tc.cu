@@ -650,27 +650,38 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 ++q;
                 if (c == nchunks - 1) {
                     // epilogue from the final sums, overlapping the next chunks' MMAs
-#pragma unroll 1
-                    for (int gi = 0; gi < ng; ++gi) {
-                        if (ok) {
-                            int iv[GT];  // this group's sums (predicated moves keep rs in registers)
+                    if constexpr (EPI == EPI_GU || EPI == EPI_F32) {
+                        // unrolled over the groups, so that each group's sums are a
+                        // fixed slice of rs (no selection of registers per group)
 #pragma unroll
-                            for (int g2 = 0; g2 < NGRP; ++g2)
-                                if (g2 == gi) {
-#pragma unroll
-                                    for (int j = 0; j < GT; ++j) iv[j] = rs[g2 * GT + j];
-                                }
-                            const int j0 = tok0 + gi * GT;
-                            if constexpr (EPI == EPI_GU || EPI == EPI_F32) {
+                        for (int gi = 0; gi < NGRP; ++gi) {
+                            if (ok && gi < ng) {
+                                const int (&iv)[GT] = *reinterpret_cast<const int(*)[GT]>(&rs[gi * GT]);
                                 float* buf = reinterpret_cast<float*>(my_stg + (ngrp_done & 1) * STG_BYTES);
-                                if (!epilogue_staged<EPI>(P, ti, row, lane, j0, iv, buf, &tmO, wgb, leader))
+                                if (!epilogue_staged<EPI>(P, ti, row, lane, tok0 + gi * GT, iv, buf, &tmO, wgb,
+                                                          leader))
                                     ok = false;
                                 ++ngrp_done;
-                            } else if (EPI == EPI_I32 && P.tma_out && j0 + GT <= ti.nvalid) {
-                                if (!epilogue_tma<EPI>(P, ti, row, lane, j0, iv, my_stg, &tmO, wgb, leader))
-                                    ok = false;
-                            } else {
-                                epilogue_direct<EPI>(P, ti, row, lane, j0, iv);
+                            }
+                        }
+                    } else {
+#pragma unroll 1
+                        for (int gi = 0; gi < ng; ++gi) {
+                            if (ok) {
+                                int iv[GT];  // this group's sums (predicated moves keep rs in registers)
+#pragma unroll
+                                for (int g2 = 0; g2 < NGRP; ++g2)
+                                    if (g2 == gi) {
+#pragma unroll
+                                        for (int j = 0; j < GT; ++j) iv[j] = rs[g2 * GT + j];
+                                    }
+                                const int j0 = tok0 + gi * GT;
+                                if (EPI == EPI_I32 && P.tma_out && j0 + GT <= ti.nvalid) {
+                                    if (!epilogue_tma<EPI>(P, ti, row, lane, j0, iv, my_stg, &tmO, wgb, leader))
+                                        ok = false;
+                                } else {
+                                    epilogue_direct<EPI>(P, ti, row, lane, j0, iv);
+                                }
                             }
                         }
                     }
