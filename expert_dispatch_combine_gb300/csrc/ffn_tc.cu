@@ -325,18 +325,22 @@ __device__ __forceinline__ bool epilogue_tma(const Params& P, const TileInfo& ti
 // group's barrier, and before that barrier the leader waits for the previous
 // group's tensor store to have read its buffer, so a buffer is free again
 // when the group after next writes it.
-template <int EPI>
+// The token scales of the warpgroup's columns and the channel scale come in
+// from the tile's start (srv[q]: token tok0 + 32 q + lane, 0 past the tile's
+// rows; sd: 0 past the outputs), so that no group waits on a global load;
+// tl0 is the group's first column within the warpgroup's half (a constant
+// once the group loop is unrolled).
+template <int EPI, int NQ>
 __device__ __forceinline__ bool epilogue_staged(const Params& P, const TileInfo& ti, int row,
-                                                int lane, int j0, const int (&iv)[GT], float* stg,
+                                                int lane, int j0, int tl0, const int (&iv)[GT],
+                                                const float (&srv)[NQ], float sd, float* stg,
                                                 const CUtensorMap* tmO, WgBarrier& wg, bool leader) {
     const int nv = min(GT, ti.nvalid - j0);  // valid tokens in this group (>= 1)
-    const float sr_l = lane < nv ? P.s_row[ti.r0 + j0 + lane] : 0.f;
     const int col = ti.mb * 128 + row;
     const bool chok = col < P.nout;
-    const float sd = chok ? P.s_ch[(long long)ti.set * P.rows_per_set + col] : 0.f;
 #pragma unroll
     for (int j = 0; j < GT; ++j) {
-        const float sr = __shfl_sync(0xffffffffu, sr_l, j);
+        const float sr = __shfl_sync(0xffffffffu, srv[(tl0 + j) >> 5], (tl0 + j) & 31);
         stg[j * 128 + row] = __fmul_rn(__fmul_rn(__int2float_rn(iv[j]), sr), sd);  // 0 off the edge
     }
     ptx::fence_proxy_async_smem();
@@ -622,6 +626,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             e_next = tile_entry(P, tile + gridDim.x, total_tiles);
             const int tok0 = h * HALF;
             const int ng = max(0, min(NGRP, (ti.nmma - tok0 + GT - 1) / GT));
+            // the staged epilogue's scales, loaded while the tile's chunks run
+            constexpr int NQ = HALF / 32;
+            float srv[NQ];
+            float sdv = 0.f;
+            if constexpr (EPI == EPI_GU || EPI == EPI_F32) {
+#pragma unroll
+                for (int qq = 0; qq < NQ; ++qq) {
+                    const int t = tok0 + 32 * qq + lane;
+                    srv[qq] = t < ti.nvalid ? P.s_row[ti.r0 + t] : 0.f;
+                }
+                const int col = ti.mb * 128 + row;
+                sdv = col < P.nout ? P.s_ch[(long long)ti.set * P.rows_per_set + col] : 0.f;
+            }
             for (int c = 0; ok && c < nchunks; ++c) {
                 const uint32_t b = q & 1;
                 if (!warp_wait(accfull(b), (q >> 1) & 1, P.err)) {
@@ -658,8 +675,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                             if (ok && gi < ng) {
                                 const int (&iv)[GT] = *reinterpret_cast<const int(*)[GT]>(&rs[gi * GT]);
                                 float* buf = reinterpret_cast<float*>(my_stg + (ngrp_done & 1) * STG_BYTES);
-                                if (!epilogue_staged<EPI>(P, ti, row, lane, tok0 + gi * GT, iv, buf, &tmO, wgb,
-                                                          leader))
+                                if (!epilogue_staged<EPI, NQ>(P, ti, row, lane, tok0 + gi * GT, gi * GT, iv, srv,
+                                                              sdv, buf, &tmO, wgb, leader))
                                     ok = false;
                                 ++ngrp_done;
                             }
