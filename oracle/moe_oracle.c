@@ -100,7 +100,8 @@ uint16_t orc_round_f32_to_bf16(float v) { return orc_f32_to_bf16(v); }
  *   r = (x - n*LN2_HI) - n*LN2_LO    (LN2_HI has 14 significant bits, so
  *                                      n*LN2_HI is exact for |n| <= 127)
  *   p = 1 + r(1 + r(1/2 + r(1/6 + r(1/24 + r(1/120 + r(1/720 + r/5040))))))
- *       evaluated by Horner from the innermost term, the coefficients being
+ *       evaluated by Horner from the innermost term, each step a fused
+ *       multiply-add p = fma(r, p, c) (one rounding), the coefficients being
  *       the binary32 values nearest 1/m!
  *   e = p * 2^n                       (exact power-of-two scaling)
  * This is Cody and Waite's argument reduction followed by the Taylor series
@@ -122,10 +123,8 @@ float orc_exp_spec(float x)
     float r = x - a;
     r = r - b;
     float p = c[7];
-    for (int m = 6; m >= 0; --m) {
-        float rp = r * p;
-        p = c[m] + rp;
-    }
+    for (int m = 6; m >= 0; --m)
+        p = fmaf(r, p, c[m]);
     int ni = (int)n;
     uint32_t bits = (uint32_t)(ni + 127) << 23;
     float s;
