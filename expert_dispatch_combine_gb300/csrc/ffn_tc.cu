@@ -27,14 +27,16 @@
 //     swizzle), TMA-loaded in 32-row boxes so that small experts only load
 //     the rows they have; the MMA N is the tile's token count rounded up to 16.
 //   TMEM (512 columns): two BN-column fp32 accumulators, so that the drain
-//     of one 1024-K chunk overlaps the MMAs of the next, and the rest in
-//     pairs of 32-column A slots (two pairs at BN = 192, three at 160).  The
-//     int32 running sums live in registers of two drain warpgroups (BN / 2
-//     token columns each).
-//   Issue: the single MMA thread waits once per PAIR of 64-K stages (8 MMAs):
-//     each wait costs the issuing thread a few hundred cycles, which 4 MMAs
-//     of N <= 224 do not cover but 8 do.  The converter fills the A slots of
-//     one pair while the MMAs of the others run.
+//     of one 1024-K chunk overlaps the MMAs of the next, and (int8 form) the
+//     rest in pairs of 32-column A slots (two pairs at BN = 192, six at the
+//     64-token decode tiles).  The int32 running sums live in registers of
+//     two drain warpgroups (BN / 2 token columns each).
+//   Issue: int8 form, the single MMA thread waits once per PAIR of 64-K
+//     stages (8 MMAs): each wait costs the issuing thread a few hundred
+//     cycles, which 4 MMAs of N <= 224 do not cover but 8 do, and the
+//     converter fills the A slots of one pair while the MMAs of the others
+//     run; fp16 form, one wait per 48 KB stage (4 MMAs of N up to 256), since
+//     pairs of such stages would leave only two ring slots.
 //   Epilogue: each 16-token group is scaled, staged in shared memory and
 //     written with one TMA tensor store (partial groups use plain stores).
 // The gate/up GEMM computes the gate and up projections g, u of all 2I
