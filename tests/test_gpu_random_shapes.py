@@ -78,3 +78,28 @@ def test_random_shape_layer_vs_oracle(c):
     w = synth.custom("rand", seed=77, T=c["T"], H=c["H"], E_log=c["E_log"], E_phys=c["E_phys"],
                      k=c["k"], I=c["I"], R=c["R"], S=c["S"], zipf=c["zipf"], eplb=c["eplb"])
     _full_layer_check(w, c["cfmt"], f16_weights=c["f16"])
+
+
+def _large(seed: int) -> dict:
+    """Shapes with many token tiles per expert on the fp16 copies: 4096 to
+    8192 routed rows over 8 or 16 experts, skewed so that the hottest ones
+    span more than one raster band of 8 token tiles."""
+    rng = np.random.default_rng(2000 + seed)
+    R = 8
+    E_log = int(rng.choice([8, 16]))
+    k = int(rng.choice([2, 4]))
+    T = 8 * int(rng.integers(512 // k, 1024 // k + 1))
+    H = 64 * int(rng.integers(4, 17))
+    I = 64 * int(rng.integers(2, 9))
+    return dict(T=T, H=H, E_log=E_log, E_phys=E_log, k=k, I=I, R=R, S=8, zipf=float(rng.choice([1.2, 1.6])),
+                eplb=False, f16=True, cfmt=B.MOE_MSG_INT8)
+
+
+LARGE = [_large(s) for s in range(4)]
+
+
+@pytest.mark.parametrize("c", LARGE, ids=[_id(c) for c in LARGE])
+def test_random_large_shape_layer_vs_oracle(c):
+    w = synth.custom("rand_large", seed=78, T=c["T"], H=c["H"], E_log=c["E_log"], E_phys=c["E_phys"],
+                     k=c["k"], I=c["I"], R=c["R"], S=c["S"], zipf=c["zipf"], eplb=False)
+    _full_layer_check(w, c["cfmt"], f16_weights=True)
