@@ -22,7 +22,10 @@
 //     memory (the A-from-TMEM form of tcgen05.mma);
 //     fp16 copies (made once by moe_weights_to_f16, twice the bytes): TMA
 //     loads them straight into shared memory and the MMA reads both operands
-//     from there (the SS form); no conversion on the SM, 256-token tiles;
+//     from there (the SS form); no conversion on the SM, 256-token tiles, run
+//     by CTA pairs (cta_group::2: a cluster of two CTAs computes 256 channels
+//     of a tile with M = 256 MMAs issued by the even CTA, each CTA staging its
+//     own 128 weight rows and half of the tokens);
 //   B operand = activations, up to BN tokens per tile (fp16, K-major, 128B
 //     swizzle), TMA-loaded in 32-row boxes so that small experts only load
 //     the rows they have; the MMA N is the tile's token count rounded up to 16.
@@ -35,8 +38,11 @@
 //     stages (8 MMAs): each wait costs the issuing thread a few hundred
 //     cycles, which 4 MMAs of N <= 224 do not cover but 8 do, and the
 //     converter fills the A slots of one pair while the MMAs of the others
-//     run; fp16 form, one wait per 48 KB stage (4 MMAs of N up to 256), since
-//     pairs of such stages would leave only two ring slots.
+//     run; fp16 form on CTA pairs, one wait per pair of 32 KB stages (8 M =
+//     256 MMAs, three ring slots).  The MMA thread's per-wait cost bounds the
+//     pipeline (one 64-K stage took about 340 ns whatever the tile on a single
+//     CTA, one wait per 48 KB stage); the pair does twice the tensor work per
+//     wait and stage.
 //   Epilogue: each 16-token group is scaled, staged in shared memory and
 //     written with one TMA tensor store (partial groups use plain stores).
 // The gate/up GEMM computes the gate and up projections g, u of all 2I
@@ -91,20 +97,27 @@ constexpr int THREADS = 512;
 // wins: BN 256 with four 48 KB stages (measured 0.84 of the bf16 peak on 1024
 // rows per expert, against 0.76 / 0.67 / 0.58 / 0.49 at BN 224 / 192 / 160 /
 // 128).
-template <int BNV, bool AF16 = false>
+// CTA pairs (PAIR, fp16 weights, 256-token tiles): the two CTAs of a cluster
+// run a tile of 256 channels with one M = 256 MMA per K step; each stages its
+// own 128 weight rows and half of the tile's tokens, 32 KB a stage, six
+// stages in pairs (one wait for 8 MMAs, three ring slots).  The per-stage
+// control cost (the MMA thread's wait, issue and commit) bounds the
+// single-CTA form; the pair form does twice the tensor work per wait.
+template <int BNV, bool AF16 = false, bool PAIR = false>
 struct Tile {
     static constexpr int BN = BNV;                            // tokens per tile
     static constexpr int A_BYTES = AF16 ? 128 * BK * 2 : 128 * BK;  // weights per stage (16 / 8 KB)
-    static constexpr int B_BYTES = BN * BK * 2;               // fp16 activations per stage
+    static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;  // this CTA's fp16 activations per stage
     static constexpr int STAGE_BYTES = B_BYTES + A_BYTES;
     // shared-memory stages: for fp16 weights as many as fit beside the
     // epilogue staging buffers and the barriers
     static constexpr int NS_F16 = (227 * 1024 - 4 * STG_BYTES - 2048) / STAGE_BYTES;
     static constexpr int NS = AF16 ? NS_F16 : (BN == 64 ? 12 : 6);
     // stages per pipeline step (one full/empty barrier pair and one wait of
-    // the MMA thread per step): pairs for int8 weights, single stages for
-    // fp16 weights, whose 48 KB stages would leave only two pair slots
-    static constexpr int SPS = AF16 ? 1 : 2;
+    // the MMA thread per step): pairs for int8 weights and for CTA pairs,
+    // single stages for fp16 weights on one CTA, whose 48 KB stages would
+    // leave only two pair slots
+    static constexpr int SPS = (AF16 && !PAIR) ? 1 : 2;
     static constexpr int NP = NS / SPS;                       // step slots
     static constexpr uint32_t TM_A = 2 * BN;                  // after the two accumulators
     static constexpr int NAP_FIT = (TM_COLS - TM_A) / 64;     // A-slot pairs that fit in TMEM
@@ -117,9 +130,12 @@ struct Tile {
     static_assert(BN % 32 == 0 && BN <= 256 && HALF % GT == 0 && NS % SPS == 0 && CK % SPS == 0, "tile shape");
     static_assert(B_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "operands start on 128B-swizzle atoms");
     static_assert(SMEM_BYTES <= 227 * 1024, "dynamic shared memory per CTA");
+    static_assert(!PAIR || (AF16 && BN == 256), "CTA pairs take fp16 weights and 256-token tiles");
     static_assert(AF16 ? TM_A <= TM_COLS : (NAP >= 2 && TM_A + NAP * 64 <= TM_COLS),
                   "two accumulators (and, for int8 weights, two or more A-slot pairs) in TMEM");
 };
+// the fp16-copy GEMMs run as CTA pairs
+constexpr bool kPairF16 = true;
 // token tiles per raster band (tile order, below)
 constexpr int kRasterTokenTiles = 8;
 constexpr int BN_LARGE = kTcTileRows, BN_DECODE = kTcMinTileRows, BN_F16 = kTcTileRowsF16;
@@ -362,7 +378,8 @@ __device__ __forceinline__ bool epilogue_staged(const Params& P, const TileInfo&
         if (p == 0 && j < nv) atomicMax(&P.rowmax[ti.r0 + j0 + j], __float_as_uint(m));
     }
     if (nv == GT && P.tma_out) {
-        if (leader) {
+        // (a CTA pair's last tile may hold a channel block wholly beyond nout)
+        if (leader && ti.mb * 128 < P.nout) {
             ptx::tma_store_2d(tmO, ti.mb * 128, ti.r0 + j0, ptx::smem_addr(stg));
             ptx::bulk_commit();
         }
@@ -374,12 +391,32 @@ __device__ __forceinline__ bool epilogue_staged(const Params& P, const TileInfo&
     return true;
 }
 
-template <int EPI, int BNV, bool AF16>
+// The persistent tile loop's worker index and count: the CTA's, or for CTA
+// pairs the pair's.  Read at each use: holding them (and a capturing decode
+// lambda) in registers across the whole kernel measured 12% slower on the
+// int8-weight GEMMs.
+template <bool PAIR>
+__device__ __forceinline__ int tile_worker() {
+    return PAIR ? (int)ptx::cluster_id_x() : (int)blockIdx.x;
+}
+template <bool PAIR>
+__device__ __forceinline__ int tile_workers() {
+    return PAIR ? (int)ptx::cluster_count_x() : (int)gridDim.x;
+}
+// a pair's tile names its 256-channel block; each CTA takes its 128
+template <bool PAIR>
+__device__ __forceinline__ TileInfo decode_tile(const Params& P, int tile, const TileRef& r, uint32_t rank) {
+    TileInfo t = decode(P, tile, r);
+    if constexpr (PAIR) t.mb = 2 * t.mb + (int)rank;
+    return t;
+}
+
+template <int EPI, int BNV, bool AF16, bool PAIR = false>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                const __grid_constant__ CUtensorMap tmXb,
                const __grid_constant__ CUtensorMap tmO, const Params P) {
-    using TL = Tile<BNV, AF16>;
+    using TL = Tile<BNV, AF16, PAIR>;
     constexpr int BN = TL::BN, NS = TL::NS, NP = TL::NP, NAP = TL::NAB, HALF = TL::HALF, NGRP = TL::NGRP;
     constexpr int SPS = TL::SPS, CKP = CK / SPS;  // stages per step; steps per exact chunk
     constexpr int A_BYTES = TL::A_BYTES, B_BYTES = TL::B_BYTES, STAGE_BYTES = TL::STAGE_BYTES;
@@ -393,6 +430,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE_BYTES + 4 * STG_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // CTA pairs: this CTA's rank in its pair (0 issues the MMAs); tiles go to
+    // pairs, the pair's index and count (tile_worker / tile_workers) replacing
+    // the CTA's
+    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
 
     auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
     auto fullp = [&](int sp) { return bar(sp); };        // the stages of step slot sp loaded
@@ -411,7 +452,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         for (int p = 0; p < NAP; ++p) ptx::mbar_init(afull(p), 4);
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accfull(b), 1);
-            ptx::mbar_init(accempty(b), 8);
+            ptx::mbar_init(accempty(b), PAIR ? 16 : 8);  // pairs: both CTAs' drain warps
         }
         ptx::mbar_init(done_bar, 1);
         ptx::mbar_init(wg_bar(0), 4);
@@ -425,11 +466,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         if (EPI != EPI_BF16MSG) ptx::prefetch_tmap(&tmO);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), TM_COLS);
-        ptx::tmem_relinquish();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), TM_COLS);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_addr(tmem_slot), TM_COLS);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) ptx::cluster_sync();  // the peer's barriers exist before any remote arrival
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -448,17 +495,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             // expect_tx for both stages' bytes, then the loads of both.
             uint32_t pr = 0;  // stage pairs issued
             bool ok = true;
-            TileRef e_next = tile_entry(P, blockIdx.x, total_tiles);
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const TileInfo ti = decode(P, tile, e_next);
-                e_next = tile_entry(P, tile + gridDim.x, total_tiles);
+            TileRef e_next = tile_entry(P, tile_worker<PAIR>(), total_tiles);
+            for (int tile = tile_worker<PAIR>(); ok && tile < total_tiles; tile += tile_workers<PAIR>()) {
+                const TileInfo ti = decode_tile<PAIR>(P, tile, e_next, rank);
+                e_next = tile_entry(P, tile + tile_workers<PAIR>(), total_tiles);
                 const int yw0 = ti.set * P.rows_per_set + ti.mb * 128;
                 const int yw1 = yw0 + P.box1_off;
-                // nearly full tiles take their activations in one BN-row box
-                // (same shared-memory image as the 32-row boxes), ragged ones
-                // only the 32-row boxes they need
-                const int nb = (ti.nmma + BOX_ROWS - 1) / BOX_ROWS;
-                const bool one_box = nb == BN / BOX_ROWS;
+                // nearly full tiles take their activations in one box of all
+                // the CTA's rows (same shared-memory image as the 32-row
+                // boxes), ragged ones only the 32-row boxes they need; in a
+                // pair each CTA takes one half of the MMA's N (the even CTA
+                // the first)
+                const int brows = PAIR ? ti.nmma / 2 : ti.nmma;
+                const int brow0 = PAIR ? ti.r0 + (int)rank * brows : ti.r0;
+                const int nb = (brows + BOX_ROWS - 1) / BOX_ROWS;
+                const bool one_box = nb == (PAIR ? BN / 2 : BN) / BOX_ROWS;
                 const uint32_t bytes = SPS * (A_BYTES + nb * BOX_BYTES);
                 for (int kp = 0; kp < KSP; ++kp, ++pr) {
                     const int sp = pr % NP;
@@ -466,32 +517,62 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                         ok = false;
                         break;
                     }
-                    ptx::mbar_expect_tx(fullp(sp), bytes);
+                    if constexpr (PAIR) {
+                        // both CTAs' loads complete on the even CTA's barrier,
+                        // whose producer alone expects the bytes of both (the
+                        // same count: both take the same boxes).  The odd
+                        // CTA's bytes may land before that arrival; the phase
+                        // cannot complete without it, and the odd CTA cannot
+                        // load the slot again before the MMAs of this phase
+                        // released it.
+                        const uint32_t fb = ptx::mapa(fullp(sp), 0);
+                        if (rank == 0) ptx::mbar_expect_tx(fullp(sp), 2 * bytes);
 #pragma unroll
-                    for (int j = 0; j < SPS; ++j) {
-                        const uint32_t st = ptx::smem_addr(stages + (SPS * sp + j) * STAGE_BYTES);
-                        const int x = (SPS * kp + j) * BK;  // beyond K (padding stage): zero fill
-                        if constexpr (AF16) {  // one 128-row fp16 box, 128B swizzle
-                            ptx::tma_load_2d(st + B_BYTES, &tmW, x, yw0, fullp(sp));
-                        } else {               // two 64-row int8 boxes, 64B swizzle
-                            ptx::tma_load_2d(st + B_BYTES, &tmW, x, yw0, fullp(sp));
-                            ptx::tma_load_2d(st + B_BYTES + 4096, &tmW, x, yw1, fullp(sp));
+                        for (int j = 0; j < SPS; ++j) {
+                            const uint32_t st = ptx::smem_addr(stages + (SPS * sp + j) * STAGE_BYTES);
+                            const int x = (SPS * kp + j) * BK;  // beyond K (padding stage): zero fill
+                            ptx::tma_load_2d_pair(st + B_BYTES, &tmW, x, yw0, fb);
+                            if (one_box) {
+                                ptx::tma_load_2d_pair(st, &tmXb, x, brow0, fb);
+                            } else {
+                                for (int b = 0; b < nb; ++b)
+                                    ptx::tma_load_2d_pair(st + b * BOX_BYTES, &tmX, x, brow0 + b * BOX_ROWS, fb);
+                            }
                         }
-                        if (one_box) {
-                            ptx::tma_load_2d(st, &tmXb, x, ti.r0, fullp(sp));
-                        } else {
-                            for (int b = 0; b < nb; ++b)
-                                ptx::tma_load_2d(st + b * BOX_BYTES, &tmX, x, ti.r0 + b * BOX_ROWS, fullp(sp));
+                    } else {
+                        ptx::mbar_expect_tx(fullp(sp), bytes);
+#pragma unroll
+                        for (int j = 0; j < SPS; ++j) {
+                            const uint32_t st = ptx::smem_addr(stages + (SPS * sp + j) * STAGE_BYTES);
+                            const int x = (SPS * kp + j) * BK;  // beyond K (padding stage): zero fill
+                            if constexpr (AF16) {  // one 128-row fp16 box, 128B swizzle
+                                ptx::tma_load_2d(st + B_BYTES, &tmW, x, yw0, fullp(sp));
+                            } else {               // two 64-row int8 boxes, 64B swizzle
+                                ptx::tma_load_2d(st + B_BYTES, &tmW, x, yw0, fullp(sp));
+                                ptx::tma_load_2d(st + B_BYTES + 4096, &tmW, x, yw1, fullp(sp));
+                            }
+                            if (one_box) {
+                                ptx::tma_load_2d(st, &tmXb, x, ti.r0, fullp(sp));
+                            } else {
+                                for (int b = 0; b < nb; ++b)
+                                    ptx::tma_load_2d(st + b * BOX_BYTES, &tmX, x, ti.r0 + b * BOX_ROWS, fullp(sp));
+                            }
                         }
                     }
                 }
             }
             if (!ok) {  // let the loads already issued land before leaving
-                for (uint32_t j = (pr > NP ? pr - NP : 0); j < pr; ++j)
-                    mbar_wait_quiet(fullp(j % NP), (j / NP) & 1, DRAIN_NS);
+                if (!PAIR || rank == 0) {
+                    for (uint32_t j = (pr > NP ? pr - NP : 0); j < pr; ++j)
+                        mbar_wait_quiet(fullp(j % NP), (j / NP) & 1, DRAIN_NS);
+                } else {  // the odd CTA's loads count on the even CTA's barriers
+                    const uint64_t t0 = ptx::globaltimer();
+                    while (ptx::globaltimer() - t0 < DRAIN_NS) __nanosleep(1000);
+                }
             }
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1 && lane == 0 && (!PAIR || rank == 0)) {
             // --------------------------------------------- MMA issuer
+            // (pairs: the even CTA issues the pair's M = 256 MMAs)
             // Per step: one wait (int8 weights: for the converted weights of
             // the stage pair, which the converter signals only after it has
             // seen the pair's loads land; fp16 weights: for the stage's loads),
@@ -501,11 +582,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             bool ok = true;
             const uint64_t bdesc0 = ptx::sdesc_k_sw128(ptx::smem_addr(stages));
             const uint64_t adesc0 = ptx::sdesc_k_sw128(ptx::smem_addr(stages + B_BYTES));
-            TileRef e_next = tile_entry(P, blockIdx.x, total_tiles);
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const TileInfo ti = decode(P, tile, e_next);
-                e_next = tile_entry(P, tile + gridDim.x, total_tiles);
-                const uint32_t idesc = ptx::idesc_f16_f32(128, ti.nmma);
+            TileRef e_next = tile_entry(P, tile_worker<PAIR>(), total_tiles);
+            for (int tile = tile_worker<PAIR>(); ok && tile < total_tiles; tile += tile_workers<PAIR>()) {
+                const TileInfo ti = decode_tile<PAIR>(P, tile, e_next, rank);
+                e_next = tile_entry(P, tile + tile_workers<PAIR>(), total_tiles);
+                const uint32_t idesc = ptx::idesc_f16_f32(PAIR ? 256 : 128, ti.nmma);
                 for (int kp = 0; kp < KSP; ++kp, ++pr) {
                     const bool first = (kp % CKP) == 0;
                     const bool last = (kp % CKP) == CKP - 1 || kp == KSP - 1;
@@ -532,11 +613,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                         // the A and B images have the same layout: one K step
                         // (16 elements, 32 bytes) is +2 in both descriptors
                         const uint64_t ad = adesc0 + soff;
-                        ptx::mma_f16_ss(d, ad, bd, idesc, first ? 0u : 1u);
 #pragma unroll
-                        for (int kk = 1; kk < SPS * BK / 16; ++kk) {
+                        for (int kk = 0; kk < SPS * BK / 16; ++kk) {
                             const uint64_t o = (kk >> 2) * (STAGE_BYTES >> 4) + (kk & 3) * 2;
-                            ptx::mma_f16_ss(d, ad + o, bd + o, idesc, 1u);
+                            const uint32_t acc = (kk > 0 || !first) ? 1u : 0u;
+                            if constexpr (PAIR) ptx::mma_f16_ss_pair(d, ad + o, bd + o, idesc, acc);
+                            else ptx::mma_f16_ss(d, ad + o, bd + o, idesc, acc);
                         }
                     } else {
                         const uint32_t abase = tmem + TM_A + (pr % NAP) * 64;
@@ -546,15 +628,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                             ptx::mma_f16_ts(d, abase + kk * 8,
                                             bd + (kk >> 2) * (STAGE_BYTES >> 4) + (kk & 3) * 2, idesc, 1u);
                     }
-                    ptx::tc_commit(emptyp(sp));  // both stages and their A slots are consumed
+                    // the step's stages (and A slots) are consumed; pairs: in both CTAs
+                    if constexpr (PAIR) ptx::tc_commit_pair(emptyp(sp), 3);
+                    else ptx::tc_commit(emptyp(sp));
                     if (last) {
-                        ptx::tc_commit(accfull(b));
+                        if constexpr (PAIR) ptx::tc_commit_pair(accfull(b), 3);
+                        else ptx::tc_commit(accfull(b));
                         ++q;
                     }
                 }
             }
             // every MMA issued above must be complete before TMEM is freed
-            ptx::tc_commit(done_bar);
+            if constexpr (PAIR) ptx::tc_commit_pair(done_bar, 1);
+            else ptx::tc_commit(done_bar);
             mbar_wait_quiet(done_bar, 0, WAIT_NS);
         }
     } else if (wgi == 1 && AF16) {
@@ -570,7 +656,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         const int sw = (row >> 1) & 3;
         uint32_t pr = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        for (int tile = tile_worker<PAIR>(); ok && tile < total_tiles; tile += tile_workers<PAIR>()) {
             for (int kp = 0; kp < KSP; ++kp, ++pr) {
                 const int sp = pr % NP;
                 // The A slots of pair pr were last read by the MMAs of pair
@@ -622,10 +708,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         uint32_t q = 0;
         bool ok = true;
         WgBarrier wgb{wg_bar(h), 0};
-        TileRef e_next = tile_entry(P, blockIdx.x, total_tiles);
-        for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-            const TileInfo ti = decode(P, tile, e_next);
-            e_next = tile_entry(P, tile + gridDim.x, total_tiles);
+        TileRef e_next = tile_entry(P, tile_worker<PAIR>(), total_tiles);
+        for (int tile = tile_worker<PAIR>(); ok && tile < total_tiles; tile += tile_workers<PAIR>()) {
+            const TileInfo ti = decode_tile<PAIR>(P, tile, e_next, rank);
+            e_next = tile_entry(P, tile + tile_workers<PAIR>(), total_tiles);
             const int tok0 = h * HALF;
             const int ng = max(0, min(NGRP, (ti.nmma - tok0 + GT - 1) / GT));
             // the staged epilogue's scales, loaded while the tile's chunks run
@@ -665,7 +751,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(accempty(b));  // buffer free for the MMA
+                if (lane == 0) {  // buffer free for the MMA (pairs: the even CTA's barrier)
+                    if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::mapa(accempty(b), 0));
+                    else ptx::mbar_arrive(accempty(b));
+                }
                 ++q;
                 if (c == nchunks - 1) {
                     // epilogue from the final sums, overlapping the next chunks' MMAs
@@ -713,8 +802,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     // ------------------------------------------------------- teardown
     ptx::tc_fence_before();
     __syncthreads();
+    // pairs: the even CTA's MMAs (which read this CTA's shared memory and
+    // write its tensor memory) have completed, and no remote arrival is due
+    if constexpr (PAIR) ptx::cluster_sync();
     ptx::tc_fence_after();
-    if (warp == 1) ptx::tmem_dealloc(tmem, TM_COLS);
+    if (warp == 1) {
+        if constexpr (PAIR) ptx::tmem_dealloc_pair(tmem, TM_COLS);
+        else ptx::tmem_dealloc(tmem, TM_COLS);
+    }
 }
 
 // ------------------------------------------------------------ helpers
@@ -1104,19 +1199,54 @@ int sm_count() {
     return cached[dev];
 }
 
-template <int EPI, int BNV, bool AF16 = false>
+// Persistent grid: one CTA per SM, or, for CTA pairs, as many two-CTA
+// clusters as the device holds at once (a GPC with an odd number of SMs
+// leaves one out).  The clusters never wait on one another.
+template <int EPI, int BNV, bool AF16 = false, bool PAIR = false>
 cudaError_t launch_gemm(const Params& P, const CUtensorMap& w, const CUtensorMap (&x)[2],
                         const CUtensorMap& o, cudaStream_t st) {
-    constexpr int smem = Tile<BNV, AF16>::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, BNV, AF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    constexpr int smem = Tile<BNV, AF16, PAIR>::SMEM_BYTES;
+    auto* kern = gemm_tc_kernel<EPI, BNV, AF16, PAIR>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int slot = EPI == EPI_GU ? 0 : 1;
-    if (cudaEvent_t ev = prof_event(slot, 0)) cudaEventRecord(ev, st);
-    gemm_tc_kernel<EPI, BNV, AF16><<<sm_count(), THREADS, smem, st>>>(w, x[0], x[1], o, P);
-    if (cudaEvent_t ev = prof_event(slot, 1)) cudaEventRecord(ev, st);
-    count_launches(1);
-    return cudaGetLastError();
+    if constexpr (PAIR) {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(sm_count() & ~1));
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        static int clusters[64][4] = {};  // per device and kernel form
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev < 0 || dev >= 64) dev = 0;
+        int& nc = clusters[dev][EPI];
+        if (!nc) {
+            int n = 0;
+            if ((e = cudaOccupancyMaxActiveClusters(&n, (const void*)kern, &cfg)) != cudaSuccess) return e;
+            if (n < 1) return cudaErrorInvalidConfiguration;
+            nc = std::min(n, sm_count() / 2);
+        }
+        cfg.gridDim = dim3((unsigned)(2 * nc));
+        if (cudaEvent_t ev = prof_event(slot, 0)) cudaEventRecord(ev, st);
+        e = cudaLaunchKernelEx(&cfg, kern, w, x[0], x[1], o, P);
+        if (cudaEvent_t ev = prof_event(slot, 1)) cudaEventRecord(ev, st);
+        count_launches(1);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    } else {
+        if (cudaEvent_t ev = prof_event(slot, 0)) cudaEventRecord(ev, st);
+        kern<<<sm_count(), THREADS, smem, st>>>(w, x[0], x[1], o, P);
+        if (cudaEvent_t ev = prof_event(slot, 1)) cudaEventRecord(ev, st);
+        count_launches(1);
+        return cudaGetLastError();
+    }
 }
 
 bool weight_map(CUtensorMap* m, const int8_t* w, int K, uint64_t rows) {
@@ -1183,7 +1313,7 @@ cudaError_t launch_grouped_gemm_tc(int n_groups, const int32_t* offsets, long lo
 
 namespace tc {
 
-template <int BNV, bool AF16>
+template <int BNV, bool AF16, bool PAIR = false>
 cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                    const int32_t* expert_offsets, const int32_t* expert_rows,
                    const moe_expert_weights& w, void* cbuf, long long scale_off, void* ws,
@@ -1233,9 +1363,10 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
                                   weight_map(&mwd, w.w_down_f16, d.I, (uint64_t)E_w * d.H)
                             : weight_map(&mwgu, w.w_gate_up, d.H, (uint64_t)E_w * 2 * d.I) &&
                                   weight_map(&mwd, w.w_down, d.I, (uint64_t)E_w * d.H);
-    if (!wmaps || !act_map(mx1, a16, d.H, (uint64_t)M, BNV) ||
+    constexpr int XBOX = PAIR ? BNV / 2 : BNV;  // a CTA's token rows of a full tile
+    if (!wmaps || !act_map(mx1, a16, d.H, (uint64_t)M, XBOX) ||
         !out_map(&mo1, gubuf, false, (uint64_t)2 * d.I, (uint64_t)M, 128) ||
-        !act_map(mx2, hq16, d.I, (uint64_t)M, BNV))
+        !act_map(mx2, hq16, d.I, (uint64_t)M, XBOX))
         return cudaErrorInvalidValue;
     const bool y_tma = int8_ret && d.H >= 128;
     if (y_tma) {
@@ -1244,13 +1375,14 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
         mo2 = mo1;  // unused
     }
 
+    constexpr int CB = PAIR ? 256 : 128;  // channels per tile
     Params P1 = {};
     P1.G = d.E_phys; P1.offsets = expert_offsets; P1.tile_prefix = tp; P1.ttab = ttab;
     P1.g2s = w.phys_to_weight;
-    P1.K = d.H; P1.rows_per_set = 2 * d.I; P1.nout = 2 * d.I; P1.mb_count = 2 * d.I / 128; P1.box1_off = 64;
+    P1.K = d.H; P1.rows_per_set = 2 * d.I; P1.nout = 2 * d.I; P1.mb_count = (2 * d.I + CB - 1) / CB; P1.box1_off = 64;
     P1.s_row = s_row; P1.s_ch = w.s_gate_up; P1.out_f32 = gubuf; P1.err = err;
     P1.tma_out = 1;
-    if ((e = launch_gemm<EPI_GU, BNV, AF16>(P1, mwgu, mx1, mo1, st)) != cudaSuccess) return e;
+    if ((e = launch_gemm<EPI_GU, BNV, AF16, PAIR>(P1, mwgu, mx1, mo1, st)) != cudaSuccess) return e;
     if (narrow > 0 &&
         (e = launch_gemv_gate_up(d, dbuf, meta, expert_offsets, expert_rows, w, gubuf, err, nlist, 2,
                                  st)) != cudaSuccess)
@@ -1261,11 +1393,11 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     Params P2 = {};
     P2.G = d.E_phys; P2.offsets = expert_offsets; P2.tile_prefix = tp; P2.ttab = ttab;
     P2.g2s = w.phys_to_weight;
-    P2.K = d.I; P2.rows_per_set = d.H; P2.nout = d.H; P2.mb_count = (d.H + 127) / 128; P2.box1_off = 64;
+    P2.K = d.I; P2.rows_per_set = d.H; P2.nout = d.H; P2.mb_count = (d.H + CB - 1) / CB; P2.box1_off = 64;
     P2.s_row = sh; P2.s_ch = w.s_down; P2.err = err; P2.tma_out = y_tma;
     if (int8_ret) {
         P2.out_f32 = ybuf; P2.rowmax = ymax;
-        if ((e = launch_gemm<EPI_F32, BNV, AF16>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
+        if ((e = launch_gemm<EPI_F32, BNV, AF16, PAIR>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
         if (narrow > 0 &&
             (e = launch_gemv_down(d, expert_offsets, w, hq16, sh, ybuf, ymax, err, nlist, 3, st)) !=
                 cudaSuccess)
@@ -1300,7 +1432,7 @@ cudaError_t ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
     } else {
         P2.expert_rows = expert_rows; P2.meta = meta; P2.cbuf = cb; P2.crow = d.crow; P2.k = d.k; P2.lb = d.lb;
         P2.S = d.S; P2.nslots = d.nslots;
-        if ((e = launch_gemm<EPI_BF16MSG, BNV, AF16>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
+        if ((e = launch_gemm<EPI_BF16MSG, BNV, AF16, PAIR>(P2, mwd, mx2, mo2, st)) != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
@@ -1376,7 +1508,7 @@ cudaError_t launch_ffn_tc(const Dims& d, const void* dbuf, long long meta_off,
         return tc::ffn_tc<tc::BN_DECODE, false>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
                                                 scale_off, ws, wl, st, fc, clear, rows_ready);
     if (w.w_gate_up_f16 && w.w_down_f16)
-        return tc::ffn_tc<tc::BN_F16, true>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
+        return tc::ffn_tc<tc::BN_F16, true, tc::kPairF16>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
                                             scale_off, ws, wl, st, fc, clear, rows_ready);
     return tc::ffn_tc<tc::BN_LARGE, false>(d, dbuf, meta_off, expert_offsets, expert_rows, w, cbuf,
                                            scale_off, ws, wl, st, fc, clear, rows_ready);
