@@ -25,7 +25,9 @@ namespace moe {
 namespace {
 
 // --------------------------------------------------------- tile prefix
-// tile_prefix[g] = sum_{g' < g} ceil(M_g' / BM), g = 0..G (one block).
+// tile_prefix[g] = sum_{g' < g} ceil(M_g' / BM), g = 0..G (one block); BM is
+// a multiple of 16.  With a non-null `table`, entry tile_prefix[g] + j
+// describes token tile j of group g: (weight set, first row, rows, g).
 // The offsets and weight sets are caller data.  Unless offsets[0] = 0, the
 // offsets never decrease, offsets[G] <= max_rows and every weight set lies in
 // [0, n_sets), the kernel posts MOE_ERR_INDEX and describes no tile at all,
@@ -103,10 +105,19 @@ tile_prefix_kernel(int G, int BM, const int32_t* __restrict__ offsets, long long
         if (g < G) {
             tile_prefix[g] = incl - n;
             if (table) {
+                // the group's rows split evenly over its n tiles in units of
+                // 16 rows (the MMA's N step): u or u + 1 units a tile, at
+                // most BM rows, the last tile holding the remainder, so only
+                // it rounds its rows up, not n - 1 full tiles and a ragged one
                 const int r0 = offsets[g], m = offsets[g + 1] - r0;
                 const int set = g2s ? g2s[g] : g;
-                for (int j = 0; j < n; ++j)
-                    table[incl - n + j] = make_int4(set, r0 + j * BM, min(BM, m - j * BM), g);
+                const int units = (m + 15) / 16;
+                const int u = n > 0 ? units / n : 0, extra = units - u * n;
+                for (int j = 0; j < n; ++j) {
+                    const int start = 16 * (j * u + min(j, extra));
+                    const int rows = min(16 * (u + (j < extra ? 1 : 0)), m - start);
+                    table[incl - n + j] = make_int4(set, r0 + start, rows, g);
+                }
             }
         }
         __syncthreads();
