@@ -188,8 +188,9 @@ struct TileInfo {
 // the band's token tiles side by side.  CTAs that start together then share
 // each weight block (one DRAM read for the band, taken in step), while a
 // band's activations stay few enough to live in L2 across its channel
-// blocks.  Each role loads the table entry of its next tile one tile ahead,
-// so the three dependent loads hide behind the current tile.
+// blocks.  Each role reads the table entry of its next tile when the current
+// one starts.  The entry is three dependent reads, and the role waits for the
+// first two in line; spreading all three over earlier tiles measured no faster.
 struct TileRef {
     int4 e;  // token-tile table entry
     int mb;  // channel block
