@@ -96,6 +96,18 @@ def test_expert_ffn_path_choice(lib):
         path(T=0)
 
 
+def test_smoke_reaches_the_tensor_core_gemms(lib):
+    """smoke()'s fp16-copy layer is above the decode size, so moe_layer runs
+    its expert FFN on the tensor-core GEMMs (on the copies: CTA pairs), with
+    no expert left to the matrix-vector kernels (H, I not multiples of 512)."""
+    import __graft_entry__ as g
+    w = synth.custom("smoke_f16", **g.SMOKE_F16)
+    shape = B.Shape(w.T, w.H, w.E_log, w.E_phys, w.k, w.I, w.R, w.S)
+    assert w.T * w.k > 32 * w.E_phys
+    assert B.moe_expert_ffn_path(shape) == B.MOE_FFN_TENSOR_CORE
+    assert B.moe_expert_ffn_narrow_rows(shape) == 0
+
+
 @pytest.mark.parametrize("bad", [
     dict(T=0), dict(H=24), dict(I=8), dict(k=0), dict(k=17), dict(E_phys=8),
     dict(n_ranks=3), dict(n_src_ranks=5), dict(dispatch_fmt=2),
